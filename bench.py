@@ -1,0 +1,532 @@
+#!/usr/bin/env python3
+"""Benchmark of the logical-rank all-reduce on one GB300 (one JSON line).
+
+Headline workload: R=2 logical ranks, fp16, N=131072 elements per rank (256 KiB,
+the host all-reduce's payload cap), pinned-host slots, calls replayed from a
+CUDA graph.  A step is one graph replay of C calls (every call of the step has
+its own input and output buffers, so inputs are fresh each call); L2 is
+flushed (a 256 MiB write) before every step, outside the timed events.
+
+value = algbw = S / (time per call), S = per-rank payload bytes (GB/s, 1e9).
+Also reported: us/call, the host-link roofline of the exchange kernel (with
+the link bandwidth measured in the same run by the library's probe kernels),
+an end-to-end figure through the C ABI with host buffers, the HBM-slot
+workloads (R=8 bf16, 16/64 MiB), the complex64 allgather, and the CPU oracle
+timed on the host's cores.
+
+--impl reference runs the CPU oracle instead (the reference arm of this
+build): the same metric, config and unit, each step a bounded sample.
+
+--gpus N (under torchrun) runs N independent replicas, one per GPU: the
+all-reduce's ranks are logical ranks on one GPU, so there is nothing to shard
+across GPUs.  The step time is the max over GPUs; value sums the replicas.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "all-reduce us/call and algbw GB/s vs payload, R logical ranks on 1 GB300 (graph)"
+UNIT = "GB/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--calls", type=int, default=100, help="all-reduce calls per step (graph length)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sweep", default=None, help="run the payload sweep; write JSON lines to this file")
+    ap.add_argument("--sweep-calls", type=int, default=1000)
+    ap.add_argument("--no-extras", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------- dist
+
+class Dist:
+    def __init__(self, n_gpus):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl"
+            try:
+                import torch
+                if not torch.cuda.is_available():
+                    backend = "gloo"
+            except Exception:
+                backend = "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = "cuda" if torch.cuda.is_available() and self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def max_over_ranks(values):
+    """The slowest replica sets the step time."""
+    return max(values)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (clocks and throttle reasons)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"tda_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9 and p[1].replace(".", "").isdigit():
+                    rows.append(p)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows
+                                                          if r[3].replace(".", "").isdigit())}
+
+
+# ------------------------------------------------------------- measurement
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except Exception:
+        return {}
+
+
+class Workload:
+    """R ranks, C calls, one graph; every call has its own device buffers."""
+
+    def __init__(self, op, R, dtype, numel, slots, calls, config, dist="uniform"):
+        import torch
+        import tensor_decode_all_gb300 as tda
+        from tensor_decode_all_gb300 import inputs
+        self.torch = torch
+        self.op, self.R, self.dtype, self.numel, self.slots, self.C = op, R, dtype, numel, slots, calls
+        tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "c64": torch.complex64}[dtype]
+        self.tdt = tdt
+        self.h = tda.Handle(R, tdt, numel, slots)
+        self.streams = [torch.cuda.Stream() for _ in range(R)]
+        out_n = numel * (R if op == "allgather" else 1)
+        # inputs [C][numel] per rank, contiguous, so one copy moves a whole step
+        self.ins = [torch.empty((calls, numel), dtype=tdt, device="cuda") for _ in range(R)]
+        self.outs = [torch.empty((calls, out_n), dtype=tdt, device="cuda") for _ in range(R)]
+        self.host_in = []
+        isz = 8 if dtype == "c64" else 2
+        distinct = min(calls, 8) if numel * isz <= (1 << 20) else (2 if numel * isz <= (16 << 20) else 1)
+        per_call = []
+        for c in range(distinct):
+            if op == "allgather":
+                per_call.append([z.view(np.uint8) for z in inputs.allgather_inputs(config, R, numel, c)])
+            else:
+                per_call.append([x.view(np.uint8) for x in inputs.allreduce_inputs(config, R, numel, dtype, dist, c)])
+        for r in range(R):
+            host = np.stack([per_call[c % distinct][r] for c in range(calls)])
+            self.host_in.append(host)
+            self.ins[r].copy_(torch.from_numpy(host).view(tdt).view(calls, numel))
+        self.graph = None
+
+    def capture(self):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                cap = torch.cuda.current_stream()
+                for s in self.streams:
+                    s.wait_stream(cap)
+                for c in range(self.C):
+                    for r in range(self.R):
+                        getattr(self.h, self.op)(r, self.ins[r][c], self.outs[r][c], self.streams[r])
+                for s in self.streams:
+                    cap.wait_stream(s)
+        torch.cuda.current_stream().wait_stream(side)
+        self.graph = g
+        return g
+
+    def check(self, calls=(0, -1)):
+        """Bit-exact comparison of sampled calls with the CPU oracle."""
+        import oracle
+        self.torch.cuda.synchronize()
+        self.h.check()
+        for c in calls:
+            c = c % self.C
+            xs = [self.host_in[r][c] for r in range(self.R)]
+            if self.op == "allgather":
+                want = oracle.allgather(xs, ranks=[0])[0]
+            else:
+                want = oracle.allreduce([x.view(np.uint16) for x in xs], self.dtype, ranks=[0])[0].view(np.uint8)
+            for r in range(self.R):
+                got = self.outs[r][c].cpu()
+                got = got.view(self.torch.uint8).numpy() if self.dtype != "c64" else got.numpy().view(np.uint8)
+                if not np.array_equal(got, want):
+                    raise AssertionError(f"bench parity: {self.op} call {c} rank {r} differs from the oracle")
+        return len(calls) * self.R
+
+    def time_graph(self, steps, warmup, flush):
+        torch = self.torch
+        if self.graph is None:
+            self.capture()
+        cur = torch.cuda.current_stream()
+        for _ in range(warmup):
+            flush.zero_()
+            self.graph.replay()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(cur)
+            self.graph.replay()
+            b.record(cur)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]  # ms per step
+
+    def time_e2e(self, steps):
+        """Pinned host in -> device, C eager calls per rank through the C ABI,
+        device -> pinned host out; CUDA events on the origin stream."""
+        torch = self.torch
+        pin_in = [torch.from_numpy(self.host_in[r]).view(self.tdt).view(self.C, self.numel).pin_memory()
+                  for r in range(self.R)]
+        pin_out = [torch.empty(self.outs[r].shape, dtype=self.tdt).pin_memory() for r in range(self.R)]
+        cur = torch.cuda.current_stream()
+        times = []
+        for step in range(steps + 1):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(cur)
+            for r in range(self.R):
+                self.ins[r].copy_(pin_in[r], non_blocking=True)
+            for s in self.streams:
+                s.wait_stream(cur)
+            for c in range(self.C):
+                for r in range(self.R):
+                    getattr(self.h, self.op)(r, self.ins[r][c], self.outs[r][c], self.streams[r])
+            for s in self.streams:
+                cur.wait_stream(s)
+            for r in range(self.R):
+                pin_out[r].copy_(self.outs[r], non_blocking=True)
+            b.record(cur)
+            b.synchronize()
+            if step:  # the first step warms the pinned buffers
+                times.append(a.elapsed_time(b))
+        h2d = sum(t.numel() * t.element_size() for t in pin_in)
+        d2h = sum(t.numel() * t.element_size() for t in pin_out)
+        return times, h2d, d2h
+
+    def close(self):
+        self.graph = None
+        self.h.destroy()
+
+
+def algo_bytes(op, R, S, slots):
+    """Algorithmic bytes of one call (all R ranks).
+
+    pinned-host all-reduce: host-link writes W = R*S (each rank publishes once),
+      reads Rd = R*(R-1)*S (each rank fetches every peer's chunk);
+    HBM all-reduce: DRAM 4*R*S (inputs, slot writes, slot reads once, outputs);
+    allgather: HBM R*S + R*S + R*S + R*R*S; pinned W = R*S, Rd = R*(R-1)*S.
+    """
+    if slots == "pinned":
+        return {"link_write": R * S, "link_read": R * (R - 1) * S}
+    if op == "allreduce":
+        return {"dram": 4 * R * S}
+    return {"dram": 3 * R * S + R * R * S}
+
+
+def roofline(op, R, S, slots, t_call_s, link, hbm_gbs):
+    b = algo_bytes(op, R, S, slots)
+    if slots == "pinned":
+        w = b["link_write"] / (link["bidir_write_gbs"] * 1e9)
+        rd = b["link_read"] / (link["bidir_read_gbs"] * 1e9)
+        if w >= rd:
+            bytes_, peak, which = b["link_write"], link["bidir_write_gbs"], "write"
+        else:
+            bytes_, peak, which = b["link_read"], link["bidir_read_gbs"], "read"
+        achieved = bytes_ / t_call_s / 1e9
+        return {"bound": "host_link", "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None, "direction": which,
+                "algorithmic_bytes_per_call": bytes_,
+                "peak_source": "measured in this run: ar_probe_host_link, both directions at once"}
+    achieved = b["dram"] / t_call_s / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_gbs, "unit": "GB/s",
+            "frac": round(achieved / hbm_gbs, 4), "traffic": None, "algorithmic_bytes_per_call": b["dram"],
+            "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)"}
+
+
+def summarize(op, R, dtype, numel, slots, ms_steps, C, link, hbm_gbs):
+    isz = 8 if dtype == "c64" else 2
+    S = numel * isz
+    total_ms = sum(ms_steps)
+    t_call = total_ms * 1e-3 / (len(ms_steps) * C)
+    out_bytes = S * (R if op == "allgather" else 1)
+    return {"op": op, "R": R, "dtype": dtype, "numel": numel, "bytes_per_rank": S, "slots": slots,
+            "us_per_call": round(t_call * 1e6, 3),
+            "us_per_call_median_step": round(statistics.median(ms_steps) * 1e3 / C, 3),
+            "algbw_gbs": round(out_bytes / t_call / 1e9, 3),
+            "busbw_gbs": round(S / t_call / 1e9 * ((2 * (R - 1) / R) if op == "allreduce" else (R - 1) / R), 3)
+            if R > 1 else None,
+            "roofline": roofline(op, R, S, slots, t_call, link, hbm_gbs), "calls": len(ms_steps) * C}
+
+
+def cpu_baseline(R, dtype, numel, seconds=10.0, config=2, dist="normal4"):
+    """The oracle as it stands, all host cores, on a bounded sample of calls."""
+    import oracle
+    from tensor_decode_all_gb300 import inputs
+    cores = oracle.max_threads()
+    xs = inputs.allreduce_inputs(config, R, numel, dtype, dist, 0)
+    oracle.allreduce(xs, dtype, nthreads=cores)  # warm
+    t0 = time.perf_counter()
+    calls = 0
+    while time.perf_counter() - t0 < seconds:
+        oracle.allreduce(xs, dtype, nthreads=cores)  # every rank's output, as the job computes
+        calls += 1
+    dt = time.perf_counter() - t0
+    S = numel * 2
+    return {"value": round(S * calls / dt / 1e9, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "us_per_call": round(dt / calls * 1e6, 2),
+            "sample": f"{calls} calls of the headline workload (R={R} {dtype} N={numel}, all {R} ranks' "
+                      f"outputs) in {dt:.1f} s"}
+
+
+def run_ours(args, dist):
+    import torch
+    import tensor_decode_all_gb300 as tda
+    dev = dist.local if torch.cuda.device_count() > dist.local else 0
+    torch.cuda.set_device(dev)
+    tda.build()
+    peaks = measured_peaks()
+    hbm_gbs = float(peaks.get("hbm_gbs", 6800.0))
+    hbm_src = "MEASURED_PEAKS.json (of measured)" if "hbm_gbs" in peaks else "fallback 6.8 TB/s (of fallback)"
+    link = tda.ar_probe_host_link(64 << 20, 10)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    R, numel, C = 2, 131072, args.calls
+    w = Workload("allreduce", R, "f16", numel, "pinned", C, config=2, dist="normal4")
+    w.capture()
+    w.time_graph(1, 0, flush)
+    checked = w.check(calls=(0, 1, C // 2, -1))
+    dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        ms = w.time_graph(args.steps, args.warmup, flush)
+    clocks = clk.summary()
+    checked += w.check(calls=(0, -1))
+    total_s = dist.max(sum(ms) * 1e-3)
+    head = summarize("allreduce", R, "f16", numel, "pinned", ms, C, link, hbm_gbs)
+    S = numel * 2
+    n = dist.world
+    value = n * S * len(ms) * C / total_s / 1e9
+
+    e2e_times, h2d, d2h = w.time_e2e(min(args.steps, 30))
+    e2e_s = dist.max(sum(e2e_times) * 1e-3)
+    e2e_value = n * S * len(e2e_times) * C / e2e_s / 1e9
+    w.close()
+
+    extras = {}
+    if not args.no_extras:
+        for name, (op, RR, dt, nn, sl, cfg, dd, cc, st) in {
+            "r8_bf16_393216_hbm": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20),
+            "r8_bf16_16MiB_hbm": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 10, 10),
+            "r8_bf16_64MiB_hbm": ("allreduce", 8, "bf16", 32 << 20, "hbm", 5, "uniform", 4, 10),
+            "r2_fp16_16MiB_hbm": ("allreduce", 2, "f16", 8 << 20, "hbm", 5, "uniform", 10, 10),
+            "allgather_c64_r4_hbm": ("allgather", 4, "c64", 500000, "hbm", 4, None, 20, 10),
+            "allgather_c64_r8_hbm": ("allgather", 8, "c64", 500000, "hbm", 4, None, 20, 10),
+            "allgather_c64_r4_pinned": ("allgather", 4, "c64", 500000, "pinned", 4, None, 5, 5),
+        }.items():
+            wx = Workload(op, RR, dt, nn, sl, cc, config=cfg, dist=dd or "uniform")
+            wx.capture()
+            wx.time_graph(1, 0, flush)
+            wx.check(calls=(0, -1))
+            msx = wx.time_graph(st, 2, flush)
+            wx.check(calls=(-1,))
+            extras[name] = summarize(op, RR, dt, nn, sl, msx, cc, link, hbm_gbs)
+            wx.close()
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": n, "steps": len(ms),
+        "warmup": args.warmup, "ms_per_step": round(total_s * 1e3 / len(ms), 4),
+        "us_per_call": head["us_per_call"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded 4*N(0,1) cast to fp16)",
+        "config": {"workload": "R=2 logical ranks, fp16, N=131072 per rank (256 KiB), pinned-host slots, "
+                               "graph-replayed", "R": R, "numel": numel, "bytes_per_rank": S,
+                   "calls_per_step": C, "slots": "pinned_host",
+                   "l2": "flushed (256 MiB write) before every step, outside the timed events",
+                   "parallelism": f"replicas x{n} (logical ranks share one GPU)"},
+        "roofline": head["roofline"],
+        "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": f"{C} eager ar_allreduce calls per rank per step, with the step's inputs copied from "
+                       "pinned host memory before and outputs copied back after, inside CUDA events"},
+        "gpu_launches": len(ms) * C * R,
+        "clocks": clocks,
+        "parity": f"bit-exact vs CPU oracle on {checked} sampled (call, rank) outputs",
+        "host_link_probe_gbs": {k: round(v, 2) for k, v in link.items()},
+        "hbm_peak": {"gbs": hbm_gbs, "source": hbm_src},
+        "workloads": extras,
+    }
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(R, "f16", numel)
+    return line
+
+
+def run_reference(args, dist):
+    """The CPU oracle as the reference arm: same workload, metric and unit."""
+    if dist.rank != 0:
+        return None
+    import oracle
+    from tensor_decode_all_gb300 import inputs
+    oracle.build()
+    R, numel, dtype = 2, 131072, "f16"
+    cores = oracle.max_threads()
+    xs = inputs.allreduce_inputs(2, R, numel, dtype, "normal4", 0)
+    calls_per_step = 20
+    for _ in range(args.warmup):
+        for _ in range(calls_per_step):
+            oracle.allreduce(xs, dtype, nthreads=cores)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        for _ in range(calls_per_step):
+            oracle.allreduce(xs, dtype, nthreads=cores)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    S = numel * 2
+    value = S * calls_per_step * len(times) / total / 1e9
+    sample = f"{calls_per_step} calls per step of R={R} {dtype} N={numel} (all ranks' outputs), {cores} threads"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": dist.world,
+            "steps": len(times), "warmup": args.warmup, "ms_per_step": round(total * 1e3 / len(times), 3),
+            "us_per_call": round(total / (len(times) * calls_per_step) * 1e6, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic (seeded 4*N(0,1) cast to fp16)",
+            "config": {"workload": "R=2 logical ranks, fp16, N=131072 per rank (256 KiB), CPU oracle",
+                       "R": R, "numel": numel},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_sweep(args, dist):
+    """Payload sweep 2 KiB..64 MiB, fp16/bf16, R=2/4/8, pinned vs HBM slots;
+    oracle parity on the first and last call of every cell."""
+    import torch
+    import tensor_decode_all_gb300 as tda
+    torch.cuda.set_device(0)
+    tda.build()
+    peaks = measured_peaks()
+    hbm_gbs = float(peaks.get("hbm_gbs", 6800.0))
+    link = tda.ar_probe_host_link(64 << 20, 10)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    with open(args.sweep, "w") as f:
+        for slots in ("hbm", "pinned"):
+            for dtype in ("f16", "bf16"):
+                for R in (2, 4, 8):
+                    for k in range(11, 27):
+                        S = 1 << k
+                        numel = S // 2
+                        total = args.sweep_calls
+                        C = max(1, min(100, (256 << 20) // max(1, R * S * 2)))
+                        steps = max(1, total // C)
+                        w = Workload("allreduce", R, dtype, numel, slots, C, config=5, dist="uniform")
+                        w.capture()
+                        w.time_graph(1, 0, flush)
+                        w.check(calls=(0, -1))
+                        ms = w.time_graph(steps, 2, flush)
+                        w.check(calls=(0, -1))
+                        row = summarize("allreduce", R, dtype, numel, slots, ms, C, link, hbm_gbs)
+                        row["parity"] = "bit-exact (first and last call)"
+                        f.write(json.dumps(row) + "\n")
+                        f.flush()
+                        w.close()
+                        print(f"{slots:6s} {dtype:4s} R={R} S={S:>9d}: {row['us_per_call']:9.2f} us/call "
+                              f"{row['algbw_gbs']:9.2f} GB/s frac={row['roofline']['frac']}", flush=True)
+    return None
+
+
+def main():
+    args = parse()
+    dist = Dist(args.gpus)
+    try:
+        if args.impl == "reference":
+            line = run_reference(args, dist)
+        elif args.sweep:
+            line = run_sweep(args, dist)
+        else:
+            line = run_ours(args, dist)
+        if line is not None and dist.rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,260 @@
+/*
+ * ar.h -- C ABI of the logical-rank all-reduce / allgather library (libtda_ar.so).
+ *
+ * R "logical ranks" share one GPU.  Each rank is a kernel launched on its own
+ * non-blocking stream; the R kernels of one call run at the same time and meet
+ * through a shared, double-buffered slot and per-block flags.  The operation
+ * is the flag-synchronised exchange-and-add of "[Kernel] Two-rank FP16
+ * all-reduce through pinned host memory for GPUs without P2P" (1Cat-vLLM pull
+ * 1216), section "Purpose": every block writes its chunk to a slot, fences,
+ * raises a per-block flag, waits for its peers' flags and adds their chunks,
+ * with one rounding; slots alternate by call parity; nothing runs on the CPU
+ * and nothing synchronises a stream, so calls can be captured in CUDA graphs.
+ * That page is about two ranks; this library takes 1 <= R <= 8 and sums in
+ * rank order 0..R-1 on every rank (the order matters from three ranks on:
+ * "[SM120] Add optional FlashInfer PCIe-IPC all-reduce for switch-free hosts",
+ * section "Accuracy").
+ *
+ * Conventions for every entry point:
+ *   - Pointers named in/out are device-accessible addresses (cudaMalloc'd or
+ *     mapped pinned host memory) owned by the caller, 16-byte aligned.
+ *   - `stream` is a cudaStream_t created with cudaStreamNonBlocking, owned by
+ *     the caller.  The legacy default stream, the per-thread default stream and
+ *     blocking streams are refused (AR_ESTREAM): a stream that serialises with
+ *     the legacy stream can hold back a peer rank's kernel while this rank's
+ *     kernel waits for it ("fix(group): run each rank on a non-blocking
+ *     stream", Algorithmiq src-method pull 75, sections "What" and "Why").
+ *   - Return value: AR_OK (0) or an ar_code below.  A call that returns an
+ *     error other than AR_ECUDA has enqueued nothing, so the caller can keep
+ *     its own fallback path ("[SM120] Add optional FlashInfer PCIe-IPC
+ *     all-reduce for switch-free hosts", section "Modifications": a shape the
+ *     backend cannot take is reported and the caller keeps NCCL).
+ *   - Errors found on the device (a peer that never arrives) cannot be
+ *     returned by the enqueueing call; they are recorded in the handle and read
+ *     with ar_status() after the caller has synchronised.
+ */
+#ifndef TDA_AR_H
+#define TDA_AR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define AR_API __attribute__((visibility("default")))
+#else
+#define AR_API
+#endif
+
+/* A CUDA stream handle (identical to cudaStream_t), spelled without CUDA headers. */
+typedef struct CUstream_st *ar_stream_t;
+
+typedef struct ar_handle ar_handle;
+
+/* Element types.  AR_F16 = IEEE binary16, AR_BF16 = bfloat16 (all-reduce and
+ * allgather); AR_C64 = complex64, two binary32 (allgather only: the pages
+ * gather complex64 tensors and never reduce them). */
+enum ar_dtype { AR_F16 = 1, AR_BF16 = 2, AR_C64 = 3 };
+
+/* Where the shared slots and flags live.
+ * AR_SLOT_PINNED_HOST: page-locked host memory mapped into the GPU
+ *   (cudaHostAlloc mapped|portable), as on the pages, where two GPUs without
+ *   peer access both map it ("[Kernel] Two-rank FP16 all-reduce through pinned
+ *   host memory for GPUs without P2P", section "Purpose").  Flags use
+ *   system-scope release/acquire.
+ * AR_SLOT_HBM: device memory of this GPU; flags use GPU-scope release/acquire. */
+enum ar_slot_kind { AR_SLOT_PINNED_HOST = 0, AR_SLOT_HBM = 1 };
+
+enum ar_code {
+    AR_OK = 0,
+    AR_EINVAL = 1,    /* bad handle, rank, R, dtype, slot kind, NULL or misaligned pointer,
+                         wrong current device, or an operation the handle's dtype lacks */
+    AR_ETOOBIG = 2,   /* numel > max_numel: declined, nothing enqueued; the workspace
+                         cannot grow after ar_create ("[SM120] Add optional FlashInfer
+                         PCIe-IPC all-reduce for switch-free hosts", section "Modifications") */
+    AR_ESTREAM = 3,   /* NULL, legacy, per-thread-default or blocking stream, or the same
+                         stream as another rank's pending call of the same sequence number */
+    AR_ENOMEM = 4,    /* slot, flag or counter allocation failed in ar_create */
+    AR_ECUDA = 5,     /* a CUDA runtime call failed (launch error, no device, ...) */
+    AR_ETIMEOUT = 6,  /* recorded on the device: a block waited longer than the timeout for
+                         a peer's flag.  Outputs of that call and of every later call are
+                         undefined until ar_reset(). */
+    AR_ESTATE = 7     /* the handle needs ar_reset() (a device error is recorded) */
+};
+
+/* Details of the first device-side error recorded in a handle. */
+typedef struct ar_error_info {
+    int32_t code;       /* AR_OK or AR_ETIMEOUT */
+    int32_t rank;       /* rank whose block gave up waiting */
+    int32_t block;      /* that block's index */
+    int32_t peer;       /* the first peer whose flag had not arrived */
+    uint64_t want;      /* flag value the block waited for */
+    uint64_t seen;      /* flag value it last saw */
+} ar_error_info;
+
+/* Static facts about a handle, for tests and tools. */
+typedef struct ar_info {
+    int32_t R, dtype, slot_kind, device;
+    int32_t threads;        /* threads per block of the exchange kernels */
+    int32_t max_blocks;     /* blocks per rank at most: R * max_blocks blocks fit on the GPU at once */
+    int32_t sm_count;
+    int32_t blocks_per_sm;  /* occupancy of the exchange kernel */
+    uint64_t max_numel;
+    uint64_t slot_bytes;    /* bytes of one (parity, rank) slot, a multiple of 256 */
+    uint64_t total_slot_bytes; /* 2 * R * slot_bytes: the allocation that cannot grow */
+    uint64_t timeout_ns;
+} ar_info;
+
+/* Launch plan of one call, computed on the host (no GPU needed). */
+typedef struct ar_plan {
+    int32_t blocks;         /* grid size per rank (same on every rank) */
+    int32_t threads;        /* threads per block */
+    int32_t vec_bytes;      /* bytes per vector access: 16 for all-reduce */
+    int32_t unroll;         /* vectors per thread per tile */
+    uint64_t tile_bytes;    /* bytes a block handles per stage (threads * unroll * vec_bytes) */
+    uint64_t tiles;         /* ceil(bytes / tile_bytes); tile t goes to block t % blocks, stage t / blocks */
+    uint64_t max_stages;    /* stages of block 0 = ceil(tiles / blocks) */
+} ar_plan;
+
+/*
+ * ar_create -- allocate a handle for R logical ranks.
+ *
+ * R in [1, 8]; dtype an ar_dtype; max_numel >= 1 elements per rank; slot_kind an
+ * ar_slot_kind.  Allocates, owned by the library until ar_destroy():
+ *   slots   [2 parities][R ranks][slot_bytes], slot_bytes = round_up(max_numel *
+ *           itemsize, 256), in pinned host or HBM memory per slot_kind.  The size
+ *           is fixed here and cannot grow: the cost law is 2 * R * max_numel *
+ *           itemsize, as for the workspace in "[SM120] Add optional FlashInfer
+ *           PCIe-IPC all-reduce for switch-free hosts", section "Modifications";
+ *   flags   one 64-bit flag per (rank, block), each on its own 128-byte line, in
+ *           the same memory as the slots;
+ *   counters one 64-bit stage counter and one 64-bit call counter per (rank,
+ *           block), in device memory: the call parity that picks the slot buffer
+ *           comes from them, never from the host, so captured graphs replay
+ *           correctly.
+ * All of it starts at zero.  Uses the current CUDA device, which every later
+ * call must also have current.  Returns NULL on failure; ar_last_error() then
+ * gives the code (AR_EINVAL, AR_ENOMEM or AR_ECUDA).
+ * The wait timeout starts at 1 s, or at the value of the environment variable
+ * AR_SPIN_TIMEOUT_NS if set (bounded device spin: "fix(qwen3): re-enable CUDA
+ * Graph under TP via startup decode-graph pre-capture", openinfer pull 611,
+ * section "Description": without one, a wedged rank waits forever).
+ */
+AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind);
+
+/* Code of the last failed ar_create() on this thread (AR_OK if none). */
+AR_API int ar_last_error(void);
+
+/*
+ * ar_allreduce -- enqueue rank `rank`'s part of one all-reduce on `stream`.
+ *
+ * in:  numel elements of the handle's dtype (AR_F16 or AR_BF16), contiguous,
+ *      16-byte aligned, device-accessible, owned by the caller.
+ * out: numel elements, same rules; out == in is allowed (in place), any other
+ *      overlap is not.
+ * After all R ranks have enqueued their call with the same numel and their
+ * streams have run it, every out_r[i] holds
+ *     RNE( f32(x_0[i]) + f32(x_1[i]) + ... + f32(x_{R-1}[i]) )
+ * with binary32 additions left to right in rank order and one rounding to the
+ * dtype: the same bits on every rank.
+ * Contract between ranks: every rank 0..R-1 issues the same sequence of calls on
+ * this handle with the same numel, each rank on its own non-blocking stream,
+ * and the R kernels of a call must be able to run at the same time (they wait
+ * for each other on the device).  No host synchronisation and no CPU work is
+ * done: the call may be captured into a CUDA graph (all R ranks' calls in the
+ * same graph, or graphs launched together).
+ * numel == 0 enqueues nothing and returns AR_OK.
+ * Errors: AR_EINVAL, AR_ETOOBIG, AR_ESTREAM, AR_ESTATE (a device error is
+ * recorded: call ar_reset first), AR_ECUDA (launch failed).
+ */
+AR_API int ar_allreduce(ar_handle *h, int rank, const void *in, void *out, size_t numel,
+                        ar_stream_t stream);
+
+/*
+ * ar_allgather -- enqueue rank `rank`'s part of one allgather on `stream`.
+ *
+ * in:  numel elements of the handle's dtype (any dtype; AR_C64 is the pages'
+ *      case, the complex64 S_j and core uploads of "fix(group): run each rank
+ *      on a non-blocking stream", section "Why"), 16-byte aligned.
+ * out: R * numel elements: after the call every rank's out holds shard 0, then
+ *      shard 1, ..., then shard R-1 (rank-major concatenation), bit for bit.
+ *      out must not overlap in.
+ * Same contract between ranks, errors and graph rules as ar_allreduce.
+ */
+AR_API int ar_allgather(ar_handle *h, int rank, const void *in, void *out, size_t numel,
+                        ar_stream_t stream);
+
+/*
+ * ar_status -- the first device-side error recorded in the handle (AR_OK or
+ * AR_ETIMEOUT), copied into *info if info is not NULL.  Reads mapped host
+ * memory only (no CUDA call); the answer covers the kernels the caller has
+ * already synchronised with.
+ */
+AR_API int ar_status(ar_handle *h, ar_error_info *info);
+
+/*
+ * ar_reset -- synchronise the device, then zero every flag, counter and the
+ * error record.  Required after AR_ETIMEOUT; afterwards the handle behaves as
+ * if just created.  No graph that uses the handle may be running.
+ */
+AR_API int ar_reset(ar_handle *h);
+
+/*
+ * ar_destroy -- synchronise the device and free everything ar_create
+ * allocated.  Every CUDA graph that captured calls on this handle must be
+ * destroyed first (captured kernels hold the handle's addresses; teardown
+ * order as in "[SM120] Add optional FlashInfer PCIe-IPC all-reduce for
+ * switch-free hosts", review of destroy(): release the workspace before what
+ * it depends on, and "fix(qwen3): re-enable CUDA Graph under TP ...", section
+ * "Description": graphs go before the communicator).  NULL is a no-op.
+ */
+AR_API int ar_destroy(ar_handle *h);
+
+/* Set the device wait timeout in nanoseconds (>= 1000).  Applies to calls
+ * enqueued afterwards; a captured graph keeps the value in force at capture. */
+AR_API int ar_set_timeout(ar_handle *h, uint64_t timeout_ns);
+
+/* Static facts about the handle. */
+AR_API int ar_query(const ar_handle *h, ar_info *info);
+
+/*
+ * ar_plan_for -- the launch plan ar_allreduce (op 0) or ar_allgather (op 1)
+ * would use for numel elements on this handle.  Pure host arithmetic.
+ */
+AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan);
+
+/*
+ * ar_plan_compute -- the same plan from explicit machine facts, so the host
+ * logic can be checked without a GPU: R ranks, `bytes` per rank, vector size
+ * vec_bytes (16, 8, 4, 2 or 1), `threads` per block, and a GPU that holds
+ * sm_count * blocks_per_sm blocks of the kernel at once.
+ */
+AR_API int ar_plan_compute(int R, uint64_t bytes, int vec_bytes, int threads, int sm_count,
+                           int blocks_per_sm, ar_plan *plan);
+
+/* Human-readable name of an ar_code.  Never NULL. */
+AR_API const char *ar_strerror(int code);
+
+/*
+ * Bandwidth probes: the denominators of the roofline.  Each allocates its own
+ * buffers, runs its copy kernels `reps` times on a private non-blocking stream,
+ * times them with CUDA events and frees everything.
+ *
+ * ar_probe_host_link: GPU kernels stream `bytes` to mapped pinned host memory
+ *   (write), from it (read), and both at once (two kernels on two streams).
+ *   gbs[0] = write GB/s, gbs[1] = read GB/s, gbs[2] = write GB/s while reading,
+ *   gbs[3] = read GB/s while writing.  (1 GB = 1e9 bytes.)
+ * ar_probe_hbm_copy: a device-to-device copy kernel over `bytes`; *gbs counts
+ *   read + write bytes.
+ */
+AR_API int ar_probe_host_link(uint64_t bytes, int reps, double gbs[4]);
+AR_API int ar_probe_hbm_copy(uint64_t bytes, int reps, double *gbs);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TDA_AR_H */

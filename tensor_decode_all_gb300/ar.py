@@ -1,0 +1,290 @@
+"""Python binding of include/ar.h (ctypes; argument marshalling only).
+
+Every step of the exchange runs in libtda_ar.so.  PyTorch is used only to hand
+over device pointers (``tensor.data_ptr()``) and streams
+(``torch.cuda.Stream.cuda_stream``).  If the library is not built, every call
+raises: there is no CPU path.
+
+Module-level functions carry the C names (``ar_create``, ``ar_allreduce``, ...)
+and take raw pointers / stream handles as ints.  ``Handle`` wraps one
+``ar_handle*`` for tensor arguments.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from . import build as _build
+
+AR_F16, AR_BF16, AR_C64 = 1, 2, 3
+AR_SLOT_PINNED_HOST, AR_SLOT_HBM = 0, 1
+AR_OK, AR_EINVAL, AR_ETOOBIG, AR_ESTREAM, AR_ENOMEM, AR_ECUDA, AR_ETIMEOUT, AR_ESTATE = range(8)
+CODE_NAMES = {0: "AR_OK", 1: "AR_EINVAL", 2: "AR_ETOOBIG", 3: "AR_ESTREAM", 4: "AR_ENOMEM",
+              5: "AR_ECUDA", 6: "AR_ETIMEOUT", 7: "AR_ESTATE"}
+ITEMSIZE = {AR_F16: 2, AR_BF16: 2, AR_C64: 8}
+SLOT_KINDS = {"pinned": AR_SLOT_PINNED_HOST, "pinned_host": AR_SLOT_PINNED_HOST, "host": AR_SLOT_PINNED_HOST,
+              "hbm": AR_SLOT_HBM, "device": AR_SLOT_HBM}
+
+
+class ArError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = int(code)
+        super().__init__(f"{what}: {strerror(code)}" if what else strerror(code))
+
+
+class ErrorInfo(ctypes.Structure):
+    _fields_ = [("code", ctypes.c_int32), ("rank", ctypes.c_int32), ("block", ctypes.c_int32),
+                ("peer", ctypes.c_int32), ("want", ctypes.c_uint64), ("seen", ctypes.c_uint64)]
+
+
+class Info(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_int32), ("dtype", ctypes.c_int32), ("slot_kind", ctypes.c_int32),
+                ("device", ctypes.c_int32), ("threads", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
+                ("sm_count", ctypes.c_int32), ("blocks_per_sm", ctypes.c_int32),
+                ("max_numel", ctypes.c_uint64), ("slot_bytes", ctypes.c_uint64),
+                ("total_slot_bytes", ctypes.c_uint64), ("timeout_ns", ctypes.c_uint64)]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("blocks", ctypes.c_int32), ("threads", ctypes.c_int32), ("vec_bytes", ctypes.c_int32),
+                ("unroll", ctypes.c_int32), ("tile_bytes", ctypes.c_uint64), ("tiles", ctypes.c_uint64),
+                ("max_stages", ctypes.c_uint64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded libtda_ar.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build it with "
+                                   "tensor_decode_all_gb300.build.build() (there is no CPU fallback)")
+            L = ctypes.CDLL(path)
+            vp, sz, i32, u64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint64
+            L.ar_create.argtypes = [i32, i32, sz, i32]
+            L.ar_create.restype = vp
+            L.ar_last_error.restype = i32
+            for name in ("ar_allreduce", "ar_allgather"):
+                f = getattr(L, name)
+                f.argtypes = [vp, i32, vp, vp, sz, vp]
+                f.restype = i32
+            L.ar_status.argtypes = [vp, ctypes.POINTER(ErrorInfo)]
+            L.ar_reset.argtypes = [vp]
+            L.ar_destroy.argtypes = [vp]
+            L.ar_set_timeout.argtypes = [vp, u64]
+            L.ar_query.argtypes = [vp, ctypes.POINTER(Info)]
+            L.ar_plan_for.argtypes = [vp, i32, sz, ctypes.POINTER(Plan)]
+            L.ar_plan_compute.argtypes = [i32, u64, i32, i32, i32, i32, ctypes.POINTER(Plan)]
+            L.ar_strerror.argtypes = [i32]
+            L.ar_strerror.restype = ctypes.c_char_p
+            L.ar_probe_host_link.argtypes = [u64, i32, ctypes.POINTER(ctypes.c_double)]
+            L.ar_probe_hbm_copy.argtypes = [u64, i32, ctypes.POINTER(ctypes.c_double)]
+            _lib = L
+    return _lib
+
+
+def declared_symbols(header: str | None = None):
+    """Names of the entry points include/ar.h declares."""
+    header = header or os.path.join(_build.INCLUDE, "ar.h")
+    text = open(header).read()
+    return sorted(set(re.findall(r"AR_API\s+[^;(]*?\b(ar_\w+)\s*\(", text)))
+
+
+# ---------------------------------------------------------------- C names
+
+def ar_create(R: int, dtype: int, max_numel: int, slot_kind: int) -> int:
+    return lib().ar_create(R, dtype, max_numel, slot_kind) or 0
+
+
+def ar_last_error() -> int:
+    return lib().ar_last_error()
+
+
+def ar_allreduce(h: int, rank: int, inp: int, out: int, numel: int, stream: int) -> int:
+    return lib().ar_allreduce(h, rank, inp, out, numel, stream)
+
+
+def ar_allgather(h: int, rank: int, inp: int, out: int, numel: int, stream: int) -> int:
+    return lib().ar_allgather(h, rank, inp, out, numel, stream)
+
+
+def ar_status(h: int) -> ErrorInfo:
+    info = ErrorInfo()
+    lib().ar_status(h, ctypes.byref(info))
+    return info
+
+
+def ar_reset(h: int) -> int:
+    return lib().ar_reset(h)
+
+
+def ar_destroy(h: int) -> int:
+    return lib().ar_destroy(h)
+
+
+def ar_set_timeout(h: int, ns: int) -> int:
+    return lib().ar_set_timeout(h, ns)
+
+
+def ar_query(h: int) -> Info:
+    info = Info()
+    rc = lib().ar_query(h, ctypes.byref(info))
+    if rc:
+        raise ArError(rc, "ar_query")
+    return info
+
+
+def ar_plan_for(h: int, op: int, numel: int) -> Plan:
+    p = Plan()
+    rc = lib().ar_plan_for(h, op, numel, ctypes.byref(p))
+    if rc:
+        raise ArError(rc, "ar_plan_for")
+    return p
+
+
+def ar_plan_compute(R, nbytes, vec_bytes, threads, sm_count, blocks_per_sm) -> Plan:
+    p = Plan()
+    rc = lib().ar_plan_compute(R, nbytes, vec_bytes, threads, sm_count, blocks_per_sm, ctypes.byref(p))
+    if rc:
+        raise ArError(rc, "ar_plan_compute")
+    return p
+
+
+def strerror(code: int) -> str:
+    try:
+        return lib().ar_strerror(int(code)).decode()
+    except RuntimeError:
+        return CODE_NAMES.get(int(code), f"code {code}")
+
+
+ar_strerror = strerror
+
+
+def ar_probe_host_link(nbytes: int, reps: int):
+    out = (ctypes.c_double * 4)()
+    rc = lib().ar_probe_host_link(nbytes, reps, out)
+    if rc:
+        raise ArError(rc, "ar_probe_host_link")
+    return {"write_gbs": out[0], "read_gbs": out[1], "bidir_write_gbs": out[2], "bidir_read_gbs": out[3]}
+
+
+def ar_probe_hbm_copy(nbytes: int, reps: int) -> float:
+    out = ctypes.c_double()
+    rc = lib().ar_probe_hbm_copy(nbytes, reps, ctypes.byref(out))
+    if rc:
+        raise ArError(rc, "ar_probe_hbm_copy")
+    return out.value
+
+
+# ------------------------------------------------------------- tensor API
+
+def _dtype_code(dtype) -> int:
+    if isinstance(dtype, int):
+        return dtype
+    import torch
+    table = {torch.float16: AR_F16, torch.bfloat16: AR_BF16, torch.complex64: AR_C64}
+    if dtype in table:
+        return table[dtype]
+    return {"f16": AR_F16, "fp16": AR_F16, "bf16": AR_BF16, "c64": AR_C64, "complex64": AR_C64}[str(dtype)]
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+class Handle:
+    """One ar_handle: R logical ranks, one dtype, fixed max_numel, one slot kind."""
+
+    def __init__(self, R: int, dtype, max_numel: int, slot_kind="hbm"):
+        self.R = int(R)
+        self.dtype = _dtype_code(dtype)
+        self.slot_kind = SLOT_KINDS[slot_kind] if isinstance(slot_kind, str) else int(slot_kind)
+        self.max_numel = int(max_numel)
+        self._h = ar_create(self.R, self.dtype, self.max_numel, self.slot_kind)
+        if not self._h:
+            raise ArError(ar_last_error(), "ar_create")
+
+    @property
+    def ptr(self) -> int:
+        if not self._h:
+            raise RuntimeError("handle destroyed")
+        return self._h
+
+    def allreduce(self, rank: int, inp, out, stream=None) -> None:
+        rc = ar_allreduce(self.ptr, rank, inp.data_ptr(), out.data_ptr(), inp.numel(), _stream_handle(stream))
+        if rc:
+            raise ArError(rc, f"ar_allreduce(rank={rank})")
+
+    def allgather(self, rank: int, inp, out, stream=None) -> None:
+        rc = ar_allgather(self.ptr, rank, inp.data_ptr(), out.data_ptr(), inp.numel(), _stream_handle(stream))
+        if rc:
+            raise ArError(rc, f"ar_allgather(rank={rank})")
+
+    def allreduce_all(self, ins, outs, streams) -> None:
+        """Enqueue all R ranks' calls (rank r on streams[r])."""
+        for r in range(self.R):
+            self.allreduce(r, ins[r], outs[r], streams[r])
+
+    def allgather_all(self, ins, outs, streams) -> None:
+        for r in range(self.R):
+            self.allgather(r, ins[r], outs[r], streams[r])
+
+    def status(self) -> ErrorInfo:
+        return ar_status(self.ptr)
+
+    def check(self) -> None:
+        st = self.status()
+        if st.code:
+            raise ArError(st.code, f"device (rank {st.rank} block {st.block} waited on peer {st.peer}: "
+                                   f"want {st.want} seen {st.seen})")
+
+    def reset(self) -> None:
+        rc = ar_reset(self.ptr)
+        if rc:
+            raise ArError(rc, "ar_reset")
+
+    def set_timeout(self, ns: int) -> None:
+        rc = ar_set_timeout(self.ptr, int(ns))
+        if rc:
+            raise ArError(rc, "ar_set_timeout")
+
+    def info(self) -> Info:
+        return ar_query(self.ptr)
+
+    def plan(self, op: str, numel: int) -> Plan:
+        return ar_plan_for(self.ptr, 0 if op == "allreduce" else 1, numel)
+
+    def destroy(self) -> None:
+        if self._h:
+            h, self._h = self._h, 0
+            rc = ar_destroy(h)
+            if rc:
+                raise ArError(rc, "ar_destroy")
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.destroy()
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass

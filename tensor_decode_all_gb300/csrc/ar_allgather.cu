@@ -1,0 +1,184 @@
+// ar_allgather.cu -- the allgather kernel of one logical rank.
+//
+// Every rank ends with out = shard_0 || shard_1 || ... || shard_{R-1}, the
+// rank-major concatenation used for the complex64 S_j and core uploads in
+// "fix(group): run each rank on a non-blocking stream" (Algorithmiq
+// src-method pull 75, sections "What" and "Why").  It uses the same slot and
+// flag protocol as the all-reduce: per stage, a block copies its tile of the
+// shard into slot[parity][r] and into its own place in out, raises its flag,
+// waits for its peers' flags for the same block index, then copies the peers'
+// tiles from their slots into their places in out.  Pure copies: the result
+// is bit-exact, NaN payloads included.
+#include "ar_internal.h"
+#include "ar_sync.cuh"
+
+namespace tda {
+namespace {
+
+template <int VW>
+struct Vec;
+template <>
+struct Vec<16> {
+    using T = uint4;
+    static __device__ __forceinline__ T ldcg(const void *p) { return ld_cg_v4(p); }
+};
+template <>
+struct Vec<8> {
+    using T = uint2;
+    static __device__ __forceinline__ T ldcg(const void *p) { return ld_cg_v2(p); }
+};
+template <>
+struct Vec<4> {
+    using T = unsigned int;
+    static __device__ __forceinline__ T ldcg(const void *p) { return ld_cg_u32(p); }
+};
+template <>
+struct Vec<2> {
+    using T = unsigned short;
+    static __device__ __forceinline__ T ldcg(const void *p) { return ld_cg_u16(p); }
+};
+template <>
+struct Vec<1> {
+    using T = unsigned char;
+    static __device__ __forceinline__ T ldcg(const void *p) { return ld_cg_u8(p); }
+};
+
+template <int VW, int R, int U>
+__global__ void __launch_bounds__(kThreads)
+    allgather_kernel(const uint8_t *in, uint8_t *out, uint64_t bytes, int rank, DevState d) {
+    using V = typename Vec<VW>::T;
+    __shared__ unsigned long long s_seq;
+    __shared__ unsigned long long s_calls;
+    __shared__ int s_bail;
+
+    const int b = blockIdx.x;
+    const int B = gridDim.x;
+    const int tid = threadIdx.x;
+    const uint64_t nv = bytes / VW;
+    constexpr uint64_t kTileVecs = (uint64_t)kThreads * U;
+    const uint64_t ntiles = (nv + kTileVecs - 1) / kTileVecs;
+    const uint64_t nstages = ntiles > (uint64_t)b ? (ntiles - b + B - 1) / B : 0;
+
+    if (tid == 0) {
+        const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
+        s_seq = c.seq;
+        s_calls = c.calls;
+        s_bail = 0;
+    }
+    const V *src = reinterpret_cast<const V *>(in);
+    V *dst = reinterpret_cast<V *>(out);
+
+    V own[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint64_t v = (uint64_t)b * kTileVecs + (uint64_t)u * kThreads + tid;
+        if (v < nv) own[u] = src[v];
+    }
+    __syncthreads();
+    const unsigned long long seq = s_seq;
+    const int parity = (int)(s_calls & 1ull);
+    const uint64_t slot_vecs = d.slot_bytes / VW;
+    V *const slot_base = reinterpret_cast<V *>(d.slots) + (uint64_t)parity * R * slot_vecs;
+    V *const my_slot = slot_base + (uint64_t)rank * slot_vecs;
+
+    for (uint64_t s = 0; s < nstages; ++s) {
+        const uint64_t tile = (uint64_t)b + s * B;
+        const uint64_t v0 = tile * kTileVecs + tid;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint64_t v = v0 + (uint64_t)u * kThreads;
+            if (v < nv) {
+                my_slot[v] = own[u];
+                dst[(uint64_t)rank * nv + v] = own[u];
+            }
+        }
+        __syncthreads();
+        if (tid == 0) publish_stage(d, rank, b, seq + s + 1);
+
+        V nxt[U];
+        if (s + 1 < nstages) {
+            const uint64_t vn = (tile + B) * kTileVecs + tid;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint64_t v = vn + (uint64_t)u * kThreads;
+                if (v < nv) nxt[u] = src[v];
+            }
+        }
+
+        if (wait_peers(d, R, rank, b, seq + s + 1, &s_bail)) return;
+
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint64_t v = v0 + (uint64_t)u * kThreads;
+            if (v < nv) {
+                V vals[R];
+#pragma unroll
+                for (int p = 0; p < R; ++p)
+                    if (p != rank) vals[p] = Vec<VW>::ldcg(slot_base + (uint64_t)p * slot_vecs + v);
+#pragma unroll
+                for (int p = 0; p < R; ++p)
+                    if (p != rank) dst[(uint64_t)p * nv + v] = vals[p];
+            }
+        }
+        if (s + 1 < nstages) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) own[u] = nxt[u];
+        }
+    }
+
+    if (tid == 0) {
+        Ctr c;
+        c.seq = seq + nstages;
+        c.calls = s_calls + 1;
+        d.ctr[(size_t)rank * d.bmax + b] = c;
+    }
+}
+
+template <int VW, int U>
+const void *allgather_ptr_ru(int R) {
+    switch (R) {
+        case 1: return (const void *)allgather_kernel<VW, 1, U>;
+        case 2: return (const void *)allgather_kernel<VW, 2, U>;
+        case 3: return (const void *)allgather_kernel<VW, 3, U>;
+        case 4: return (const void *)allgather_kernel<VW, 4, U>;
+        case 5: return (const void *)allgather_kernel<VW, 5, U>;
+        case 6: return (const void *)allgather_kernel<VW, 6, U>;
+        case 7: return (const void *)allgather_kernel<VW, 7, U>;
+        case 8: return (const void *)allgather_kernel<VW, 8, U>;
+        default: return nullptr;
+    }
+}
+
+template <int VW>
+const void *allgather_ptr_r(int R, int U) {
+    return U == 1 ? allgather_ptr_ru<VW, 1>(R) : allgather_ptr_ru<VW, 2>(R);
+}
+
+}  // namespace
+
+const void *allgather_kernel_ptr(int vec_bytes, int R, int unroll) {
+    switch (vec_bytes) {
+        case 16: return allgather_ptr_r<16>(R, unroll);
+        case 8: return allgather_ptr_r<8>(R, unroll);
+        case 4: return allgather_ptr_r<4>(R, unroll);
+        case 2: return allgather_ptr_r<2>(R, unroll);
+        case 1: return allgather_ptr_r<1>(R, unroll);
+        default: return nullptr;
+    }
+}
+
+cudaError_t launch_allgather(int vec_bytes, int R, int unroll, int blocks, cudaStream_t s,
+                             const void *in, void *out, uint64_t bytes, int rank,
+                             const DevState &d) {
+    const void *k = allgather_kernel_ptr(vec_bytes, R, unroll);
+    if (!k) return cudaErrorInvalidValue;
+    const uint8_t *a0 = static_cast<const uint8_t *>(in);
+    uint8_t *a1 = static_cast<uint8_t *>(out);
+    uint64_t a2 = bytes;
+    int a3 = rank;
+    DevState a4 = d;
+    void *args[] = {&a0, &a1, &a2, &a3, &a4};
+    return cudaLaunchKernel(k, dim3(blocks), dim3(kThreads), args, 0, s);
+}
+
+}  // namespace tda

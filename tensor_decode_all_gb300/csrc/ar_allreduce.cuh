@@ -1,0 +1,240 @@
+// ar_allreduce.cuh -- the exchange-and-add kernel of one logical rank.
+//
+// One launch per rank per call; all R launches of a call run at the same time
+// on their own streams.  Block b of every rank handles the same tiles (tile t
+// belongs to block t % B, in stage t / B), so block b pairs only with block b
+// of its peers, through one flag per (rank, block).
+//
+// Per stage, each block of rank r ("[Kernel] Two-rank FP16 all-reduce through
+// pinned host memory for GPUs without P2P", section "Purpose"):
+//   1. loads its tile of in_r (16 B per thread per vector, coalesced);
+//   2. stores it into slot[parity][r] (parity = the block's call count & 1, so a
+//      rank one call ahead never overwrites a slot a peer still reads);
+//   3. barrier; thread 0 raises flag[r][b] to the new stage count (release);
+//   4. warp 0 waits until flag[p][b] reaches the same count for every p != r
+//      (acquire, bounded by the timeout); barrier;
+//   5. loads the peers' tiles from their slots (its own stays in registers),
+//      adds all R contributions in fp32 in rank order 0..R-1 with
+//      round-to-nearest adds (no fused multiply-add), rounds once to the
+//      16-bit type and stores out_r.
+// The next stage's input is loaded before the wait, so the load overlaps the
+// flag round trip.  After the last stage thread 0 advances the block's
+// counters.  Every rank computes the same bits: the order of the adds is the
+// rank order everywhere ("[SM120] Add optional FlashInfer PCIe-IPC all-reduce
+// for switch-free hosts", section "Accuracy": at eight ranks the order decides
+// the last bf16 bit).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ar_internal.h"
+#include "ar_sync.cuh"
+
+namespace tda {
+
+struct F16Ops {
+    static __device__ __forceinline__ float2 widen2(uint32_t w) {
+        __half2 h;
+        memcpy(&h, &w, 4);
+        return __half22float2(h);
+    }
+    static __device__ __forceinline__ uint32_t narrow2(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        uint32_t w;
+        memcpy(&w, &h, 4);
+        return w;
+    }
+};
+
+struct BF16Ops {
+    static __device__ __forceinline__ float2 widen2(uint32_t w) {
+        // bfloat16 is the upper half of a binary32: widening is a shift.
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+    static __device__ __forceinline__ uint32_t narrow2(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        uint32_t w;
+        memcpy(&w, &h, 4);
+        return w;
+    }
+};
+
+// acc[0..7] (+)= the 8 elements of v.
+template <class Ops, bool kFirst>
+__device__ __forceinline__ void accumulate8(float (&acc)[8], const uint4 &v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 f = Ops::widen2(w[j]);
+        if (kFirst) {
+            acc[2 * j] = f.x;
+            acc[2 * j + 1] = f.y;
+        } else {
+            acc[2 * j] = __fadd_rn(acc[2 * j], f.x);
+            acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], f.y);
+        }
+    }
+}
+
+template <class Ops>
+__device__ __forceinline__ uint4 narrow8(const float (&acc)[8]) {
+    uint4 r;
+    r.x = Ops::narrow2(acc[0], acc[1]);
+    r.y = Ops::narrow2(acc[2], acc[3]);
+    r.z = Ops::narrow2(acc[4], acc[5]);
+    r.w = Ops::narrow2(acc[6], acc[7]);
+    return r;
+}
+
+// Load vector v of the caller's input: a full 16-byte vector, or the partial
+// last vector (tail elements, zero-filled), or nothing past the end.
+__device__ __forceinline__ uint4 load_own(const uint16_t *in, uint64_t v, uint64_t nvec_full,
+                                          int tail) {
+    if (v < nvec_full) return *reinterpret_cast<const uint4 *>(in + v * 8);
+    uint4 r = make_uint4(0u, 0u, 0u, 0u);
+    if (v == nvec_full && tail) {
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        for (int j = 0; j < tail; ++j) {
+            const uint32_t e = in[v * 8 + j];
+            w[j >> 1] |= e << ((j & 1) * 16);
+        }
+        r = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    return r;
+}
+
+__device__ __forceinline__ void store_out(uint16_t *out, uint64_t v, uint64_t nvec_full, int tail,
+                                          const uint4 &r) {
+    if (v < nvec_full) {
+        *reinterpret_cast<uint4 *>(out + v * 8) = r;
+    } else if (v == nvec_full && tail) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+        for (int j = 0; j < tail; ++j) out[v * 8 + j] = (uint16_t)(w[j >> 1] >> ((j & 1) * 16));
+    }
+}
+
+template <class Ops, int R, int U>
+__global__ void __launch_bounds__(kThreads)
+    allreduce_kernel(const uint16_t *in, uint16_t *out, uint64_t numel, int rank, DevState d) {
+    __shared__ unsigned long long s_seq;
+    __shared__ unsigned long long s_calls;
+    __shared__ int s_bail;
+
+    const int b = blockIdx.x;
+    const int B = gridDim.x;
+    const int tid = threadIdx.x;
+    const uint64_t nvec_full = numel / 8;
+    const int tail = (int)(numel % 8);
+    const uint64_t nv = nvec_full + (tail ? 1 : 0);
+    constexpr uint64_t kTileVecs = (uint64_t)kThreads * U;
+    const uint64_t ntiles = (nv + kTileVecs - 1) / kTileVecs;
+    const uint64_t nstages = ntiles > (uint64_t)b ? (ntiles - b + B - 1) / B : 0;
+
+    if (tid == 0) {
+        const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
+        s_seq = c.seq;
+        s_calls = c.calls;
+        s_bail = 0;
+    }
+
+    // Stage 0's own input, loaded while thread 0 fetches the counters.
+    uint4 own[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint64_t v = (uint64_t)b * kTileVecs + (uint64_t)u * kThreads + tid;
+        own[u] = load_own(in, v, nvec_full, tail);
+    }
+    __syncthreads();
+    const unsigned long long seq = s_seq;
+    const int parity = (int)(s_calls & 1ull);
+    const uint64_t slot_vecs = d.slot_bytes / 16;
+    uint4 *const slot_base = reinterpret_cast<uint4 *>(d.slots) + (uint64_t)parity * R * slot_vecs;
+    uint4 *const my_slot = slot_base + (uint64_t)rank * slot_vecs;
+
+    for (uint64_t s = 0; s < nstages; ++s) {
+        const uint64_t tile = (uint64_t)b + s * B;
+        const uint64_t v0 = tile * kTileVecs + tid;
+
+        // 2. publish this stage's data
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint64_t v = v0 + (uint64_t)u * kThreads;
+            if (v < nv) my_slot[v] = own[u];
+        }
+        __syncthreads();
+        // 3. raise the flag
+        if (tid == 0) publish_stage(d, rank, b, seq + s + 1);
+
+        // next stage's input, overlapping the wait
+        uint4 nxt[U];
+        if (s + 1 < nstages) {
+            const uint64_t vn = (tile + B) * kTileVecs + tid;
+#pragma unroll
+            for (int u = 0; u < U; ++u) nxt[u] = load_own(in, vn + (uint64_t)u * kThreads, nvec_full, tail);
+        }
+
+        // 4. wait for the peers
+        if (wait_peers(d, R, rank, b, seq + s + 1, &s_bail)) return;
+
+        // 5. gather, add in rank order, round once, store
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint64_t v = v0 + (uint64_t)u * kThreads;
+            if (v < nv) {
+                uint4 vals[R];
+#pragma unroll
+                for (int p = 0; p < R; ++p) {
+                    if (p == rank)
+                        vals[p] = own[u];
+                    else
+                        vals[p] = ld_cg_v4(slot_base + (uint64_t)p * slot_vecs + v);
+                }
+                float acc[8];
+                accumulate8<Ops, true>(acc, vals[0]);
+#pragma unroll
+                for (int p = 1; p < R; ++p) accumulate8<Ops, false>(acc, vals[p]);
+                store_out(out, v, nvec_full, tail, narrow8<Ops>(acc));
+            }
+        }
+        if (s + 1 < nstages) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) own[u] = nxt[u];
+        }
+    }
+
+    if (tid == 0) {
+        Ctr c;
+        c.seq = seq + nstages;
+        c.calls = s_calls + 1;
+        d.ctr[(size_t)rank * d.bmax + b] = c;
+    }
+}
+
+}  // namespace tda
+
+namespace tda {
+
+// Kernel entry for (element ops, R, unroll), as an untyped address for
+// cudaLaunchKernel and the occupancy calculator.
+template <class Ops, int U>
+const void *allreduce_ptr_ru(int R) {
+    switch (R) {
+        case 1: return (const void *)allreduce_kernel<Ops, 1, U>;
+        case 2: return (const void *)allreduce_kernel<Ops, 2, U>;
+        case 3: return (const void *)allreduce_kernel<Ops, 3, U>;
+        case 4: return (const void *)allreduce_kernel<Ops, 4, U>;
+        case 5: return (const void *)allreduce_kernel<Ops, 5, U>;
+        case 6: return (const void *)allreduce_kernel<Ops, 6, U>;
+        case 7: return (const void *)allreduce_kernel<Ops, 7, U>;
+        case 8: return (const void *)allreduce_kernel<Ops, 8, U>;
+        default: return nullptr;
+    }
+}
+
+template <class Ops>
+const void *allreduce_ptr(int R, int U) {
+    return U == 1 ? allreduce_ptr_ru<Ops, 1>(R) : allreduce_ptr_ru<Ops, 2>(R);
+}
+
+}  // namespace tda

@@ -1,0 +1,6 @@
+// Instantiates the exchange-and-add kernels for bfloat16.
+#include "ar_allreduce.cuh"
+
+namespace tda {
+const void *allreduce_kernel_ptr_bf16(int R, int U) { return allreduce_ptr<BF16Ops>(R, U); }
+}  // namespace tda

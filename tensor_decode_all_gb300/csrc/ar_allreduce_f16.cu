@@ -1,0 +1,6 @@
+// Instantiates the exchange-and-add kernels for IEEE binary16.
+#include "ar_allreduce.cuh"
+
+namespace tda {
+const void *allreduce_kernel_ptr_f16(int R, int U) { return allreduce_ptr<F16Ops>(R, U); }
+}  // namespace tda

@@ -1,0 +1,442 @@
+// ar_api.cu -- the C ABI declared in include/ar.h: handles, slot allocation,
+// argument checks, launch planning and the enqueue calls.
+//
+// The enqueue calls (ar_allreduce, ar_allgather) do no host synchronisation
+// and no CPU work beyond argument checks, so they may be captured in CUDA
+// graphs ("[Kernel] Two-rank FP16 all-reduce through pinned host memory for
+// GPUs without P2P", section "Purpose").  Every decline happens before any
+// CUDA work is enqueued and returns its own code, so a caller can keep its
+// fallback path ("[SM120] Add optional FlashInfer PCIe-IPC all-reduce for
+// switch-free hosts", section "Modifications").
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "ar_internal.h"
+
+using tda::Ctr;
+using tda::DevState;
+
+struct ar_handle {
+    int R = 0, dtype = 0, kind = 0, device = 0;
+    uint64_t max_numel = 0, itemsize = 0, slot_bytes = 0;
+    int sm_count = 0, blocks_per_sm = 0, bmax = 0;
+    void *slots_host = nullptr;            // pinned kind: host address of the slots
+    uint8_t *slots_dev = nullptr;          // device address of the slots
+    void *flags_host = nullptr;            // pinned kind: host address of the flags
+    unsigned long long *flags_dev = nullptr;
+    uint64_t flags_bytes = 0;
+    Ctr *ctr = nullptr;                    // [R][bmax] then the abort word
+    unsigned int *abort_word = nullptr;
+    uint64_t ctr_bytes = 0;
+    ar_error_info *err_host = nullptr;
+    ar_error_info *err_dev = nullptr;
+    std::atomic<uint64_t> timeout_ns{1000000000ull};
+    // Host-side record of each rank's latest call, to refuse two ranks of one
+    // call sequence number on the same stream (that pairing cannot finish).
+    std::atomic<uint64_t> host_calls[tda::kMaxRanks];
+    std::atomic<uintptr_t> host_stream[tda::kMaxRanks];
+};
+
+namespace {
+
+thread_local int g_last_error = AR_OK;
+
+uint64_t itemsize_of(int dtype) {
+    switch (dtype) {
+        case AR_F16: return 2;
+        case AR_BF16: return 2;
+        case AR_C64: return 8;
+        default: return 0;
+    }
+}
+
+uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+bool valid_stream_handle(cudaStream_t s) {
+    return s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread;
+}
+
+int check_stream(cudaStream_t s) {
+    if (!valid_stream_handle(s)) return AR_ESTREAM;
+    unsigned int flags = 0;
+    if (cudaStreamGetFlags(s, &flags) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ESTREAM;
+    }
+    if (!(flags & cudaStreamNonBlocking)) return AR_ESTREAM;
+    return AR_OK;
+}
+
+int check_device(const ar_handle *h) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ECUDA;
+    }
+    return dev == h->device ? AR_OK : AR_EINVAL;
+}
+
+DevState dev_state(const ar_handle *h) {
+    DevState d;
+    d.slots = h->slots_dev;
+    d.flags = h->flags_dev;
+    d.ctr = h->ctr;
+    d.abort_word = h->abort_word;
+    d.err = h->err_dev;
+    d.slot_bytes = h->slot_bytes;
+    d.timeout_ns = h->timeout_ns.load(std::memory_order_relaxed);
+    d.bmax = h->bmax;
+    d.sys_scope = h->kind == AR_SLOT_PINNED_HOST ? 1 : 0;
+    return d;
+}
+
+void free_all(ar_handle *h) {
+    if (h->slots_host) cudaFreeHost(h->slots_host);
+    else if (h->slots_dev) cudaFree(h->slots_dev);
+    if (h->flags_host) cudaFreeHost(h->flags_host);
+    else if (h->flags_dev) cudaFree(h->flags_dev);
+    if (h->ctr) cudaFree(h->ctr);
+    if (h->err_host) cudaFreeHost(h->err_host);
+    (void)cudaGetLastError();
+    h->slots_host = nullptr;
+    h->slots_dev = nullptr;
+    h->flags_host = nullptr;
+    h->flags_dev = nullptr;
+    h->ctr = nullptr;
+    h->abort_word = nullptr;
+    h->err_host = nullptr;
+    h->err_dev = nullptr;
+}
+
+// Zero flags, counters, abort word and error record.  Caller has synchronised.
+int zero_state(ar_handle *h) {
+    if (h->flags_host) std::memset(h->flags_host, 0, h->flags_bytes);
+    else if (cudaMemset(h->flags_dev, 0, h->flags_bytes) != cudaSuccess) return AR_ECUDA;
+    if (cudaMemset(h->ctr, 0, h->ctr_bytes) != cudaSuccess) return AR_ECUDA;
+    std::memset((void *)h->err_host, 0, sizeof(ar_error_info));
+    for (int r = 0; r < tda::kMaxRanks; ++r) {
+        h->host_calls[r].store(0);
+        h->host_stream[r].store(0);
+    }
+    if (cudaDeviceSynchronize() != cudaSuccess) return AR_ECUDA;
+    return AR_OK;
+}
+
+// Smallest occupancy over every kernel variant this handle may launch, so
+// that R * bmax blocks of any of them fit on the GPU at the same time.
+int handle_occupancy(int R, int dtype, int *bps_out) {
+    int bps = 1 << 30;
+    auto take = [&](const void *k) -> bool {
+        if (!k) return false;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, tda::kThreads, 0) != cudaSuccess)
+            return false;
+        if (n < bps) bps = n;
+        return true;
+    };
+    for (int u = 1; u <= 2; ++u) {
+        if (dtype == AR_F16 || dtype == AR_BF16)
+            if (!take(tda::allreduce_kernel_ptr(dtype, R, u))) return AR_ECUDA;
+        for (int vw = 1; vw <= 16; vw *= 2)
+            if (!take(tda::allgather_kernel_ptr(vw, R, u))) return AR_ECUDA;
+    }
+    if (bps < 1) return AR_ECUDA;
+    *bps_out = bps;
+    return AR_OK;
+}
+
+int plan_compute(int R, uint64_t bytes, int vec, int threads, int sms, int bps, ar_plan *p) {
+    if (!p || R < 1 || R > tda::kMaxRanks || threads < 32 || threads % 32 || sms < 1 || bps < 1)
+        return AR_EINVAL;
+    if (vec != 16 && vec != 8 && vec != 4 && vec != 2 && vec != 1) return AR_EINVAL;
+    std::memset(p, 0, sizeof(*p));
+    const uint64_t bmax = (uint64_t)sms * (uint64_t)bps / (uint64_t)R;
+    if (bmax < 1) return AR_EINVAL;
+    const uint64_t nv = (bytes + vec - 1) / vec;
+    // Two vectors per thread per stage once every block has at least two
+    // stages' worth of single vectors; one otherwise (spreads small payloads
+    // over more blocks).
+    const int unroll = nv >= bmax * (uint64_t)threads * 2 ? 2 : 1;
+    const uint64_t tile_vecs = (uint64_t)threads * unroll;
+    const uint64_t tiles = (nv + tile_vecs - 1) / tile_vecs;
+    const uint64_t blocks = tiles < bmax ? tiles : bmax;
+    p->blocks = (int32_t)blocks;
+    p->threads = threads;
+    p->vec_bytes = vec;
+    p->unroll = unroll;
+    p->tile_bytes = tile_vecs * (uint64_t)vec;
+    p->tiles = tiles;
+    p->max_stages = blocks ? (tiles + blocks - 1) / blocks : 0;
+    return AR_OK;
+}
+
+// Largest power-of-two vector width (<= 16) dividing the byte count and both
+// addresses: the allgather writes shard p at out + p * bytes.
+int allgather_vec(uint64_t bytes, const void *in, const void *out) {
+    const uintptr_t a = (uintptr_t)in | (uintptr_t)out;
+    int vw = 16;
+    while (vw > 1 && ((bytes % vw) || (a % vw))) vw >>= 1;
+    return vw;
+}
+
+int max_blocks_override() {
+    const char *e = std::getenv("AR_MAX_BLOCKS");
+    if (!e || !*e) return 0;
+    const long v = std::strtol(e, nullptr, 10);
+    return v > 0 ? (int)v : 0;
+}
+
+// Common checks and bookkeeping of one enqueue call.
+int begin_call(ar_handle *h, int rank, const void *in, void *out, size_t numel, cudaStream_t s,
+               uint64_t *call_index) {
+    if (!h || rank < 0 || rank >= h->R) return AR_EINVAL;
+    if (numel > h->max_numel) return AR_ETOOBIG;
+    if (numel == 0) return AR_OK;
+    if (!in || !out) return AR_EINVAL;
+    int rc = check_stream(s);
+    if (rc != AR_OK) return rc;
+    rc = check_device(h);
+    if (rc != AR_OK) return rc;
+    if (h->err_host->code != AR_OK) return AR_ESTATE;
+    const uint64_t c = h->host_calls[rank].fetch_add(1, std::memory_order_acq_rel) + 1;
+    for (int p = 0; p < h->R; ++p) {
+        if (p == rank) continue;
+        if (h->host_calls[p].load(std::memory_order_acquire) == c &&
+            h->host_stream[p].load(std::memory_order_acquire) == (uintptr_t)s) {
+            h->host_calls[rank].fetch_sub(1, std::memory_order_acq_rel);
+            return AR_ESTREAM;
+        }
+    }
+    h->host_stream[rank].store((uintptr_t)s, std::memory_order_release);
+    *call_index = c;
+    return AR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+AR_API int ar_last_error(void) { return g_last_error; }
+
+AR_API const char *ar_strerror(int code) {
+    switch (code) {
+        case AR_OK: return "AR_OK: success";
+        case AR_EINVAL: return "AR_EINVAL: invalid argument";
+        case AR_ETOOBIG: return "AR_ETOOBIG: numel exceeds the handle's max_numel";
+        case AR_ESTREAM: return "AR_ESTREAM: stream is NULL, legacy, per-thread default, blocking, or another rank's";
+        case AR_ENOMEM: return "AR_ENOMEM: allocation failed";
+        case AR_ECUDA: return "AR_ECUDA: a CUDA runtime call failed";
+        case AR_ETIMEOUT: return "AR_ETIMEOUT: a block timed out waiting for a peer's flag";
+        case AR_ESTATE: return "AR_ESTATE: a device error is recorded; call ar_reset";
+        default: return "unknown ar error code";
+    }
+}
+
+AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
+    g_last_error = AR_OK;
+    const uint64_t isz = itemsize_of(dtype);
+    if (R < 1 || R > tda::kMaxRanks || isz == 0 || max_numel < 1 ||
+        (slot_kind != AR_SLOT_PINNED_HOST && slot_kind != AR_SLOT_HBM) ||
+        max_numel > (uint64_t)1 << 40) {
+        g_last_error = AR_EINVAL;
+        return nullptr;
+    }
+    ar_handle *h = new (std::nothrow) ar_handle();
+    if (!h) {
+        g_last_error = AR_ENOMEM;
+        return nullptr;
+    }
+    auto fail = [&](int code) -> ar_handle * {
+        free_all(h);
+        delete h;
+        g_last_error = code;
+        return nullptr;
+    };
+    h->R = R;
+    h->dtype = dtype;
+    h->kind = slot_kind;
+    h->max_numel = max_numel;
+    h->itemsize = isz;
+    h->slot_bytes = round_up(max_numel * isz, tda::kSlotAlign);
+    if (const char *e = std::getenv("AR_SPIN_TIMEOUT_NS")) {
+        const unsigned long long v = std::strtoull(e, nullptr, 10);
+        if (v >= 1000ull) h->timeout_ns.store(v);
+    }
+    if (cudaGetDevice(&h->device) != cudaSuccess) return fail(AR_ECUDA);
+    if (cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess)
+        return fail(AR_ECUDA);
+    int rc = handle_occupancy(R, dtype, &h->blocks_per_sm);
+    if (rc != AR_OK) return fail(rc);
+    h->bmax = h->sm_count * h->blocks_per_sm / R;
+    if (const int cap = max_blocks_override()) h->bmax = cap < h->bmax ? cap : h->bmax;
+    if (h->bmax < 1) return fail(AR_ECUDA);
+
+    const uint64_t slots_total = 2ull * (uint64_t)R * h->slot_bytes;
+    h->flags_bytes = (uint64_t)R * (uint64_t)h->bmax * tda::kFlagStrideWords * 8ull;
+    h->ctr_bytes = round_up((uint64_t)R * (uint64_t)h->bmax * sizeof(Ctr), 256) + 256;
+
+    if (slot_kind == AR_SLOT_PINNED_HOST) {
+        const unsigned fl = cudaHostAllocMapped | cudaHostAllocPortable;
+        if (cudaHostAlloc(&h->slots_host, slots_total, fl) != cudaSuccess) return fail(AR_ENOMEM);
+        if (cudaHostGetDevicePointer((void **)&h->slots_dev, h->slots_host, 0) != cudaSuccess)
+            return fail(AR_ECUDA);
+        if (cudaHostAlloc(&h->flags_host, h->flags_bytes, fl) != cudaSuccess) return fail(AR_ENOMEM);
+        if (cudaHostGetDevicePointer((void **)&h->flags_dev, h->flags_host, 0) != cudaSuccess)
+            return fail(AR_ECUDA);
+        std::memset(h->slots_host, 0, slots_total);
+    } else {
+        if (cudaMalloc((void **)&h->slots_dev, slots_total) != cudaSuccess) return fail(AR_ENOMEM);
+        if (cudaMalloc((void **)&h->flags_dev, h->flags_bytes) != cudaSuccess) return fail(AR_ENOMEM);
+        if (cudaMemset(h->slots_dev, 0, slots_total) != cudaSuccess) return fail(AR_ECUDA);
+    }
+    if (cudaMalloc((void **)&h->ctr, h->ctr_bytes) != cudaSuccess) return fail(AR_ENOMEM);
+    h->abort_word = reinterpret_cast<unsigned int *>(reinterpret_cast<uint8_t *>(h->ctr) + h->ctr_bytes - 256);
+    if (cudaHostAlloc((void **)&h->err_host, sizeof(ar_error_info),
+                      cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess)
+        return fail(AR_ENOMEM);
+    if (cudaHostGetDevicePointer((void **)&h->err_dev, h->err_host, 0) != cudaSuccess)
+        return fail(AR_ECUDA);
+    rc = zero_state(h);
+    if (rc != AR_OK) return fail(rc);
+    return h;
+}
+
+AR_API int ar_allreduce(ar_handle *h, int rank, const void *in, void *out, size_t numel,
+                        ar_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (h && h->dtype != AR_F16 && h->dtype != AR_BF16) return AR_EINVAL;
+    if (((uintptr_t)in | (uintptr_t)out) % 16) return AR_EINVAL;
+    uint64_t call = 0;
+    int rc = begin_call(h, rank, in, out, numel, s, &call);
+    if (rc != AR_OK || numel == 0) return rc;
+    ar_plan plan;
+    rc = plan_compute(h->R, numel * h->itemsize, 16, tda::kThreads, h->sm_count, h->blocks_per_sm, &plan);
+    if (rc != AR_OK) return rc;
+    int blocks = plan.blocks < h->bmax ? plan.blocks : h->bmax;
+    const cudaError_t e = tda::launch_allreduce(h->dtype, h->R, plan.unroll, blocks, s, in, out,
+                                                numel, rank, dev_state(h));
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ECUDA;
+    }
+    return AR_OK;
+}
+
+AR_API int ar_allgather(ar_handle *h, int rank, const void *in, void *out, size_t numel,
+                        ar_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (((uintptr_t)in | (uintptr_t)out) % 16) return AR_EINVAL;
+    uint64_t call = 0;
+    int rc = begin_call(h, rank, in, out, numel, s, &call);
+    if (rc != AR_OK || numel == 0) return rc;
+    const uint64_t bytes = numel * h->itemsize;
+    const int vw = allgather_vec(bytes, in, out);
+    ar_plan plan;
+    rc = plan_compute(h->R, bytes, vw, tda::kThreads, h->sm_count, h->blocks_per_sm, &plan);
+    if (rc != AR_OK) return rc;
+    int blocks = plan.blocks < h->bmax ? plan.blocks : h->bmax;
+    const cudaError_t e = tda::launch_allgather(vw, h->R, plan.unroll, blocks, s, in, out, bytes,
+                                                rank, dev_state(h));
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ECUDA;
+    }
+    return AR_OK;
+}
+
+AR_API int ar_status(ar_handle *h, ar_error_info *info) {
+    if (!h) return AR_EINVAL;
+    ar_error_info e;
+    std::memcpy(&e, (const void *)h->err_host, sizeof(e));
+    if (info) *info = e;
+    return e.code;
+}
+
+AR_API int ar_reset(ar_handle *h) {
+    if (!h) return AR_EINVAL;
+    if (check_device(h) != AR_OK) return AR_EINVAL;
+    if (cudaDeviceSynchronize() != cudaSuccess) return AR_ECUDA;
+    return zero_state(h);
+}
+
+AR_API int ar_destroy(ar_handle *h) {
+    if (!h) return AR_OK;
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (dev != h->device) cudaSetDevice(h->device);
+    const cudaError_t e = cudaDeviceSynchronize();
+    free_all(h);
+    if (dev >= 0 && dev != h->device) cudaSetDevice(dev);
+    delete h;
+    return e == cudaSuccess ? AR_OK : AR_ECUDA;
+}
+
+AR_API int ar_set_timeout(ar_handle *h, uint64_t timeout_ns) {
+    if (!h || timeout_ns < 1000ull) return AR_EINVAL;
+    h->timeout_ns.store(timeout_ns);
+    return AR_OK;
+}
+
+AR_API int ar_query(const ar_handle *h, ar_info *info) {
+    if (!h || !info) return AR_EINVAL;
+    info->R = h->R;
+    info->dtype = h->dtype;
+    info->slot_kind = h->kind;
+    info->device = h->device;
+    info->threads = tda::kThreads;
+    info->max_blocks = h->bmax;
+    info->sm_count = h->sm_count;
+    info->blocks_per_sm = h->blocks_per_sm;
+    info->max_numel = h->max_numel;
+    info->slot_bytes = h->slot_bytes;
+    info->total_slot_bytes = 2ull * (uint64_t)h->R * h->slot_bytes;
+    info->timeout_ns = h->timeout_ns.load();
+    return AR_OK;
+}
+
+AR_API int ar_plan_compute(int R, uint64_t bytes, int vec_bytes, int threads, int sm_count,
+                           int blocks_per_sm, ar_plan *plan) {
+    return plan_compute(R, bytes, vec_bytes, threads, sm_count, blocks_per_sm, plan);
+}
+
+AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) {
+    if (!h || !plan || (op != 0 && op != 1)) return AR_EINVAL;
+    if (numel > h->max_numel) return AR_ETOOBIG;
+    const uint64_t bytes = numel * h->itemsize;
+    const int vec = op == 0 ? 16 : allgather_vec(bytes, nullptr, nullptr);
+    int rc = plan_compute(h->R, bytes, vec, tda::kThreads, h->sm_count, h->blocks_per_sm, plan);
+    if (rc == AR_OK && plan->blocks > h->bmax) {
+        plan->blocks = h->bmax;
+        plan->max_stages = (plan->tiles + h->bmax - 1) / h->bmax;
+    }
+    return rc;
+}
+
+}  // extern "C"
+
+namespace tda {
+
+const void *allreduce_kernel_ptr(int dtype, int R, int unroll) {
+    if (dtype == AR_F16) return allreduce_kernel_ptr_f16(R, unroll);
+    if (dtype == AR_BF16) return allreduce_kernel_ptr_bf16(R, unroll);
+    return nullptr;
+}
+
+cudaError_t launch_allreduce(int dtype, int R, int unroll, int blocks, cudaStream_t s,
+                             const void *in, void *out, uint64_t numel, int rank,
+                             const DevState &d) {
+    const void *k = allreduce_kernel_ptr(dtype, R, unroll);
+    if (!k) return cudaErrorInvalidValue;
+    const uint16_t *a0 = static_cast<const uint16_t *>(in);
+    uint16_t *a1 = static_cast<uint16_t *>(out);
+    uint64_t a2 = numel;
+    int a3 = rank;
+    DevState a4 = d;
+    void *args[] = {&a0, &a1, &a2, &a3, &a4};
+    return cudaLaunchKernel(k, dim3(blocks), dim3(kThreads), args, 0, s);
+}
+
+}  // namespace tda

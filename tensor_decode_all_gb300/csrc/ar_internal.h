@@ -1,0 +1,60 @@
+// ar_internal.h -- declarations shared by the library's translation units.
+//
+// Memory layout of one handle (all addresses as seen by the GPU):
+//   slots : [2 parities][R ranks][slot_bytes]        pinned host or HBM
+//   flags : [R ranks][bmax blocks] x 128 B lines     same memory as the slots;
+//           word 0 of each line is the flag, a 64-bit count of published stages
+//   ctr   : [R ranks][bmax blocks] x {seq, calls}    HBM; private to one block
+//   abort : one 32-bit word in HBM, non-zero once any block has given up
+//   err   : one ar_error_info in mapped pinned host memory
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ar.h"
+
+namespace tda {
+
+constexpr int kMaxRanks = 8;
+constexpr int kThreads = 256;           // threads per block of the exchange kernels
+constexpr int kFlagStrideWords = 16;    // 16 x 8 B = one 128-byte line per flag
+constexpr uint64_t kSlotAlign = 256;
+
+// Per-(rank, block) counters.  `seq` counts the stages this block has
+// published over all calls (its flag's value at the end of the last call);
+// `calls` counts the calls it took part in, whose parity picks the slot buffer.
+struct Ctr {
+    unsigned long long seq;
+    unsigned long long calls;
+};
+
+// Everything a rank's kernel needs besides its own in/out pointers.  Passed
+// by value as a kernel argument (captured graphs keep a copy).
+struct DevState {
+    uint8_t *slots;            // [2][R][slot_bytes]
+    unsigned long long *flags; // [R][bmax][kFlagStrideWords]
+    Ctr *ctr;                  // [R][bmax]
+    unsigned int *abort_word;  // sticky, HBM
+    ar_error_info *err;        // device alias of mapped host memory
+    uint64_t slot_bytes;
+    uint64_t timeout_ns;
+    int bmax;
+    int sys_scope;             // 1: slots/flags in host memory, system-scope ordering
+};
+
+// Launchers (one per kernel family).  Return cudaSuccess or the launch error.
+cudaError_t launch_allreduce(int dtype, int R, int unroll, int blocks, cudaStream_t s,
+                             const void *in, void *out, uint64_t numel, int rank,
+                             const DevState &d);
+cudaError_t launch_allgather(int vec_bytes, int R, int unroll, int blocks, cudaStream_t s,
+                             const void *in, void *out, uint64_t bytes, int rank,
+                             const DevState &d);
+
+// Kernel entry addresses, for occupancy queries.
+const void *allreduce_kernel_ptr(int dtype, int R, int unroll);
+const void *allreduce_kernel_ptr_f16(int R, int unroll);   // ar_allreduce_f16.cu
+const void *allreduce_kernel_ptr_bf16(int R, int unroll);  // ar_allreduce_bf16.cu
+const void *allgather_kernel_ptr(int vec_bytes, int R, int unroll);
+
+}  // namespace tda

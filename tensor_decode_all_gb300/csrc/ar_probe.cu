@@ -1,0 +1,166 @@
+// ar_probe.cu -- bandwidth probes that give the roofline denominators.
+//
+// Host link: zero-copy kernels that stream to and from mapped pinned host
+// memory with 16-byte accesses, alone and both directions at once (the pages'
+// peer-copy probe measures both directions at once too: "fix(group): run each
+// rank on a non-blocking stream", section "Why").  HBM: a 16-byte copy kernel
+// between two device buffers.  Every probe owns its buffers and a private
+// non-blocking stream, and times with CUDA events on that stream.
+#include <cstring>
+
+#include "ar_internal.h"
+
+namespace {
+
+__global__ void probe_write_kernel(uint4 *dst, uint64_t nvec) {
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    const uint4 v = make_uint4(0x3c003c00u, blockIdx.x, threadIdx.x, 0x12345678u);
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) dst[i] = v;
+}
+
+__global__ void probe_read_kernel(const uint4 *src, uint64_t nvec, unsigned int *sink) {
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    unsigned int x = 0;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+        const uint4 v = src[i];
+        x ^= v.x ^ v.y ^ v.z ^ v.w;
+    }
+    if (x == 0x9e3779b9u) sink[0] = x;  // keeps the loads alive; practically never taken
+}
+
+__global__ void probe_copy_kernel(uint4 *dst, const uint4 *src, uint64_t nvec) {
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) dst[i] = src[i];
+}
+
+int grid_for(const void *k, int threads) {
+    int dev = 0, sms = 0, occ = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, threads, 0);
+    if (occ < 1) occ = 1;
+    return sms * occ;
+}
+
+struct Timer {
+    cudaEvent_t a = nullptr, b = nullptr;
+    Timer() {
+        cudaEventCreate(&a);
+        cudaEventCreate(&b);
+    }
+    ~Timer() {
+        cudaEventDestroy(a);
+        cudaEventDestroy(b);
+    }
+};
+
+}  // namespace
+
+extern "C" {
+
+AR_API int ar_probe_host_link(uint64_t bytes, int reps, double gbs[4]) {
+    if (!gbs || reps < 1 || bytes < 16 || bytes % 16) return AR_EINVAL;
+    const int threads = 512;
+    const uint64_t nvec = bytes / 16;
+    void *hw = nullptr, *hr = nullptr;
+    uint4 *dw = nullptr, *dr = nullptr;
+    unsigned int *sink = nullptr;
+    cudaStream_t s1 = nullptr, s2 = nullptr;
+    int rc = AR_OK;
+    const unsigned fl = cudaHostAllocMapped | cudaHostAllocPortable;
+    if (cudaHostAlloc(&hw, bytes, fl) != cudaSuccess || cudaHostAlloc(&hr, bytes, fl) != cudaSuccess ||
+        cudaMalloc((void **)&sink, 256) != cudaSuccess) {
+        rc = AR_ENOMEM;
+    }
+    if (rc == AR_OK) {
+        std::memset(hw, 0, bytes);
+        std::memset(hr, 1, bytes);
+        if (cudaHostGetDevicePointer((void **)&dw, hw, 0) != cudaSuccess ||
+            cudaHostGetDevicePointer((void **)&dr, hr, 0) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&s1, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&s2, cudaStreamNonBlocking) != cudaSuccess)
+            rc = AR_ECUDA;
+    }
+    if (rc == AR_OK) {
+        const int gw = grid_for((const void *)probe_write_kernel, threads);
+        const int gr = grid_for((const void *)probe_read_kernel, threads);
+        Timer t1, t2, t0;
+        float ms = 0.f;
+        // warm up both directions once
+        probe_write_kernel<<<gw, threads, 0, s1>>>(dw, nvec);
+        probe_read_kernel<<<gr, threads, 0, s1>>>(dr, nvec, sink);
+        cudaStreamSynchronize(s1);
+        // write alone
+        cudaEventRecord(t1.a, s1);
+        for (int i = 0; i < reps; ++i) probe_write_kernel<<<gw, threads, 0, s1>>>(dw, nvec);
+        cudaEventRecord(t1.b, s1);
+        cudaEventSynchronize(t1.b);
+        cudaEventElapsedTime(&ms, t1.a, t1.b);
+        gbs[0] = (double)bytes * reps / (ms * 1e-3) / 1e9;
+        // read alone
+        cudaEventRecord(t1.a, s1);
+        for (int i = 0; i < reps; ++i) probe_read_kernel<<<gr, threads, 0, s1>>>(dr, nvec, sink);
+        cudaEventRecord(t1.b, s1);
+        cudaEventSynchronize(t1.b);
+        cudaEventElapsedTime(&ms, t1.a, t1.b);
+        gbs[1] = (double)bytes * reps / (ms * 1e-3) / 1e9;
+        // both at once: half the SMs' worth of blocks each, on two streams
+        cudaEventRecord(t0.a, s1);
+        cudaStreamWaitEvent(s2, t0.a, 0);
+        cudaEventRecord(t1.a, s1);
+        cudaEventRecord(t2.a, s2);
+        for (int i = 0; i < reps; ++i) {
+            probe_write_kernel<<<gw / 2, threads, 0, s1>>>(dw, nvec);
+            probe_read_kernel<<<gr / 2, threads, 0, s2>>>(dr, nvec, sink);
+        }
+        cudaEventRecord(t1.b, s1);
+        cudaEventRecord(t2.b, s2);
+        cudaEventSynchronize(t1.b);
+        cudaEventSynchronize(t2.b);
+        cudaEventElapsedTime(&ms, t1.a, t1.b);
+        gbs[2] = (double)bytes * reps / (ms * 1e-3) / 1e9;
+        cudaEventElapsedTime(&ms, t2.a, t2.b);
+        gbs[3] = (double)bytes * reps / (ms * 1e-3) / 1e9;
+        if (cudaGetLastError() != cudaSuccess) rc = AR_ECUDA;
+    }
+    if (s1) cudaStreamDestroy(s1);
+    if (s2) cudaStreamDestroy(s2);
+    if (hw) cudaFreeHost(hw);
+    if (hr) cudaFreeHost(hr);
+    if (sink) cudaFree(sink);
+    (void)cudaGetLastError();
+    return rc;
+}
+
+AR_API int ar_probe_hbm_copy(uint64_t bytes, int reps, double *gbs) {
+    if (!gbs || reps < 1 || bytes < 16 || bytes % 16) return AR_EINVAL;
+    const int threads = 512;
+    uint4 *a = nullptr, *b = nullptr;
+    cudaStream_t s = nullptr;
+    int rc = AR_OK;
+    if (cudaMalloc((void **)&a, bytes) != cudaSuccess || cudaMalloc((void **)&b, bytes) != cudaSuccess)
+        rc = AR_ENOMEM;
+    if (rc == AR_OK && (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess ||
+                        cudaMemsetAsync(a, 1, bytes, s) != cudaSuccess))
+        rc = AR_ECUDA;
+    if (rc == AR_OK) {
+        const int g = grid_for((const void *)probe_copy_kernel, threads);
+        Timer t;
+        float ms = 0.f;
+        probe_copy_kernel<<<g, threads, 0, s>>>(b, a, bytes / 16);
+        cudaEventRecord(t.a, s);
+        for (int i = 0; i < reps; ++i) probe_copy_kernel<<<g, threads, 0, s>>>(i & 1 ? a : b, i & 1 ? b : a, bytes / 16);
+        cudaEventRecord(t.b, s);
+        cudaEventSynchronize(t.b);
+        cudaEventElapsedTime(&ms, t.a, t.b);
+        *gbs = 2.0 * (double)bytes * reps / (ms * 1e-3) / 1e9;
+        if (cudaGetLastError() != cudaSuccess) rc = AR_ECUDA;
+    }
+    if (s) cudaStreamDestroy(s);
+    if (a) cudaFree(a);
+    if (b) cudaFree(b);
+    (void)cudaGetLastError();
+    return rc;
+}
+
+}  // extern "C"

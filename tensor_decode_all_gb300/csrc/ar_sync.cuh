@@ -1,0 +1,169 @@
+// ar_sync.cuh -- the per-block flag protocol of the exchange kernels.
+//
+// Publish: after every thread of the block has stored its part of the stage
+// into the rank's slot, the block passes a barrier and thread 0 stores the new
+// stage count into the block's flag with release semantics.  Wait: lanes of
+// warp 0 poll their peer's flag for the same block index with acquire
+// semantics until it reaches the stage count this rank needs, then the block
+// passes a barrier.  The release -> acquire pair plus the two barriers order
+// the peer's slot stores before this block's slot loads ("[Kernel] Two-rank
+// FP16 all-reduce through pinned host memory for GPUs without P2P", section
+// "Purpose": write the chunk, fence, raise a per-block flag, wait for the
+// peer's flag, then read).
+//
+// Scope: slots and flags in mapped host memory use .sys (the pages' case: two
+// GPUs reach the host buffer); in HBM they use .gpu.
+//
+// Every wait is bounded by %globaltimer.  A block that runs out of time sets
+// the sticky abort word, records itself in the handle's error record (the
+// first one only) and leaves the kernel without writing its output; later
+// waits on the same handle see the abort word and leave at once.  No wait is
+// unbounded, so no call can hang the GPU.
+#pragma once
+
+#include <cstdint>
+
+#include "ar_internal.h"
+
+namespace tda {
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p, int sys) {
+    unsigned long long v;
+    if (sys)
+        asm volatile("ld.acquire.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    else
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v, int sys) {
+    if (sys)
+        asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+    else
+        asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned int ld_relaxed_u32(const unsigned int *p) {
+    unsigned int v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// 16-byte load that bypasses L1: peer slot data is read once per call and must
+// never come from a line cached by an earlier call.
+__device__ __forceinline__ uint4 ld_cg_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint2 ld_cg_v2(const void *p) {
+    uint2 v;
+    asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned int ld_cg_u32(const void *p) {
+    unsigned int v;
+    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned short ld_cg_u16(const void *p) {
+    unsigned short v;
+    asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned char ld_cg_u8(const void *p) {
+    unsigned short v;
+    asm volatile("ld.global.cg.u8 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
+    return (unsigned char)v;
+}
+
+__device__ __forceinline__ unsigned long long *flag_ptr(const DevState &d, int rank, int block) {
+    return d.flags + ((size_t)rank * d.bmax + block) * kFlagStrideWords;
+}
+
+// Thread 0, after a barrier that follows the block's slot stores: publish.
+__device__ __forceinline__ void publish_stage(const DevState &d, int rank, int block,
+                                              unsigned long long value) {
+    st_release_u64(flag_ptr(d, rank, block), value, d.sys_scope);
+}
+
+// Record the first device-side error of the handle (lane that gave up).
+static __device__ __noinline__ void record_timeout(const DevState &d, int rank, int block, int peer,
+                                            unsigned long long want, unsigned long long seen) {
+    if (atomicCAS(d.abort_word, 0u, 1u) == 0u) {
+        volatile ar_error_info *e = d.err;
+        e->rank = rank;
+        e->block = block;
+        e->peer = peer;
+        e->want = want;
+        e->seen = seen;
+        __threadfence_system();
+        e->code = AR_ETIMEOUT;
+        __threadfence_system();
+    }
+}
+
+// Called by all threads of the block.  Warp 0 waits until every peer p != rank
+// has published at least `target` stages for block `block`.  Returns true if
+// the block must leave (timeout here or abort elsewhere).  Ends with a barrier.
+__device__ __forceinline__ bool wait_peers(const DevState &d, int R, int rank, int block,
+                                           unsigned long long target, int *s_bail) {
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const bool mine = lane < R && lane != rank;
+        const unsigned long long *f = mine ? flag_ptr(d, lane, block) : nullptr;
+        unsigned long long seen = 0;
+        bool ok = true;
+        if (mine) {
+            seen = ld_acquire_u64(f, d.sys_scope);
+            ok = seen >= target;
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+            const unsigned long long t0 = global_timer_ns();
+            unsigned int iter = 0;
+            for (;;) {
+                if (!ok) {
+                    seen = ld_acquire_u64(f, d.sys_scope);
+                    ok = seen >= target;
+                }
+                if (__all_sync(0xffffffffu, ok)) break;
+                int stop = 0;
+                if (lane == 0) {
+                    if (ld_relaxed_u32(d.abort_word) != 0u)
+                        stop = 1;
+                    else if (global_timer_ns() - t0 > d.timeout_ns)
+                        stop = 2;
+                }
+                stop = __shfl_sync(0xffffffffu, stop, 0);
+                if (stop) {
+                    if (stop == 2) {
+                        const unsigned int late = __ballot_sync(0xffffffffu, !ok);
+                        const int peer = __ffs(late) - 1;
+                        const unsigned long long peer_seen = __shfl_sync(0xffffffffu, seen, peer);
+                        if (lane == 0) record_timeout(d, rank, block, peer, target, peer_seen);
+                    }
+                    if (lane == 0) *s_bail = 1;
+                    break;
+                }
+                if (++iter > 64u) __nanosleep(64);
+            }
+        }
+    }
+    __syncthreads();
+    return *s_bail != 0;
+}
+
+}  // namespace tda

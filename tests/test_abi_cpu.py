@@ -1,0 +1,98 @@
+"""C-ABI checks that need no GPU: the library builds, loads and exports every
+entry point include/ar.h declares; host-side argument checks and the launch
+plan arithmetic behave as documented."""
+import ctypes
+
+import pytest
+
+import tensor_decode_all_gb300 as tda
+from tensor_decode_all_gb300 import ar
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tda.build()
+    return tda.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = tda.declared_symbols()
+    assert len(names) >= 14, names
+    for n in ("ar_create", "ar_allreduce", "ar_allgather", "ar_destroy", "ar_status", "ar_reset",
+              "ar_strerror"):
+        assert n in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ar.h but not exported"
+
+
+def test_strerror_names_every_code(lib):
+    for code, name in ar.CODE_NAMES.items():
+        assert tda.strerror(code).startswith(name)
+    assert "unknown" in tda.strerror(999)
+
+
+def test_create_rejects_bad_arguments_before_touching_cuda(lib):
+    for args in [(0, 1, 10, 0), (9, 1, 10, 0), (2, 0, 10, 0), (2, 4, 10, 0), (2, 1, 0, 0), (2, 1, 10, 2),
+                 (2, 1, 10, -1)]:
+        assert tda.ar_create(*args) == 0
+        assert tda.ar_last_error() == ar.AR_EINVAL, args
+
+
+def test_null_handle_calls(lib):
+    assert tda.ar_allreduce(0, 0, 16, 16, 8, 123) == ar.AR_EINVAL
+    assert tda.ar_allgather(0, 0, 16, 16, 8, 123) == ar.AR_EINVAL
+    assert tda.ar_reset(0) == ar.AR_EINVAL
+    assert tda.ar_destroy(0) == ar.AR_OK
+    assert tda.ar_set_timeout(0, 10**9) == ar.AR_EINVAL
+    assert lib.ar_status(None, None) == ar.AR_EINVAL
+    assert lib.ar_query(None, None) == ar.AR_EINVAL
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("vec", [16, 8, 2, 1])
+def test_plan_invariants(lib, R, vec):
+    sms, bps, threads = 152, 6, 256
+    bmax = sms * bps // R
+    sizes = [1, 15, 16, 17, 4095, 4096, 8192, 262144, 786432, 1 << 24, (1 << 26) + 12345, 3 << 27]
+    for nbytes in sizes:
+        if nbytes % vec:
+            continue
+        p = tda.ar_plan_compute(R, nbytes, vec, threads, sms, bps)
+        nv = -(-nbytes // vec)
+        assert p.threads == threads and p.vec_bytes == vec
+        assert p.unroll in (1, 2)
+        assert p.tile_bytes == threads * p.unroll * vec
+        # tiles cover the payload, and no tile is empty
+        assert p.tiles * threads * p.unroll >= nv > (p.tiles - 1) * threads * p.unroll
+        # every block has at least one tile; all ranks' blocks fit at once
+        assert 1 <= p.blocks <= min(p.tiles, bmax)
+        assert R * p.blocks <= sms * bps
+        assert p.max_stages == -(-p.tiles // p.blocks)
+        # small payloads: one tile per block, spread as wide as allowed
+        if nv <= bmax * threads:
+            assert p.unroll == 1 and p.max_stages == 1
+
+
+def test_plan_zero_bytes_and_bad_args(lib):
+    p = tda.ar_plan_compute(2, 0, 16, 256, 152, 6)
+    assert p.blocks == 0 and p.tiles == 0
+    with pytest.raises(tda.ArError):
+        tda.ar_plan_compute(9, 16, 16, 256, 152, 6)
+    with pytest.raises(tda.ArError):
+        tda.ar_plan_compute(2, 16, 3, 256, 152, 6)
+    with pytest.raises(tda.ArError):
+        tda.ar_plan_compute(8, 16, 16, 256, 1, 1)  # 8 ranks cannot each get a block
+
+
+def test_struct_layouts_match_header(lib):
+    # ar_error_info: 4 x int32 + 2 x uint64; ar_info: 8 x int32 + 4 x uint64; ar_plan: 4 x int32 + 3 x uint64
+    assert ctypes.sizeof(ar.ErrorInfo) == 32
+    assert ctypes.sizeof(ar.Info) == 64
+    assert ctypes.sizeof(ar.Plan) == 40
+
+
+def test_no_cpu_fallback_when_library_missing(monkeypatch, tmp_path):
+    monkeypatch.setattr(ar, "_lib", None)
+    monkeypatch.setattr(ar._build, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        ar.lib()

@@ -1,0 +1,50 @@
+"""bench.py's replica mode on CPU: two gloo ranks, max-over-ranks timing and
+rank-0-only reference arm.  (The all-reduce's ranks are logical ranks on one
+GPU; across GPUs the bench only runs independent replicas.)"""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    d = bench.Dist(world)
+    try:
+        assert d.pg is not None and d.pg.get_backend() == "gloo"
+        d.barrier()
+        slowest = d.max(1.0 + rank)          # rank 1 is the slow one
+        args = type("A", (), {"warmup": 0, "steps": 1})()
+        ref = bench.run_reference(args, d) if rank != 0 else "skipped"
+        q.put((rank, slowest, ref))
+    finally:
+        d.close()
+
+
+def test_two_gloo_ranks_take_the_max_and_only_rank0_reports():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=5) for _ in range(world))
+    assert [g[1] for g in got] == [2.0, 2.0]
+    assert got[1][2] is None  # rank 1 prints nothing on the reference arm
+
+
+def test_max_over_ranks_helper():
+    import bench
+    assert bench.max_over_ranks([1.0, 3.5, 2.0]) == 3.5

@@ -1,0 +1,193 @@
+"""GPU parity of the all-reduce against the CPU oracle (bit-exact).
+
+The oracle's result is unique (fixed rank order, one rounding), so every
+element of every rank must match its bits; only NaN payloads are exempt.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tensor_decode_all_gb300 import inputs
+from tests.gpu_helpers import assert_bits_equal, capture, enqueue, rank_streams, to_bits, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _handle(R, dtype, max_numel, slots):
+    import tensor_decode_all_gb300 as tda
+    return tda.Handle(R, {"f16": torch.float16, "bf16": torch.bfloat16}[dtype], max_numel, slots)
+
+
+def _run_once(R, dtype, numel, slots, dist="uniform", config=5, call=0, h=None):
+    xs = inputs.allreduce_inputs(config, R, numel, dtype, dist, call)
+    own = h is None
+    h = h or _handle(R, dtype, max(numel, 1), slots)
+    streams = rank_streams(R)
+    ins = [to_dev(x, dtype) for x in xs]
+    outs = [torch.empty_like(t) for t in ins]
+    enqueue(h, "allreduce", ins, outs, streams)
+    torch.cuda.synchronize()
+    h.check()
+    want = oracle.allreduce(xs, dtype, ranks=[0])[0]
+    for r in range(R):
+        assert_bits_equal(to_bits(outs[r]), want, dtype, f"R={R} {dtype} n={numel} {slots} rank {r}")
+    if own:
+        h.destroy()
+
+
+def test_config1_r2_fp16_4096_pinned_fresh_inputs_every_call():
+    """Workload 1: 100 eager calls, fresh inputs each call; every call, both
+    ranks equal the oracle, which equals RNE16(a + b) (the two-rank closed form)."""
+    R, n = 2, 4096
+    h = _handle(R, "f16", n, "pinned")
+    streams = rank_streams(R)
+    for call in range(100):
+        xs = inputs.allreduce_inputs(1, R, n, "f16", "uniform", call)
+        ins = [to_dev(x, "f16") for x in xs]
+        outs = [torch.empty_like(t) for t in ins]
+        enqueue(h, "allreduce", ins, outs, streams)
+        torch.cuda.synchronize()
+        want = oracle.allreduce(xs, "f16", ranks=[0])[0]
+        closed = (xs[0].view(np.float16).astype(np.float64)
+                  + xs[1].view(np.float16).astype(np.float64)).astype(np.float16).view(np.uint16)
+        assert np.array_equal(want, closed)
+        for r in range(R):
+            assert_bits_equal(to_bits(outs[r]), want, "f16", f"call {call} rank {r}")
+    h.check()
+    h.destroy()
+
+
+@pytest.mark.parametrize("slots", ["pinned", "hbm"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 5, 8])
+def test_ranks_dtypes_slots(R, dtype, slots):
+    # several tiles per block, plus a ragged tail of 5 elements
+    _run_once(R, dtype, 256 * 8 * 2 * 7 + 5, slots)
+
+
+@pytest.mark.parametrize("numel", [1, 2, 7, 8, 9, 15, 2047, 2048, 2049, 4095, 65536 + 3, 1000003])
+def test_edge_sizes(numel):
+    _run_once(4, "bf16", numel, "hbm")
+    _run_once(2, "f16", numel, "pinned")
+
+
+def test_max_numel_exactly_and_one_over():
+    import tensor_decode_all_gb300 as tda
+    n = 12345
+    h = _handle(2, "f16", n, "hbm")
+    _run_once(2, "f16", n, "hbm", h=h)
+    t = torch.zeros(n + 8, dtype=torch.float16, device="cuda")
+    s = rank_streams(2)
+    rc = tda.ar_allreduce(h.ptr, 0, t.data_ptr(), t.data_ptr(), n + 1, s[0].cuda_stream)
+    assert rc == tda.ar.AR_ETOOBIG
+    h.destroy()
+
+
+def test_config2_graph_1000_calls_double_buffered():
+    """Workload 2: R=2 fp16 N=131072 pinned-host; a graph of 100 calls, each
+    with its own input and output buffers, replayed 10 times with the inputs
+    refilled between replays (1000 calls, both parities see different data)."""
+    R, n, C, REPLAYS = 2, 131072, 100, 10
+    h = _handle(R, "f16", n, "pinned")
+    streams = rank_streams(R)
+    ins = [[torch.empty(n, dtype=torch.float16, device="cuda") for _ in range(R)] for _ in range(C)]
+    outs = [[torch.empty(n, dtype=torch.float16, device="cuda") for _ in range(R)] for _ in range(C)]
+    g = capture(h, "allreduce", ins, outs, streams)
+    for rep in range(REPLAYS):
+        xs_all = []
+        for c in range(C):
+            xs = inputs.allreduce_inputs(2, R, n, "f16", "normal4", rep * C + c)
+            for r in range(R):
+                ins[c][r].copy_(to_dev(xs[r], "f16"))
+            xs_all.append(xs)
+        g.replay()
+        torch.cuda.synchronize()
+        h.check()
+        for c in (0, 1, C // 2, C - 2, C - 1) if rep < REPLAYS - 1 else range(C):
+            want = oracle.allreduce(xs_all[c], "f16", ranks=[0])[0]
+            for r in range(R):
+                assert_bits_equal(to_bits(outs[c][r]), want, "f16", f"replay {rep} call {c} rank {r}")
+    del g
+    h.destroy()
+
+
+def test_config3_r8_bf16_hbm_graph():
+    """Workload 3: R=8, bf16, N=393216, HBM slots, graph-replayed calls."""
+    R, n, C, REPLAYS = 8, 393216, 10, 4
+    h = _handle(R, "bf16", n, "hbm")
+    streams = rank_streams(R)
+    ins = [[torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(R)] for _ in range(C)]
+    outs = [[torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(R)] for _ in range(C)]
+    g = capture(h, "allreduce", ins, outs, streams)
+    for rep in range(REPLAYS):
+        xs_all = []
+        for c in range(C):
+            xs = inputs.allreduce_inputs(3, R, n, "bf16", "normal", rep * C + c)
+            for r in range(R):
+                ins[c][r].copy_(to_dev(xs[r], "bf16"))
+            xs_all.append(xs)
+        g.replay()
+        torch.cuda.synchronize()
+        h.check()
+        for c in range(C):
+            want = oracle.allreduce(xs_all[c], "bf16", ranks=[0])[0]
+            for r in range(R):
+                assert_bits_equal(to_bits(outs[c][r]), want, "bf16", f"replay {rep} call {c} rank {r}")
+    del g
+    h.destroy()
+
+
+def test_in_place():
+    R, n, dtype = 4, 70001, "bf16"
+    xs = inputs.allreduce_inputs(5, R, n, dtype, "uniform", 7)
+    h = _handle(R, dtype, n, "hbm")
+    bufs = [to_dev(x, dtype) for x in xs]
+    enqueue(h, "allreduce", bufs, bufs, rank_streams(R))
+    torch.cuda.synchronize()
+    h.check()
+    want = oracle.allreduce(xs, dtype, ranks=[0])[0]
+    for r in range(R):
+        assert_bits_equal(to_bits(bufs[r]), want, dtype, f"in place rank {r}")
+    h.destroy()
+
+
+def test_every_output_element_is_written():
+    """Outputs pre-filled with a NaN sentinel; inputs hold no NaN, so no NaN may
+    remain (a slot path that dropped data would also fail the oracle check)."""
+    R, n = 2, 100003
+    xs = inputs.allreduce_inputs(5, R, n, "f16", "uniform", 3)
+    h = _handle(R, "f16", n, "pinned")
+    ins = [to_dev(x, "f16") for x in xs]
+    outs = [torch.full((n,), float("nan"), dtype=torch.float16, device="cuda") for _ in range(R)]
+    enqueue(h, "allreduce", ins, outs, rank_streams(R))
+    torch.cuda.synchronize()
+    for r in range(R):
+        assert not torch.isnan(outs[r]).any()
+    want = oracle.allreduce(xs, "f16", ranks=[0])[0]
+    for r in range(R):
+        assert_bits_equal(to_bits(outs[r]), want, "f16", f"rank {r}")
+    h.destroy()
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_special_values(dtype):
+    """Random bit patterns: subnormals, infinities, NaNs, overflow."""
+    R, n = 3, 50000
+    rng = np.random.default_rng(99)
+    xs = [rng.integers(0, 65536, n, dtype=np.uint32).astype(np.uint16) for _ in range(R)]
+    h = _handle(R, dtype, n, "hbm")
+    ins = [to_dev(x, dtype) for x in xs]
+    outs = [torch.empty_like(t) for t in ins]
+    enqueue(h, "allreduce", ins, outs, rank_streams(R))
+    torch.cuda.synchronize()
+    want = oracle.allreduce(xs, dtype, ranks=[0])[0]
+    for r in range(R):
+        assert_bits_equal(to_bits(outs[r]), want, dtype, f"rank {r}")
+    h.destroy()
