@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--sweep-calls", type=int, default=1000)
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", default=None, choices=sorted(PROFILE_WORKLOADS),
+                    help="graph replays of one workload only (for ncu --graph-profiling graph)")
     return ap.parse_args()
 
 
@@ -439,6 +441,35 @@ def run_ours(args, dist):
     return line
 
 
+# name: (op, R, dtype, numel, slots, config, dist, calls per graph)
+PROFILE_WORKLOADS = {
+    "r2_fp16_256KiB_pinned": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 100),
+    "r2_fp16_256KiB_pinned_1call": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 1),
+    "r8_bf16_768KiB_hbm": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100),
+    "r8_bf16_16MiB_hbm_1call": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 1),
+    "allgather_c64_r8_hbm_1call": ("allgather", 8, "c64", 500000, "hbm", 4, "normal", 1),
+}
+
+
+def run_profile(args, dist):
+    """Only graph replays (no eager rank calls: a profiler that serialises
+    kernels would keep the ranks of one call apart).  Prints timing, no JSON."""
+    import torch
+    import tensor_decode_all_gb300 as tda
+    torch.cuda.set_device(0)
+    tda.build()
+    op, R, dt, n, sl, cfg, dd, C = PROFILE_WORKLOADS[args.profile]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    w = Workload(op, R, dt, n, sl, C, config=cfg, dist=dd)
+    w.capture()
+    ms = w.time_graph(args.steps, args.warmup, flush)
+    w.check(calls=(0, -1))
+    print(f"profile {args.profile}: {len(ms)} steps x {C} calls, "
+          f"{sum(ms) * 1e3 / (len(ms) * C):.3f} us/call (graph)", flush=True)
+    w.close()
+    return None
+
+
 def run_reference(args, dist):
     """The CPU oracle as the reference arm: same workload, metric and unit."""
     if dist.rank != 0:
@@ -518,6 +549,8 @@ def main():
     try:
         if args.impl == "reference":
             line = run_reference(args, dist)
+        elif args.profile:
+            line = run_profile(args, dist)
         elif args.sweep:
             line = run_sweep(args, dist)
         else:

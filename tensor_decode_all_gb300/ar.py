@@ -16,7 +16,7 @@ import os
 import re
 import threading
 
-from . import build as _build
+from . import builder as _build
 
 AR_F16, AR_BF16, AR_C64 = 1, 2, 3
 AR_SLOT_PINNED_HOST, AR_SLOT_HBM = 0, 1
@@ -69,7 +69,7 @@ def lib():
             path = _build.LIB
             if not os.path.exists(path):
                 raise RuntimeError(f"{path} is missing: build it with "
-                                   "tensor_decode_all_gb300.build.build() (there is no CPU fallback)")
+                                   "tensor_decode_all_gb300.build() (there is no CPU fallback)")
             L = ctypes.CDLL(path)
             vp, sz, i32, u64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint64
             L.ar_create.argtypes = [i32, i32, sz, i32]

@@ -200,7 +200,7 @@ int begin_call(ar_handle *h, int rank, const void *in, void *out, size_t numel, 
     if (rc != AR_OK) return rc;
     rc = check_device(h);
     if (rc != AR_OK) return rc;
-    if (h->err_host->code != AR_OK) return AR_ESTATE;
+    if (*reinterpret_cast<volatile int32_t *>(&h->err_host->code) != AR_OK) return AR_ESTATE;
     const uint64_t c = h->host_calls[rank].fetch_add(1, std::memory_order_acq_rel) + 1;
     for (int p = 0; p < h->R; ++p) {
         if (p == rank) continue;
@@ -349,8 +349,14 @@ AR_API int ar_allgather(ar_handle *h, int rank, const void *in, void *out, size_
 
 AR_API int ar_status(ar_handle *h, ar_error_info *info) {
     if (!h) return AR_EINVAL;
+    const volatile ar_error_info *v = h->err_host;
     ar_error_info e;
-    std::memcpy(&e, (const void *)h->err_host, sizeof(e));
+    e.code = v->code;
+    e.rank = v->rank;
+    e.block = v->block;
+    e.peer = v->peer;
+    e.want = v->want;
+    e.seen = v->seen;
     if (info) *info = e;
     return e.code;
 }
