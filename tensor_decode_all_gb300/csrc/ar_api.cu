@@ -59,8 +59,21 @@ bool valid_stream_handle(cudaStream_t s) {
     return s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread;
 }
 
+// The blocking/non-blocking rule matters for eager launches (a blocking stream
+// serialises with the legacy stream).  Under stream capture the call becomes a
+// graph node whose ordering comes from the graph's edges, and querying the
+// flags of a capturing stream invalidates the capture (cudaStreamGetFlags
+// returns success but the capture is dead), so the flags are only read
+// outside capture.
 int check_stream(cudaStream_t s) {
     if (!valid_stream_handle(s)) return AR_ESTREAM;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ESTREAM;
+    }
+    if (cs == cudaStreamCaptureStatusActive) return AR_OK;
+    if (cs != cudaStreamCaptureStatusNone) return AR_ESTREAM;  // an invalidated capture
     unsigned int flags = 0;
     if (cudaStreamGetFlags(s, &flags) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -126,11 +139,16 @@ int zero_state(ar_handle *h) {
 }
 
 // Smallest occupancy over every kernel variant this handle may launch, so
-// that R * bmax blocks of any of them fit on the GPU at the same time.
+// that R * bmax blocks of any of them fit on the GPU at the same time.  Also
+// loads each variant into the context now (cudaFuncGetAttributes), so that no
+// kernel is loaded lazily while its first launch is being captured into a
+// graph: module loading during capture invalidates the capture.
 int handle_occupancy(int R, int dtype, int *bps_out) {
     int bps = 1 << 30;
     auto take = [&](const void *k) -> bool {
         if (!k) return false;
+        cudaFuncAttributes attr;
+        if (cudaFuncGetAttributes(&attr, k) != cudaSuccess) return false;
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, tda::kThreads, 0) != cudaSuccess)
             return false;
