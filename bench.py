@@ -169,7 +169,7 @@ def measured_peaks():
 class Workload:
     """R ranks, C calls, one graph; every call has its own device buffers."""
 
-    def __init__(self, op, R, dtype, numel, slots, calls, config, dist="uniform"):
+    def __init__(self, op, R, dtype, numel, slots, calls, config, dist="uniform", algo=None):
         import torch
         import tensor_decode_all_gb300 as tda
         from tensor_decode_all_gb300 import inputs
@@ -178,6 +178,10 @@ class Workload:
         tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "c64": torch.complex64}[dtype]
         self.tdt = tdt
         self.h = tda.Handle(R, tdt, numel, slots)
+        if algo:
+            self.h.set_algo(algo)
+        self.algo = "allgather" if op == "allgather" else \
+            ("twoshot" if self.h.plan("allreduce", numel).algo == 1 else "oneshot")
         self.streams = [torch.cuda.Stream() for _ in range(R)]
         out_n = numel * (R if op == "allgather" else 1)
         # inputs [C][numel] per rank, contiguous, so one copy moves a whole step
@@ -326,13 +330,13 @@ def roofline(op, R, S, slots, t_call_s, link, hbm_gbs):
             "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)"}
 
 
-def summarize(op, R, dtype, numel, slots, ms_steps, C, link, hbm_gbs):
+def summarize(op, R, dtype, numel, slots, ms_steps, C, link, hbm_gbs, algo=None):
     isz = 8 if dtype == "c64" else 2
     S = numel * isz
     total_ms = sum(ms_steps)
     t_call = total_ms * 1e-3 / (len(ms_steps) * C)
     out_bytes = S * (R if op == "allgather" else 1)
-    return {"op": op, "R": R, "dtype": dtype, "numel": numel, "bytes_per_rank": S, "slots": slots,
+    return {"op": op, "algo": algo, "R": R, "dtype": dtype, "numel": numel, "bytes_per_rank": S, "slots": slots,
             "us_per_call": round(t_call * 1e6, 3),
             "us_per_call_median_step": round(statistics.median(ms_steps) * 1e3 / C, 3),
             "algbw_gbs": round(out_bytes / t_call / 1e9, 3),
@@ -385,7 +389,7 @@ def run_ours(args, dist):
     clocks = clk.summary()
     checked += w.check(calls=(0, -1))
     total_s = dist.max(sum(ms) * 1e-3)
-    head = summarize("allreduce", R, "f16", numel, "pinned", ms, C, link, hbm_gbs)
+    head = summarize("allreduce", R, "f16", numel, "pinned", ms, C, link, hbm_gbs, w.algo)
     S = numel * 2
     n = dist.world
     value = n * S * len(ms) * C / total_s / 1e9
@@ -397,22 +401,25 @@ def run_ours(args, dist):
 
     extras = {}
     if not args.no_extras:
-        for name, (op, RR, dt, nn, sl, cfg, dd, cc, st) in {
-            "r8_bf16_393216_hbm": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20),
-            "r8_bf16_16MiB_hbm": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 10, 10),
-            "r8_bf16_64MiB_hbm": ("allreduce", 8, "bf16", 32 << 20, "hbm", 5, "uniform", 4, 10),
-            "r2_fp16_16MiB_hbm": ("allreduce", 2, "f16", 8 << 20, "hbm", 5, "uniform", 10, 10),
-            "allgather_c64_r4_hbm": ("allgather", 4, "c64", 500000, "hbm", 4, None, 20, 10),
-            "allgather_c64_r8_hbm": ("allgather", 8, "c64", 500000, "hbm", 4, None, 20, 10),
-            "allgather_c64_r4_pinned": ("allgather", 4, "c64", 500000, "pinned", 4, None, 5, 5),
+        for name, (op, RR, dt, nn, sl, cfg, dd, cc, st, al) in {
+            "r2_fp16_4096_pinned": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", 100, 20, None),
+            "r8_bf16_393216_hbm": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20, None),
+            "r8_bf16_16MiB_hbm": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 10, 10, None),
+            "r8_bf16_16MiB_hbm_oneshot": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 10, 10, "oneshot"),
+            "r8_bf16_64MiB_hbm": ("allreduce", 8, "bf16", 32 << 20, "hbm", 5, "uniform", 4, 10, None),
+            "r2_fp16_16MiB_hbm": ("allreduce", 2, "f16", 8 << 20, "hbm", 5, "uniform", 10, 10, None),
+            "allgather_c64_r4_hbm": ("allgather", 4, "c64", 500000, "hbm", 4, None, 20, 10, None),
+            "allgather_c64_r8_hbm": ("allgather", 8, "c64", 500000, "hbm", 4, None, 20, 10, None),
+            "allgather_c64_r4_pinned": ("allgather", 4, "c64", 500000, "pinned", 4, None, 5, 5, None),
+            "allgather_c64_r8_pinned": ("allgather", 8, "c64", 500000, "pinned", 4, None, 5, 5, None),
         }.items():
-            wx = Workload(op, RR, dt, nn, sl, cc, config=cfg, dist=dd or "uniform")
+            wx = Workload(op, RR, dt, nn, sl, cc, config=cfg, dist=dd or "uniform", algo=al)
             wx.capture()
             wx.time_graph(1, 0, flush)
             wx.check(calls=(0, -1))
             msx = wx.time_graph(st, 2, flush)
             wx.check(calls=(-1,))
-            extras[name] = summarize(op, RR, dt, nn, sl, msx, cc, link, hbm_gbs)
+            extras[name] = summarize(op, RR, dt, nn, sl, msx, cc, link, hbm_gbs, wx.algo)
             wx.close()
 
     line = {
@@ -447,6 +454,7 @@ PROFILE_WORKLOADS = {
     "r2_fp16_256KiB_pinned_1call": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 1),
     "r8_bf16_768KiB_hbm": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100),
     "r8_bf16_16MiB_hbm_1call": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 1),
+    "r8_bf16_16MiB_hbm_oneshot_1call": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 1),
     "allgather_c64_r8_hbm_1call": ("allgather", 8, "c64", 500000, "hbm", 4, "normal", 1),
 }
 
@@ -460,7 +468,7 @@ def run_profile(args, dist):
     tda.build()
     op, R, dt, n, sl, cfg, dd, C = PROFILE_WORKLOADS[args.profile]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-    w = Workload(op, R, dt, n, sl, C, config=cfg, dist=dd)
+    w = Workload(op, R, dt, n, sl, C, config=cfg, dist=dd, algo="oneshot" if "oneshot" in args.profile else None)
     w.capture()
     ms = w.time_graph(args.steps, args.warmup, flush)
     w.check(calls=(0, -1))
@@ -533,7 +541,7 @@ def run_sweep(args, dist):
                         w.check(calls=(0, -1))
                         ms = w.time_graph(steps, 2, flush)
                         w.check(calls=(0, -1))
-                        row = summarize("allreduce", R, dtype, numel, slots, ms, C, link, hbm_gbs)
+                        row = summarize("allreduce", R, dtype, numel, slots, ms, C, link, hbm_gbs, w.algo)
                         row["parity"] = "bit-exact (first and last call)"
                         f.write(json.dumps(row) + "\n")
                         f.flush()

@@ -85,6 +85,15 @@ enum ar_code {
     AR_ESTATE = 7     /* the handle needs ar_reset() (a device error is recorded) */
 };
 
+/* How an all-reduce call moves its data (both give the same bits).
+ * AR_ALGO_ONESHOT: one flag round per tile; every rank reads every peer's tile
+ *   (the pages' exchange-and-add).  Per call, peer-slot reads are R*(R-1)*S.
+ * AR_ALGO_TWOSHOT: two flag rounds per tile; rank r reduces the r-th sub-tile
+ *   for everyone, then every rank copies the R reduced sub-tiles.  Per call,
+ *   slot reads are about 2*R*S; for large payloads at R >= 4.
+ * AR_ALGO_AUTO: chosen per call by ar_choose_algo(). */
+enum ar_algo { AR_ALGO_AUTO = -1, AR_ALGO_ONESHOT = 0, AR_ALGO_TWOSHOT = 1 };
+
 /* Details of the first device-side error recorded in a handle. */
 typedef struct ar_error_info {
     int32_t code;       /* AR_OK or AR_ETIMEOUT */
@@ -99,9 +108,13 @@ typedef struct ar_error_info {
 typedef struct ar_info {
     int32_t R, dtype, slot_kind, device;
     int32_t threads;        /* threads per block of the exchange kernels */
-    int32_t max_blocks;     /* blocks per rank at most: R * max_blocks blocks fit on the GPU at once */
+    int32_t max_blocks;     /* flag/counter slots per rank: an upper bound on blocks per rank */
     int32_t sm_count;
-    int32_t blocks_per_sm;  /* occupancy of the exchange kernel */
+    int32_t blocks_per_sm;  /* occupancy of the one-shot all-reduce kernels */
+    int32_t blocks_per_sm_twoshot;   /* ... of the two-shot all-reduce kernels */
+    int32_t blocks_per_sm_allgather; /* ... of the allgather kernels */
+    int32_t algo;           /* AR_ALGO_AUTO unless forced with ar_set_algo */
+    int32_t reserved;
     uint64_t max_numel;
     uint64_t slot_bytes;    /* bytes of one (parity, rank) slot, a multiple of 256 */
     uint64_t total_slot_bytes; /* 2 * R * slot_bytes: the allocation that cannot grow */
@@ -110,10 +123,12 @@ typedef struct ar_info {
 
 /* Launch plan of one call, computed on the host (no GPU needed). */
 typedef struct ar_plan {
-    int32_t blocks;         /* grid size per rank (same on every rank) */
+    int32_t blocks;         /* grid size per rank (same on every rank); R * blocks fit on the GPU */
     int32_t threads;        /* threads per block */
     int32_t vec_bytes;      /* bytes per vector access: 16 for all-reduce */
-    int32_t unroll;         /* vectors per thread per tile */
+    int32_t unroll;         /* vectors per thread per tile (R for the two-shot form) */
+    int32_t algo;           /* AR_ALGO_ONESHOT or AR_ALGO_TWOSHOT (allgather: one-shot) */
+    int32_t flag_rounds;    /* flag rounds per tile: 1 or 2 */
     uint64_t tile_bytes;    /* bytes a block handles per stage (threads * unroll * vec_bytes) */
     uint64_t tiles;         /* ceil(bytes / tile_bytes); tile t goes to block t % blocks, stage t / blocks */
     uint64_t max_stages;    /* stages of block 0 = ceil(tiles / blocks) */
@@ -229,11 +244,22 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan);
 /*
  * ar_plan_compute -- the same plan from explicit machine facts, so the host
  * logic can be checked without a GPU: R ranks, `bytes` per rank, vector size
- * vec_bytes (16, 8, 4, 2 or 1), `threads` per block, and a GPU that holds
- * sm_count * blocks_per_sm blocks of the kernel at once.
+ * vec_bytes (16, 8, 4, 2 or 1), algo AR_ALGO_ONESHOT or AR_ALGO_TWOSHOT,
+ * `threads` per block, and a GPU that holds sm_count * blocks_per_sm blocks of
+ * the kernel at once.
  */
-AR_API int ar_plan_compute(int R, uint64_t bytes, int vec_bytes, int threads, int sm_count,
+AR_API int ar_plan_compute(int R, uint64_t bytes, int vec_bytes, int algo, int threads, int sm_count,
                            int blocks_per_sm, ar_plan *plan);
+
+/* The all-reduce form AR_ALGO_AUTO picks for R ranks and `bytes` per rank:
+ * two-shot for R >= 4 and bytes >= 1 MiB, one-shot otherwise.  Pure host
+ * arithmetic. */
+AR_API int ar_choose_algo(int R, uint64_t bytes);
+
+/* Force the all-reduce form of a handle (AR_ALGO_AUTO restores the rule).  The
+ * environment variable AR_ALGO=oneshot|twoshot sets it at ar_create.  Every
+ * rank of a call must see the same setting; set it before enqueuing. */
+AR_API int ar_set_algo(ar_handle *h, int algo);
 
 /* Human-readable name of an ar_code.  Never NULL. */
 AR_API const char *ar_strerror(int code);

@@ -20,6 +20,8 @@ from . import builder as _build
 
 AR_F16, AR_BF16, AR_C64 = 1, 2, 3
 AR_SLOT_PINNED_HOST, AR_SLOT_HBM = 0, 1
+AR_ALGO_AUTO, AR_ALGO_ONESHOT, AR_ALGO_TWOSHOT = -1, 0, 1
+ALGOS = {"auto": AR_ALGO_AUTO, "oneshot": AR_ALGO_ONESHOT, "twoshot": AR_ALGO_TWOSHOT}
 AR_OK, AR_EINVAL, AR_ETOOBIG, AR_ESTREAM, AR_ENOMEM, AR_ECUDA, AR_ETIMEOUT, AR_ESTATE = range(8)
 CODE_NAMES = {0: "AR_OK", 1: "AR_EINVAL", 2: "AR_ETOOBIG", 3: "AR_ESTREAM", 4: "AR_ENOMEM",
               5: "AR_ECUDA", 6: "AR_ETIMEOUT", 7: "AR_ESTATE"}
@@ -43,13 +45,16 @@ class Info(ctypes.Structure):
     _fields_ = [("R", ctypes.c_int32), ("dtype", ctypes.c_int32), ("slot_kind", ctypes.c_int32),
                 ("device", ctypes.c_int32), ("threads", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
                 ("sm_count", ctypes.c_int32), ("blocks_per_sm", ctypes.c_int32),
+                ("blocks_per_sm_twoshot", ctypes.c_int32), ("blocks_per_sm_allgather", ctypes.c_int32),
+                ("algo", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("max_numel", ctypes.c_uint64), ("slot_bytes", ctypes.c_uint64),
                 ("total_slot_bytes", ctypes.c_uint64), ("timeout_ns", ctypes.c_uint64)]
 
 
 class Plan(ctypes.Structure):
     _fields_ = [("blocks", ctypes.c_int32), ("threads", ctypes.c_int32), ("vec_bytes", ctypes.c_int32),
-                ("unroll", ctypes.c_int32), ("tile_bytes", ctypes.c_uint64), ("tiles", ctypes.c_uint64),
+                ("unroll", ctypes.c_int32), ("algo", ctypes.c_int32), ("flag_rounds", ctypes.c_int32),
+                ("tile_bytes", ctypes.c_uint64), ("tiles", ctypes.c_uint64),
                 ("max_stages", ctypes.c_uint64)]
 
 
@@ -85,7 +90,9 @@ def lib():
             L.ar_set_timeout.argtypes = [vp, u64]
             L.ar_query.argtypes = [vp, ctypes.POINTER(Info)]
             L.ar_plan_for.argtypes = [vp, i32, sz, ctypes.POINTER(Plan)]
-            L.ar_plan_compute.argtypes = [i32, u64, i32, i32, i32, i32, ctypes.POINTER(Plan)]
+            L.ar_plan_compute.argtypes = [i32, u64, i32, i32, i32, i32, i32, ctypes.POINTER(Plan)]
+            L.ar_choose_algo.argtypes = [i32, u64]
+            L.ar_set_algo.argtypes = [vp, i32]
             L.ar_strerror.argtypes = [i32]
             L.ar_strerror.restype = ctypes.c_char_p
             L.ar_probe_host_link.argtypes = [u64, i32, ctypes.POINTER(ctypes.c_double)]
@@ -153,12 +160,20 @@ def ar_plan_for(h: int, op: int, numel: int) -> Plan:
     return p
 
 
-def ar_plan_compute(R, nbytes, vec_bytes, threads, sm_count, blocks_per_sm) -> Plan:
+def ar_plan_compute(R, nbytes, vec_bytes, algo, threads, sm_count, blocks_per_sm) -> Plan:
     p = Plan()
-    rc = lib().ar_plan_compute(R, nbytes, vec_bytes, threads, sm_count, blocks_per_sm, ctypes.byref(p))
+    rc = lib().ar_plan_compute(R, nbytes, vec_bytes, algo, threads, sm_count, blocks_per_sm, ctypes.byref(p))
     if rc:
         raise ArError(rc, "ar_plan_compute")
     return p
+
+
+def ar_choose_algo(R: int, nbytes: int) -> int:
+    return lib().ar_choose_algo(R, nbytes)
+
+
+def ar_set_algo(h: int, algo: int) -> int:
+    return lib().ar_set_algo(h, algo)
 
 
 def strerror(code: int) -> str:
@@ -263,6 +278,13 @@ class Handle:
         rc = ar_set_timeout(self.ptr, int(ns))
         if rc:
             raise ArError(rc, "ar_set_timeout")
+
+    def set_algo(self, algo) -> None:
+        """'auto', 'oneshot' or 'twoshot' (or an AR_ALGO_* code)."""
+        code = ALGOS[algo] if isinstance(algo, str) else int(algo)
+        rc = ar_set_algo(self.ptr, code)
+        if rc:
+            raise ArError(rc, "ar_set_algo")
 
     def info(self) -> Info:
         return ar_query(self.ptr)

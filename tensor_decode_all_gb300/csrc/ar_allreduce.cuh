@@ -62,7 +62,7 @@ struct BF16Ops {
 
 // acc[0..7] (+)= the 8 elements of v.
 template <class Ops, bool kFirst>
-__device__ __forceinline__ void accumulate8(float (&acc)[8], const uint4 &v) {
+__device__ __forceinline__ void accumulate8(float (&acc)[8], const uint4 v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -89,28 +89,39 @@ __device__ __forceinline__ uint4 narrow8(const float (&acc)[8]) {
 
 // Load vector v of the caller's input: a full 16-byte vector, or the partial
 // last vector (tail elements, zero-filled), or nothing past the end.
+// (Element j of a vector lives in 32-bit word j / 2; the tail paths pick the
+// word with selects rather than an indexed array, which would need local memory.)
 __device__ __forceinline__ uint4 load_own(const uint16_t *in, uint64_t v, uint64_t nvec_full,
                                           int tail) {
     if (v < nvec_full) return *reinterpret_cast<const uint4 *>(in + v * 8);
     uint4 r = make_uint4(0u, 0u, 0u, 0u);
     if (v == nvec_full && tail) {
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        for (int j = 0; j < tail; ++j) {
-            const uint32_t e = in[v * 8 + j];
-            w[j >> 1] |= e << ((j & 1) * 16);
+#pragma unroll
+        for (int j = 0; j < 7; ++j) {
+            if (j < tail) {
+                const uint32_t e = (uint32_t)in[v * 8 + j] << ((j & 1) * 16);
+                if (j < 2) r.x |= e;
+                else if (j < 4) r.y |= e;
+                else if (j < 6) r.z |= e;
+                else r.w |= e;
+            }
         }
-        r = make_uint4(w[0], w[1], w[2], w[3]);
     }
     return r;
 }
 
 __device__ __forceinline__ void store_out(uint16_t *out, uint64_t v, uint64_t nvec_full, int tail,
-                                          const uint4 &r) {
+                                          const uint4 r) {
     if (v < nvec_full) {
         *reinterpret_cast<uint4 *>(out + v * 8) = r;
     } else if (v == nvec_full && tail) {
-        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-        for (int j = 0; j < tail; ++j) out[v * 8 + j] = (uint16_t)(w[j >> 1] >> ((j & 1) * 16));
+#pragma unroll
+        for (int j = 0; j < 7; ++j) {
+            if (j < tail) {
+                const uint32_t w = j < 2 ? r.x : (j < 4 ? r.y : (j < 6 ? r.z : r.w));
+                out[v * 8 + j] = (uint16_t)(w >> ((j & 1) * 16));
+            }
+        }
     }
 }
 
@@ -182,13 +193,15 @@ __global__ void __launch_bounds__(kThreads)
         for (int u = 0; u < U; ++u) {
             const uint64_t v = v0 + (uint64_t)u * kThreads;
             if (v < nv) {
+                // (A per-p select of the value, not a store into vals[p] under
+                // "p == rank": the compiler turns the latter into a store to
+                // vals[rank], a runtime index that needs local memory.)
                 uint4 vals[R];
 #pragma unroll
                 for (int p = 0; p < R; ++p) {
-                    if (p == rank)
-                        vals[p] = own[u];
-                    else
-                        vals[p] = ld_cg_v4(slot_base + (uint64_t)p * slot_vecs + v);
+                    uint4 peer = own[u];
+                    if (p != rank) peer = ld_cg_v4(slot_base + (uint64_t)p * slot_vecs + v);
+                    vals[p] = peer;
                 }
                 float acc[8];
                 accumulate8<Ops, true>(acc, vals[0]);
@@ -206,6 +219,108 @@ __global__ void __launch_bounds__(kThreads)
     if (tid == 0) {
         Ctr c;
         c.seq = seq + nstages;
+        c.calls = s_calls + 1;
+        d.ctr[(size_t)rank * d.bmax + b] = c;
+    }
+}
+
+// Two-shot variant, for large payloads at R >= 4, where the one-shot form's
+// R * (R - 1) * S bytes of peer-slot reads per call saturate L2.  A tile is R
+// sub-tiles of kThreads vectors.  Per stage, each block of rank r:
+//   1. copies the whole tile of in_r into slot[parity][r]; barrier; raises its
+//      flag to seq + 2s + 1 (release);
+//   2. waits for every peer's flag to reach seq + 2s + 1; reduces sub-tile r:
+//      reads it from all R slots, adds in fp32 in rank order 0..R-1, rounds
+//      once, and overwrites sub-tile r of its own slot with the result (only
+//      rank r ever reads sub-tile r of any slot in this round); barrier; raises
+//      its flag to seq + 2s + 2;
+//   3. waits for every peer's flag to reach seq + 2s + 2; copies sub-tile p of
+//      slot p (rank p's rounded result) into out_r for every p.
+// Each element is reduced once, by one rank, in rank order, so every rank
+// receives the same bits as the one-shot form and the oracle.  Per call, slot
+// reads fall from R * (R - 1) * S to about 2 * R * S bytes.
+template <class Ops, int R>
+__global__ void __launch_bounds__(kThreads, 4)
+    allreduce_twoshot_kernel(const uint16_t *in, uint16_t *out, uint64_t numel, int rank, DevState d) {
+    __shared__ unsigned long long s_seq;
+    __shared__ unsigned long long s_calls;
+    __shared__ int s_bail;
+
+    const int b = blockIdx.x;
+    const int B = gridDim.x;
+    const int tid = threadIdx.x;
+    const uint64_t nvec_full = numel / 8;
+    const int tail = (int)(numel % 8);
+    const uint64_t nv = nvec_full + (tail ? 1 : 0);
+    constexpr uint64_t kTileVecs = (uint64_t)kThreads * R;
+    const uint64_t ntiles = (nv + kTileVecs - 1) / kTileVecs;
+    const uint64_t nstages = ntiles > (uint64_t)b ? (ntiles - b + B - 1) / B : 0;
+
+    if (tid == 0) {
+        const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
+        s_seq = c.seq;
+        s_calls = c.calls;
+        s_bail = 0;
+    }
+    __syncthreads();
+    const unsigned long long seq = s_seq;
+    const int parity = (int)(s_calls & 1ull);
+    const uint64_t slot_vecs = d.slot_bytes / 16;
+    uint4 *const slot_base = reinterpret_cast<uint4 *>(d.slots) + (uint64_t)parity * R * slot_vecs;
+    uint4 *const my_slot = slot_base + (uint64_t)rank * slot_vecs;
+
+    for (uint64_t s = 0; s < nstages; ++s) {
+        const uint64_t t0 = ((uint64_t)b + s * B) * kTileVecs + tid;
+
+        // 1. publish the whole tile
+        uint4 pub[R];
+#pragma unroll
+        for (int u = 0; u < R; ++u) pub[u] = load_own(in, t0 + (uint64_t)u * kThreads, nvec_full, tail);
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+            const uint64_t v = t0 + (uint64_t)u * kThreads;
+            if (v < nv) my_slot[v] = pub[u];
+        }
+        __syncthreads();
+        if (tid == 0) publish_stage(d, rank, b, seq + 2 * s + 1);
+        if (wait_peers(d, R, rank, b, seq + 2 * s + 1, &s_bail)) return;
+
+        // 2. reduce sub-tile `rank` in rank order; the result replaces it in my slot
+        const uint64_t vr = t0 + (uint64_t)rank * kThreads;
+        uint4 res = make_uint4(0u, 0u, 0u, 0u);
+        if (vr < nv) {
+            uint4 vals[R];
+#pragma unroll
+            for (int p = 0; p < R; ++p) vals[p] = ld_cg_v4(slot_base + (uint64_t)p * slot_vecs + vr);
+            float acc[8];
+            accumulate8<Ops, true>(acc, vals[0]);
+#pragma unroll
+            for (int p = 1; p < R; ++p) accumulate8<Ops, false>(acc, vals[p]);
+            res = narrow8<Ops>(acc);
+            my_slot[vr] = res;
+        }
+        __syncthreads();
+        if (tid == 0) publish_stage(d, rank, b, seq + 2 * s + 2);
+        if (wait_peers(d, R, rank, b, seq + 2 * s + 2, &s_bail)) return;
+
+        // 3. gather the R rounded sub-tiles
+        uint4 got[R];
+#pragma unroll
+        for (int p = 0; p < R; ++p) {
+            const uint64_t v = t0 + (uint64_t)p * kThreads;
+            got[p] = res;
+            if (p != rank && v < nv) got[p] = ld_cg_v4(slot_base + (uint64_t)p * slot_vecs + v);
+        }
+#pragma unroll
+        for (int p = 0; p < R; ++p) {
+            const uint64_t v = t0 + (uint64_t)p * kThreads;
+            if (v < nv) store_out(out, v, nvec_full, tail, got[p]);
+        }
+    }
+
+    if (tid == 0) {
+        Ctr c;
+        c.seq = seq + 2 * nstages;
         c.calls = s_calls + 1;
         d.ctr[(size_t)rank * d.bmax + b] = c;
     }
@@ -233,7 +348,25 @@ const void *allreduce_ptr_ru(int R) {
 }
 
 template <class Ops>
+const void *allreduce_twoshot_ptr(int R) {
+    switch (R) {
+        case 1: return (const void *)allreduce_twoshot_kernel<Ops, 1>;
+        case 2: return (const void *)allreduce_twoshot_kernel<Ops, 2>;
+        case 3: return (const void *)allreduce_twoshot_kernel<Ops, 3>;
+        case 4: return (const void *)allreduce_twoshot_kernel<Ops, 4>;
+        case 5: return (const void *)allreduce_twoshot_kernel<Ops, 5>;
+        case 6: return (const void *)allreduce_twoshot_kernel<Ops, 6>;
+        case 7: return (const void *)allreduce_twoshot_kernel<Ops, 7>;
+        case 8: return (const void *)allreduce_twoshot_kernel<Ops, 8>;
+        default: return nullptr;
+    }
+}
+
+// unroll 1 or 2: one-shot with that many vectors per thread per stage;
+// kTwoShot: the two-shot form.
+template <class Ops>
 const void *allreduce_ptr(int R, int U) {
+    if (U == kTwoShot) return allreduce_twoshot_ptr<Ops>(R);
     return U == 1 ? allreduce_ptr_ru<Ops, 1>(R) : allreduce_ptr_ru<Ops, 2>(R);
 }
 

@@ -22,7 +22,10 @@ using tda::DevState;
 struct ar_handle {
     int R = 0, dtype = 0, kind = 0, device = 0;
     uint64_t max_numel = 0, itemsize = 0, slot_bytes = 0;
-    int sm_count = 0, blocks_per_sm = 0, bmax = 0;
+    int sm_count = 0;
+    int bps_one = 0, bps_two = 0, bps_ag = 0;  // occupancy per kernel family
+    int bmax = 0;                              // flag/counter slots per rank
+    int algo = AR_ALGO_AUTO;
     void *slots_host = nullptr;            // pinned kind: host address of the slots
     uint8_t *slots_dev = nullptr;          // device address of the slots
     void *flags_host = nullptr;            // pinned kind: host address of the flags
@@ -138,50 +141,65 @@ int zero_state(ar_handle *h) {
     return AR_OK;
 }
 
-// Smallest occupancy over every kernel variant this handle may launch, so
-// that R * bmax blocks of any of them fit on the GPU at the same time.  Also
-// loads each variant into the context now (cudaFuncGetAttributes), so that no
-// kernel is loaded lazily while its first launch is being captured into a
-// graph: module loading during capture invalidates the capture.
-int handle_occupancy(int R, int dtype, int *bps_out) {
-    int bps = 1 << 30;
-    auto take = [&](const void *k) -> bool {
-        if (!k) return false;
-        cudaFuncAttributes attr;
-        if (cudaFuncGetAttributes(&attr, k) != cudaSuccess) return false;
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, tda::kThreads, 0) != cudaSuccess)
-            return false;
-        if (n < bps) bps = n;
-        return true;
-    };
-    for (int u = 1; u <= 2; ++u) {
-        if (dtype == AR_F16 || dtype == AR_BF16)
-            if (!take(tda::allreduce_kernel_ptr(dtype, R, u))) return AR_ECUDA;
-        for (int vw = 1; vw <= 16; vw *= 2)
-            if (!take(tda::allgather_kernel_ptr(vw, R, u))) return AR_ECUDA;
-    }
-    if (bps < 1) return AR_ECUDA;
-    *bps_out = bps;
+// Occupancy of each kernel family a handle may launch (the smallest over the
+// family's variants), so that R * blocks of any launched variant fit on the GPU
+// at the same time: the co-residency the spin-waits need.  Also loads each
+// variant into the context now (cudaFuncGetAttributes), so that no kernel is
+// loaded lazily while its first launch is being captured into a graph.
+int kernel_occupancy(const void *k, int *bps) {
+    if (!k) return AR_ECUDA;
+    cudaFuncAttributes attr;
+    if (cudaFuncGetAttributes(&attr, k) != cudaSuccess) return AR_ECUDA;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, tda::kThreads, 0) != cudaSuccess) return AR_ECUDA;
+    if (n < *bps) *bps = n;
     return AR_OK;
 }
 
-int plan_compute(int R, uint64_t bytes, int vec, int threads, int sms, int bps, ar_plan *p) {
+int handle_occupancy(ar_handle *h) {
+    int one = 1 << 30, two = 1 << 30, ag = 1 << 30;
+    int rc = AR_OK;
+    if (h->dtype == AR_F16 || h->dtype == AR_BF16) {
+        for (int u = 1; u <= 2 && rc == AR_OK; ++u) rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, u), &one);
+        if (rc == AR_OK) rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, tda::kTwoShot), &two);
+    }
+    for (int u = 1; u <= 2 && rc == AR_OK; ++u)
+        for (int vw = 1; vw <= 16 && rc == AR_OK; vw *= 2) rc = kernel_occupancy(tda::allgather_kernel_ptr(vw, h->R, u), &ag);
+    if (rc != AR_OK) return rc;
+    if (one == 1 << 30) one = ag;
+    if (two == 1 << 30) two = ag;
+    if (one < 1 || two < 1 || ag < 1) return AR_ECUDA;
+    h->bps_one = one;
+    h->bps_two = two;
+    h->bps_ag = ag;
+    return AR_OK;
+}
+
+int choose_algo(int R, uint64_t bytes) {
+    return (R >= 4 && bytes >= (1ull << 20)) ? AR_ALGO_TWOSHOT : AR_ALGO_ONESHOT;
+}
+
+int plan_compute(int R, uint64_t bytes, int vec, int algo, int threads, int sms, int bps, ar_plan *p) {
     if (!p || R < 1 || R > tda::kMaxRanks || threads < 32 || threads % 32 || sms < 1 || bps < 1)
         return AR_EINVAL;
     if (vec != 16 && vec != 8 && vec != 4 && vec != 2 && vec != 1) return AR_EINVAL;
+    if (algo != AR_ALGO_ONESHOT && algo != AR_ALGO_TWOSHOT) return AR_EINVAL;
+    if (algo == AR_ALGO_TWOSHOT && vec != 16) return AR_EINVAL;
     std::memset(p, 0, sizeof(*p));
     const uint64_t bmax = (uint64_t)sms * (uint64_t)bps / (uint64_t)R;
     if (bmax < 1) return AR_EINVAL;
     const uint64_t nv = (bytes + vec - 1) / vec;
-    // Two vectors per thread per stage once every block has at least two
-    // stages' worth of single vectors; one otherwise (spreads small payloads
-    // over more blocks).
-    const int unroll = nv >= bmax * (uint64_t)threads * 2 ? 2 : 1;
+    // One-shot: two vectors per thread per stage once every block has at least
+    // two stages' worth of single vectors; one otherwise (spreads small
+    // payloads over more blocks).  Two-shot: one sub-tile of `threads` vectors
+    // per rank, so R vectors per thread per stage.
+    const int unroll = algo == AR_ALGO_TWOSHOT ? R : (nv >= bmax * (uint64_t)threads * 2 ? 2 : 1);
     const uint64_t tile_vecs = (uint64_t)threads * unroll;
     const uint64_t tiles = (nv + tile_vecs - 1) / tile_vecs;
     const uint64_t blocks = tiles < bmax ? tiles : bmax;
     p->blocks = (int32_t)blocks;
+    p->algo = algo;
+    p->flag_rounds = algo == AR_ALGO_TWOSHOT ? 2 : 1;
     p->threads = threads;
     p->vec_bytes = vec;
     p->unroll = unroll;
@@ -286,9 +304,15 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
     if (cudaGetDevice(&h->device) != cudaSuccess) return fail(AR_ECUDA);
     if (cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess)
         return fail(AR_ECUDA);
-    int rc = handle_occupancy(R, dtype, &h->blocks_per_sm);
+    if (const char *e = std::getenv("AR_ALGO")) {
+        if (!std::strcmp(e, "oneshot")) h->algo = AR_ALGO_ONESHOT;
+        else if (!std::strcmp(e, "twoshot")) h->algo = AR_ALGO_TWOSHOT;
+    }
+    int rc = handle_occupancy(h);
     if (rc != AR_OK) return fail(rc);
-    h->bmax = h->sm_count * h->blocks_per_sm / R;
+    int bps_max = h->bps_one > h->bps_two ? h->bps_one : h->bps_two;
+    if (h->bps_ag > bps_max) bps_max = h->bps_ag;
+    h->bmax = h->sm_count * bps_max / R;
     if (const int cap = max_blocks_override()) h->bmax = cap < h->bmax ? cap : h->bmax;
     if (h->bmax < 1) return fail(AR_ECUDA);
 
@@ -330,11 +354,15 @@ AR_API int ar_allreduce(ar_handle *h, int rank, const void *in, void *out, size_
     uint64_t call = 0;
     int rc = begin_call(h, rank, in, out, numel, s, &call);
     if (rc != AR_OK || numel == 0) return rc;
+    const uint64_t bytes = numel * h->itemsize;
+    const int algo = h->algo == AR_ALGO_AUTO ? choose_algo(h->R, bytes) : h->algo;
     ar_plan plan;
-    rc = plan_compute(h->R, numel * h->itemsize, 16, tda::kThreads, h->sm_count, h->blocks_per_sm, &plan);
+    rc = plan_compute(h->R, bytes, 16, algo, tda::kThreads, h->sm_count,
+                      algo == AR_ALGO_TWOSHOT ? h->bps_two : h->bps_one, &plan);
     if (rc != AR_OK) return rc;
     int blocks = plan.blocks < h->bmax ? plan.blocks : h->bmax;
-    const cudaError_t e = tda::launch_allreduce(h->dtype, h->R, plan.unroll, blocks, s, in, out,
+    const int variant = algo == AR_ALGO_TWOSHOT ? tda::kTwoShot : plan.unroll;
+    const cudaError_t e = tda::launch_allreduce(h->dtype, h->R, variant, blocks, s, in, out,
                                                 numel, rank, dev_state(h));
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
@@ -353,7 +381,7 @@ AR_API int ar_allgather(ar_handle *h, int rank, const void *in, void *out, size_
     const uint64_t bytes = numel * h->itemsize;
     const int vw = allgather_vec(bytes, in, out);
     ar_plan plan;
-    rc = plan_compute(h->R, bytes, vw, tda::kThreads, h->sm_count, h->blocks_per_sm, &plan);
+    rc = plan_compute(h->R, bytes, vw, AR_ALGO_ONESHOT, tda::kThreads, h->sm_count, h->bps_ag, &plan);
     if (rc != AR_OK) return rc;
     int blocks = plan.blocks < h->bmax ? plan.blocks : h->bmax;
     const cudaError_t e = tda::launch_allgather(vw, h->R, plan.unroll, blocks, s, in, out, bytes,
@@ -413,7 +441,11 @@ AR_API int ar_query(const ar_handle *h, ar_info *info) {
     info->threads = tda::kThreads;
     info->max_blocks = h->bmax;
     info->sm_count = h->sm_count;
-    info->blocks_per_sm = h->blocks_per_sm;
+    info->blocks_per_sm = h->bps_one;
+    info->blocks_per_sm_twoshot = h->bps_two;
+    info->blocks_per_sm_allgather = h->bps_ag;
+    info->algo = h->algo;
+    info->reserved = 0;
     info->max_numel = h->max_numel;
     info->slot_bytes = h->slot_bytes;
     info->total_slot_bytes = 2ull * (uint64_t)h->R * h->slot_bytes;
@@ -421,9 +453,18 @@ AR_API int ar_query(const ar_handle *h, ar_info *info) {
     return AR_OK;
 }
 
-AR_API int ar_plan_compute(int R, uint64_t bytes, int vec_bytes, int threads, int sm_count,
+AR_API int ar_plan_compute(int R, uint64_t bytes, int vec_bytes, int algo, int threads, int sm_count,
                            int blocks_per_sm, ar_plan *plan) {
-    return plan_compute(R, bytes, vec_bytes, threads, sm_count, blocks_per_sm, plan);
+    return plan_compute(R, bytes, vec_bytes, algo, threads, sm_count, blocks_per_sm, plan);
+}
+
+AR_API int ar_choose_algo(int R, uint64_t bytes) { return choose_algo(R, bytes); }
+
+AR_API int ar_set_algo(ar_handle *h, int algo) {
+    if (!h || (algo != AR_ALGO_AUTO && algo != AR_ALGO_ONESHOT && algo != AR_ALGO_TWOSHOT)) return AR_EINVAL;
+    if (algo == AR_ALGO_TWOSHOT && h->dtype == AR_C64) return AR_EINVAL;
+    h->algo = algo;
+    return AR_OK;
 }
 
 AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) {
@@ -431,7 +472,12 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) 
     if (numel > h->max_numel) return AR_ETOOBIG;
     const uint64_t bytes = numel * h->itemsize;
     const int vec = op == 0 ? 16 : allgather_vec(bytes, nullptr, nullptr);
-    int rc = plan_compute(h->R, bytes, vec, tda::kThreads, h->sm_count, h->blocks_per_sm, plan);
+    int algo = AR_ALGO_ONESHOT, bps = h->bps_ag;
+    if (op == 0) {
+        algo = h->algo == AR_ALGO_AUTO ? choose_algo(h->R, bytes) : h->algo;
+        bps = algo == AR_ALGO_TWOSHOT ? h->bps_two : h->bps_one;
+    }
+    int rc = plan_compute(h->R, bytes, vec, algo, tda::kThreads, h->sm_count, bps, plan);
     if (rc == AR_OK && plan->blocks > h->bmax) {
         plan->blocks = h->bmax;
         plan->max_stages = (plan->tiles + h->bmax - 1) / h->bmax;

@@ -20,6 +20,7 @@ constexpr int kMaxRanks = 8;
 constexpr int kThreads = 256;           // threads per block of the exchange kernels
 constexpr int kFlagStrideWords = 16;    // 16 x 8 B = one 128-byte line per flag
 constexpr uint64_t kSlotAlign = 256;
+constexpr int kTwoShot = -2;            // "unroll" code that selects the two-shot kernel
 
 // Per-(rank, block) counters.  `seq` counts the stages this block has
 // published over all calls (its flag's value at the end of the last call);

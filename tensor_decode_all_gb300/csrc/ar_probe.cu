@@ -12,16 +12,34 @@
 
 namespace {
 
+// Each thread keeps kUnroll independent 16-byte accesses in flight per loop
+// trip: over a long-latency link the bandwidth a kernel sees is bytes in
+// flight / latency.
+constexpr int kUnroll = 8;
+
 __global__ void probe_write_kernel(uint4 *dst, uint64_t nvec) {
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     const uint4 v = make_uint4(0x3c003c00u, blockIdx.x, threadIdx.x, 0x12345678u);
-    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) dst[i] = v;
+    uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + (kUnroll - 1) * stride < nvec; i += kUnroll * stride) {
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) dst[i + k * stride] = v;
+    }
+    for (; i < nvec; i += stride) dst[i] = v;
 }
 
 __global__ void probe_read_kernel(const uint4 *src, uint64_t nvec, unsigned int *sink) {
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     unsigned int x = 0;
-    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+    uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + (kUnroll - 1) * stride < nvec; i += kUnroll * stride) {
+        uint4 v[kUnroll];
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) v[k] = src[i + k * stride];
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) x ^= v[k].x ^ v[k].y ^ v[k].z ^ v[k].w;
+    }
+    for (; i < nvec; i += stride) {
         const uint4 v = src[i];
         x ^= v.x ^ v.y ^ v.z ^ v.w;
     }
@@ -30,7 +48,15 @@ __global__ void probe_read_kernel(const uint4 *src, uint64_t nvec, unsigned int 
 
 __global__ void probe_copy_kernel(uint4 *dst, const uint4 *src, uint64_t nvec) {
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) dst[i] = src[i];
+    uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + (kUnroll - 1) * stride < nvec; i += kUnroll * stride) {
+        uint4 v[kUnroll];
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) v[k] = src[i + k * stride];
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) dst[i + k * stride] = v[k];
+    }
+    for (; i < nvec; i += stride) dst[i] = src[i];
 }
 
 int grid_for(const void *k, int threads) {

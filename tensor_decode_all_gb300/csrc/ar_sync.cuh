@@ -55,39 +55,20 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
     return t;
 }
 
-// 16-byte load that bypasses L1: peer slot data is read once per call and must
-// never come from a line cached by an earlier call.
-__device__ __forceinline__ uint4 ld_cg_v4(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p)
-                 : "memory");
-    return v;
-}
-
-__device__ __forceinline__ uint2 ld_cg_v2(const void *p) {
-    uint2 v;
-    asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
-    return v;
-}
-
+// Loads that bypass L1 (cache at L2 only): peer slot data is read once per
+// call and must never come from a line an earlier call left in L1.  These are
+// plain data loads; their ordering after a peer's release comes from the
+// acquire on the flag and the barrier that follows it.
+__device__ __forceinline__ uint4 ld_cg_v4(const void *p) { return __ldcg(reinterpret_cast<const uint4 *>(p)); }
+__device__ __forceinline__ uint2 ld_cg_v2(const void *p) { return __ldcg(reinterpret_cast<const uint2 *>(p)); }
 __device__ __forceinline__ unsigned int ld_cg_u32(const void *p) {
-    unsigned int v;
-    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
+    return __ldcg(reinterpret_cast<const unsigned int *>(p));
 }
-
 __device__ __forceinline__ unsigned short ld_cg_u16(const void *p) {
-    unsigned short v;
-    asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
-    return v;
+    return __ldcg(reinterpret_cast<const unsigned short *>(p));
 }
-
 __device__ __forceinline__ unsigned char ld_cg_u8(const void *p) {
-    unsigned short v;
-    asm volatile("ld.global.cg.u8 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
-    return (unsigned char)v;
+    return __ldcg(reinterpret_cast<const unsigned char *>(p));
 }
 
 __device__ __forceinline__ unsigned long long *flag_ptr(const DevState &d, int rank, int block) {

@@ -48,19 +48,27 @@ def test_null_handle_calls(lib):
     assert lib.ar_query(None, None) == ar.AR_EINVAL
 
 
+@pytest.mark.parametrize("algo", [ar.AR_ALGO_ONESHOT, ar.AR_ALGO_TWOSHOT])
 @pytest.mark.parametrize("R", [1, 2, 3, 4, 8])
 @pytest.mark.parametrize("vec", [16, 8, 2, 1])
-def test_plan_invariants(lib, R, vec):
+def test_plan_invariants(lib, R, vec, algo):
+    if algo == ar.AR_ALGO_TWOSHOT and vec != 16:
+        with pytest.raises(tda.ArError):
+            tda.ar_plan_compute(R, 4096, vec, algo, 256, 152, 6)
+        return
     sms, bps, threads = 152, 6, 256
     bmax = sms * bps // R
     sizes = [1, 15, 16, 17, 4095, 4096, 8192, 262144, 786432, 1 << 24, (1 << 26) + 12345, 3 << 27]
     for nbytes in sizes:
         if nbytes % vec:
             continue
-        p = tda.ar_plan_compute(R, nbytes, vec, threads, sms, bps)
+        p = tda.ar_plan_compute(R, nbytes, vec, algo, threads, sms, bps)
         nv = -(-nbytes // vec)
-        assert p.threads == threads and p.vec_bytes == vec
-        assert p.unroll in (1, 2)
+        assert p.threads == threads and p.vec_bytes == vec and p.algo == algo
+        if algo == ar.AR_ALGO_TWOSHOT:
+            assert p.unroll == R and p.flag_rounds == 2   # one sub-tile of `threads` vectors per rank
+        else:
+            assert p.unroll in (1, 2) and p.flag_rounds == 1
         assert p.tile_bytes == threads * p.unroll * vec
         # tiles cover the payload, and no tile is empty
         assert p.tiles * threads * p.unroll >= nv > (p.tiles - 1) * threads * p.unroll
@@ -68,27 +76,38 @@ def test_plan_invariants(lib, R, vec):
         assert 1 <= p.blocks <= min(p.tiles, bmax)
         assert R * p.blocks <= sms * bps
         assert p.max_stages == -(-p.tiles // p.blocks)
-        # small payloads: one tile per block, spread as wide as allowed
-        if nv <= bmax * threads:
+        # one-shot, small payloads: one tile per block, spread as wide as allowed
+        if algo == ar.AR_ALGO_ONESHOT and nv <= bmax * threads:
             assert p.unroll == 1 and p.max_stages == 1
 
 
 def test_plan_zero_bytes_and_bad_args(lib):
-    p = tda.ar_plan_compute(2, 0, 16, 256, 152, 6)
+    p = tda.ar_plan_compute(2, 0, 16, ar.AR_ALGO_ONESHOT, 256, 152, 6)
     assert p.blocks == 0 and p.tiles == 0
     with pytest.raises(tda.ArError):
-        tda.ar_plan_compute(9, 16, 16, 256, 152, 6)
+        tda.ar_plan_compute(9, 16, 16, ar.AR_ALGO_ONESHOT, 256, 152, 6)
     with pytest.raises(tda.ArError):
-        tda.ar_plan_compute(2, 16, 3, 256, 152, 6)
+        tda.ar_plan_compute(2, 16, 3, ar.AR_ALGO_ONESHOT, 256, 152, 6)
     with pytest.raises(tda.ArError):
-        tda.ar_plan_compute(8, 16, 16, 256, 1, 1)  # 8 ranks cannot each get a block
+        tda.ar_plan_compute(2, 16, 16, ar.AR_ALGO_AUTO, 256, 152, 6)  # the caller resolves AUTO
+    with pytest.raises(tda.ArError):
+        tda.ar_plan_compute(8, 16, 16, ar.AR_ALGO_ONESHOT, 256, 1, 1)  # 8 ranks cannot each get a block
+
+
+def test_choose_algo_rule(lib):
+    for R in (1, 2, 3):
+        assert tda.ar_choose_algo(R, 1 << 30) == ar.AR_ALGO_ONESHOT
+    for R in (4, 8):
+        assert tda.ar_choose_algo(R, (1 << 20) - 1) == ar.AR_ALGO_ONESHOT
+        assert tda.ar_choose_algo(R, 1 << 20) == ar.AR_ALGO_TWOSHOT
+    assert tda.ar_set_algo(0, ar.AR_ALGO_ONESHOT) == ar.AR_EINVAL
 
 
 def test_struct_layouts_match_header(lib):
-    # ar_error_info: 4 x int32 + 2 x uint64; ar_info: 8 x int32 + 4 x uint64; ar_plan: 4 x int32 + 3 x uint64
+    # ar_error_info: 4 x int32 + 2 x uint64; ar_info: 12 x int32 + 4 x uint64; ar_plan: 6 x int32 + 3 x uint64
     assert ctypes.sizeof(ar.ErrorInfo) == 32
-    assert ctypes.sizeof(ar.Info) == 64
-    assert ctypes.sizeof(ar.Plan) == 40
+    assert ctypes.sizeof(ar.Info) == 80
+    assert ctypes.sizeof(ar.Plan) == 48
 
 
 def test_no_cpu_fallback_when_library_missing(monkeypatch, tmp_path):

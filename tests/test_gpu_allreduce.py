@@ -25,10 +25,12 @@ def _handle(R, dtype, max_numel, slots):
     return tda.Handle(R, {"f16": torch.float16, "bf16": torch.bfloat16}[dtype], max_numel, slots)
 
 
-def _run_once(R, dtype, numel, slots, dist="uniform", config=5, call=0, h=None):
+def _run_once(R, dtype, numel, slots, dist="uniform", config=5, call=0, h=None, algo=None):
     xs = inputs.allreduce_inputs(config, R, numel, dtype, dist, call)
     own = h is None
     h = h or _handle(R, dtype, max(numel, 1), slots)
+    if algo is not None:
+        h.set_algo(algo)
     streams = rank_streams(R)
     ins = [to_dev(x, dtype) for x in xs]
     outs = [torch.empty_like(t) for t in ins]
@@ -76,6 +78,36 @@ def test_ranks_dtypes_slots(R, dtype, slots):
 def test_edge_sizes(numel):
     _run_once(4, "bf16", numel, "hbm")
     _run_once(2, "f16", numel, "pinned")
+    _run_once(8, "bf16", numel, "hbm", algo="twoshot")
+    _run_once(5, "f16", numel, "pinned", algo="twoshot")
+
+
+@pytest.mark.parametrize("slots", ["pinned", "hbm"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 6, 8])
+def test_twoshot_forced(R, dtype, slots):
+    """The two-shot form reduces each sub-tile once, in rank order, on one
+    rank: the same bits as the oracle (several stages, ragged tail)."""
+    _run_once(R, dtype, 256 * 8 * R * 5 + 3, slots, algo="twoshot")
+
+
+def test_auto_picks_twoshot_at_16MiB_r8():
+    import tensor_decode_all_gb300 as tda
+    R, n = 8, 8 << 20
+    h = _handle(R, "bf16", n, "hbm")
+    assert h.plan("allreduce", n).algo == tda.ar.AR_ALGO_TWOSHOT
+    assert h.plan("allreduce", 4096).algo == tda.ar.AR_ALGO_ONESHOT
+    _run_once(R, "bf16", n, "hbm", h=h)
+    h.destroy()
+
+
+def test_oneshot_then_twoshot_on_one_handle():
+    """Switching forms between calls keeps the counters and flags consistent."""
+    R, n = 4, 300001
+    h = _handle(R, "f16", n, "hbm")
+    for k, algo in enumerate(["oneshot", "twoshot", "twoshot", "oneshot", "twoshot"]):
+        _run_once(R, "f16", n, "hbm", call=k, h=h, algo=algo)
+    h.destroy()
 
 
 def test_max_numel_exactly_and_one_over():
@@ -144,10 +176,12 @@ def test_config3_r8_bf16_hbm_graph():
     h.destroy()
 
 
-def test_in_place():
+@pytest.mark.parametrize("algo", ["oneshot", "twoshot"])
+def test_in_place(algo):
     R, n, dtype = 4, 70001, "bf16"
     xs = inputs.allreduce_inputs(5, R, n, dtype, "uniform", 7)
     h = _handle(R, dtype, n, "hbm")
+    h.set_algo(algo)
     bufs = [to_dev(x, dtype) for x in xs]
     enqueue(h, "allreduce", bufs, bufs, rank_streams(R))
     torch.cuda.synchronize()

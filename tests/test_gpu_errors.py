@@ -165,12 +165,17 @@ def test_query_and_plan():
     h = tda.Handle(8, torch.bfloat16, 393216, "hbm")
     info = h.info()
     assert info.R == 8 and info.max_blocks >= 1
-    assert info.max_blocks * 8 <= info.sm_count * info.blocks_per_sm
+    bps = (info.blocks_per_sm, info.blocks_per_sm_twoshot, info.blocks_per_sm_allgather)
+    assert min(bps) >= 1
+    assert info.max_blocks * 8 <= info.sm_count * max(bps)
     assert info.slot_bytes == 393216 * 2
     assert info.total_slot_bytes == 2 * 8 * info.slot_bytes
     p = h.plan("allreduce", 393216)
-    assert 1 <= p.blocks <= info.max_blocks
+    assert p.algo == 0 and 1 <= p.blocks and p.blocks * 8 <= info.sm_count * info.blocks_per_sm
     assert p.tiles * p.tile_bytes >= 393216 * 2
+    h.set_algo("twoshot")
+    p = h.plan("allreduce", 393216)
+    assert p.algo == 1 and p.flag_rounds == 2 and p.blocks * 8 <= info.sm_count * info.blocks_per_sm_twoshot
     h.destroy()
 
 
