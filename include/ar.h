@@ -114,7 +114,7 @@ typedef struct ar_info {
     int32_t blocks_per_sm_twoshot;   /* ... of the two-shot all-reduce kernels */
     int32_t blocks_per_sm_allgather; /* ... of the allgather kernels */
     int32_t algo;           /* AR_ALGO_AUTO unless forced with ar_set_algo */
-    int32_t reserved;
+    int32_t pdl;            /* 1 if calls launch as programmatic dependents (ar_set_pdl) */
     uint64_t max_numel;
     uint64_t slot_bytes;    /* bytes of one (parity, rank) slot, a multiple of 256 */
     uint64_t total_slot_bytes; /* 2 * R * slot_bytes: the allocation that cannot grow */
@@ -255,6 +255,16 @@ AR_API int ar_plan_compute(int R, uint64_t bytes, int vec_bytes, int algo, int t
  * two-shot for R >= 4 and bytes >= 1 MiB, one-shot otherwise.  Pure host
  * arithmetic. */
 AR_API int ar_choose_algo(int R, uint64_t bytes);
+
+/* Launch this handle's kernels as programmatic dependents of the preceding
+ * work on their stream (CUDA programmatic dependent launch), so that a rank's
+ * next kernel is scheduled while its current one finishes.  Each kernel still
+ * waits for the preceding kernel to complete, and for its writes to be
+ * visible, before it reads or writes any memory, and releases its dependents
+ * only after its last write; the bits do not change.  Off by default; the
+ * environment variable AR_PDL=1 sets it at ar_create.  Applies to calls
+ * enqueued (or captured) afterwards. */
+AR_API int ar_set_pdl(ar_handle *h, int enable);
 
 /* Force the all-reduce form of a handle (AR_ALGO_AUTO restores the rule).  The
  * environment variable AR_ALGO=oneshot|twoshot sets it at ar_create.  Every

@@ -46,7 +46,7 @@ class Info(ctypes.Structure):
                 ("device", ctypes.c_int32), ("threads", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
                 ("sm_count", ctypes.c_int32), ("blocks_per_sm", ctypes.c_int32),
                 ("blocks_per_sm_twoshot", ctypes.c_int32), ("blocks_per_sm_allgather", ctypes.c_int32),
-                ("algo", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("algo", ctypes.c_int32), ("pdl", ctypes.c_int32),
                 ("max_numel", ctypes.c_uint64), ("slot_bytes", ctypes.c_uint64),
                 ("total_slot_bytes", ctypes.c_uint64), ("timeout_ns", ctypes.c_uint64)]
 
@@ -93,6 +93,7 @@ def lib():
             L.ar_plan_compute.argtypes = [i32, u64, i32, i32, i32, i32, i32, ctypes.POINTER(Plan)]
             L.ar_choose_algo.argtypes = [i32, u64]
             L.ar_set_algo.argtypes = [vp, i32]
+            L.ar_set_pdl.argtypes = [vp, i32]
             L.ar_strerror.argtypes = [i32]
             L.ar_strerror.restype = ctypes.c_char_p
             L.ar_probe_host_link.argtypes = [u64, i32, ctypes.POINTER(ctypes.c_double)]
@@ -174,6 +175,10 @@ def ar_choose_algo(R: int, nbytes: int) -> int:
 
 def ar_set_algo(h: int, algo: int) -> int:
     return lib().ar_set_algo(h, algo)
+
+
+def ar_set_pdl(h: int, enable: bool) -> int:
+    return lib().ar_set_pdl(h, 1 if enable else 0)
 
 
 def strerror(code: int) -> str:
@@ -285,6 +290,11 @@ class Handle:
         rc = ar_set_algo(self.ptr, code)
         if rc:
             raise ArError(rc, "ar_set_algo")
+
+    def set_pdl(self, enable: bool) -> None:
+        rc = ar_set_pdl(self.ptr, enable)
+        if rc:
+            raise ArError(rc, "ar_set_pdl")
 
     def info(self) -> Info:
         return ar_query(self.ptr)

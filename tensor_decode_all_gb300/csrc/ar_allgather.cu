@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(kThreads)
     const uint64_t ntiles = (nv + kTileVecs - 1) / kTileVecs;
     const uint64_t nstages = ntiles > (uint64_t)b ? (ntiles - b + B - 1) / B : 0;
 
+    pdl_wait();
     if (tid == 0) {
         const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
         s_seq = c.seq;
@@ -132,6 +133,7 @@ __global__ void __launch_bounds__(kThreads)
         c.calls = s_calls + 1;
         d.ctr[(size_t)rank * d.bmax + b] = c;
     }
+    pdl_trigger();
 }
 
 template <int VW, int U>
@@ -169,7 +171,7 @@ const void *allgather_kernel_ptr(int vec_bytes, int R, int unroll) {
 
 cudaError_t launch_allgather(int vec_bytes, int R, int unroll, int blocks, cudaStream_t s,
                              const void *in, void *out, uint64_t bytes, int rank,
-                             const DevState &d) {
+                             const DevState &d, bool pdl) {
     const void *k = allgather_kernel_ptr(vec_bytes, R, unroll);
     if (!k) return cudaErrorInvalidValue;
     const uint8_t *a0 = static_cast<const uint8_t *>(in);
@@ -178,7 +180,7 @@ cudaError_t launch_allgather(int vec_bytes, int R, int unroll, int blocks, cudaS
     int a3 = rank;
     DevState a4 = d;
     void *args[] = {&a0, &a1, &a2, &a3, &a4};
-    return cudaLaunchKernel(k, dim3(blocks), dim3(kThreads), args, 0, s);
+    return launch(k, blocks, s, args, pdl);
 }
 
 }  // namespace tda

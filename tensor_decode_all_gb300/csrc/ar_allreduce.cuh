@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(kThreads)
     const uint64_t ntiles = (nv + kTileVecs - 1) / kTileVecs;
     const uint64_t nstages = ntiles > (uint64_t)b ? (ntiles - b + B - 1) / B : 0;
 
+    pdl_wait();
     if (tid == 0) {
         const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
         s_seq = c.seq;
@@ -222,6 +223,7 @@ __global__ void __launch_bounds__(kThreads)
         c.calls = s_calls + 1;
         d.ctr[(size_t)rank * d.bmax + b] = c;
     }
+    pdl_trigger();
 }
 
 // Two-shot variant, for large payloads at R >= 4, where the one-shot form's
@@ -256,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     const uint64_t ntiles = (nv + kTileVecs - 1) / kTileVecs;
     const uint64_t nstages = ntiles > (uint64_t)b ? (ntiles - b + B - 1) / B : 0;
 
+    pdl_wait();
     if (tid == 0) {
         const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
         s_seq = c.seq;
@@ -324,6 +327,7 @@ __global__ void __launch_bounds__(kThreads, 4)
         c.calls = s_calls + 1;
         d.ctr[(size_t)rank * d.bmax + b] = c;
     }
+    pdl_trigger();
 }
 
 }  // namespace tda

@@ -26,6 +26,7 @@ struct ar_handle {
     int bps_one = 0, bps_two = 0, bps_ag = 0;  // occupancy per kernel family
     int bmax = 0;                              // flag/counter slots per rank
     int algo = AR_ALGO_AUTO;
+    bool pdl = false;                          // launch as programmatic dependents
     void *slots_host = nullptr;            // pinned kind: host address of the slots
     uint8_t *slots_dev = nullptr;          // device address of the slots
     void *flags_host = nullptr;            // pinned kind: host address of the flags
@@ -304,6 +305,7 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
     if (cudaGetDevice(&h->device) != cudaSuccess) return fail(AR_ECUDA);
     if (cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess)
         return fail(AR_ECUDA);
+    if (const char *e = std::getenv("AR_PDL")) h->pdl = e[0] == '1';
     if (const char *e = std::getenv("AR_ALGO")) {
         if (!std::strcmp(e, "oneshot")) h->algo = AR_ALGO_ONESHOT;
         else if (!std::strcmp(e, "twoshot")) h->algo = AR_ALGO_TWOSHOT;
@@ -363,7 +365,7 @@ AR_API int ar_allreduce(ar_handle *h, int rank, const void *in, void *out, size_
     int blocks = plan.blocks < h->bmax ? plan.blocks : h->bmax;
     const int variant = algo == AR_ALGO_TWOSHOT ? tda::kTwoShot : plan.unroll;
     const cudaError_t e = tda::launch_allreduce(h->dtype, h->R, variant, blocks, s, in, out,
-                                                numel, rank, dev_state(h));
+                                                numel, rank, dev_state(h), h->pdl);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return AR_ECUDA;
@@ -385,7 +387,7 @@ AR_API int ar_allgather(ar_handle *h, int rank, const void *in, void *out, size_
     if (rc != AR_OK) return rc;
     int blocks = plan.blocks < h->bmax ? plan.blocks : h->bmax;
     const cudaError_t e = tda::launch_allgather(vw, h->R, plan.unroll, blocks, s, in, out, bytes,
-                                                rank, dev_state(h));
+                                                rank, dev_state(h), h->pdl);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return AR_ECUDA;
@@ -445,7 +447,7 @@ AR_API int ar_query(const ar_handle *h, ar_info *info) {
     info->blocks_per_sm_twoshot = h->bps_two;
     info->blocks_per_sm_allgather = h->bps_ag;
     info->algo = h->algo;
-    info->reserved = 0;
+    info->pdl = h->pdl ? 1 : 0;
     info->max_numel = h->max_numel;
     info->slot_bytes = h->slot_bytes;
     info->total_slot_bytes = 2ull * (uint64_t)h->R * h->slot_bytes;
@@ -459,6 +461,12 @@ AR_API int ar_plan_compute(int R, uint64_t bytes, int vec_bytes, int algo, int t
 }
 
 AR_API int ar_choose_algo(int R, uint64_t bytes) { return choose_algo(R, bytes); }
+
+AR_API int ar_set_pdl(ar_handle *h, int enable) {
+    if (!h) return AR_EINVAL;
+    h->pdl = enable != 0;
+    return AR_OK;
+}
 
 AR_API int ar_set_algo(ar_handle *h, int algo) {
     if (!h || (algo != AR_ALGO_AUTO && algo != AR_ALGO_ONESHOT && algo != AR_ALGO_TWOSHOT)) return AR_EINVAL;
@@ -497,7 +505,7 @@ const void *allreduce_kernel_ptr(int dtype, int R, int unroll) {
 
 cudaError_t launch_allreduce(int dtype, int R, int unroll, int blocks, cudaStream_t s,
                              const void *in, void *out, uint64_t numel, int rank,
-                             const DevState &d) {
+                             const DevState &d, bool pdl) {
     const void *k = allreduce_kernel_ptr(dtype, R, unroll);
     if (!k) return cudaErrorInvalidValue;
     const uint16_t *a0 = static_cast<const uint16_t *>(in);
@@ -506,7 +514,23 @@ cudaError_t launch_allreduce(int dtype, int R, int unroll, int blocks, cudaStrea
     int a3 = rank;
     DevState a4 = d;
     void *args[] = {&a0, &a1, &a2, &a3, &a4};
-    return cudaLaunchKernel(k, dim3(blocks), dim3(kThreads), args, 0, s);
+    return launch(k, blocks, s, args, pdl);
+}
+
+cudaError_t launch(const void *k, int blocks, cudaStream_t s, void **args, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelExC(&cfg, k, args);
 }
 
 }  // namespace tda

@@ -44,13 +44,17 @@ struct DevState {
     int sys_scope;             // 1: slots/flags in host memory, system-scope ordering
 };
 
+// Launch kernel k with `blocks` x kThreads on s; with pdl, as a programmatic
+// dependent of the preceding work on s.
+cudaError_t launch(const void *k, int blocks, cudaStream_t s, void **args, bool pdl);
+
 // Launchers (one per kernel family).  Return cudaSuccess or the launch error.
 cudaError_t launch_allreduce(int dtype, int R, int unroll, int blocks, cudaStream_t s,
                              const void *in, void *out, uint64_t numel, int rank,
-                             const DevState &d);
+                             const DevState &d, bool pdl);
 cudaError_t launch_allgather(int vec_bytes, int R, int unroll, int blocks, cudaStream_t s,
                              const void *in, void *out, uint64_t bytes, int rank,
-                             const DevState &d);
+                             const DevState &d, bool pdl);
 
 // Kernel entry addresses, for occupancy queries.
 const void *allreduce_kernel_ptr(int dtype, int R, int unroll);

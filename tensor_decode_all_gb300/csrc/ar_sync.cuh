@@ -71,6 +71,15 @@ __device__ __forceinline__ unsigned char ld_cg_u8(const void *p) {
     return __ldcg(reinterpret_cast<const unsigned char *>(p));
 }
 
+// Programmatic dependent launch.  When a rank's next call is launched with the
+// programmatic-serialization attribute, its blocks may become resident before
+// this call ends.  Each kernel therefore waits (griddepcontrol.wait: the
+// preceding kernel has completed and its memory is visible) before it touches
+// any memory, and lets its dependents start only after its last write.  Both
+// instructions do nothing when the launch has no programmatic dependency.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ unsigned long long *flag_ptr(const DevState &d, int rank, int block) {
     return d.flags + ((size_t)rank * d.bmax + block) * kFlagStrideWords;
 }
