@@ -271,6 +271,36 @@ AR_API int ar_set_pdl(ar_handle *h, int enable);
  * rank of a call must see the same setting; set it before enqueuing. */
 AR_API int ar_set_algo(ar_handle *h, int algo);
 
+/*
+ * ar_allreduce_noalloc -- an all-reduce that allocates nothing.  The paper has
+ * no counterpart: this entry point is for callers that cannot allocate device
+ * memory where they reduce -- code running inside another library's memory
+ * pool or arena, which owns every allocation on the device; code on a
+ * latency-critical path where cudaMalloc, which can synchronise the device,
+ * is not allowed; runtimes that reserve all memory once at start-up.
+ *
+ * One call reduces all R ranks (1 <= R <= 8) at once: ins[r] and outs[r]
+ * (host arrays of R device pointers, each 16-byte aligned, owned by the
+ * caller) hold rank r's numel elements of dtype (AR_F16 or AR_BF16); every
+ * outs[r] receives the same bits as ar_allreduce: the rank-order fp32 sum with
+ * one rounding.  outs[r] == ins[r] is allowed.
+ * Working memory: the exchange slots (R ranks x at most 1 MiB), per-block flags
+ * and an abort word live in one file-scope device array of 8 MiB + 64 KiB +
+ * 256 B, which every GPU that loads this library holds until the process
+ * exits.  The call allocates nothing.  numel > 524288 (more than 1 MiB per
+ * rank) returns AR_ETOOBIG and enqueues nothing.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and the kernels' occupancy; make that first call
+ * before any stream capture.  Each call clears the flags (cudaMemsetAsync on
+ * `stream`) and then launches one cooperative grid of blocks x R on `stream`,
+ * so all R ranks' blocks are resident together.  Every call shares the array
+ * and it keeps the last call's contents: calls that overlap on the GPU (on
+ * streams with no ordering between them) race and give undefined results.
+ * Errors: AR_EINVAL, AR_ETOOBIG, AR_ECUDA.
+ */
+AR_API int ar_allreduce_noalloc(int R, int dtype, const void *const *ins, void *const *outs, size_t numel,
+                                ar_stream_t stream);
+
 /* Human-readable name of an ar_code.  Never NULL. */
 AR_API const char *ar_strerror(int code);
 

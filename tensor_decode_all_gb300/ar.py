@@ -94,6 +94,8 @@ def lib():
             L.ar_choose_algo.argtypes = [i32, u64]
             L.ar_set_algo.argtypes = [vp, i32]
             L.ar_set_pdl.argtypes = [vp, i32]
+            L.ar_allreduce_noalloc.argtypes = [i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, vp]
+            L.ar_allreduce_noalloc.restype = i32
             L.ar_strerror.argtypes = [i32]
             L.ar_strerror.restype = ctypes.c_char_p
             L.ar_probe_host_link.argtypes = [u64, i32, ctypes.POINTER(ctypes.c_double)]
@@ -125,6 +127,13 @@ def ar_allreduce(h: int, rank: int, inp: int, out: int, numel: int, stream: int)
 
 def ar_allgather(h: int, rank: int, inp: int, out: int, numel: int, stream: int) -> int:
     return lib().ar_allgather(h, rank, inp, out, numel, stream)
+
+
+def ar_allreduce_noalloc(R: int, dtype: int, ins, outs, numel: int, stream: int) -> int:
+    """All R ranks in one call, with no allocation (ins/outs: R device pointers)."""
+    arr_in = (ctypes.c_void_p * R)(*[int(p) for p in ins])
+    arr_out = (ctypes.c_void_p * R)(*[int(p) for p in outs])
+    return lib().ar_allreduce_noalloc(R, dtype, arr_in, arr_out, numel, stream)
 
 
 def ar_status(h: int) -> ErrorInfo:
