@@ -261,8 +261,8 @@ AR_API int ar_choose_algo(int R, uint64_t bytes);
  * next kernel is scheduled while its current one finishes.  Each kernel still
  * waits for the preceding kernel to complete, and for its writes to be
  * visible, before it reads or writes any memory, and releases its dependents
- * only after its last write; the bits do not change.  Off by default; the
- * environment variable AR_PDL=1 sets it at ar_create.  Applies to calls
+ * only after its last write; the bits do not change.  On by default; the
+ * environment variable AR_PDL=0 turns it off at ar_create.  Applies to calls
  * enqueued (or captured) afterwards. */
 AR_API int ar_set_pdl(ar_handle *h, int enable);
 

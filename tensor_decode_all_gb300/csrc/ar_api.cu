@@ -26,7 +26,7 @@ struct ar_handle {
     int bps_one = 0, bps_two = 0, bps_ag = 0;  // occupancy per kernel family
     int bmax = 0;                              // flag/counter slots per rank
     int algo = AR_ALGO_AUTO;
-    bool pdl = false;                          // launch as programmatic dependents
+    bool pdl = true;                           // launch as programmatic dependents
     void *slots_host = nullptr;            // pinned kind: host address of the slots
     uint8_t *slots_dev = nullptr;          // device address of the slots
     void *flags_host = nullptr;            // pinned kind: host address of the flags
@@ -305,7 +305,7 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
     if (cudaGetDevice(&h->device) != cudaSuccess) return fail(AR_ECUDA);
     if (cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess)
         return fail(AR_ECUDA);
-    if (const char *e = std::getenv("AR_PDL")) h->pdl = e[0] == '1';
+    if (const char *e = std::getenv("AR_PDL")) h->pdl = e[0] != '0';
     if (const char *e = std::getenv("AR_ALGO")) {
         if (!std::strcmp(e, "oneshot")) h->algo = AR_ALGO_ONESHOT;
         else if (!std::strcmp(e, "twoshot")) h->algo = AR_ALGO_TWOSHOT;
