@@ -51,6 +51,13 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sweep", default=None, help="run the payload sweep; write JSON lines to this file")
     ap.add_argument("--sweep-calls", type=int, default=1000)
+    ap.add_argument("--sweep-both", action="store_true",
+                    help="in the sweep, run both all-reduce forms where they compete (R >= 3, 64 KiB..8 MiB)")
+    ap.add_argument("--sweep-slots", default="hbm,pinned")
+    ap.add_argument("--sweep-dtypes", default="f16,bf16")
+    ap.add_argument("--sweep-ranks", default="2,4,8")
+    ap.add_argument("--sweep-min-kib", type=int, default=2)
+    ap.add_argument("--sweep-max-kib", type=int, default=65536)
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", default=None, choices=sorted(PROFILE_WORKLOADS),
@@ -157,6 +164,32 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- measurement
+
+KERNEL_SOURCES = ("ar_allreduce.cuh", "ar_sync.cuh", "ar_internal.h", "ar_allreduce_f16.cu", "ar_allreduce_bf16.cu")
+
+
+def kernel_source_sha256() -> str:
+    """Hash of the sources the all-reduce kernels are compiled from."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "tensor_decode_all_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(name: str):
+    """DRAM and host-link bytes per call of a workload, from the committed ncu
+    summary (profiles/traffic.json), or None if the kernels changed since."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    if t.get("kernel_source_sha256") != kernel_source_sha256():
+        return None
+    return t.get("workloads", {}).get(name)
+
 
 def measured_peaks():
     try:
@@ -295,15 +328,21 @@ class Workload:
         self.h.destroy()
 
 
-def algo_bytes(op, R, S, slots):
+def algo_bytes(op, R, S, slots, algo=None):
     """Algorithmic bytes of one call (all R ranks).
 
-    pinned-host all-reduce: host-link writes W = R*S (each rank publishes once),
-      reads Rd = R*(R-1)*S (each rank fetches every peer's chunk);
-    HBM all-reduce: DRAM 4*R*S (inputs, slot writes, slot reads once, outputs);
+    pinned-host all-reduce, one-shot: host-link writes W = R*S (each rank
+      publishes once), reads Rd = R*(R-1)*S (each rank fetches every peer's chunk);
+    pinned-host all-reduce, two-shot: W = R*S published + S of reduced results,
+      Rd = R*S (every rank reads its sub-tile from all R slots) + (R-1)*S
+      (every rank reads the R-1 other reduced sub-tiles);
+    HBM all-reduce (either form): DRAM 4*R*S (inputs, slot writes, slot reads
+      once, outputs);
     allgather: HBM R*S + R*S + R*S + R*R*S; pinned W = R*S, Rd = R*(R-1)*S.
     """
     if slots == "pinned":
+        if op == "allreduce" and algo == "twoshot":
+            return {"link_write": (R + 1) * S, "link_read": (2 * R - 1) * S}
         return {"link_write": R * S, "link_read": R * (R - 1) * S}
     if op == "allreduce":
         return {"dram": 4 * R * S}
@@ -319,8 +358,8 @@ def link_floor_s(W, Rd, link):
     return max(W / (link["write_gbs"] * gb), Rd / (link["read_gbs"] * gb), (W + Rd) / both)
 
 
-def roofline(op, R, S, slots, t_call_s, link, hbm_gbs):
-    b = algo_bytes(op, R, S, slots)
+def roofline(op, R, S, slots, t_call_s, link, hbm_gbs, algo=None):
+    b = algo_bytes(op, R, S, slots, algo)
     if slots == "pinned":
         W, Rd = b["link_write"], b["link_read"]
         t_min = link_floor_s(W, Rd, link)
@@ -349,7 +388,7 @@ def summarize(op, R, dtype, numel, slots, ms_steps, C, link, hbm_gbs, algo=None)
             "algbw_gbs": round(out_bytes / t_call / 1e9, 3),
             "busbw_gbs": round(S / t_call / 1e9 * ((2 * (R - 1) / R) if op == "allreduce" else (R - 1) / R), 3)
             if R > 1 else None,
-            "roofline": roofline(op, R, S, slots, t_call, link, hbm_gbs), "calls": len(ms_steps) * C}
+            "roofline": roofline(op, R, S, slots, t_call, link, hbm_gbs, algo), "calls": len(ms_steps) * C}
 
 
 def cpu_baseline(R, dtype, numel, seconds=10.0, config=2, dist="normal4"):
@@ -397,6 +436,12 @@ def run_ours(args, dist):
     checked += w.check(calls=(0, -1))
     total_s = dist.max(sum(ms) * 1e-3)
     head = summarize("allreduce", R, "f16", numel, "pinned", ms, C, link, hbm_gbs, w.algo)
+    prof = profiled_traffic("r2_fp16_256KiB_pinned")
+    if prof:
+        head["roofline"]["traffic"] = prof["dram_bytes_per_call"]
+        head["roofline"]["link_traffic"] = {"read": prof["link_read_bytes_per_call"],
+                                            "write": prof["link_write_bytes_per_call"],
+                                            "source": prof["source"]}
     S = numel * 2
     n = dist.world
     value = n * S * len(ms) * C / total_s / 1e9
@@ -427,6 +472,9 @@ def run_ours(args, dist):
             msx = wx.time_graph(st, 2, flush)
             wx.check(calls=(-1,))
             extras[name] = summarize(op, RR, dt, nn, sl, msx, cc, link, hbm_gbs, wx.algo)
+            prof = profiled_traffic(name)
+            if prof:
+                extras[name]["roofline"]["traffic"] = prof["dram_bytes_per_call"]
             wx.close()
 
     line = {
@@ -532,31 +580,38 @@ def run_sweep(args, dist):
     hbm_gbs = float(peaks.get("hbm_gbs", 6800.0))
     link = tda.ar_probe_host_link(64 << 20, 10)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    cells = []
+    for slots in args.sweep_slots.split(","):
+        for dtype in args.sweep_dtypes.split(","):
+            for R in [int(x) for x in args.sweep_ranks.split(",")]:
+                for k in range(11, 27):
+                    S = 1 << k
+                    if not (args.sweep_min_kib << 10) <= S <= (args.sweep_max_kib << 10):
+                        continue
+                    both = args.sweep_both and R >= 3 and (64 << 10) <= S <= (8 << 20)
+                    for algo in (("oneshot", "twoshot") if both else (None,)):
+                        cells.append((slots, dtype, R, S, algo))
     with open(args.sweep, "w") as f:
-        for slots in ("hbm", "pinned"):
-            for dtype in ("f16", "bf16"):
-                for R in (2, 4, 8):
-                    for k in range(11, 27):
-                        S = 1 << k
-                        numel = S // 2
-                        total = args.sweep_calls
-                        if slots == "pinned" and R * S >= (64 << 20):
-                            total = min(total, 100)  # ~20 ms per call over the host link: bound the wall time
-                        C = max(1, min(100, (256 << 20) // max(1, R * S * 2)))
-                        steps = max(1, total // C)
-                        w = Workload("allreduce", R, dtype, numel, slots, C, config=5, dist="uniform")
-                        w.capture()
-                        w.time_graph(1, 0, flush)
-                        w.check(calls=(0, -1))
-                        ms = w.time_graph(steps, 2, flush)
-                        w.check(calls=(0, -1))
-                        row = summarize("allreduce", R, dtype, numel, slots, ms, C, link, hbm_gbs, w.algo)
-                        row["parity"] = "bit-exact (first and last call)"
-                        f.write(json.dumps(row) + "\n")
-                        f.flush()
-                        w.close()
-                        print(f"{slots:6s} {dtype:4s} R={R} S={S:>9d}: {row['us_per_call']:9.2f} us/call "
-                              f"{row['algbw_gbs']:9.2f} GB/s frac={row['roofline']['frac']}", flush=True)
+        for slots, dtype, R, S, algo in cells:
+            numel = S // 2
+            total = args.sweep_calls
+            if slots == "pinned" and R * S >= (64 << 20):
+                total = min(total, 100)  # ~20 ms per call over the host link: bound the wall time
+            C = max(1, min(100, (256 << 20) // max(1, R * S * 2)))
+            steps = max(1, total // C)
+            w = Workload("allreduce", R, dtype, numel, slots, C, config=5, dist="uniform", algo=algo)
+            w.capture()
+            w.time_graph(1, 0, flush)
+            w.check(calls=(0, -1))
+            ms = w.time_graph(steps, 2, flush)
+            w.check(calls=(0, -1))
+            row = summarize("allreduce", R, dtype, numel, slots, ms, C, link, hbm_gbs, w.algo)
+            row["parity"] = "bit-exact (first and last call)"
+            f.write(json.dumps(row) + "\n")
+            f.flush()
+            w.close()
+            print(f"{slots:6s} {dtype:4s} R={R} S={S:>9d} {w.algo:8s}: {row['us_per_call']:9.2f} us/call "
+                  f"{row['algbw_gbs']:9.2f} GB/s frac={row['roofline']['frac']}", flush=True)
     return None
 
 
