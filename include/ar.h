@@ -251,10 +251,13 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan);
 AR_API int ar_plan_compute(int R, uint64_t bytes, int vec_bytes, int algo, int threads, int sm_count,
                            int blocks_per_sm, ar_plan *plan);
 
-/* The all-reduce form AR_ALGO_AUTO picks for R ranks and `bytes` per rank:
- * two-shot for R >= 4 and bytes >= 1 MiB, one-shot otherwise.  Pure host
- * arithmetic. */
-AR_API int ar_choose_algo(int R, uint64_t bytes);
+/* The all-reduce form AR_ALGO_AUTO picks for R ranks, `bytes` per rank and a
+ * slot kind (a tactic table measured on a GB300): one-shot for R <= 3;
+ * two-shot from 512 KiB (R >= 8) or 2 MiB (R = 4..7) with HBM slots, and from
+ * 64 KiB (R >= 8) or 256 KiB (R = 4..7) with pinned-host slots, where one-shot
+ * reads R(R-1)S bytes over the host link against two-shot's (2R-1)S.  Pure
+ * host arithmetic. */
+AR_API int ar_choose_algo(int R, uint64_t bytes, int slot_kind);
 
 /* Launch this handle's kernels as programmatic dependents of the preceding
  * work on their stream (CUDA programmatic dependent launch), so that a rank's

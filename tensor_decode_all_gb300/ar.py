@@ -91,7 +91,7 @@ def lib():
             L.ar_query.argtypes = [vp, ctypes.POINTER(Info)]
             L.ar_plan_for.argtypes = [vp, i32, sz, ctypes.POINTER(Plan)]
             L.ar_plan_compute.argtypes = [i32, u64, i32, i32, i32, i32, i32, ctypes.POINTER(Plan)]
-            L.ar_choose_algo.argtypes = [i32, u64]
+            L.ar_choose_algo.argtypes = [i32, u64, i32]
             L.ar_set_algo.argtypes = [vp, i32]
             L.ar_set_pdl.argtypes = [vp, i32]
             L.ar_allreduce_noalloc.argtypes = [i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, vp]
@@ -178,8 +178,8 @@ def ar_plan_compute(R, nbytes, vec_bytes, algo, threads, sm_count, blocks_per_sm
     return p
 
 
-def ar_choose_algo(R: int, nbytes: int) -> int:
-    return lib().ar_choose_algo(R, nbytes)
+def ar_choose_algo(R: int, nbytes: int, slot_kind: int) -> int:
+    return lib().ar_choose_algo(R, nbytes, slot_kind)
 
 
 def ar_set_algo(h: int, algo: int) -> int:

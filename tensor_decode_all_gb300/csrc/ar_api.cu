@@ -176,8 +176,19 @@ int handle_occupancy(ar_handle *h) {
     return AR_OK;
 }
 
-int choose_algo(int R, uint64_t bytes) {
-    return (R >= 4 && bytes >= (1ull << 20)) ? AR_ALGO_TWOSHOT : AR_ALGO_ONESHOT;
+// Measured on a GB300 (one-shot vs two-shot, bf16, 64 KiB..8 MiB per rank):
+// in HBM two-shot wins from 512 KiB at R = 8 and from about 2 MiB at R = 4;
+// over the host link, where one-shot reads R(R-1)S bytes against two-shot's
+// (2R-1)S, it wins from 64 KiB at R = 8 and from 256 KiB at R = 4.  Ranks in
+// between take the threshold of the smaller measured R; R <= 3 stays one-shot.
+int choose_algo(int R, uint64_t bytes, int slot_kind) {
+    if (R < 4) return AR_ALGO_ONESHOT;
+    uint64_t threshold;
+    if (slot_kind == AR_SLOT_PINNED_HOST)
+        threshold = R >= 8 ? (64ull << 10) : (256ull << 10);
+    else
+        threshold = R >= 8 ? (512ull << 10) : (2ull << 20);
+    return bytes >= threshold ? AR_ALGO_TWOSHOT : AR_ALGO_ONESHOT;
 }
 
 int plan_compute(int R, uint64_t bytes, int vec, int algo, int threads, int sms, int bps, ar_plan *p) {
@@ -357,7 +368,7 @@ AR_API int ar_allreduce(ar_handle *h, int rank, const void *in, void *out, size_
     int rc = begin_call(h, rank, in, out, numel, s, &call);
     if (rc != AR_OK || numel == 0) return rc;
     const uint64_t bytes = numel * h->itemsize;
-    const int algo = h->algo == AR_ALGO_AUTO ? choose_algo(h->R, bytes) : h->algo;
+    const int algo = h->algo == AR_ALGO_AUTO ? choose_algo(h->R, bytes, h->kind) : h->algo;
     ar_plan plan;
     rc = plan_compute(h->R, bytes, 16, algo, tda::kThreads, h->sm_count,
                       algo == AR_ALGO_TWOSHOT ? h->bps_two : h->bps_one, &plan);
@@ -460,7 +471,7 @@ AR_API int ar_plan_compute(int R, uint64_t bytes, int vec_bytes, int algo, int t
     return plan_compute(R, bytes, vec_bytes, algo, threads, sm_count, blocks_per_sm, plan);
 }
 
-AR_API int ar_choose_algo(int R, uint64_t bytes) { return choose_algo(R, bytes); }
+AR_API int ar_choose_algo(int R, uint64_t bytes, int slot_kind) { return choose_algo(R, bytes, slot_kind); }
 
 AR_API int ar_set_pdl(ar_handle *h, int enable) {
     if (!h) return AR_EINVAL;
@@ -482,7 +493,7 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) 
     const int vec = op == 0 ? 16 : allgather_vec(bytes, nullptr, nullptr);
     int algo = AR_ALGO_ONESHOT, bps = h->bps_ag;
     if (op == 0) {
-        algo = h->algo == AR_ALGO_AUTO ? choose_algo(h->R, bytes) : h->algo;
+        algo = h->algo == AR_ALGO_AUTO ? choose_algo(h->R, bytes, h->kind) : h->algo;
         bps = algo == AR_ALGO_TWOSHOT ? h->bps_two : h->bps_one;
     }
     int rc = plan_compute(h->R, bytes, vec, algo, tda::kThreads, h->sm_count, bps, plan);

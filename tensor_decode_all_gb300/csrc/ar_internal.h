@@ -17,7 +17,7 @@
 namespace tda {
 
 constexpr int kMaxRanks = 8;
-constexpr int kThreads = 256;           // threads per block of the exchange kernels
+constexpr int kThreads = 256;           // threads per block of the exchange kernels (>= 64: see kPollWarp)
 constexpr int kFlagStrideWords = 16;    // 16 x 8 B = one 128-byte line per flag
 constexpr uint64_t kSlotAlign = 256;
 constexpr int kTwoShot = -2;            // "unroll" code that selects the two-shot kernel

@@ -106,13 +106,21 @@ static __device__ __noinline__ void record_timeout(const DevState &d, int rank, 
     }
 }
 
-// Called by all threads of the block.  Warp 0 waits until every peer p != rank
-// has published at least `target` stages for block `block`.  Returns true if
-// the block must leave (timeout here or abort elsewhere).  Ends with a barrier.
+// The warp that polls peers' flags.  It is not warp 0, whose thread 0 raises
+// this block's own flag just before: a release stalls its warp until the
+// block's slot stores are acknowledged (over the host link that is the whole
+// write), and the peers' flags can be watched meanwhile.  A block may read its
+// peers' data before its own release completes: nothing it reads depends on it.
+constexpr int kPollWarp = 1;
+
+// Called by all threads of the block.  Warp kPollWarp waits until every peer
+// p != rank has published at least `target` stages for block `block`.  Returns
+// true if the block must leave (timeout here or abort elsewhere).  Ends with a
+// barrier.
 __device__ __forceinline__ bool wait_peers(const DevState &d, int R, int rank, int block,
                                            unsigned long long target, int *s_bail) {
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
+    if ((threadIdx.x >> 5) == kPollWarp) {
+        const int lane = threadIdx.x & 31;
         const bool mine = lane < R && lane != rank;
         const unsigned long long *f = mine ? flag_ptr(d, lane, block) : nullptr;
         unsigned long long seen = 0;

@@ -95,11 +95,15 @@ def test_plan_zero_bytes_and_bad_args(lib):
 
 
 def test_choose_algo_rule(lib):
-    for R in (1, 2, 3):
-        assert tda.ar_choose_algo(R, 1 << 30) == ar.AR_ALGO_ONESHOT
-    for R in (4, 8):
-        assert tda.ar_choose_algo(R, (1 << 20) - 1) == ar.AR_ALGO_ONESHOT
-        assert tda.ar_choose_algo(R, 1 << 20) == ar.AR_ALGO_TWOSHOT
+    for kind in (ar.AR_SLOT_HBM, ar.AR_SLOT_PINNED_HOST):
+        for R in (1, 2, 3):
+            assert tda.ar_choose_algo(R, 1 << 30, kind) == ar.AR_ALGO_ONESHOT
+    # thresholds from the measured crossover (R, HBM, pinned host)
+    for R, hbm, pinned in ((4, 2 << 20, 256 << 10), (7, 2 << 20, 256 << 10), (8, 512 << 10, 64 << 10)):
+        assert tda.ar_choose_algo(R, hbm - 1, ar.AR_SLOT_HBM) == ar.AR_ALGO_ONESHOT
+        assert tda.ar_choose_algo(R, hbm, ar.AR_SLOT_HBM) == ar.AR_ALGO_TWOSHOT
+        assert tda.ar_choose_algo(R, pinned - 1, ar.AR_SLOT_PINNED_HOST) == ar.AR_ALGO_ONESHOT
+        assert tda.ar_choose_algo(R, pinned, ar.AR_SLOT_PINNED_HOST) == ar.AR_ALGO_TWOSHOT
     assert tda.ar_set_algo(0, ar.AR_ALGO_ONESHOT) == ar.AR_EINVAL
 
 

@@ -171,6 +171,9 @@ def test_query_and_plan():
     assert info.slot_bytes == 393216 * 2
     assert info.total_slot_bytes == 2 * 8 * info.slot_bytes
     p = h.plan("allreduce", 393216)
+    assert p.algo == tda.ar_choose_algo(8, 393216 * 2, tda.AR_SLOT_HBM)
+    h.set_algo("oneshot")
+    p = h.plan("allreduce", 393216)
     assert p.algo == 0 and 1 <= p.blocks and p.blocks * 8 <= info.sm_count * info.blocks_per_sm
     assert p.tiles * p.tile_bytes >= 393216 * 2
     h.set_algo("twoshot")
