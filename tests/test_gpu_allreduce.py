@@ -225,3 +225,32 @@ def test_special_values(dtype):
     for r in range(R):
         assert_bits_equal(to_bits(outs[r]), want, dtype, f"rank {r}")
     h.destroy()
+
+
+@pytest.mark.parametrize("slots", ["pinned", "hbm"])
+def test_programmatic_dependent_launch_on_and_off_agree(slots):
+    """A graph of back-to-back calls with each rank's kernels launched as
+    programmatic dependents (the default) and without: same bits, equal to the
+    oracle on every call."""
+    R, n, C = 4, 50001, 12
+    outs_by_mode = {}
+    xs_all = [inputs.allreduce_inputs(5, R, n, "bf16", "uniform", 200 + c) for c in range(C)]
+    for pdl in (True, False):
+        h = _handle(R, "bf16", n, slots)
+        h.set_pdl(pdl)
+        streams = rank_streams(R)
+        ins = [[to_dev(x, "bf16") for x in xs] for xs in xs_all]
+        outs = [[torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(R)] for _ in range(C)]
+        g = capture(h, "allreduce", ins, outs, streams)
+        g.replay()
+        g.replay()
+        torch.cuda.synchronize()
+        h.check()
+        outs_by_mode[pdl] = [[to_bits(t) for t in row] for row in outs]
+        del g
+        h.destroy()
+    for c in range(C):
+        want = oracle.allreduce(xs_all[c], "bf16", ranks=[0])[0]
+        for r in range(R):
+            assert_bits_equal(outs_by_mode[True][c][r], want, "bf16", f"pdl on, call {c} rank {r}")
+            assert_bits_equal(outs_by_mode[False][c][r], want, "bf16", f"pdl off, call {c} rank {r}")
