@@ -126,9 +126,11 @@ typedef struct ar_plan {
     int32_t blocks;         /* grid size per rank (same on every rank); R * blocks fit on the GPU */
     int32_t threads;        /* threads per block */
     int32_t vec_bytes;      /* bytes per vector access: 16 for all-reduce */
-    int32_t unroll;         /* vectors per thread per tile (R for the two-shot form) */
+    int32_t unroll;         /* vectors per thread per tile (two-shot: R * subtile_vecs / threads, rounded up) */
     int32_t algo;           /* AR_ALGO_ONESHOT or AR_ALGO_TWOSHOT (allgather: one-shot) */
     int32_t flag_rounds;    /* flag rounds per tile: 1 or 2 */
+    int32_t subtile_vecs;   /* two-shot: vectors per sub-tile (64, 128 or 256; a tile is R sub-tiles); else 0 */
+    int32_t reserved;
     uint64_t tile_bytes;    /* bytes a block handles per stage (threads * unroll * vec_bytes) */
     uint64_t tiles;         /* ceil(bytes / tile_bytes); tile t goes to block t % blocks, stage t / blocks */
     uint64_t max_stages;    /* stages of block 0 = ceil(tiles / blocks) */
@@ -246,7 +248,9 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan);
  * logic can be checked without a GPU: R ranks, `bytes` per rank, vector size
  * vec_bytes (16, 8, 4, 2 or 1), algo AR_ALGO_ONESHOT or AR_ALGO_TWOSHOT,
  * `threads` per block, and a GPU that holds sm_count * blocks_per_sm blocks of
- * the kernel at once.
+ * the kernel at once.  Two-shot plans here use 256-vector sub-tiles; a handle
+ * with HBM slots uses 128 when that leaves more than half its blocks idle
+ * (ar_plan_for shows its choice).
  */
 AR_API int ar_plan_compute(int R, uint64_t bytes, int vec_bytes, int algo, int threads, int sm_count,
                            int blocks_per_sm, ar_plan *plan);

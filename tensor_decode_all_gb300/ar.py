@@ -54,6 +54,7 @@ class Info(ctypes.Structure):
 class Plan(ctypes.Structure):
     _fields_ = [("blocks", ctypes.c_int32), ("threads", ctypes.c_int32), ("vec_bytes", ctypes.c_int32),
                 ("unroll", ctypes.c_int32), ("algo", ctypes.c_int32), ("flag_rounds", ctypes.c_int32),
+                ("subtile_vecs", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("tile_bytes", ctypes.c_uint64), ("tiles", ctypes.c_uint64),
                 ("max_stages", ctypes.c_uint64)]
 

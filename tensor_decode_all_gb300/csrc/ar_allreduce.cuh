@@ -228,7 +228,8 @@ __global__ void __launch_bounds__(kThreads)
 
 // Two-shot variant, for large payloads at R >= 4, where the one-shot form's
 // R * (R - 1) * S bytes of peer-slot reads per call saturate L2.  A tile is R
-// sub-tiles of kThreads vectors.  Per stage, each block of rank r:
+// sub-tiles of SUB vectors (SUB = 256, 128 or 64: smaller sub-tiles spread a
+// mid-sized payload over more blocks).  Per stage, each block of rank r:
 //   1. copies the whole tile of in_r into slot[parity][r]; barrier; raises its
 //      flag to seq + 2s + 1 (release);
 //   2. waits for every peer's flag to reach seq + 2s + 1; reduces sub-tile r:
@@ -241,9 +242,10 @@ __global__ void __launch_bounds__(kThreads)
 // Each element is reduced once, by one rank, in rank order, so every rank
 // receives the same bits as the one-shot form and the oracle.  Per call, slot
 // reads fall from R * (R - 1) * S to about 2 * R * S bytes.
-template <class Ops, int R>
+template <class Ops, int R, int SUB>
 __global__ void __launch_bounds__(kThreads, 4)
     allreduce_twoshot_kernel(const uint16_t *in, uint16_t *out, uint64_t numel, int rank, DevState d) {
+    static_assert(SUB == 64 || SUB == 128 || SUB == 256, "sub-tile of 64, 128 or 256 vectors");
     __shared__ unsigned long long s_seq;
     __shared__ unsigned long long s_calls;
     __shared__ int s_bail;
@@ -254,7 +256,9 @@ __global__ void __launch_bounds__(kThreads, 4)
     const uint64_t nvec_full = numel / 8;
     const int tail = (int)(numel % 8);
     const uint64_t nv = nvec_full + (tail ? 1 : 0);
-    constexpr uint64_t kTileVecs = (uint64_t)kThreads * R;
+    constexpr uint64_t kTileVecs = (uint64_t)SUB * R;
+    // vectors each thread moves in phases 1 and 3
+    constexpr int kPer = (int)((kTileVecs + kThreads - 1) / kThreads);
     const uint64_t ntiles = (nv + kTileVecs - 1) / kTileVecs;
     const uint64_t nstages = ntiles > (uint64_t)b ? (ntiles - b + B - 1) / B : 0;
 
@@ -273,25 +277,28 @@ __global__ void __launch_bounds__(kThreads, 4)
     uint4 *const my_slot = slot_base + (uint64_t)rank * slot_vecs;
 
     for (uint64_t s = 0; s < nstages; ++s) {
-        const uint64_t t0 = ((uint64_t)b + s * B) * kTileVecs + tid;
+        const uint64_t tbase = ((uint64_t)b + s * B) * kTileVecs;
 
-        // 1. publish the whole tile
-        uint4 pub[R];
+        // 1. publish the whole tile (tile-local vector u * kThreads + tid)
+        uint4 pub[kPer];
 #pragma unroll
-        for (int u = 0; u < R; ++u) pub[u] = load_own(in, t0 + (uint64_t)u * kThreads, nvec_full, tail);
+        for (int u = 0; u < kPer; ++u) {
+            const uint64_t li = (uint64_t)u * kThreads + tid;
+            pub[u] = li < kTileVecs ? load_own(in, tbase + li, nvec_full, tail) : make_uint4(0u, 0u, 0u, 0u);
+        }
 #pragma unroll
-        for (int u = 0; u < R; ++u) {
-            const uint64_t v = t0 + (uint64_t)u * kThreads;
-            if (v < nv) my_slot[v] = pub[u];
+        for (int u = 0; u < kPer; ++u) {
+            const uint64_t li = (uint64_t)u * kThreads + tid;
+            if (li < kTileVecs && tbase + li < nv) my_slot[tbase + li] = pub[u];
         }
         __syncthreads();
         if (tid == 0) publish_stage(d, rank, b, seq + 2 * s + 1);
         if (wait_peers(d, R, rank, b, seq + 2 * s + 1, &s_bail)) return;
 
         // 2. reduce sub-tile `rank` in rank order; the result replaces it in my slot
-        const uint64_t vr = t0 + (uint64_t)rank * kThreads;
+        const uint64_t vr = tbase + (uint64_t)rank * SUB + tid;
         uint4 res = make_uint4(0u, 0u, 0u, 0u);
-        if (vr < nv) {
+        if (tid < SUB && vr < nv) {
             uint4 vals[R];
 #pragma unroll
             for (int p = 0; p < R; ++p) vals[p] = ld_cg_v4(slot_base + (uint64_t)p * slot_vecs + vr);
@@ -307,17 +314,31 @@ __global__ void __launch_bounds__(kThreads, 4)
         if (wait_peers(d, R, rank, b, seq + 2 * s + 2, &s_bail)) return;
 
         // 3. gather the R rounded sub-tiles
-        uint4 got[R];
+        uint4 got[kPer];
+        if constexpr (SUB == kThreads) {
+            // tile-local vector u * kThreads + tid lies in sub-tile u; this
+            // thread reduced vector tid of sub-tile `rank` itself
 #pragma unroll
-        for (int p = 0; p < R; ++p) {
-            const uint64_t v = t0 + (uint64_t)p * kThreads;
-            got[p] = res;
-            if (p != rank && v < nv) got[p] = ld_cg_v4(slot_base + (uint64_t)p * slot_vecs + v);
+            for (int u = 0; u < kPer; ++u) {
+                const uint64_t v = tbase + (uint64_t)u * kThreads + tid;
+                got[u] = res;
+                if (u != rank && v < nv) got[u] = ld_cg_v4(slot_base + (uint64_t)u * slot_vecs + v);
+            }
+        } else {
+            // a sub-tile is narrower than the block: read every result, this
+            // rank's included, from the slots (the barrier above orders them)
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const uint64_t li = (uint64_t)u * kThreads + tid;
+                const uint64_t v = tbase + li;
+                got[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (li < kTileVecs && v < nv) got[u] = ld_cg_v4(slot_base + (li / SUB) * slot_vecs + v);
+            }
         }
 #pragma unroll
-        for (int p = 0; p < R; ++p) {
-            const uint64_t v = t0 + (uint64_t)p * kThreads;
-            if (v < nv) store_out(out, v, nvec_full, tail, got[p]);
+        for (int u = 0; u < kPer; ++u) {
+            const uint64_t li = (uint64_t)u * kThreads + tid;
+            if (li < kTileVecs && tbase + li < nv) store_out(out, tbase + li, nvec_full, tail, got[u]);
         }
     }
 
@@ -351,26 +372,36 @@ const void *allreduce_ptr_ru(int R) {
     }
 }
 
-template <class Ops>
-const void *allreduce_twoshot_ptr(int R) {
+template <class Ops, int SUB>
+const void *allreduce_twoshot_ptr_r(int R) {
     switch (R) {
-        case 1: return (const void *)allreduce_twoshot_kernel<Ops, 1>;
-        case 2: return (const void *)allreduce_twoshot_kernel<Ops, 2>;
-        case 3: return (const void *)allreduce_twoshot_kernel<Ops, 3>;
-        case 4: return (const void *)allreduce_twoshot_kernel<Ops, 4>;
-        case 5: return (const void *)allreduce_twoshot_kernel<Ops, 5>;
-        case 6: return (const void *)allreduce_twoshot_kernel<Ops, 6>;
-        case 7: return (const void *)allreduce_twoshot_kernel<Ops, 7>;
-        case 8: return (const void *)allreduce_twoshot_kernel<Ops, 8>;
+        case 1: return (const void *)allreduce_twoshot_kernel<Ops, 1, SUB>;
+        case 2: return (const void *)allreduce_twoshot_kernel<Ops, 2, SUB>;
+        case 3: return (const void *)allreduce_twoshot_kernel<Ops, 3, SUB>;
+        case 4: return (const void *)allreduce_twoshot_kernel<Ops, 4, SUB>;
+        case 5: return (const void *)allreduce_twoshot_kernel<Ops, 5, SUB>;
+        case 6: return (const void *)allreduce_twoshot_kernel<Ops, 6, SUB>;
+        case 7: return (const void *)allreduce_twoshot_kernel<Ops, 7, SUB>;
+        case 8: return (const void *)allreduce_twoshot_kernel<Ops, 8, SUB>;
         default: return nullptr;
     }
 }
 
-// unroll 1 or 2: one-shot with that many vectors per thread per stage;
-// kTwoShot: the two-shot form.
+template <class Ops>
+const void *allreduce_twoshot_ptr(int R, int sub) {
+    switch (sub) {
+        case 256: return allreduce_twoshot_ptr_r<Ops, 256>(R);
+        case 128: return allreduce_twoshot_ptr_r<Ops, 128>(R);
+        case 64: return allreduce_twoshot_ptr_r<Ops, 64>(R);
+        default: return nullptr;
+    }
+}
+
+// U = 1 or 2: one-shot with that many vectors per thread per stage;
+// U = twoshot_variant(sub): the two-shot form with sub-tiles of `sub` vectors.
 template <class Ops>
 const void *allreduce_ptr(int R, int U) {
-    if (U == kTwoShot) return allreduce_twoshot_ptr<Ops>(R);
+    if (U < 0) return allreduce_twoshot_ptr<Ops>(R, twoshot_sub(U));
     return U == 1 ? allreduce_ptr_ru<Ops, 1>(R) : allreduce_ptr_ru<Ops, 2>(R);
 }
 

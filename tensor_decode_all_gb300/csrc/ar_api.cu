@@ -26,6 +26,7 @@ struct ar_handle {
     int bps_one = 0, bps_two = 0, bps_ag = 0;  // occupancy per kernel family
     int bmax = 0;                              // flag/counter slots per rank
     int algo = AR_ALGO_AUTO;
+    int twoshot_sub = 0;                       // AR_TWOSHOT_SUB (64/128/256), for experiments; 0 = rule
     bool pdl = true;                           // launch as programmatic dependents
     void *slots_host = nullptr;            // pinned kind: host address of the slots
     uint8_t *slots_dev = nullptr;          // device address of the slots
@@ -162,7 +163,8 @@ int handle_occupancy(ar_handle *h) {
     int rc = AR_OK;
     if (h->dtype == AR_F16 || h->dtype == AR_BF16) {
         for (int u = 1; u <= 2 && rc == AR_OK; ++u) rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, u), &one);
-        if (rc == AR_OK) rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, tda::kTwoShot), &two);
+        for (int sub = 64; sub <= 256 && rc == AR_OK; sub *= 2)
+            rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, tda::twoshot_variant(sub)), &two);
     }
     for (int u = 1; u <= 2 && rc == AR_OK; ++u)
         for (int vw = 1; vw <= 16 && rc == AR_OK; vw *= 2) rc = kernel_occupancy(tda::allgather_kernel_ptr(vw, h->R, u), &ag);
@@ -191,7 +193,31 @@ int choose_algo(int R, uint64_t bytes, int slot_kind) {
     return bytes >= threshold ? AR_ALGO_TWOSHOT : AR_ALGO_ONESHOT;
 }
 
+// Sub-tile size (vectors) of the two-shot form.  256 unless the slots are in
+// HBM and 256-vector sub-tiles would give fewer than half the blocks the GPU
+// can hold: then 128, which spreads a mid-sized call over twice the blocks.
+// Measured on a GB300, bf16: R=8 768 KiB HBM 9.9 -> 9.5 us; from 2 MiB up,
+// and over the host link, 256 is as fast or faster.
+int twoshot_sub_for(int R, uint64_t nv, uint64_t bmax, int slot_kind) {
+    if (slot_kind != AR_SLOT_HBM) return 256;
+    const uint64_t tiles256 = (nv + 256ull * R - 1) / (256ull * R);
+    return 2 * tiles256 < bmax ? 128 : 256;
+}
+
+int plan_compute_sub(int R, uint64_t bytes, int vec, int algo, int sub, int threads, int sms, int bps, ar_plan *p);
+
+int handle_twoshot_sub(const ar_handle *h, uint64_t bytes) {
+    if (h->twoshot_sub) return h->twoshot_sub;
+    const uint64_t bmax = (uint64_t)h->sm_count * (uint64_t)h->bps_two / (uint64_t)h->R;
+    return twoshot_sub_for(h->R, (bytes + 15) / 16, bmax, h->kind);
+}
+
 int plan_compute(int R, uint64_t bytes, int vec, int algo, int threads, int sms, int bps, ar_plan *p) {
+    return plan_compute_sub(R, bytes, vec, algo, 0, threads, sms, bps, p);
+}
+
+// sub: two-shot sub-tile in vectors (64, 128, 256), or 0 for 256.
+int plan_compute_sub(int R, uint64_t bytes, int vec, int algo, int sub, int threads, int sms, int bps, ar_plan *p) {
     if (!p || R < 1 || R > tda::kMaxRanks || threads < 32 || threads % 32 || sms < 1 || bps < 1)
         return AR_EINVAL;
     if (vec != 16 && vec != 8 && vec != 4 && vec != 2 && vec != 1) return AR_EINVAL;
@@ -205,13 +231,17 @@ int plan_compute(int R, uint64_t bytes, int vec, int algo, int threads, int sms,
     // two stages' worth of single vectors; one otherwise (spreads small
     // payloads over more blocks).  Two-shot: one sub-tile of `threads` vectors
     // per rank, so R vectors per thread per stage.
-    const int unroll = algo == AR_ALGO_TWOSHOT ? R : (nv >= bmax * (uint64_t)threads * 2 ? 2 : 1);
-    const uint64_t tile_vecs = (uint64_t)threads * unroll;
+    if (algo == AR_ALGO_TWOSHOT && sub == 0) sub = 256;
+    if (algo == AR_ALGO_TWOSHOT && sub != 64 && sub != 128 && sub != 256) return AR_EINVAL;
+    const uint64_t tile_vecs = algo == AR_ALGO_TWOSHOT ? (uint64_t)R * (uint64_t)sub
+                                                       : (uint64_t)threads * (nv >= bmax * (uint64_t)threads * 2 ? 2 : 1);
+    const int unroll = (int)((tile_vecs + threads - 1) / threads);
     const uint64_t tiles = (nv + tile_vecs - 1) / tile_vecs;
     const uint64_t blocks = tiles < bmax ? tiles : bmax;
     p->blocks = (int32_t)blocks;
     p->algo = algo;
     p->flag_rounds = algo == AR_ALGO_TWOSHOT ? 2 : 1;
+    p->subtile_vecs = algo == AR_ALGO_TWOSHOT ? sub : 0;
     p->threads = threads;
     p->vec_bytes = vec;
     p->unroll = unroll;
@@ -317,6 +347,10 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
     if (cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess)
         return fail(AR_ECUDA);
     if (const char *e = std::getenv("AR_PDL")) h->pdl = e[0] != '0';
+    if (const char *e = std::getenv("AR_TWOSHOT_SUB")) {
+        const long v = std::strtol(e, nullptr, 10);
+        if (v == 64 || v == 128 || v == 256) h->twoshot_sub = (int)v;
+    }
     if (const char *e = std::getenv("AR_ALGO")) {
         if (!std::strcmp(e, "oneshot")) h->algo = AR_ALGO_ONESHOT;
         else if (!std::strcmp(e, "twoshot")) h->algo = AR_ALGO_TWOSHOT;
@@ -370,11 +404,11 @@ AR_API int ar_allreduce(ar_handle *h, int rank, const void *in, void *out, size_
     const uint64_t bytes = numel * h->itemsize;
     const int algo = h->algo == AR_ALGO_AUTO ? choose_algo(h->R, bytes, h->kind) : h->algo;
     ar_plan plan;
-    rc = plan_compute(h->R, bytes, 16, algo, tda::kThreads, h->sm_count,
-                      algo == AR_ALGO_TWOSHOT ? h->bps_two : h->bps_one, &plan);
+    rc = plan_compute_sub(h->R, bytes, 16, algo, handle_twoshot_sub(h, bytes), tda::kThreads, h->sm_count,
+                          algo == AR_ALGO_TWOSHOT ? h->bps_two : h->bps_one, &plan);
     if (rc != AR_OK) return rc;
     int blocks = plan.blocks < h->bmax ? plan.blocks : h->bmax;
-    const int variant = algo == AR_ALGO_TWOSHOT ? tda::kTwoShot : plan.unroll;
+    const int variant = algo == AR_ALGO_TWOSHOT ? tda::twoshot_variant(plan.subtile_vecs) : plan.unroll;
     const cudaError_t e = tda::launch_allreduce(h->dtype, h->R, variant, blocks, s, in, out,
                                                 numel, rank, dev_state(h), h->pdl);
     if (e != cudaSuccess) {
@@ -496,7 +530,8 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) 
         algo = h->algo == AR_ALGO_AUTO ? choose_algo(h->R, bytes, h->kind) : h->algo;
         bps = algo == AR_ALGO_TWOSHOT ? h->bps_two : h->bps_one;
     }
-    int rc = plan_compute(h->R, bytes, vec, algo, tda::kThreads, h->sm_count, bps, plan);
+    int rc = plan_compute_sub(h->R, bytes, vec, algo, op == 0 ? handle_twoshot_sub(h, bytes) : 0, tda::kThreads,
+                              h->sm_count, bps, plan);
     if (rc == AR_OK && plan->blocks > h->bmax) {
         plan->blocks = h->bmax;
         plan->max_stages = (plan->tiles + h->bmax - 1) / h->bmax;

@@ -20,7 +20,10 @@ constexpr int kMaxRanks = 8;
 constexpr int kThreads = 256;           // threads per block of the exchange kernels (>= 64: see kPollWarp)
 constexpr int kFlagStrideWords = 16;    // 16 x 8 B = one 128-byte line per flag
 constexpr uint64_t kSlotAlign = 256;
-constexpr int kTwoShot = -2;            // "unroll" code that selects the two-shot kernel
+// Kernel variant codes for the two-shot form: a negative "unroll" whose
+// magnitude is the sub-tile size in vectors (256, 128 or 64).
+constexpr int twoshot_variant(int sub) { return -sub; }
+constexpr int twoshot_sub(int variant) { return -variant; }
 
 // Per-(rank, block) counters.  `seq` counts the stages this block has
 // published over all calls (its flag's value at the end of the last call);

@@ -66,12 +66,16 @@ def test_plan_invariants(lib, R, vec, algo):
         nv = -(-nbytes // vec)
         assert p.threads == threads and p.vec_bytes == vec and p.algo == algo
         if algo == ar.AR_ALGO_TWOSHOT:
-            assert p.unroll == R and p.flag_rounds == 2   # one sub-tile of `threads` vectors per rank
+            assert p.flag_rounds == 2 and p.subtile_vecs in (64, 128, 256)
+            assert p.tile_bytes == R * p.subtile_vecs * vec          # R sub-tiles per tile
+            assert p.unroll == -(-R * p.subtile_vecs // threads)
         else:
             assert p.unroll in (1, 2) and p.flag_rounds == 1
-        assert p.tile_bytes == threads * p.unroll * vec
+        if algo == ar.AR_ALGO_ONESHOT:
+            assert p.tile_bytes == threads * p.unroll * vec and p.subtile_vecs == 0
         # tiles cover the payload, and no tile is empty
-        assert p.tiles * threads * p.unroll >= nv > (p.tiles - 1) * threads * p.unroll
+        tile_vecs = p.tile_bytes // vec
+        assert p.tiles * tile_vecs >= nv > (p.tiles - 1) * tile_vecs
         # every block has at least one tile; all ranks' blocks fit at once
         assert 1 <= p.blocks <= min(p.tiles, bmax)
         assert R * p.blocks <= sms * bps
@@ -108,10 +112,10 @@ def test_choose_algo_rule(lib):
 
 
 def test_struct_layouts_match_header(lib):
-    # ar_error_info: 4 x int32 + 2 x uint64; ar_info: 12 x int32 + 4 x uint64; ar_plan: 6 x int32 + 3 x uint64
+    # ar_error_info: 4 x int32 + 2 x uint64; ar_info: 12 x int32 + 4 x uint64; ar_plan: 8 x int32 + 3 x uint64
     assert ctypes.sizeof(ar.ErrorInfo) == 32
     assert ctypes.sizeof(ar.Info) == 80
-    assert ctypes.sizeof(ar.Plan) == 48
+    assert ctypes.sizeof(ar.Plan) == 56
 
 
 def test_no_cpu_fallback_when_library_missing(monkeypatch, tmp_path):

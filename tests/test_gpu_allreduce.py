@@ -254,3 +254,17 @@ def test_programmatic_dependent_launch_on_and_off_agree(slots):
         for r in range(R):
             assert_bits_equal(outs_by_mode[True][c][r], want, "bf16", f"pdl on, call {c} rank {r}")
             assert_bits_equal(outs_by_mode[False][c][r], want, "bf16", f"pdl off, call {c} rank {r}")
+
+
+@pytest.mark.parametrize("sub", [64, 128, 256])
+@pytest.mark.parametrize("R,slots", [(3, "hbm"), (4, "pinned"), (8, "hbm"), (8, "pinned")])
+def test_twoshot_subtile_sizes(sub, R, slots, monkeypatch):
+    """Every two-shot sub-tile size gives the oracle's bits (several stages,
+    partial last tile, ragged tail)."""
+    monkeypatch.setenv("AR_TWOSHOT_SUB", str(sub))
+    n = 8 * sub * R * 7 + 8 * 37 + 5
+    h = _handle(R, "bf16", n, slots)
+    h.set_algo("twoshot")
+    assert h.plan("allreduce", n).subtile_vecs == sub
+    _run_once(R, "bf16", n, slots, h=h)
+    h.destroy()

@@ -179,6 +179,11 @@ def test_query_and_plan():
     h.set_algo("twoshot")
     p = h.plan("allreduce", 393216)
     assert p.algo == 1 and p.flag_rounds == 2 and p.blocks * 8 <= info.sm_count * info.blocks_per_sm_twoshot
+    # HBM slots: 128-vector sub-tiles when 256-vector ones would fill under half the blocks
+    nv = 393216 // 8
+    tiles256 = -(-nv // (256 * 8))
+    bmax = info.sm_count * info.blocks_per_sm_twoshot // 8
+    assert p.subtile_vecs == (128 if 2 * tiles256 < bmax else 256)
     h.destroy()
 
 
