@@ -576,6 +576,7 @@ PROFILE_WORKLOADS = {
     "r2_fp16_256KiB_pinned": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 100),
     "r2_fp16_256KiB_pinned_1call": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 1),
     "r8_bf16_768KiB_hbm": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100),
+    "r8_bf16_768KiB_hbm_1call": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 1),
     "r8_bf16_16MiB_hbm_1call": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 1),
     "r8_bf16_16MiB_hbm_oneshot_1call": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 1),
     "allgather_c64_r8_hbm_1call": ("allgather", 8, "c64", 500000, "hbm", 4, "normal", 1),
