@@ -267,8 +267,9 @@ AR_API int ar_choose_algo(int R, uint64_t bytes, int slot_kind);
  * work on their stream (CUDA programmatic dependent launch), so that a rank's
  * next kernel is scheduled while its current one finishes.  Each kernel still
  * waits for the preceding kernel to complete, and for its writes to be
- * visible, before it reads or writes any memory, and releases its dependents
- * only after its last write; the bits do not change.  On by default; the
+ * visible, before it reads or writes any memory, and lets its dependents be
+ * scheduled only once all blocks of the call's ranks are resident (after its
+ * last wait for its peers' flags); the bits do not change.  On by default; the
  * environment variable AR_PDL=0 turns it off at ar_create.  Applies to calls
  * enqueued (or captured) afterwards. */
 AR_API int ar_set_pdl(ar_handle *h, int enable);

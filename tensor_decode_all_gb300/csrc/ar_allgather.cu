@@ -107,6 +107,9 @@ __global__ void __launch_bounds__(kThreads)
         }
 
         if (wait_peers(d, R, rank, b, seq + s + 1, &s_bail)) return;
+        // Every peer block of this call has now published its last stage, so
+        // all of them are resident: this rank's next call may be scheduled.
+        if (s + 1 == nstages) pdl_trigger();
 
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -133,7 +136,6 @@ __global__ void __launch_bounds__(kThreads)
         c.calls = s_calls + 1;
         d.ctr[(size_t)rank * d.bmax + b] = c;
     }
-    pdl_trigger();
 }
 
 template <int VW, int U>

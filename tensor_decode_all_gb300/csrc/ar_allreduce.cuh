@@ -188,6 +188,9 @@ __global__ void __launch_bounds__(kThreads)
 
         // 4. wait for the peers
         if (wait_peers(d, R, rank, b, seq + s + 1, &s_bail)) return;
+        // Every peer block of this call has now published its last stage, so
+        // all of them are resident: this rank's next call may be scheduled.
+        if (s + 1 == nstages) pdl_trigger();
 
         // 5. gather, add in rank order, round once, store
 #pragma unroll
@@ -223,7 +226,6 @@ __global__ void __launch_bounds__(kThreads)
         c.calls = s_calls + 1;
         d.ctr[(size_t)rank * d.bmax + b] = c;
     }
-    pdl_trigger();
 }
 
 // Two-shot variant, for large payloads at R >= 4, where the one-shot form's
@@ -312,6 +314,9 @@ __global__ void __launch_bounds__(kThreads, 4)
         __syncthreads();
         if (tid == 0) publish_stage(d, rank, b, seq + 2 * s + 2);
         if (wait_peers(d, R, rank, b, seq + 2 * s + 2, &s_bail)) return;
+        // Every peer block of this call has now published its last stage, so
+        // all of them are resident: this rank's next call may be scheduled.
+        if (s + 1 == nstages) pdl_trigger();
 
         // 3. gather the R rounded sub-tiles
         uint4 got[kPer];
@@ -348,7 +353,6 @@ __global__ void __launch_bounds__(kThreads, 4)
         c.calls = s_calls + 1;
         d.ctr[(size_t)rank * d.bmax + b] = c;
     }
-    pdl_trigger();
 }
 
 }  // namespace tda

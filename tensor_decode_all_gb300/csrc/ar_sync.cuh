@@ -75,7 +75,10 @@ __device__ __forceinline__ unsigned char ld_cg_u8(const void *p) {
 // programmatic-serialization attribute, its blocks may become resident before
 // this call ends.  Each kernel therefore waits (griddepcontrol.wait: the
 // preceding kernel has completed and its memory is visible) before it touches
-// any memory, and lets its dependents start only after its last write.  Both
+// any memory.  A block lets its dependents be scheduled once it has seen its
+// peers' last flags: by then every block of every rank of this call is
+// resident, so the next call's early blocks cannot keep a peer block of this
+// call from being scheduled (which would leave this call waiting for it).  Both
 // instructions do nothing when the launch has no programmatic dependency.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
