@@ -169,12 +169,17 @@ KERNEL_SOURCES = ("ar_allreduce.cuh", "ar_sync.cuh", "ar_internal.h", "ar_allred
 
 
 def kernel_source_sha256() -> str:
-    """Hash of the sources the all-reduce kernels are compiled from."""
+    """Hash of the code (comments and blank space removed) the all-reduce
+    kernels are compiled from: profiled counters stay valid across comment edits."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "tensor_decode_all_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "tensor_decode_all_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()
 
 

@@ -6,10 +6,11 @@
  * through a shared, double-buffered slot and per-block flags.  The operation
  * is the flag-synchronised exchange-and-add of "[Kernel] Two-rank FP16
  * all-reduce through pinned host memory for GPUs without P2P" (1Cat-vLLM pull
- * 1216), section "Purpose": every block writes its chunk to a slot, fences,
- * raises a per-block flag, waits for its peers' flags and adds their chunks,
- * with one rounding; slots alternate by call parity; nothing runs on the CPU
- * and nothing synchronises a stream, so calls can be captured in CUDA graphs.
+ * 1216), section "Purpose": a block publishes its share of the data in a shared
+ * slot, makes it visible before it sets its own flag, and sums once it has seen
+ * the flags of the matching blocks of the other ranks, rounding a single time;
+ * consecutive calls use the two halves of the slot in turn; the host only
+ * enqueues kernels and never waits, so the calls can be captured in CUDA graphs.
  * That page is about two ranks; this library takes 1 <= R <= 8 and sums in
  * rank order 0..R-1 on every rank (the order matters from three ranks on:
  * "[SM120] Add optional FlashInfer PCIe-IPC all-reduce for switch-free hosts",

@@ -6,10 +6,9 @@
 // warp 0 poll their peer's flag for the same block index with acquire
 // semantics until it reaches the stage count this rank needs, then the block
 // passes a barrier.  The release -> acquire pair plus the two barriers order
-// the peer's slot stores before this block's slot loads ("[Kernel] Two-rank
-// FP16 all-reduce through pinned host memory for GPUs without P2P", section
-// "Purpose": write the chunk, fence, raise a per-block flag, wait for the
-// peer's flag, then read).
+// the peer's slot stores before this block's slot loads (the data-then-flag
+// order of "[Kernel] Two-rank FP16 all-reduce through pinned host memory for
+// GPUs without P2P", section "Purpose").
 //
 // Scope: slots and flags in mapped host memory use .sys (the pages' case: two
 // GPUs reach the host buffer); in HBM they use .gpu.

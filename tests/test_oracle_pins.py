@@ -11,7 +11,8 @@ or by mathematics, never against a retyping of its own formula:
   SIGNUM Newsletter 30(3), 1995).  So the two-rank result must equal the
   correctly rounded sum RNE16(a + b), which "[Kernel] Two-rank FP16 all-reduce
   through pinned host memory for GPUs without P2P" (section "Purpose") also
-  implies: one FP16 rounding, commutative, the same bits as a two-rank NCCL sum;
+  states: a single FP16 rounding, independent of operand order, matching a
+  two-rank NCCL sum bit for bit;
 * library routines for the special cases that reduce to them: numpy's
   float64 -> float16 and float32 -> float16 casts and torch's
   float32 -> bfloat16 cast (all round to nearest even);
