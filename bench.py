@@ -671,7 +671,8 @@ def run_sweep(args, dist):
             total = args.sweep_calls
             if slots == "pinned" and R * S >= (64 << 20):
                 total = min(total, 100)  # ~20 ms per call over the host link: bound the wall time
-            C = max(1, min(100, (256 << 20) // max(1, R * S * 2)))
+            # at least 4 calls per graph, so a step is not dominated by one graph launch
+            C = max(4, min(100, (256 << 20) // max(1, R * S * 2)))
             steps = max(1, total // C)
             w = Workload("allreduce", R, dtype, numel, slots, C, config=5, dist="uniform", algo=algo)
             w.capture()

@@ -192,3 +192,64 @@ def test_probes_run():
     link = tda.ar_probe_host_link(64 << 20, 5)
     assert all(v > 1.0 for v in link.values()), link
     assert tda.ar_probe_hbm_copy(1 << 30, 5) > 100.0
+
+
+def test_one_host_thread_per_rank():
+    """Each rank's calls enqueued from its own host thread, as separate
+    processes would: the C ABI's host-side bookkeeping is thread-safe and every
+    call still matches the oracle."""
+    import threading
+    tda = _tda()
+    R, n, CALLS = 4, 20001, 50
+    h = tda.Handle(R, torch.bfloat16, n, "hbm")
+    streams = rank_streams(R)
+    xs = [inputs.allreduce_inputs(5, R, n, "bf16", "uniform", 300 + c) for c in range(CALLS)]
+    ins = [[to_dev(x, "bf16") for x in xc] for xc in xs]
+    outs = [[torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(R)] for _ in range(CALLS)]
+    torch.cuda.synchronize()
+    errors = []
+
+    def rank_thread(r):
+        try:
+            for c in range(CALLS):
+                h.allreduce(r, ins[c][r], outs[c][r], streams[r])
+        except Exception as e:  # pragma: no cover - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=rank_thread, args=(r,)) for r in range(R)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    h.check()
+    for c in (0, CALLS // 2, CALLS - 1):
+        want = oracle.allreduce(xs[c], "bf16", ranks=[0])[0]
+        for r in range(R):
+            assert_bits_equal(to_bits(outs[c][r]), want, "bf16", f"call {c} rank {r}")
+    h.destroy()
+
+
+def test_allreduce_and_allgather_interleaved_on_one_handle():
+    """The two operations share a handle's counters and flags."""
+    tda = _tda()
+    R, n = 3, 10007
+    h = tda.Handle(R, torch.float16, n, "pinned")
+    streams = rank_streams(R)
+    for k in range(6):
+        xs = inputs.allreduce_inputs(5, R, n, "f16", "uniform", 400 + k)
+        ins = [to_dev(x, "f16") for x in xs]
+        if k % 2 == 0:
+            outs = [torch.empty_like(t) for t in ins]
+            enqueue(h, "allreduce", ins, outs, streams)
+            want = oracle.allreduce(xs, "f16", ranks=[0])[0]
+        else:
+            outs = [torch.empty(R * n, dtype=torch.float16, device="cuda") for _ in range(R)]
+            enqueue(h, "allgather", ins, outs, streams)
+            want = oracle.allgather(xs, ranks=[0])[0].view(np.uint16)
+        torch.cuda.synchronize()
+        h.check()
+        for r in range(R):
+            assert_bits_equal(to_bits(outs[r]), want, "f16", f"step {k} rank {r}")
+    h.destroy()
