@@ -165,12 +165,14 @@ class ClockSampler:
 
 # ------------------------------------------------------------- measurement
 
-KERNEL_SOURCES = ("ar_allreduce.cuh", "ar_sync.cuh", "ar_internal.h", "ar_allreduce_f16.cu", "ar_allreduce_bf16.cu")
+KERNEL_SOURCES = ("ar_allreduce.cuh", "ar_sync.cuh", "ar_internal.h", "ar_allreduce_f16.cu", "ar_allreduce_bf16.cu",
+                  "ar_allgather.cu")
 
 
 def kernel_source_sha256() -> str:
-    """Hash of the code (comments and blank space removed) the all-reduce
-    kernels are compiled from: profiled counters stay valid across comment edits."""
+    """Hash of the code (comments and blank space removed) the all-reduce and
+    allgather kernels are compiled from: profiled counters stay valid across
+    comment edits."""
     import hashlib
     import re
     h = hashlib.sha256()

@@ -244,8 +244,16 @@ __global__ void __launch_bounds__(kThreads)
 // Each element is reduced once, by one rank, in rank order, so every rank
 // receives the same bits as the one-shot form and the oracle.  Per call, slot
 // reads fall from R * (R - 1) * S to about 2 * R * S bytes.
+//
+// Blocks per SM: the form is bound by the latency of its two flag rounds per
+// stage, so more resident blocks keep more tiles in flight.  Up to R = 4 the
+// kernel fits in 40 registers without spilling and runs 6 blocks per SM; above
+// that the sub-tile accumulators need more, and it keeps 4.
+template <int R>
+constexpr int twoshot_min_blocks() { return R <= 4 ? 6 : 4; }
+
 template <class Ops, int R, int SUB>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
     allreduce_twoshot_kernel(const uint16_t *in, uint16_t *out, uint64_t numel, int rank, DevState d) {
     static_assert(SUB == 64 || SUB == 128 || SUB == 256, "sub-tile of 64, 128 or 256 vectors");
     __shared__ unsigned long long s_seq;
