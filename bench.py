@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--sweep-slots", default="hbm,pinned")
     ap.add_argument("--sweep-dtypes", default="f16,bf16")
     ap.add_argument("--sweep-ranks", default="2,4,8")
+    ap.add_argument("--sweep-fused", action="store_true",
+                    help="in the sweep, run every call as one cooperative launch of all ranks (ar_allreduce_fused)")
     ap.add_argument("--sweep-min-kib", type=int, default=2)
     ap.add_argument("--sweep-max-kib", type=int, default=65536)
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
@@ -209,12 +211,13 @@ def measured_peaks():
 class Workload:
     """R ranks, C calls, one graph; every call has its own device buffers."""
 
-    def __init__(self, op, R, dtype, numel, slots, calls, config, dist="uniform", algo=None):
+    def __init__(self, op, R, dtype, numel, slots, calls, config, dist="uniform", algo=None, fused=False):
         import torch
         import tensor_decode_all_gb300 as tda
         from tensor_decode_all_gb300 import inputs
         self.torch = torch
         self.op, self.R, self.dtype, self.numel, self.slots, self.C = op, R, dtype, numel, slots, calls
+        self.fused = fused  # one cooperative launch for all ranks of a call, instead of R launches
         tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "c64": torch.complex64}[dtype]
         self.tdt = tdt
         self.h = tda.Handle(R, tdt, numel, slots)
@@ -250,13 +253,18 @@ class Workload:
         with torch.cuda.stream(side):
             with torch.cuda.graph(g, stream=side):
                 cap = torch.cuda.current_stream()
-                for s in self.streams:
-                    s.wait_stream(cap)
-                for c in range(self.C):
-                    for r in range(self.R):
-                        getattr(self.h, self.op)(r, self.ins[r][c], self.outs[r][c], self.streams[r])
-                for s in self.streams:
-                    cap.wait_stream(s)
+                if self.fused:
+                    for c in range(self.C):
+                        getattr(self.h, self.op + "_fused")([self.ins[r][c] for r in range(self.R)],
+                                                            [self.outs[r][c] for r in range(self.R)], cap)
+                else:
+                    for s in self.streams:
+                        s.wait_stream(cap)
+                    for c in range(self.C):
+                        for r in range(self.R):
+                            getattr(self.h, self.op)(r, self.ins[r][c], self.outs[r][c], self.streams[r])
+                    for s in self.streams:
+                        cap.wait_stream(s)
         torch.cuda.current_stream().wait_stream(side)
         self.graph = g
         return g
@@ -535,14 +543,22 @@ def run_ours(args, dist):
             "allgather_c64_r8_hbm": ("allgather", 8, "c64", 500000, "hbm", 4, None, 20, 10, None),
             "allgather_c64_r4_pinned": ("allgather", 4, "c64", 500000, "pinned", 4, None, 5, 5, None),
             "allgather_c64_r8_pinned": ("allgather", 8, "c64", 500000, "pinned", 4, None, 5, 5, None),
+            # the same calls as one cooperative launch of all ranks (ar_*_fused)
+            "r2_fp16_4096_pinned_fused": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", 100, 20, None),
+            "r2_fp16_131072_pinned_fused": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 100, 20, None),
+            "r8_bf16_393216_hbm_fused": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20, None),
+            "r8_bf16_16MiB_hbm_fused": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 10, 10, None),
+            "allgather_c64_r8_hbm_fused": ("allgather", 8, "c64", 500000, "hbm", 4, None, 20, 10, None),
         }.items():
-            wx = Workload(op, RR, dt, nn, sl, cc, config=cfg, dist=dd or "uniform", algo=al)
+            fz = name.endswith("_fused")
+            wx = Workload(op, RR, dt, nn, sl, cc, config=cfg, dist=dd or "uniform", algo=al, fused=fz)
             wx.capture()
             wx.time_graph(1, 0, flush)
             wx.check(calls=(0, -1))
             msx = wx.time_graph(st, 2, flush)
             wx.check(calls=(-1,))
             extras[name] = summarize(op, RR, dt, nn, sl, msx, cc, link, hbm_gbs, wx.algo)
+            extras[name]["launch"] = "one cooperative launch per call" if fz else "one launch per rank per call"
             prof = profiled_traffic(name)
             if prof:
                 extras[name]["roofline"]["traffic"] = prof["dram_bytes_per_call"]
@@ -587,6 +603,7 @@ PROFILE_WORKLOADS = {
     "r8_bf16_16MiB_hbm_1call": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 1),
     "r8_bf16_16MiB_hbm_oneshot_1call": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 1),
     "allgather_c64_r8_hbm_1call": ("allgather", 8, "c64", 500000, "hbm", 4, "normal", 1),
+    "r8_bf16_768KiB_hbm_fused_1call": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 1),
 }
 
 
@@ -599,7 +616,8 @@ def run_profile(args, dist):
     tda.build()
     op, R, dt, n, sl, cfg, dd, C = PROFILE_WORKLOADS[args.profile]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-    w = Workload(op, R, dt, n, sl, C, config=cfg, dist=dd, algo="oneshot" if "oneshot" in args.profile else None)
+    w = Workload(op, R, dt, n, sl, C, config=cfg, dist=dd, algo="oneshot" if "oneshot" in args.profile else None,
+                 fused="fused" in args.profile)
     w.capture()
     ms = w.time_graph(args.steps, args.warmup, flush)
     w.check(calls=(0, -1))
@@ -676,7 +694,8 @@ def run_sweep(args, dist):
             # at least 4 calls per graph, so a step is not dominated by one graph launch
             C = max(4, min(100, (256 << 20) // max(1, R * S * 2)))
             steps = max(1, total // C)
-            w = Workload("allreduce", R, dtype, numel, slots, C, config=5, dist="uniform", algo=algo)
+            w = Workload("allreduce", R, dtype, numel, slots, C, config=5, dist="uniform", algo=algo,
+                         fused=args.sweep_fused)
             w.capture()
             w.time_graph(1, 0, flush)
             w.check(calls=(0, -1))
@@ -684,6 +703,7 @@ def run_sweep(args, dist):
             w.check(calls=(0, -1))
             row = summarize("allreduce", R, dtype, numel, slots, ms, C, link, hbm_gbs, w.algo)
             row["parity"] = "bit-exact (first and last call)"
+            row["launch"] = "fused" if args.sweep_fused else "per rank"
             row["host_link_probe_gbs"] = {k: round(v, 2) for k, v in link.items()}
             f.write(json.dumps(row) + "\n")
             f.flush()

@@ -206,6 +206,28 @@ AR_API int ar_allgather(ar_handle *h, int rank, const void *in, void *out, size_
                         ar_stream_t stream);
 
 /*
+ * ar_allreduce_fused / ar_allgather_fused -- one call of every rank at once,
+ * as a single launch on one stream.  Same operation, same bits and same
+ * handle state as R per-rank calls: ins[r] and outs[r] (host arrays of R
+ * device pointers, owned by the caller, each following the per-rank call's
+ * rules) are rank r's in and out.  The launch is cooperative, a grid of
+ * B x R blocks in which block (b, r) plays block b of rank r: the runtime
+ * either makes all R ranks' blocks resident together or refuses the launch
+ * (AR_ECUDA), so the ranks' waits for each other never depend on separate
+ * launches being scheduled side by side.  The pages run one rank per GPU and
+ * have no such form; on one GPU it is the co-resident way to run the ranks.
+ * Per-rank and fused calls may alternate on one handle, in order: a fused
+ * call counts as one call of every rank, and needs every rank to have issued
+ * the same number of calls before it (else AR_EINVAL, nothing enqueued).
+ * stream: non-blocking, as for the per-rank calls.  Capturable.
+ * Errors: as ar_allreduce / ar_allgather.
+ */
+AR_API int ar_allreduce_fused(ar_handle *h, const void *const *ins, void *const *outs, size_t numel,
+                              ar_stream_t stream);
+AR_API int ar_allgather_fused(ar_handle *h, const void *const *ins, void *const *outs, size_t numel,
+                              ar_stream_t stream);
+
+/*
  * ar_status -- the first device-side error recorded in the handle (AR_OK or
  * AR_ETIMEOUT), copied into *info if info is not NULL.  Reads mapped host
  * memory only (no CUDA call); the answer covers the kernels the caller has

@@ -97,6 +97,10 @@ def lib():
             L.ar_set_pdl.argtypes = [vp, i32]
             L.ar_allreduce_noalloc.argtypes = [i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, vp]
             L.ar_allreduce_noalloc.restype = i32
+            for name in ("ar_allreduce_fused", "ar_allgather_fused"):
+                f = getattr(L, name)
+                f.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, vp]
+                f.restype = i32
             L.ar_strerror.argtypes = [i32]
             L.ar_strerror.restype = ctypes.c_char_p
             L.ar_probe_host_link.argtypes = [u64, i32, ctypes.POINTER(ctypes.c_double)]
@@ -135,6 +139,20 @@ def ar_allreduce_noalloc(R: int, dtype: int, ins, outs, numel: int, stream: int)
     arr_in = (ctypes.c_void_p * R)(*[int(p) for p in ins])
     arr_out = (ctypes.c_void_p * R)(*[int(p) for p in outs])
     return lib().ar_allreduce_noalloc(R, dtype, arr_in, arr_out, numel, stream)
+
+
+def _ptr_array(ptrs):
+    ptrs = [int(p) for p in ptrs]
+    return (ctypes.c_void_p * len(ptrs))(*ptrs)
+
+
+def ar_allreduce_fused(h: int, ins, outs, numel: int, stream: int) -> int:
+    """Every rank's call at once, one cooperative launch (ins/outs: R device pointers)."""
+    return lib().ar_allreduce_fused(h, _ptr_array(ins), _ptr_array(outs), numel, stream)
+
+
+def ar_allgather_fused(h: int, ins, outs, numel: int, stream: int) -> int:
+    return lib().ar_allgather_fused(h, _ptr_array(ins), _ptr_array(outs), numel, stream)
 
 
 def ar_status(h: int) -> ErrorInfo:
@@ -274,6 +292,21 @@ class Handle:
     def allgather_all(self, ins, outs, streams) -> None:
         for r in range(self.R):
             self.allgather(r, ins[r], outs[r], streams[r])
+
+    def allreduce_fused(self, ins, outs, stream=None) -> None:
+        """All R ranks' calls as one launch on one stream (ins[r], outs[r]: rank r's tensors)."""
+        self._fused(ar_allreduce_fused, "ar_allreduce_fused", ins, outs, stream)
+
+    def allgather_fused(self, ins, outs, stream=None) -> None:
+        self._fused(ar_allgather_fused, "ar_allgather_fused", ins, outs, stream)
+
+    def _fused(self, fn, name, ins, outs, stream) -> None:
+        if len(ins) != self.R or len(outs) != self.R:
+            raise ValueError(f"{name}: need {self.R} inputs and outputs")
+        rc = fn(self.ptr, [t.data_ptr() for t in ins], [t.data_ptr() for t in outs], ins[0].numel(),
+                _stream_handle(stream))
+        if rc:
+            raise ArError(rc, name)
 
     def status(self) -> ErrorInfo:
         return ar_status(self.ptr)

@@ -43,13 +43,17 @@ struct Vec<1> {
     static __device__ __forceinline__ T ldcg(const void *p) { return ld_cg_u8(p); }
 };
 
-template <int VW, int R, int U>
+template <int VW, int R, int U, bool F>
 __global__ void __launch_bounds__(kThreads)
-    allgather_kernel(const uint8_t *in, uint8_t *out, uint64_t bytes, int rank, DevState d) {
+    allgather_kernel(const uint8_t *in_arg, uint8_t *out_arg, uint64_t bytes, int rank_arg, DevState d, RankIO io) {
     using V = typename Vec<VW>::T;
     __shared__ unsigned long long s_seq;
     __shared__ unsigned long long s_calls;
     __shared__ int s_bail;
+
+    const int rank = block_rank<F>(rank_arg);
+    const uint8_t *in = rank_ptr<R, F>(in_arg, io.in, rank);
+    uint8_t *out = rank_ptr<R, F>(out_arg, io.out, rank);
 
     const int b = blockIdx.x;
     const int B = gridDim.x;
@@ -138,51 +142,56 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-template <int VW, int U>
+template <int VW, int U, bool F>
 const void *allgather_ptr_ru(int R) {
     switch (R) {
-        case 1: return (const void *)allgather_kernel<VW, 1, U>;
-        case 2: return (const void *)allgather_kernel<VW, 2, U>;
-        case 3: return (const void *)allgather_kernel<VW, 3, U>;
-        case 4: return (const void *)allgather_kernel<VW, 4, U>;
-        case 5: return (const void *)allgather_kernel<VW, 5, U>;
-        case 6: return (const void *)allgather_kernel<VW, 6, U>;
-        case 7: return (const void *)allgather_kernel<VW, 7, U>;
-        case 8: return (const void *)allgather_kernel<VW, 8, U>;
+        case 1: return (const void *)allgather_kernel<VW, 1, U, F>;
+        case 2: return (const void *)allgather_kernel<VW, 2, U, F>;
+        case 3: return (const void *)allgather_kernel<VW, 3, U, F>;
+        case 4: return (const void *)allgather_kernel<VW, 4, U, F>;
+        case 5: return (const void *)allgather_kernel<VW, 5, U, F>;
+        case 6: return (const void *)allgather_kernel<VW, 6, U, F>;
+        case 7: return (const void *)allgather_kernel<VW, 7, U, F>;
+        case 8: return (const void *)allgather_kernel<VW, 8, U, F>;
         default: return nullptr;
     }
 }
 
+template <int VW, bool F>
+const void *allgather_ptr_rf(int R, int U) {
+    return U == 1 ? allgather_ptr_ru<VW, 1, F>(R) : allgather_ptr_ru<VW, 2, F>(R);
+}
+
 template <int VW>
-const void *allgather_ptr_r(int R, int U) {
-    return U == 1 ? allgather_ptr_ru<VW, 1>(R) : allgather_ptr_ru<VW, 2>(R);
+const void *allgather_ptr_r(int R, int U, bool fused) {
+    return fused ? allgather_ptr_rf<VW, true>(R, U) : allgather_ptr_rf<VW, false>(R, U);
 }
 
 }  // namespace
 
-const void *allgather_kernel_ptr(int vec_bytes, int R, int unroll) {
+const void *allgather_kernel_ptr(int vec_bytes, int R, int unroll, bool fused) {
     switch (vec_bytes) {
-        case 16: return allgather_ptr_r<16>(R, unroll);
-        case 8: return allgather_ptr_r<8>(R, unroll);
-        case 4: return allgather_ptr_r<4>(R, unroll);
-        case 2: return allgather_ptr_r<2>(R, unroll);
-        case 1: return allgather_ptr_r<1>(R, unroll);
+        case 16: return allgather_ptr_r<16>(R, unroll, fused);
+        case 8: return allgather_ptr_r<8>(R, unroll, fused);
+        case 4: return allgather_ptr_r<4>(R, unroll, fused);
+        case 2: return allgather_ptr_r<2>(R, unroll, fused);
+        case 1: return allgather_ptr_r<1>(R, unroll, fused);
         default: return nullptr;
     }
 }
 
 cudaError_t launch_allgather(int vec_bytes, int R, int unroll, int blocks, cudaStream_t s,
-                             const void *in, void *out, uint64_t bytes, int rank,
-                             const DevState &d, bool pdl) {
-    const void *k = allgather_kernel_ptr(vec_bytes, R, unroll);
+                             const RankIO &io, uint64_t bytes, int rank, const DevState &d, bool pdl) {
+    const void *k = allgather_kernel_ptr(vec_bytes, R, unroll, rank < 0);
     if (!k) return cudaErrorInvalidValue;
-    const uint8_t *a0 = static_cast<const uint8_t *>(in);
-    uint8_t *a1 = static_cast<uint8_t *>(out);
+    const uint8_t *a0 = static_cast<const uint8_t *>(io.in[0]);
+    uint8_t *a1 = static_cast<uint8_t *>(io.out[0]);
     uint64_t a2 = bytes;
     int a3 = rank;
     DevState a4 = d;
-    void *args[] = {&a0, &a1, &a2, &a3, &a4};
-    return launch(k, blocks, s, args, pdl);
+    RankIO a5 = io;
+    void *args[] = {&a0, &a1, &a2, &a3, &a4, &a5};
+    return launch(k, blocks, rank < 0 ? R : 1, rank < 0, s, args, pdl);
 }
 
 }  // namespace tda

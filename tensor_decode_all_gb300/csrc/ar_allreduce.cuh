@@ -1,9 +1,11 @@
 // ar_allreduce.cuh -- the exchange-and-add kernel of one logical rank.
 //
 // One launch per rank per call; all R launches of a call run at the same time
-// on their own streams.  Block b of every rank handles the same tiles (tile t
-// belongs to block t % B, in stage t / B), so block b pairs only with block b
-// of its peers, through one flag per (rank, block).
+// on their own streams.  (Or one cooperative launch of a B x R grid for all
+// ranks of a call, block (b, r) playing block b of rank r: the same code, with
+// co-residency guaranteed by the launch.)  Block b of every rank handles the
+// same tiles (tile t belongs to block t % B, in stage t / B), so block b pairs
+// only with block b of its peers, through one flag per (rank, block).
 //
 // Per stage, each block of rank r ("[Kernel] Two-rank FP16 all-reduce through
 // pinned host memory for GPUs without P2P", section "Purpose"):
@@ -125,12 +127,16 @@ __device__ __forceinline__ void store_out(uint16_t *out, uint64_t v, uint64_t nv
     }
 }
 
-template <class Ops, int R, int U>
-__global__ void __launch_bounds__(kThreads)
-    allreduce_kernel(const uint16_t *in, uint16_t *out, uint64_t numel, int rank, DevState d) {
+template <class Ops, int R, int U, bool F>
+__device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16_t *out_arg, uint64_t numel,
+                                                  int rank_arg, const DevState &d, const RankIO &io) {
     __shared__ unsigned long long s_seq;
     __shared__ unsigned long long s_calls;
     __shared__ int s_bail;
+
+    const int rank = block_rank<F>(rank_arg);
+    const uint16_t *in = rank_ptr<R, F>(in_arg, io.in, rank);
+    uint16_t *out = rank_ptr<R, F>(out_arg, io.out, rank);
 
     const int b = blockIdx.x;
     const int B = gridDim.x;
@@ -228,6 +234,22 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// One rank's launch.
+template <class Ops, int R, int U>
+__global__ void __launch_bounds__(kThreads)
+    allreduce_kernel_rank(const uint16_t *in, uint16_t *out, uint64_t numel, int rank, DevState d, RankIO io) {
+    allreduce_oneshot<Ops, R, U, false>(in, out, numel, rank, d, io);
+}
+
+// A launch of all ranks, held to the blocks per SM the one-rank kernel gets
+// unasked (5 up to R = 3, else 4): with fewer resident blocks a decode-sized
+// call would need a second stage, and a large one would move less at once.
+template <class Ops, int R, int U>
+__global__ void __launch_bounds__(kThreads, R <= 3 ? 5 : 4)
+    allreduce_kernel_all(const uint16_t *in, uint16_t *out, uint64_t numel, int rank, DevState d, RankIO io) {
+    allreduce_oneshot<Ops, R, U, true>(in, out, numel, rank, d, io);
+}
+
 // Two-shot variant, for large payloads at R >= 4, where the one-shot form's
 // R * (R - 1) * S bytes of peer-slot reads per call saturate L2.  A tile is R
 // sub-tiles of SUB vectors (SUB = 256, 128 or 64: smaller sub-tiles spread a
@@ -252,13 +274,17 @@ __global__ void __launch_bounds__(kThreads)
 template <int R>
 constexpr int twoshot_min_blocks() { return R <= 4 ? 6 : 4; }
 
-template <class Ops, int R, int SUB>
+template <class Ops, int R, int SUB, bool F>
 __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
-    allreduce_twoshot_kernel(const uint16_t *in, uint16_t *out, uint64_t numel, int rank, DevState d) {
+    allreduce_twoshot_kernel(const uint16_t *in_arg, uint16_t *out_arg, uint64_t numel, int rank_arg, DevState d, RankIO io) {
     static_assert(SUB == 64 || SUB == 128 || SUB == 256, "sub-tile of 64, 128 or 256 vectors");
     __shared__ unsigned long long s_seq;
     __shared__ unsigned long long s_calls;
     __shared__ int s_bail;
+
+    const int rank = block_rank<F>(rank_arg);
+    const uint16_t *in = rank_ptr<R, F>(in_arg, io.in, rank);
+    uint16_t *out = rank_ptr<R, F>(out_arg, io.out, rank);
 
     const int b = blockIdx.x;
     const int B = gridDim.x;
@@ -367,54 +393,65 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
 
 namespace tda {
 
-// Kernel entry for (element ops, R, unroll), as an untyped address for
-// cudaLaunchKernel and the occupancy calculator.
-template <class Ops, int U>
+// Kernel entry for (element ops, R, unroll, one rank or all ranks), as an
+// untyped address for cudaLaunchKernelExC and the occupancy calculator.
+template <class Ops, int R, int U, bool F>
+constexpr const void *oneshot_entry() {
+    return F ? (const void *)allreduce_kernel_all<Ops, R, U> : (const void *)allreduce_kernel_rank<Ops, R, U>;
+}
+
+template <class Ops, int U, bool F>
 const void *allreduce_ptr_ru(int R) {
     switch (R) {
-        case 1: return (const void *)allreduce_kernel<Ops, 1, U>;
-        case 2: return (const void *)allreduce_kernel<Ops, 2, U>;
-        case 3: return (const void *)allreduce_kernel<Ops, 3, U>;
-        case 4: return (const void *)allreduce_kernel<Ops, 4, U>;
-        case 5: return (const void *)allreduce_kernel<Ops, 5, U>;
-        case 6: return (const void *)allreduce_kernel<Ops, 6, U>;
-        case 7: return (const void *)allreduce_kernel<Ops, 7, U>;
-        case 8: return (const void *)allreduce_kernel<Ops, 8, U>;
+        case 1: return oneshot_entry<Ops, 1, U, F>();
+        case 2: return oneshot_entry<Ops, 2, U, F>();
+        case 3: return oneshot_entry<Ops, 3, U, F>();
+        case 4: return oneshot_entry<Ops, 4, U, F>();
+        case 5: return oneshot_entry<Ops, 5, U, F>();
+        case 6: return oneshot_entry<Ops, 6, U, F>();
+        case 7: return oneshot_entry<Ops, 7, U, F>();
+        case 8: return oneshot_entry<Ops, 8, U, F>();
         default: return nullptr;
     }
 }
 
-template <class Ops, int SUB>
+template <class Ops, int SUB, bool F>
 const void *allreduce_twoshot_ptr_r(int R) {
     switch (R) {
-        case 1: return (const void *)allreduce_twoshot_kernel<Ops, 1, SUB>;
-        case 2: return (const void *)allreduce_twoshot_kernel<Ops, 2, SUB>;
-        case 3: return (const void *)allreduce_twoshot_kernel<Ops, 3, SUB>;
-        case 4: return (const void *)allreduce_twoshot_kernel<Ops, 4, SUB>;
-        case 5: return (const void *)allreduce_twoshot_kernel<Ops, 5, SUB>;
-        case 6: return (const void *)allreduce_twoshot_kernel<Ops, 6, SUB>;
-        case 7: return (const void *)allreduce_twoshot_kernel<Ops, 7, SUB>;
-        case 8: return (const void *)allreduce_twoshot_kernel<Ops, 8, SUB>;
+        case 1: return (const void *)allreduce_twoshot_kernel<Ops, 1, SUB, F>;
+        case 2: return (const void *)allreduce_twoshot_kernel<Ops, 2, SUB, F>;
+        case 3: return (const void *)allreduce_twoshot_kernel<Ops, 3, SUB, F>;
+        case 4: return (const void *)allreduce_twoshot_kernel<Ops, 4, SUB, F>;
+        case 5: return (const void *)allreduce_twoshot_kernel<Ops, 5, SUB, F>;
+        case 6: return (const void *)allreduce_twoshot_kernel<Ops, 6, SUB, F>;
+        case 7: return (const void *)allreduce_twoshot_kernel<Ops, 7, SUB, F>;
+        case 8: return (const void *)allreduce_twoshot_kernel<Ops, 8, SUB, F>;
         default: return nullptr;
     }
 }
 
-template <class Ops>
+template <class Ops, bool F>
 const void *allreduce_twoshot_ptr(int R, int sub) {
     switch (sub) {
-        case 256: return allreduce_twoshot_ptr_r<Ops, 256>(R);
-        case 128: return allreduce_twoshot_ptr_r<Ops, 128>(R);
-        case 64: return allreduce_twoshot_ptr_r<Ops, 64>(R);
+        case 256: return allreduce_twoshot_ptr_r<Ops, 256, F>(R);
+        case 128: return allreduce_twoshot_ptr_r<Ops, 128, F>(R);
+        case 64: return allreduce_twoshot_ptr_r<Ops, 64, F>(R);
         default: return nullptr;
     }
 }
 
 // U = 1 or 2: one-shot with that many vectors per thread per stage;
 // U = twoshot_variant(sub): the two-shot form with sub-tiles of `sub` vectors.
+// fused: the kernel for one launch of all ranks (grid blocks x R).
+template <class Ops, bool F>
+const void *allreduce_ptr_f(int R, int U) {
+    if (U < 0) return allreduce_twoshot_ptr<Ops, F>(R, twoshot_sub(U));
+    return U == 1 ? allreduce_ptr_ru<Ops, 1, F>(R) : allreduce_ptr_ru<Ops, 2, F>(R);
+}
+
 template <class Ops>
-const void *allreduce_ptr(int R, int U) {
-    if (U < 0) return allreduce_twoshot_ptr<Ops>(R, twoshot_sub(U));
-    return U == 1 ? allreduce_ptr_ru<Ops, 1>(R) : allreduce_ptr_ru<Ops, 2>(R);
+const void *allreduce_ptr(int R, int U, bool fused) {
+    return fused ? allreduce_ptr_f<Ops, true>(R, U) : allreduce_ptr_f<Ops, false>(R, U);
 }
 
 }  // namespace tda

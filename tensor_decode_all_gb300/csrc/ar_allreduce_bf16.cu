@@ -2,5 +2,5 @@
 #include "ar_allreduce.cuh"
 
 namespace tda {
-const void *allreduce_kernel_ptr_bf16(int R, int U) { return allreduce_ptr<BF16Ops>(R, U); }
+const void *allreduce_kernel_ptr_bf16(int R, int U, bool fused) { return allreduce_ptr<BF16Ops>(R, U, fused); }
 }  // namespace tda

@@ -2,5 +2,5 @@
 #include "ar_allreduce.cuh"
 
 namespace tda {
-const void *allreduce_kernel_ptr_f16(int R, int U) { return allreduce_ptr<F16Ops>(R, U); }
+const void *allreduce_kernel_ptr_f16(int R, int U, bool fused) { return allreduce_ptr<F16Ops>(R, U, fused); }
 }  // namespace tda

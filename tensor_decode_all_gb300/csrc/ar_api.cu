@@ -23,7 +23,8 @@ struct ar_handle {
     int R = 0, dtype = 0, kind = 0, device = 0;
     uint64_t max_numel = 0, itemsize = 0, slot_bytes = 0;
     int sm_count = 0;
-    int bps_one = 0, bps_two = 0, bps_ag = 0;  // occupancy per kernel family
+    int bps_one = 0, bps_two = 0, bps_ag = 0;  // occupancy per kernel family (one rank's launch)
+    int bps_one_f = 0, bps_two_f = 0, bps_ag_f = 0;  // the same for one launch of all ranks
     int bmax = 0;                              // flag/counter slots per rank
     int algo = AR_ALGO_AUTO;
     int twoshot_sub = 0;                       // AR_TWOSHOT_SUB (64/128/256), for experiments; 0 = rule
@@ -158,24 +159,29 @@ int kernel_occupancy(const void *k, int *bps) {
     return AR_OK;
 }
 
-int handle_occupancy(ar_handle *h) {
-    int one = 1 << 30, two = 1 << 30, ag = 1 << 30;
+int family_occupancy(const ar_handle *h, bool fused, int *one, int *two, int *ag) {
+    *one = *two = *ag = 1 << 30;
     int rc = AR_OK;
     if (h->dtype == AR_F16 || h->dtype == AR_BF16) {
-        for (int u = 1; u <= 2 && rc == AR_OK; ++u) rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, u), &one);
+        for (int u = 1; u <= 2 && rc == AR_OK; ++u)
+            rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, u, fused), one);
         for (int sub = 64; sub <= 256 && rc == AR_OK; sub *= 2)
-            rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, tda::twoshot_variant(sub)), &two);
+            rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, tda::twoshot_variant(sub), fused), two);
     }
     for (int u = 1; u <= 2 && rc == AR_OK; ++u)
-        for (int vw = 1; vw <= 16 && rc == AR_OK; vw *= 2) rc = kernel_occupancy(tda::allgather_kernel_ptr(vw, h->R, u), &ag);
+        for (int vw = 1; vw <= 16 && rc == AR_OK; vw *= 2)
+            rc = kernel_occupancy(tda::allgather_kernel_ptr(vw, h->R, u, fused), ag);
     if (rc != AR_OK) return rc;
-    if (one == 1 << 30) one = ag;
-    if (two == 1 << 30) two = ag;
-    if (one < 1 || two < 1 || ag < 1) return AR_ECUDA;
-    h->bps_one = one;
-    h->bps_two = two;
-    h->bps_ag = ag;
+    if (*one == 1 << 30) *one = *ag;
+    if (*two == 1 << 30) *two = *ag;
+    if (*one < 1 || *two < 1 || *ag < 1) return AR_ECUDA;
     return AR_OK;
+}
+
+int handle_occupancy(ar_handle *h) {
+    int rc = family_occupancy(h, false, &h->bps_one, &h->bps_two, &h->bps_ag);
+    if (rc == AR_OK) rc = family_occupancy(h, true, &h->bps_one_f, &h->bps_two_f, &h->bps_ag_f);
+    return rc;
 }
 
 // Measured on a GB300 (one-shot vs two-shot, bf16, 64 KiB..8 MiB per rank):
@@ -293,6 +299,74 @@ int begin_call(ar_handle *h, int rank, const void *in, void *out, size_t numel, 
     return AR_OK;
 }
 
+// Checks and bookkeeping of a call that enqueues every rank at once: the same
+// declines as a per-rank call, for every rank's pointers, plus one rule of its
+// own: every rank must have issued the same number of calls on the handle (a
+// per-rank sequence left half-issued would pair with the wrong call).
+int begin_fused(ar_handle *h, const void *const *ins, void *const *outs, size_t numel, cudaStream_t s,
+                tda::RankIO *io) {
+    if (!h || !ins || !outs) return AR_EINVAL;
+    if (numel > h->max_numel) return AR_ETOOBIG;
+    if (numel == 0) return AR_OK;
+    *io = tda::RankIO{};
+    for (int r = 0; r < h->R; ++r) {
+        if (!ins[r] || !outs[r] || (((uintptr_t)ins[r] | (uintptr_t)outs[r]) % 16)) return AR_EINVAL;
+        io->in[r] = const_cast<void *>(ins[r]);
+        io->out[r] = outs[r];
+    }
+    int rc = check_stream(s);
+    if (rc != AR_OK) return rc;
+    rc = check_device(h);
+    if (rc != AR_OK) return rc;
+    if (*reinterpret_cast<volatile int32_t *>(&h->err_host->code) != AR_OK) return AR_ESTATE;
+    const uint64_t c = h->host_calls[0].load(std::memory_order_acquire);
+    for (int r = 1; r < h->R; ++r)
+        if (h->host_calls[r].load(std::memory_order_acquire) != c) return AR_EINVAL;
+    for (int r = 0; r < h->R; ++r) {
+        h->host_calls[r].fetch_add(1, std::memory_order_acq_rel);
+        h->host_stream[r].store((uintptr_t)s, std::memory_order_release);
+    }
+    return AR_OK;
+}
+
+// The all-reduce launch both entry points share: form, plan and grid from the
+// handle, then one launch for `rank` (or, rank < 0, all ranks at once).
+int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int rank, cudaStream_t s) {
+    const uint64_t bytes = numel * h->itemsize;
+    const int algo = h->algo == AR_ALGO_AUTO ? choose_algo(h->R, bytes, h->kind) : h->algo;
+    const bool fused = rank < 0;
+    const int bps = algo == AR_ALGO_TWOSHOT ? (fused ? h->bps_two_f : h->bps_two) : (fused ? h->bps_one_f : h->bps_one);
+    ar_plan plan;
+    int rc = plan_compute_sub(h->R, bytes, 16, algo, handle_twoshot_sub(h, bytes), tda::kThreads, h->sm_count, bps,
+                              &plan);
+    if (rc != AR_OK) return rc;
+    const int blocks = plan.blocks < h->bmax ? plan.blocks : h->bmax;
+    const int variant = algo == AR_ALGO_TWOSHOT ? tda::twoshot_variant(plan.subtile_vecs) : plan.unroll;
+    const cudaError_t e = tda::launch_allreduce(h->dtype, h->R, variant, blocks, s, io, numel, rank,
+                                                dev_state(h), h->pdl);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ECUDA;
+    }
+    return AR_OK;
+}
+
+int enqueue_allgather(ar_handle *h, const tda::RankIO &io, size_t numel, int rank, int vw, cudaStream_t s) {
+    const uint64_t bytes = numel * h->itemsize;
+    ar_plan plan;
+    int rc = plan_compute(h->R, bytes, vw, AR_ALGO_ONESHOT, tda::kThreads, h->sm_count,
+                          rank < 0 ? h->bps_ag_f : h->bps_ag, &plan);
+    if (rc != AR_OK) return rc;
+    const int blocks = plan.blocks < h->bmax ? plan.blocks : h->bmax;
+    const cudaError_t e = tda::launch_allgather(vw, h->R, plan.unroll, blocks, s, io, bytes, rank,
+                                                dev_state(h), h->pdl);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ECUDA;
+    }
+    return AR_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -362,6 +436,7 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
     // per SM already keep the link busy and more only add contention (R=4 bf16
     // 8 MiB: 382 vs 362 us), so pinned slots keep 4.
     if (h->kind == AR_SLOT_PINNED_HOST && h->bps_two > 4) h->bps_two = 4;
+    if (h->kind == AR_SLOT_PINNED_HOST && h->bps_two_f > 4) h->bps_two_f = 4;
     int bps_max = h->bps_one > h->bps_two ? h->bps_one : h->bps_two;
     if (h->bps_ag > bps_max) bps_max = h->bps_ag;
     h->bmax = h->sm_count * bps_max / R;
@@ -406,21 +481,10 @@ AR_API int ar_allreduce(ar_handle *h, int rank, const void *in, void *out, size_
     uint64_t call = 0;
     int rc = begin_call(h, rank, in, out, numel, s, &call);
     if (rc != AR_OK || numel == 0) return rc;
-    const uint64_t bytes = numel * h->itemsize;
-    const int algo = h->algo == AR_ALGO_AUTO ? choose_algo(h->R, bytes, h->kind) : h->algo;
-    ar_plan plan;
-    rc = plan_compute_sub(h->R, bytes, 16, algo, handle_twoshot_sub(h, bytes), tda::kThreads, h->sm_count,
-                          algo == AR_ALGO_TWOSHOT ? h->bps_two : h->bps_one, &plan);
-    if (rc != AR_OK) return rc;
-    int blocks = plan.blocks < h->bmax ? plan.blocks : h->bmax;
-    const int variant = algo == AR_ALGO_TWOSHOT ? tda::twoshot_variant(plan.subtile_vecs) : plan.unroll;
-    const cudaError_t e = tda::launch_allreduce(h->dtype, h->R, variant, blocks, s, in, out,
-                                                numel, rank, dev_state(h), h->pdl);
-    if (e != cudaSuccess) {
-        (void)cudaGetLastError();
-        return AR_ECUDA;
-    }
-    return AR_OK;
+    tda::RankIO io = {};
+    io.in[0] = const_cast<void *>(in);
+    io.out[0] = out;
+    return enqueue_allreduce(h, io, numel, rank, s);
 }
 
 AR_API int ar_allgather(ar_handle *h, int rank, const void *in, void *out, size_t numel,
@@ -430,19 +494,35 @@ AR_API int ar_allgather(ar_handle *h, int rank, const void *in, void *out, size_
     uint64_t call = 0;
     int rc = begin_call(h, rank, in, out, numel, s, &call);
     if (rc != AR_OK || numel == 0) return rc;
+    tda::RankIO io = {};
+    io.in[0] = const_cast<void *>(in);
+    io.out[0] = out;
+    return enqueue_allgather(h, io, numel, rank, allgather_vec(numel * h->itemsize, in, out), s);
+}
+
+AR_API int ar_allreduce_fused(ar_handle *h, const void *const *ins, void *const *outs, size_t numel,
+                              ar_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (h && h->dtype != AR_F16 && h->dtype != AR_BF16) return AR_EINVAL;
+    tda::RankIO io;
+    int rc = begin_fused(h, ins, outs, numel, s, &io);
+    if (rc != AR_OK || numel == 0) return rc;
+    return enqueue_allreduce(h, io, numel, -1, s);
+}
+
+AR_API int ar_allgather_fused(ar_handle *h, const void *const *ins, void *const *outs, size_t numel,
+                              ar_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    tda::RankIO io;
+    int rc = begin_fused(h, ins, outs, numel, s, &io);
+    if (rc != AR_OK || numel == 0) return rc;
     const uint64_t bytes = numel * h->itemsize;
-    const int vw = allgather_vec(bytes, in, out);
-    ar_plan plan;
-    rc = plan_compute(h->R, bytes, vw, AR_ALGO_ONESHOT, tda::kThreads, h->sm_count, h->bps_ag, &plan);
-    if (rc != AR_OK) return rc;
-    int blocks = plan.blocks < h->bmax ? plan.blocks : h->bmax;
-    const cudaError_t e = tda::launch_allgather(vw, h->R, plan.unroll, blocks, s, in, out, bytes,
-                                                rank, dev_state(h), h->pdl);
-    if (e != cudaSuccess) {
-        (void)cudaGetLastError();
-        return AR_ECUDA;
+    int vw = 16;
+    for (int r = 0; r < h->R; ++r) {
+        const int v = allgather_vec(bytes, ins[r], outs[r]);
+        if (v < vw) vw = v;
     }
-    return AR_OK;
+    return enqueue_allgather(h, io, numel, -1, vw, s);
 }
 
 AR_API int ar_status(ar_handle *h, ar_error_info *info) {
@@ -548,39 +628,47 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) 
 
 namespace tda {
 
-const void *allreduce_kernel_ptr(int dtype, int R, int unroll) {
-    if (dtype == AR_F16) return allreduce_kernel_ptr_f16(R, unroll);
-    if (dtype == AR_BF16) return allreduce_kernel_ptr_bf16(R, unroll);
+const void *allreduce_kernel_ptr(int dtype, int R, int unroll, bool fused) {
+    if (dtype == AR_F16) return allreduce_kernel_ptr_f16(R, unroll, fused);
+    if (dtype == AR_BF16) return allreduce_kernel_ptr_bf16(R, unroll, fused);
     return nullptr;
 }
 
 cudaError_t launch_allreduce(int dtype, int R, int unroll, int blocks, cudaStream_t s,
-                             const void *in, void *out, uint64_t numel, int rank,
-                             const DevState &d, bool pdl) {
-    const void *k = allreduce_kernel_ptr(dtype, R, unroll);
+                             const RankIO &io, uint64_t numel, int rank, const DevState &d, bool pdl) {
+    const void *k = allreduce_kernel_ptr(dtype, R, unroll, rank < 0);
     if (!k) return cudaErrorInvalidValue;
-    const uint16_t *a0 = static_cast<const uint16_t *>(in);
-    uint16_t *a1 = static_cast<uint16_t *>(out);
+    const uint16_t *a0 = static_cast<const uint16_t *>(io.in[0]);
+    uint16_t *a1 = static_cast<uint16_t *>(io.out[0]);
     uint64_t a2 = numel;
     int a3 = rank;
     DevState a4 = d;
-    void *args[] = {&a0, &a1, &a2, &a3, &a4};
-    return launch(k, blocks, s, args, pdl);
+    RankIO a5 = io;
+    void *args[] = {&a0, &a1, &a2, &a3, &a4, &a5};
+    return launch(k, blocks, rank < 0 ? R : 1, rank < 0, s, args, pdl);
 }
 
-cudaError_t launch(const void *k, int blocks, cudaStream_t s, void **args, bool pdl) {
+cudaError_t launch(const void *k, int blocks, int ranks, bool cooperative, cudaStream_t s, void **args,
+                   bool pdl) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(blocks);
+    cfg.gridDim = dim3((unsigned)blocks, (unsigned)ranks);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    int n = 0;
     if (pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
     }
+    if (cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
     return cudaLaunchKernelExC(&cfg, k, args);
 }
 

@@ -47,22 +47,36 @@ struct DevState {
     int sys_scope;             // 1: slots/flags in host memory, system-scope ordering
 };
 
-// Launch kernel k with `blocks` x kThreads on s; with pdl, as a programmatic
-// dependent of the preceding work on s.
-cudaError_t launch(const void *k, int blocks, cudaStream_t s, void **args, bool pdl);
+// The input and output pointers of every rank, passed by value to a launch
+// of all R ranks at once (grid blocks x R; block (b, r) plays block b of rank
+// r with in[r] / out[r]).  A launch for one rank passes its own pointers as
+// separate arguments, and its kernel ignores this.
+struct RankIO {
+    void *in[kMaxRanks];   // read only
+    void *out[kMaxRanks];
+};
 
-// Launchers (one per kernel family).  Return cudaSuccess or the launch error.
+// Launch kernel k on s with kThreads threads a block and a grid of `blocks`
+// (one rank) or blocks x ranks (all ranks, ranks > 1 or a negative rank
+// argument): the latter as a cooperative launch, so that the runtime either
+// makes every block resident at once or refuses the launch.  With pdl, as a
+// programmatic dependent of the preceding work on s.
+cudaError_t launch(const void *k, int blocks, int ranks, bool cooperative, cudaStream_t s, void **args,
+                   bool pdl);
+
+// Launchers (one per kernel family).  rank >= 0: that rank's kernel, `blocks`
+// blocks; rank < 0: all R ranks in one cooperative grid of blocks x R.
+// Return cudaSuccess or the launch error.
 cudaError_t launch_allreduce(int dtype, int R, int unroll, int blocks, cudaStream_t s,
-                             const void *in, void *out, uint64_t numel, int rank,
-                             const DevState &d, bool pdl);
+                             const RankIO &io, uint64_t numel, int rank, const DevState &d, bool pdl);
 cudaError_t launch_allgather(int vec_bytes, int R, int unroll, int blocks, cudaStream_t s,
-                             const void *in, void *out, uint64_t bytes, int rank,
-                             const DevState &d, bool pdl);
+                             const RankIO &io, uint64_t bytes, int rank, const DevState &d, bool pdl);
 
-// Kernel entry addresses, for occupancy queries.
-const void *allreduce_kernel_ptr(int dtype, int R, int unroll);
-const void *allreduce_kernel_ptr_f16(int R, int unroll);   // ar_allreduce_f16.cu
-const void *allreduce_kernel_ptr_bf16(int R, int unroll);  // ar_allreduce_bf16.cu
-const void *allgather_kernel_ptr(int vec_bytes, int R, int unroll);
+// Kernel entry addresses, for occupancy queries.  fused: the kernel built for
+// one launch of all ranks (grid blocks x R) rather than one rank's launch.
+const void *allreduce_kernel_ptr(int dtype, int R, int unroll, bool fused);
+const void *allreduce_kernel_ptr_f16(int R, int unroll, bool fused);   // ar_allreduce_f16.cu
+const void *allreduce_kernel_ptr_bf16(int R, int unroll, bool fused);  // ar_allreduce_bf16.cu
+const void *allgather_kernel_ptr(int vec_bytes, int R, int unroll, bool fused);
 
 }  // namespace tda

@@ -82,6 +82,25 @@ __device__ __forceinline__ unsigned char ld_cg_u8(const void *p) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// The rank a block plays, and its input and output.  A kernel built for one
+// rank's launch (F = false) takes the rank argument and its own in/out
+// arguments, unchanged.  A kernel built for a launch of all ranks at once
+// (F = true) takes the block's row of the grid and that rank's pointers from
+// io (selects over the R entries: an index into the parameter array would
+// copy it to local memory).
+template <bool F>
+__device__ __forceinline__ int block_rank(int rank_arg) { return F ? (int)blockIdx.y : rank_arg; }
+
+template <int R, bool F, class T>
+__device__ __forceinline__ T *rank_ptr(T *own, void *const (&table)[kMaxRanks], int rank) {
+    if (!F) return own;
+    T *p = static_cast<T *>(table[0]);
+#pragma unroll
+    for (int q = 1; q < R; ++q)
+        if (rank == q) p = static_cast<T *>(table[q]);
+    return p;
+}
+
 __device__ __forceinline__ unsigned long long *flag_ptr(const DevState &d, int rank, int block) {
     return d.flags + ((size_t)rank * d.bmax + block) * kFlagStrideWords;
 }
