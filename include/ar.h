@@ -137,6 +137,16 @@ typedef struct ar_plan {
     uint64_t max_stages;    /* stages of block 0 = ceil(tiles / blocks) */
 } ar_plan;
 
+/* Per-handle tactics: which all-reduce form AR_ALGO_AUTO picks by size, and the
+ * launch shape.  ar_create fills them from the built-in table (ar_choose_algo);
+ * ar_set_tactics replaces them, for instance with values measured on this GPU
+ * and stored by the caller (the Python package's tune module does both). */
+typedef struct ar_tactics {
+    uint64_t twoshot_min_bytes; /* AUTO picks two-shot from this many bytes per rank; UINT64_MAX: never */
+    int32_t twoshot_sub;        /* two-shot sub-tile in vectors: 64, 128 or 256; 0 = the size rule */
+    int32_t max_blocks;         /* cap on blocks per rank (>= 1); 0 = as many as fit (occupancy) */
+} ar_tactics;
+
 /*
  * ar_create -- allocate a handle for R logical ranks.
  *
@@ -301,6 +311,25 @@ AR_API int ar_set_pdl(ar_handle *h, int enable);
  * environment variable AR_ALGO=oneshot|twoshot sets it at ar_create.  Every
  * rank of a call must see the same setting; set it before enqueuing. */
 AR_API int ar_set_algo(ar_handle *h, int algo);
+
+/* Read or replace a handle's tactics (see ar_tactics).  Every rank shares the
+ * handle, so all ranks see the same values; change them only between calls
+ * (not while a call is half issued).  Errors: AR_EINVAL for a NULL argument,
+ * a sub-tile other than 0/64/128/256, or a negative block cap. */
+AR_API int ar_get_tactics(const ar_handle *h, ar_tactics *t);
+AR_API int ar_set_tactics(ar_handle *h, const ar_tactics *t);
+
+/*
+ * ar_supports -- would ar_allreduce (op 0) or ar_allgather (op 1) accept this
+ * call?  Makes the argument checks the enqueue calls make before any CUDA
+ * work, except the stream's (no CUDA call here): AR_OK, or the code the call
+ * would return -- AR_EINVAL (NULL handle, unknown op, all-reduce on a
+ * complex64 handle, NULL or non-16-byte-aligned in/out when numel > 0) or
+ * AR_ETOOBIG (numel > max_numel).  Lets a caller route a tensor to its
+ * fallback before it enqueues anything ("[SM120] Add optional FlashInfer
+ * PCIe-IPC all-reduce for switch-free hosts", section "Modifications").
+ */
+AR_API int ar_supports(const ar_handle *h, int op, size_t numel, const void *in, const void *out);
 
 /*
  * ar_allreduce_noalloc -- an all-reduce that allocates nothing.  The paper has

@@ -51,6 +51,11 @@ class Info(ctypes.Structure):
                 ("total_slot_bytes", ctypes.c_uint64), ("timeout_ns", ctypes.c_uint64)]
 
 
+class Tactics(ctypes.Structure):
+    _fields_ = [("twoshot_min_bytes", ctypes.c_uint64), ("twoshot_sub", ctypes.c_int32),
+                ("max_blocks", ctypes.c_int32)]
+
+
 class Plan(ctypes.Structure):
     _fields_ = [("blocks", ctypes.c_int32), ("threads", ctypes.c_int32), ("vec_bytes", ctypes.c_int32),
                 ("unroll", ctypes.c_int32), ("algo", ctypes.c_int32), ("flag_rounds", ctypes.c_int32),
@@ -95,6 +100,9 @@ def lib():
             L.ar_choose_algo.argtypes = [i32, u64, i32]
             L.ar_set_algo.argtypes = [vp, i32]
             L.ar_set_pdl.argtypes = [vp, i32]
+            L.ar_get_tactics.argtypes = [vp, ctypes.POINTER(Tactics)]
+            L.ar_set_tactics.argtypes = [vp, ctypes.POINTER(Tactics)]
+            L.ar_supports.argtypes = [vp, i32, sz, vp, vp]
             L.ar_allreduce_noalloc.argtypes = [i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, vp]
             L.ar_allreduce_noalloc.restype = i32
             for name in ("ar_allreduce_fused", "ar_allgather_fused"):
@@ -139,6 +147,22 @@ def ar_allreduce_noalloc(R: int, dtype: int, ins, outs, numel: int, stream: int)
     arr_in = (ctypes.c_void_p * R)(*[int(p) for p in ins])
     arr_out = (ctypes.c_void_p * R)(*[int(p) for p in outs])
     return lib().ar_allreduce_noalloc(R, dtype, arr_in, arr_out, numel, stream)
+
+
+def ar_get_tactics(h: int) -> Tactics:
+    t = Tactics()
+    rc = lib().ar_get_tactics(h, ctypes.byref(t))
+    if rc:
+        raise ArError(rc, "ar_get_tactics")
+    return t
+
+
+def ar_set_tactics(h: int, t: Tactics) -> int:
+    return lib().ar_set_tactics(h, ctypes.byref(t))
+
+
+def ar_supports(h: int, op: int, numel: int, inp: int, out: int) -> int:
+    return lib().ar_supports(h, op, numel, inp, out)
 
 
 def _ptr_array(ptrs):
@@ -341,6 +365,25 @@ class Handle:
 
     def info(self) -> Info:
         return ar_query(self.ptr)
+
+    def tactics(self) -> dict:
+        t = ar_get_tactics(self.ptr)
+        return {"twoshot_min_bytes": int(t.twoshot_min_bytes), "twoshot_sub": int(t.twoshot_sub),
+                "max_blocks": int(t.max_blocks)}
+
+    def set_tactics(self, twoshot_min_bytes=None, twoshot_sub=None, max_blocks=None) -> None:
+        """Replace some or all of the handle's tactics (see ar_tactics in ar.h)."""
+        cur = self.tactics()
+        t = Tactics(int(cur["twoshot_min_bytes"] if twoshot_min_bytes is None else twoshot_min_bytes),
+                    int(cur["twoshot_sub"] if twoshot_sub is None else twoshot_sub),
+                    int(cur["max_blocks"] if max_blocks is None else max_blocks))
+        rc = ar_set_tactics(self.ptr, t)
+        if rc:
+            raise ArError(rc, "ar_set_tactics")
+
+    def supports(self, op: str, inp, out) -> int:
+        """AR_OK if ar_allreduce / ar_allgather would accept these tensors, else its code."""
+        return ar_supports(self.ptr, 0 if op == "allreduce" else 1, inp.numel(), inp.data_ptr(), out.data_ptr())
 
     def plan(self, op: str, numel: int) -> Plan:
         return ar_plan_for(self.ptr, 0 if op == "allreduce" else 1, numel)

@@ -27,7 +27,9 @@ struct ar_handle {
     int bps_one_f = 0, bps_two_f = 0, bps_ag_f = 0;  // the same for one launch of all ranks
     int bmax = 0;                              // flag/counter slots per rank
     int algo = AR_ALGO_AUTO;
-    int twoshot_sub = 0;                       // AR_TWOSHOT_SUB (64/128/256), for experiments; 0 = rule
+    int twoshot_sub = 0;                       // tactic: two-shot sub-tile (64/128/256); 0 = size rule
+    uint64_t twoshot_min_bytes = ~0ull;        // tactic: AUTO picks two-shot from this size per rank
+    int max_blocks = 0;                        // tactic: cap on blocks per rank; 0 = occupancy
     bool pdl = true;                           // launch as programmatic dependents
     void *slots_host = nullptr;            // pinned kind: host address of the slots
     uint8_t *slots_dev = nullptr;          // device address of the slots
@@ -189,14 +191,28 @@ int handle_occupancy(ar_handle *h) {
 // over the host link, where one-shot reads R(R-1)S bytes against two-shot's
 // (2R-1)S, it wins from 64 KiB at R = 8 and from 256 KiB at R = 4.  Ranks in
 // between take the threshold of the smaller measured R; R <= 3 stays one-shot.
+uint64_t twoshot_threshold(int R, int slot_kind) {
+    if (R < 4) return ~0ull;
+    if (slot_kind == AR_SLOT_PINNED_HOST) return R >= 8 ? (64ull << 10) : (256ull << 10);
+    return R >= 8 ? (512ull << 10) : (2ull << 20);
+}
+
 int choose_algo(int R, uint64_t bytes, int slot_kind) {
-    if (R < 4) return AR_ALGO_ONESHOT;
-    uint64_t threshold;
-    if (slot_kind == AR_SLOT_PINNED_HOST)
-        threshold = R >= 8 ? (64ull << 10) : (256ull << 10);
-    else
-        threshold = R >= 8 ? (512ull << 10) : (2ull << 20);
-    return bytes >= threshold ? AR_ALGO_TWOSHOT : AR_ALGO_ONESHOT;
+    return bytes >= twoshot_threshold(R, slot_kind) ? AR_ALGO_TWOSHOT : AR_ALGO_ONESHOT;
+}
+
+// The form a handle's call of `bytes` per rank takes: forced, or its tactic.
+int handle_algo(const ar_handle *h, uint64_t bytes) {
+    if (h->algo != AR_ALGO_AUTO) return h->algo;
+    return bytes >= h->twoshot_min_bytes ? AR_ALGO_TWOSHOT : AR_ALGO_ONESHOT;
+}
+
+// Blocks per rank a handle launches for a plan: the plan's, within the flag
+// slots and the tactic's cap.
+int handle_blocks(const ar_handle *h, int plan_blocks) {
+    int b = plan_blocks < h->bmax ? plan_blocks : h->bmax;
+    if (h->max_blocks > 0 && b > h->max_blocks) b = h->max_blocks;
+    return b;
 }
 
 // Sub-tile size (vectors) of the two-shot form.  256 unless the slots are in
@@ -333,14 +349,14 @@ int begin_fused(ar_handle *h, const void *const *ins, void *const *outs, size_t 
 // handle, then one launch for `rank` (or, rank < 0, all ranks at once).
 int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int rank, cudaStream_t s) {
     const uint64_t bytes = numel * h->itemsize;
-    const int algo = h->algo == AR_ALGO_AUTO ? choose_algo(h->R, bytes, h->kind) : h->algo;
+    const int algo = handle_algo(h, bytes);
     const bool fused = rank < 0;
     const int bps = algo == AR_ALGO_TWOSHOT ? (fused ? h->bps_two_f : h->bps_two) : (fused ? h->bps_one_f : h->bps_one);
     ar_plan plan;
     int rc = plan_compute_sub(h->R, bytes, 16, algo, handle_twoshot_sub(h, bytes), tda::kThreads, h->sm_count, bps,
                               &plan);
     if (rc != AR_OK) return rc;
-    const int blocks = plan.blocks < h->bmax ? plan.blocks : h->bmax;
+    const int blocks = handle_blocks(h, plan.blocks);
     const int variant = algo == AR_ALGO_TWOSHOT ? tda::twoshot_variant(plan.subtile_vecs) : plan.unroll;
     const cudaError_t e = tda::launch_allreduce(h->dtype, h->R, variant, blocks, s, io, numel, rank,
                                                 dev_state(h), h->pdl);
@@ -357,7 +373,7 @@ int enqueue_allgather(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
     int rc = plan_compute(h->R, bytes, vw, AR_ALGO_ONESHOT, tda::kThreads, h->sm_count,
                           rank < 0 ? h->bps_ag_f : h->bps_ag, &plan);
     if (rc != AR_OK) return rc;
-    const int blocks = plan.blocks < h->bmax ? plan.blocks : h->bmax;
+    const int blocks = handle_blocks(h, plan.blocks);
     const cudaError_t e = tda::launch_allgather(vw, h->R, plan.unroll, blocks, s, io, bytes, rank,
                                                 dev_state(h), h->pdl);
     if (e != cudaSuccess) {
@@ -425,6 +441,7 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
         const long v = std::strtol(e, nullptr, 10);
         if (v == 64 || v == 128 || v == 256) h->twoshot_sub = (int)v;
     }
+    h->twoshot_min_bytes = twoshot_threshold(R, slot_kind);
     if (const char *e = std::getenv("AR_ALGO")) {
         if (!std::strcmp(e, "oneshot")) h->algo = AR_ALGO_ONESHOT;
         else if (!std::strcmp(e, "twoshot")) h->algo = AR_ALGO_TWOSHOT;
@@ -605,6 +622,34 @@ AR_API int ar_set_algo(ar_handle *h, int algo) {
     return AR_OK;
 }
 
+AR_API int ar_get_tactics(const ar_handle *h, ar_tactics *t) {
+    if (!h || !t) return AR_EINVAL;
+    t->twoshot_min_bytes = h->twoshot_min_bytes;
+    t->twoshot_sub = h->twoshot_sub;
+    t->max_blocks = h->max_blocks;
+    return AR_OK;
+}
+
+AR_API int ar_set_tactics(ar_handle *h, const ar_tactics *t) {
+    if (!h || !t) return AR_EINVAL;
+    if (t->twoshot_sub != 0 && t->twoshot_sub != 64 && t->twoshot_sub != 128 && t->twoshot_sub != 256)
+        return AR_EINVAL;
+    if (t->max_blocks < 0) return AR_EINVAL;
+    h->twoshot_min_bytes = t->twoshot_min_bytes;
+    h->twoshot_sub = t->twoshot_sub;
+    h->max_blocks = t->max_blocks;
+    return AR_OK;
+}
+
+AR_API int ar_supports(const ar_handle *h, int op, size_t numel, const void *in, const void *out) {
+    if (!h || (op != 0 && op != 1)) return AR_EINVAL;
+    if (op == 0 && h->dtype != AR_F16 && h->dtype != AR_BF16) return AR_EINVAL;
+    if (((uintptr_t)in | (uintptr_t)out) % 16) return AR_EINVAL;
+    if (numel > h->max_numel) return AR_ETOOBIG;
+    if (numel > 0 && (!in || !out)) return AR_EINVAL;
+    return AR_OK;
+}
+
 AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) {
     if (!h || !plan || (op != 0 && op != 1)) return AR_EINVAL;
     if (numel > h->max_numel) return AR_ETOOBIG;
@@ -612,14 +657,14 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) 
     const int vec = op == 0 ? 16 : allgather_vec(bytes, nullptr, nullptr);
     int algo = AR_ALGO_ONESHOT, bps = h->bps_ag;
     if (op == 0) {
-        algo = h->algo == AR_ALGO_AUTO ? choose_algo(h->R, bytes, h->kind) : h->algo;
+        algo = handle_algo(h, bytes);
         bps = algo == AR_ALGO_TWOSHOT ? h->bps_two : h->bps_one;
     }
     int rc = plan_compute_sub(h->R, bytes, vec, algo, op == 0 ? handle_twoshot_sub(h, bytes) : 0, tda::kThreads,
                               h->sm_count, bps, plan);
-    if (rc == AR_OK && plan->blocks > h->bmax) {
-        plan->blocks = h->bmax;
-        plan->max_stages = (plan->tiles + h->bmax - 1) / h->bmax;
+    if (rc == AR_OK && plan->blocks > 0) {
+        plan->blocks = handle_blocks(h, plan->blocks);
+        plan->max_stages = (plan->tiles + plan->blocks - 1) / plan->blocks;
     }
     return rc;
 }

@@ -1,0 +1,147 @@
+"""Measure a handle's all-reduce tactics on this GPU, and keep them.
+
+The library's built-in table (ar_choose_algo) puts the one-shot / two-shot
+crossover where it was measured on one GB300.  A caller on another GPU, or
+with another clock or memory configuration, can measure it again: ``tune``
+times both forms at power-of-two sizes, each in a CUDA graph of several calls
+of every rank (the way decode replays them), picks the smallest measured size
+from which two-shot is faster at that size and at every larger one, and sets
+it on the handle.  ``save`` / ``load`` keep the result in a JSON file keyed by
+the GPU and the handle's shape, so a later process applies it without
+measuring ("[SM120] Add optional FlashInfer PCIe-IPC all-reduce for
+switch-free hosts", section "Modifications": a tuned, per-size choice of
+kernel, with declines for what it does not support).
+
+Timing only: the results of these calls are not checked here (the tests
+check both forms against the oracle).
+"""
+from __future__ import annotations
+
+import json
+import os
+
+NEVER = (1 << 64) - 1
+DTYPE_NAMES = {1: "f16", 2: "bf16", 3: "c64"}
+SLOT_NAMES = {0: "pinned", 1: "hbm"}
+
+
+def key_for(device_name: str, sm_count: int, R: int, dtype: int, slot_kind: int) -> str:
+    """The file key of a tactic: GPU model and SM count, ranks, dtype, slot kind."""
+    return f"{device_name}|sm{sm_count}|R{R}|{DTYPE_NAMES.get(dtype, dtype)}|{SLOT_NAMES.get(slot_kind, slot_kind)}"
+
+
+def handle_key(handle) -> str:
+    import torch
+    info = handle.info()
+    return key_for(torch.cuda.get_device_name(info.device), info.sm_count, info.R, info.dtype, info.slot_kind)
+
+
+def crossover(times: dict) -> int:
+    """times: {bytes: {"oneshot": us, "twoshot": us}}.  The smallest size from
+    which two-shot is faster at that size and every larger measured size, or
+    NEVER if two-shot is not faster at the largest one."""
+    threshold = NEVER
+    for size in sorted(times, reverse=True):
+        t = times[size]
+        if t["twoshot"] < t["oneshot"]:
+            threshold = size
+        else:
+            break
+    return threshold
+
+
+def _time_form(handle, algo: str, nbytes: int, calls: int, replays: int) -> float:
+    """µs per call of one form at one size: graph of `calls` calls of every rank."""
+    import torch
+    R = handle.R
+    dt = {1: torch.float16, 2: torch.bfloat16}[handle.dtype]
+    numel = nbytes // 2
+    handle.set_algo(algo)
+    streams = [torch.cuda.Stream() for _ in range(R)]
+    ins = [[torch.rand(numel, device="cuda").to(dt) for _ in range(R)] for _ in range(calls)]
+    outs = [[torch.empty(numel, dtype=dt, device="cuda") for _ in range(R)] for _ in range(calls)]
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            cap = torch.cuda.current_stream()
+            for s in streams:
+                s.wait_stream(cap)
+            for c in range(calls):
+                for r in range(R):
+                    handle.allreduce(r, ins[c][r], outs[c][r], streams[r])
+            for s in streams:
+                cap.wait_stream(s)
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(cur)
+    for _ in range(replays):
+        g.replay()
+    b.record(cur)
+    torch.cuda.synchronize()
+    handle.check()
+    del g
+    return a.elapsed_time(b) * 1e3 / (replays * calls)
+
+
+def measure(handle, sizes=None, replays: int = 5) -> dict:
+    """{bytes: {"oneshot": us, "twoshot": us}} at power-of-two sizes from
+    64 KiB to min(8 MiB, the handle's max payload)."""
+    max_bytes = handle.max_numel * 2
+    if sizes is None:
+        sizes = [1 << k for k in range(16, 24) if (1 << k) <= max_bytes]
+    saved = handle.info().algo
+    times = {}
+    try:
+        for nbytes in sizes:
+            if nbytes > max_bytes or nbytes % 16:
+                raise ValueError(f"size {nbytes} not a multiple of 16 bytes within the handle's max payload")
+            calls = max(4, min(20, (256 << 20) // (handle.R * nbytes * 2)))
+            times[nbytes] = {algo: _time_form(handle, algo, nbytes, calls, replays) for algo in ("oneshot", "twoshot")}
+    finally:
+        handle.set_algo(saved)
+    return times
+
+
+def tune(handle, sizes=None, replays: int = 5) -> dict:
+    """Measure, set the two-shot threshold on the handle, return the tactics
+    and the measured times."""
+    if handle.dtype not in (1, 2):
+        raise ValueError("tactics apply to fp16/bf16 all-reduce handles")
+    times = measure(handle, sizes, replays)
+    handle.set_tactics(twoshot_min_bytes=crossover(times))
+    return {"tactics": handle.tactics(), "times_us": {str(k): v for k, v in times.items()}}
+
+
+def save(path: str, key: str, tactics: dict) -> None:
+    """Store one key's tactics in the JSON file at path (other keys kept)."""
+    data = {}
+    if os.path.exists(path):
+        with open(path) as f:
+            data = json.load(f)
+    data[key] = {k: int(v) for k, v in tactics.items()}
+    tmp = path + ".tmp"
+    with open(tmp, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+    os.replace(tmp, path)
+
+
+def lookup(path: str, key: str):
+    """The stored tactics of a key, or None."""
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        return json.load(f).get(key)
+
+
+def load(path: str, handle) -> bool:
+    """Apply the stored tactics for this handle's key; False if there are none."""
+    t = lookup(path, handle_key(handle))
+    if t is None:
+        return False
+    handle.set_tactics(**t)
+    return True

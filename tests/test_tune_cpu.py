@@ -1,0 +1,44 @@
+"""Host logic of the tactic tuner: the crossover rule and the tactic file."""
+import json
+
+from tensor_decode_all_gb300 import tune
+
+
+def test_crossover_smallest_size_from_which_twoshot_always_wins():
+    t = {65536: {"oneshot": 5.0, "twoshot": 6.0},
+         262144: {"oneshot": 8.0, "twoshot": 7.0},
+         1048576: {"oneshot": 20.0, "twoshot": 12.0}}
+    assert tune.crossover(t) == 262144
+
+
+def test_crossover_ignores_an_isolated_win_below_a_loss():
+    # two-shot wins at 64 KiB by noise, loses at 256 KiB, wins from 1 MiB
+    t = {65536: {"oneshot": 5.0, "twoshot": 4.9},
+         262144: {"oneshot": 8.0, "twoshot": 8.5},
+         1048576: {"oneshot": 20.0, "twoshot": 12.0}}
+    assert tune.crossover(t) == 1048576
+
+
+def test_crossover_never_when_the_largest_size_prefers_oneshot():
+    t = {65536: {"oneshot": 5.0, "twoshot": 4.0}, 1048576: {"oneshot": 10.0, "twoshot": 11.0}}
+    assert tune.crossover(t) == tune.NEVER
+    assert tune.crossover({}) == tune.NEVER
+
+
+def test_key_names_gpu_ranks_dtype_and_slots():
+    assert tune.key_for("GB300", 152, 8, 2, 1) == "GB300|sm152|R8|bf16|hbm"
+    assert tune.key_for("GB300", 152, 2, 1, 0) == "GB300|sm152|R2|f16|pinned"
+
+
+def test_save_and_lookup_keep_other_keys(tmp_path):
+    path = str(tmp_path / "tactics.json")
+    a = {"twoshot_min_bytes": 524288, "twoshot_sub": 0, "max_blocks": 0}
+    b = {"twoshot_min_bytes": tune.NEVER, "twoshot_sub": 128, "max_blocks": 12}
+    tune.save(path, "k1", a)
+    tune.save(path, "k2", b)
+    assert tune.lookup(path, "k1") == a
+    assert tune.lookup(path, "k2") == b
+    assert tune.lookup(path, "k3") is None
+    assert tune.lookup(str(tmp_path / "missing.json"), "k1") is None
+    with open(path) as f:
+        assert sorted(json.load(f)) == ["k1", "k2"]
