@@ -549,6 +549,12 @@ def run_ours(args, dist):
             "r8_bf16_393216_hbm_fused": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20, None),
             "r8_bf16_16MiB_hbm_fused": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 10, 10, None),
             "allgather_c64_r8_hbm_fused": ("allgather", 8, "c64", 500000, "hbm", 4, None, 20, 10, None),
+            # one call per graph replay: the graph-launch overhead included
+            "r2_fp16_131072_pinned_graph1": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 1, 200, None),
+            "r8_bf16_393216_hbm_graph1": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 1, 200, None),
+            "r2_fp16_131072_pinned_graph1_fused": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 1, 200,
+                                                   None),
+            "r8_bf16_393216_hbm_graph1_fused": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 1, 200, None),
         }.items():
             fz = name.endswith("_fused")
             wx = Workload(op, RR, dt, nn, sl, cc, config=cfg, dist=dd or "uniform", algo=al, fused=fz)
