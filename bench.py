@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--sweep-slots", default="hbm,pinned")
     ap.add_argument("--sweep-dtypes", default="f16,bf16")
     ap.add_argument("--sweep-ranks", default="2,4,8")
+    ap.add_argument("--sweep-algo", default=None, choices=["oneshot", "twoshot", "tagged"],
+                    help="in the sweep, force this all-reduce form in every cell")
     ap.add_argument("--sweep-fused", action="store_true",
                     help="in the sweep, run every call as one cooperative launch of all ranks (ar_allreduce_fused)")
     ap.add_argument("--sweep-min-kib", type=int, default=2)
@@ -224,7 +226,7 @@ class Workload:
         if algo:
             self.h.set_algo(algo)
         self.algo = "allgather" if op == "allgather" else \
-            ("twoshot" if self.h.plan("allreduce", numel).algo == 1 else "oneshot")
+            {0: "oneshot", 1: "twoshot", 2: "tagged"}[self.h.plan("allreduce", numel).algo]
         self.streams = [torch.cuda.Stream() for _ in range(R)]
         out_n = numel * (R if op == "allgather" else 1)
         # inputs [C][numel] per rank, contiguous, so one copy moves a whole step
@@ -689,7 +691,7 @@ def run_sweep(args, dist):
                     if not (args.sweep_min_kib << 10) <= S <= (args.sweep_max_kib << 10):
                         continue
                     both = args.sweep_both and R >= 3 and (64 << 10) <= S <= (8 << 20)
-                    for algo in (("oneshot", "twoshot") if both else (None,)):
+                    for algo in (("oneshot", "twoshot") if both else (args.sweep_algo,)):
                         cells.append((slots, dtype, R, S, algo))
     with open(args.sweep, "w") as f:
         for slots, dtype, R, S, algo in cells:

@@ -86,14 +86,20 @@ enum ar_code {
     AR_ESTATE = 7     /* the handle needs ar_reset() (a device error is recorded) */
 };
 
-/* How an all-reduce call moves its data (both give the same bits).
+/* How an all-reduce call moves its data (all give the same bits).
  * AR_ALGO_ONESHOT: one flag round per tile; every rank reads every peer's tile
  *   (the pages' exchange-and-add).  Per call, peer-slot reads are R*(R-1)*S.
  * AR_ALGO_TWOSHOT: two flag rounds per tile; rank r reduces the r-th sub-tile
  *   for everyone, then every rank copies the R reduced sub-tiles.  Per call,
  *   slot reads are about 2*R*S; for large payloads at R >= 4.
- * AR_ALGO_AUTO: chosen per call by ar_choose_algo(). */
-enum ar_algo { AR_ALGO_AUTO = -1, AR_ALGO_ONESHOT = 0, AR_ALGO_TWOSHOT = 1 };
+ * AR_ALGO_TAGGED: no flags and no fences; every 8-byte word of a separate
+ *   exchange buffer holds 4 payload bytes and a 4-byte tag naming the stage,
+ *   and a reader polls its peers' words until the tags match.  One trip over
+ *   the slot memory instead of three, at twice the bytes: for latency-bound
+ *   calls up to ar_info.tagged_capacity_bytes per rank (larger calls take the
+ *   one-shot form).  Not part of the pages' design.
+ * AR_ALGO_AUTO: chosen per call from the handle's tactics (ar_tactics). */
+enum ar_algo { AR_ALGO_AUTO = -1, AR_ALGO_ONESHOT = 0, AR_ALGO_TWOSHOT = 1, AR_ALGO_TAGGED = 2 };
 
 /* Details of the first device-side error recorded in a handle. */
 typedef struct ar_error_info {
@@ -120,6 +126,9 @@ typedef struct ar_info {
     uint64_t slot_bytes;    /* bytes of one (parity, rank) slot, a multiple of 256 */
     uint64_t total_slot_bytes; /* 2 * R * slot_bytes: the allocation that cannot grow */
     uint64_t timeout_ns;
+    uint64_t tagged_capacity_bytes;  /* largest per-rank call the tagged form takes */
+    int32_t blocks_per_sm_tagged;    /* occupancy of the tagged-form kernels */
+    int32_t reserved;
 } ar_info;
 
 /* Launch plan of one call, computed on the host (no GPU needed). */
@@ -128,7 +137,7 @@ typedef struct ar_plan {
     int32_t threads;        /* threads per block */
     int32_t vec_bytes;      /* bytes per vector access: 16 for all-reduce */
     int32_t unroll;         /* vectors per thread per tile (two-shot: R * subtile_vecs / threads, rounded up) */
-    int32_t algo;           /* AR_ALGO_ONESHOT or AR_ALGO_TWOSHOT (allgather: one-shot) */
+    int32_t algo;           /* AR_ALGO_ONESHOT, _TWOSHOT or _TAGGED (allgather: one-shot) */
     int32_t flag_rounds;    /* flag rounds per tile: 1 or 2 */
     int32_t subtile_vecs;   /* two-shot: vectors per sub-tile (64, 128 or 256; a tile is R sub-tiles); else 0 */
     int32_t reserved;
@@ -145,6 +154,7 @@ typedef struct ar_tactics {
     uint64_t twoshot_min_bytes; /* AUTO picks two-shot from this many bytes per rank; UINT64_MAX: never */
     int32_t twoshot_sub;        /* two-shot sub-tile in vectors: 64, 128 or 256; 0 = the size rule */
     int32_t max_blocks;         /* cap on blocks per rank (>= 1); 0 = as many as fit (occupancy) */
+    uint64_t tagged_max_bytes;  /* AUTO picks the tagged form up to this many bytes per rank; 0: never */
 } ar_tactics;
 
 /*

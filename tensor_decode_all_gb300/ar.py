@@ -20,8 +20,8 @@ from . import builder as _build
 
 AR_F16, AR_BF16, AR_C64 = 1, 2, 3
 AR_SLOT_PINNED_HOST, AR_SLOT_HBM = 0, 1
-AR_ALGO_AUTO, AR_ALGO_ONESHOT, AR_ALGO_TWOSHOT = -1, 0, 1
-ALGOS = {"auto": AR_ALGO_AUTO, "oneshot": AR_ALGO_ONESHOT, "twoshot": AR_ALGO_TWOSHOT}
+AR_ALGO_AUTO, AR_ALGO_ONESHOT, AR_ALGO_TWOSHOT, AR_ALGO_TAGGED = -1, 0, 1, 2
+ALGOS = {"auto": AR_ALGO_AUTO, "oneshot": AR_ALGO_ONESHOT, "twoshot": AR_ALGO_TWOSHOT, "tagged": AR_ALGO_TAGGED}
 AR_OK, AR_EINVAL, AR_ETOOBIG, AR_ESTREAM, AR_ENOMEM, AR_ECUDA, AR_ETIMEOUT, AR_ESTATE = range(8)
 CODE_NAMES = {0: "AR_OK", 1: "AR_EINVAL", 2: "AR_ETOOBIG", 3: "AR_ESTREAM", 4: "AR_ENOMEM",
               5: "AR_ECUDA", 6: "AR_ETIMEOUT", 7: "AR_ESTATE"}
@@ -48,12 +48,14 @@ class Info(ctypes.Structure):
                 ("blocks_per_sm_twoshot", ctypes.c_int32), ("blocks_per_sm_allgather", ctypes.c_int32),
                 ("algo", ctypes.c_int32), ("pdl", ctypes.c_int32),
                 ("max_numel", ctypes.c_uint64), ("slot_bytes", ctypes.c_uint64),
-                ("total_slot_bytes", ctypes.c_uint64), ("timeout_ns", ctypes.c_uint64)]
+                ("total_slot_bytes", ctypes.c_uint64), ("timeout_ns", ctypes.c_uint64),
+                ("tagged_capacity_bytes", ctypes.c_uint64), ("blocks_per_sm_tagged", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class Tactics(ctypes.Structure):
     _fields_ = [("twoshot_min_bytes", ctypes.c_uint64), ("twoshot_sub", ctypes.c_int32),
-                ("max_blocks", ctypes.c_int32)]
+                ("max_blocks", ctypes.c_int32), ("tagged_max_bytes", ctypes.c_uint64)]
 
 
 class Plan(ctypes.Structure):
@@ -369,14 +371,15 @@ class Handle:
     def tactics(self) -> dict:
         t = ar_get_tactics(self.ptr)
         return {"twoshot_min_bytes": int(t.twoshot_min_bytes), "twoshot_sub": int(t.twoshot_sub),
-                "max_blocks": int(t.max_blocks)}
+                "max_blocks": int(t.max_blocks), "tagged_max_bytes": int(t.tagged_max_bytes)}
 
-    def set_tactics(self, twoshot_min_bytes=None, twoshot_sub=None, max_blocks=None) -> None:
+    def set_tactics(self, twoshot_min_bytes=None, twoshot_sub=None, max_blocks=None, tagged_max_bytes=None) -> None:
         """Replace some or all of the handle's tactics (see ar_tactics in ar.h)."""
         cur = self.tactics()
         t = Tactics(int(cur["twoshot_min_bytes"] if twoshot_min_bytes is None else twoshot_min_bytes),
                     int(cur["twoshot_sub"] if twoshot_sub is None else twoshot_sub),
-                    int(cur["max_blocks"] if max_blocks is None else max_blocks))
+                    int(cur["max_blocks"] if max_blocks is None else max_blocks),
+                    int(cur["tagged_max_bytes"] if tagged_max_bytes is None else tagged_max_bytes))
         rc = ar_set_tactics(self.ptr, t)
         if rc:
             raise ArError(rc, "ar_set_tactics")

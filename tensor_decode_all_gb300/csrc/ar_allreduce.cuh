@@ -393,6 +393,27 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
 
 namespace tda {
 
+}  // namespace tda
+
+#include "ar_allreduce_tagged.cuh"
+
+namespace tda {
+
+template <class Ops, bool F>
+const void *allreduce_tagged_ptr(int R) {
+    switch (R) {
+        case 1: return F ? (const void *)allreduce_tagged_all<Ops, 1> : (const void *)allreduce_tagged_rank<Ops, 1>;
+        case 2: return F ? (const void *)allreduce_tagged_all<Ops, 2> : (const void *)allreduce_tagged_rank<Ops, 2>;
+        case 3: return F ? (const void *)allreduce_tagged_all<Ops, 3> : (const void *)allreduce_tagged_rank<Ops, 3>;
+        case 4: return F ? (const void *)allreduce_tagged_all<Ops, 4> : (const void *)allreduce_tagged_rank<Ops, 4>;
+        case 5: return F ? (const void *)allreduce_tagged_all<Ops, 5> : (const void *)allreduce_tagged_rank<Ops, 5>;
+        case 6: return F ? (const void *)allreduce_tagged_all<Ops, 6> : (const void *)allreduce_tagged_rank<Ops, 6>;
+        case 7: return F ? (const void *)allreduce_tagged_all<Ops, 7> : (const void *)allreduce_tagged_rank<Ops, 7>;
+        case 8: return F ? (const void *)allreduce_tagged_all<Ops, 8> : (const void *)allreduce_tagged_rank<Ops, 8>;
+        default: return nullptr;
+    }
+}
+
 // Kernel entry for (element ops, R, unroll, one rank or all ranks), as an
 // untyped address for cudaLaunchKernelExC and the occupancy calculator.
 template <class Ops, int R, int U, bool F>
@@ -441,10 +462,12 @@ const void *allreduce_twoshot_ptr(int R, int sub) {
 }
 
 // U = 1 or 2: one-shot with that many vectors per thread per stage;
-// U = twoshot_variant(sub): the two-shot form with sub-tiles of `sub` vectors.
+// U = twoshot_variant(sub): the two-shot form with sub-tiles of `sub` vectors;
+// U = kTaggedVariant: the tagged-word form.
 // fused: the kernel for one launch of all ranks (grid blocks x R).
 template <class Ops, bool F>
 const void *allreduce_ptr_f(int R, int U) {
+    if (U == kTaggedVariant) return allreduce_tagged_ptr<Ops, F>(R);
     if (U < 0) return allreduce_twoshot_ptr<Ops, F>(R, twoshot_sub(U));
     return U == 1 ? allreduce_ptr_ru<Ops, 1, F>(R) : allreduce_ptr_ru<Ops, 2, F>(R);
 }

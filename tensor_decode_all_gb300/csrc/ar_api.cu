@@ -25,11 +25,17 @@ struct ar_handle {
     int sm_count = 0;
     int bps_one = 0, bps_two = 0, bps_ag = 0;  // occupancy per kernel family (one rank's launch)
     int bps_one_f = 0, bps_two_f = 0, bps_ag_f = 0;  // the same for one launch of all ranks
+    int bps_tag = 0, bps_tag_f = 0;                  // tagged-word form (one rank / all ranks)
     int bmax = 0;                              // flag/counter slots per rank
     int algo = AR_ALGO_AUTO;
     int twoshot_sub = 0;                       // tactic: two-shot sub-tile (64/128/256); 0 = size rule
     uint64_t twoshot_min_bytes = ~0ull;        // tactic: AUTO picks two-shot from this size per rank
     int max_blocks = 0;                        // tactic: cap on blocks per rank; 0 = occupancy
+    uint64_t tagged_max_bytes = 0;             // tactic: AUTO picks the tagged form up to this size
+    uint64_t tagged_cap = 0;                   // largest call the tagged buffers hold (bytes per rank)
+    void *ll_host = nullptr;                   // pinned kind: host address of the tagged buffers
+    ulonglong2 *ll_dev = nullptr;              // [2][R][ll_vecs]
+    uint64_t ll_vecs = 0, ll_bytes = 0;
     bool pdl = true;                           // launch as programmatic dependents
     void *slots_host = nullptr;            // pinned kind: host address of the slots
     uint8_t *slots_dev = nullptr;          // device address of the slots
@@ -51,6 +57,10 @@ struct ar_handle {
 namespace {
 
 thread_local int g_last_error = AR_OK;
+
+// Largest per-rank payload of the tagged-word form (its buffers hold twice as
+// many bytes, per rank and parity).
+constexpr uint64_t kTaggedMaxBytes = 512ull << 10;
 
 uint64_t itemsize_of(int dtype) {
     switch (dtype) {
@@ -111,6 +121,8 @@ DevState dev_state(const ar_handle *h) {
     d.timeout_ns = h->timeout_ns.load(std::memory_order_relaxed);
     d.bmax = h->bmax;
     d.sys_scope = h->kind == AR_SLOT_PINNED_HOST ? 1 : 0;
+    d.ll = h->ll_dev;
+    d.ll_vecs = h->ll_vecs;
     return d;
 }
 
@@ -119,6 +131,8 @@ void free_all(ar_handle *h) {
     else if (h->slots_dev) cudaFree(h->slots_dev);
     if (h->flags_host) cudaFreeHost(h->flags_host);
     else if (h->flags_dev) cudaFree(h->flags_dev);
+    if (h->ll_host) cudaFreeHost(h->ll_host);
+    else if (h->ll_dev) cudaFree(h->ll_dev);
     if (h->ctr) cudaFree(h->ctr);
     if (h->err_host) cudaFreeHost(h->err_host);
     (void)cudaGetLastError();
@@ -126,6 +140,8 @@ void free_all(ar_handle *h) {
     h->slots_dev = nullptr;
     h->flags_host = nullptr;
     h->flags_dev = nullptr;
+    h->ll_host = nullptr;
+    h->ll_dev = nullptr;
     h->ctr = nullptr;
     h->abort_word = nullptr;
     h->err_host = nullptr;
@@ -137,6 +153,9 @@ int zero_state(ar_handle *h) {
     if (h->flags_host) std::memset(h->flags_host, 0, h->flags_bytes);
     else if (cudaMemset(h->flags_dev, 0, h->flags_bytes) != cudaSuccess) return AR_ECUDA;
     if (cudaMemset(h->ctr, 0, h->ctr_bytes) != cudaSuccess) return AR_ECUDA;
+    // Stale tagged words would carry tags the restarted counters reuse.
+    if (h->ll_host) std::memset(h->ll_host, 0, h->ll_bytes);
+    else if (h->ll_dev && cudaMemset(h->ll_dev, 0, h->ll_bytes) != cudaSuccess) return AR_ECUDA;
     std::memset((void *)h->err_host, 0, sizeof(ar_error_info));
     for (int r = 0; r < tda::kMaxRanks; ++r) {
         h->host_calls[r].store(0);
@@ -183,6 +202,16 @@ int family_occupancy(const ar_handle *h, bool fused, int *one, int *two, int *ag
 int handle_occupancy(ar_handle *h) {
     int rc = family_occupancy(h, false, &h->bps_one, &h->bps_two, &h->bps_ag);
     if (rc == AR_OK) rc = family_occupancy(h, true, &h->bps_one_f, &h->bps_two_f, &h->bps_ag_f);
+    h->bps_tag = h->bps_one;
+    h->bps_tag_f = h->bps_one_f;
+    if (rc == AR_OK && (h->dtype == AR_F16 || h->dtype == AR_BF16)) {
+        int t = 1 << 30, tf = 1 << 30;
+        rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, tda::kTaggedVariant, false), &t);
+        if (rc == AR_OK) rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, tda::kTaggedVariant, true), &tf);
+        if (rc == AR_OK && (t < 1 || tf < 1)) rc = AR_ECUDA;
+        h->bps_tag = t;
+        h->bps_tag_f = tf;
+    }
     return rc;
 }
 
@@ -203,8 +232,17 @@ int choose_algo(int R, uint64_t bytes, int slot_kind) {
 
 // The form a handle's call of `bytes` per rank takes: forced, or its tactic.
 int handle_algo(const ar_handle *h, uint64_t bytes) {
+    if (h->algo == AR_ALGO_TAGGED) return bytes <= h->tagged_cap ? AR_ALGO_TAGGED : AR_ALGO_ONESHOT;
     if (h->algo != AR_ALGO_AUTO) return h->algo;
+    if (bytes <= h->tagged_max_bytes && bytes <= h->tagged_cap) return AR_ALGO_TAGGED;
     return bytes >= h->twoshot_min_bytes ? AR_ALGO_TWOSHOT : AR_ALGO_ONESHOT;
+}
+
+// Blocks per SM of the kernel family a call of `algo` launches.
+int handle_bps(const ar_handle *h, int algo, bool fused) {
+    if (algo == AR_ALGO_TWOSHOT) return fused ? h->bps_two_f : h->bps_two;
+    if (algo == AR_ALGO_TAGGED) return fused ? h->bps_tag_f : h->bps_tag;
+    return fused ? h->bps_one_f : h->bps_one;
 }
 
 // Blocks per rank a handle launches for a plan: the plan's, within the flag
@@ -243,8 +281,8 @@ int plan_compute_sub(int R, uint64_t bytes, int vec, int algo, int sub, int thre
     if (!p || R < 1 || R > tda::kMaxRanks || threads < 32 || threads % 32 || sms < 1 || bps < 1)
         return AR_EINVAL;
     if (vec != 16 && vec != 8 && vec != 4 && vec != 2 && vec != 1) return AR_EINVAL;
-    if (algo != AR_ALGO_ONESHOT && algo != AR_ALGO_TWOSHOT) return AR_EINVAL;
-    if (algo == AR_ALGO_TWOSHOT && vec != 16) return AR_EINVAL;
+    if (algo != AR_ALGO_ONESHOT && algo != AR_ALGO_TWOSHOT && algo != AR_ALGO_TAGGED) return AR_EINVAL;
+    if (algo != AR_ALGO_ONESHOT && vec != 16) return AR_EINVAL;
     std::memset(p, 0, sizeof(*p));
     const uint64_t bmax = (uint64_t)sms * (uint64_t)bps / (uint64_t)R;
     if (bmax < 1) return AR_EINVAL;
@@ -255,8 +293,9 @@ int plan_compute_sub(int R, uint64_t bytes, int vec, int algo, int sub, int thre
     // per rank, so R vectors per thread per stage.
     if (algo == AR_ALGO_TWOSHOT && sub == 0) sub = 256;
     if (algo == AR_ALGO_TWOSHOT && sub != 64 && sub != 128 && sub != 256) return AR_EINVAL;
-    const uint64_t tile_vecs = algo == AR_ALGO_TWOSHOT ? (uint64_t)R * (uint64_t)sub
-                                                       : (uint64_t)threads * (nv >= bmax * (uint64_t)threads * 2 ? 2 : 1);
+    const uint64_t tile_vecs = algo == AR_ALGO_TWOSHOT  ? (uint64_t)R * (uint64_t)sub
+                               : algo == AR_ALGO_TAGGED ? (uint64_t)threads
+                                                        : (uint64_t)threads * (nv >= bmax * (uint64_t)threads * 2 ? 2 : 1);
     const int unroll = (int)((tile_vecs + threads - 1) / threads);
     const uint64_t tiles = (nv + tile_vecs - 1) / tile_vecs;
     const uint64_t blocks = tiles < bmax ? tiles : bmax;
@@ -351,13 +390,15 @@ int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
     const uint64_t bytes = numel * h->itemsize;
     const int algo = handle_algo(h, bytes);
     const bool fused = rank < 0;
-    const int bps = algo == AR_ALGO_TWOSHOT ? (fused ? h->bps_two_f : h->bps_two) : (fused ? h->bps_one_f : h->bps_one);
+    const int bps = handle_bps(h, algo, fused);
     ar_plan plan;
     int rc = plan_compute_sub(h->R, bytes, 16, algo, handle_twoshot_sub(h, bytes), tda::kThreads, h->sm_count, bps,
                               &plan);
     if (rc != AR_OK) return rc;
     const int blocks = handle_blocks(h, plan.blocks);
-    const int variant = algo == AR_ALGO_TWOSHOT ? tda::twoshot_variant(plan.subtile_vecs) : plan.unroll;
+    const int variant = algo == AR_ALGO_TWOSHOT  ? tda::twoshot_variant(plan.subtile_vecs)
+                        : algo == AR_ALGO_TAGGED ? tda::kTaggedVariant
+                                                 : plan.unroll;
     const cudaError_t e = tda::launch_allreduce(h->dtype, h->R, variant, blocks, s, io, numel, rank,
                                                 dev_state(h), h->pdl);
     if (e != cudaSuccess) {
@@ -445,6 +486,7 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
     if (const char *e = std::getenv("AR_ALGO")) {
         if (!std::strcmp(e, "oneshot")) h->algo = AR_ALGO_ONESHOT;
         else if (!std::strcmp(e, "twoshot")) h->algo = AR_ALGO_TWOSHOT;
+        else if (!std::strcmp(e, "tagged")) h->algo = AR_ALGO_TAGGED;
     }
     int rc = handle_occupancy(h);
     if (rc != AR_OK) return fail(rc);
@@ -456,6 +498,7 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
     if (h->kind == AR_SLOT_PINNED_HOST && h->bps_two_f > 4) h->bps_two_f = 4;
     int bps_max = h->bps_one > h->bps_two ? h->bps_one : h->bps_two;
     if (h->bps_ag > bps_max) bps_max = h->bps_ag;
+    if (h->bps_tag > bps_max) bps_max = h->bps_tag;
     h->bmax = h->sm_count * bps_max / R;
     if (const int cap = max_blocks_override()) h->bmax = cap < h->bmax ? cap : h->bmax;
     if (h->bmax < 1) return fail(AR_ECUDA);
@@ -477,6 +520,20 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
         if (cudaMalloc((void **)&h->slots_dev, slots_total) != cudaSuccess) return fail(AR_ENOMEM);
         if (cudaMalloc((void **)&h->flags_dev, h->flags_bytes) != cudaSuccess) return fail(AR_ENOMEM);
         if (cudaMemset(h->slots_dev, 0, slots_total) != cudaSuccess) return fail(AR_ECUDA);
+    }
+    // Tagged-word buffers (fp16/bf16 handles): room for calls of up to
+    // kTaggedMaxBytes per rank, at 32 bytes per 16 payload bytes.
+    if (dtype == AR_F16 || dtype == AR_BF16) {
+        h->tagged_cap = h->slot_bytes < kTaggedMaxBytes ? h->slot_bytes : kTaggedMaxBytes;
+        h->ll_vecs = h->tagged_cap / 16 * 2;
+        h->ll_bytes = 2ull * (uint64_t)R * h->ll_vecs * 16ull;
+        if (slot_kind == AR_SLOT_PINNED_HOST) {
+            if (cudaHostAlloc(&h->ll_host, h->ll_bytes, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess)
+                return fail(AR_ENOMEM);
+            if (cudaHostGetDevicePointer((void **)&h->ll_dev, h->ll_host, 0) != cudaSuccess) return fail(AR_ECUDA);
+        } else if (cudaMalloc((void **)&h->ll_dev, h->ll_bytes) != cudaSuccess) {
+            return fail(AR_ENOMEM);
+        }
     }
     if (cudaMalloc((void **)&h->ctr, h->ctr_bytes) != cudaSuccess) return fail(AR_ENOMEM);
     h->abort_word = reinterpret_cast<unsigned int *>(reinterpret_cast<uint8_t *>(h->ctr) + h->ctr_bytes - 256);
@@ -599,6 +656,9 @@ AR_API int ar_query(const ar_handle *h, ar_info *info) {
     info->slot_bytes = h->slot_bytes;
     info->total_slot_bytes = 2ull * (uint64_t)h->R * h->slot_bytes;
     info->timeout_ns = h->timeout_ns.load();
+    info->tagged_capacity_bytes = h->tagged_cap;
+    info->blocks_per_sm_tagged = h->bps_tag;
+    info->reserved = 0;
     return AR_OK;
 }
 
@@ -616,8 +676,10 @@ AR_API int ar_set_pdl(ar_handle *h, int enable) {
 }
 
 AR_API int ar_set_algo(ar_handle *h, int algo) {
-    if (!h || (algo != AR_ALGO_AUTO && algo != AR_ALGO_ONESHOT && algo != AR_ALGO_TWOSHOT)) return AR_EINVAL;
-    if (algo == AR_ALGO_TWOSHOT && h->dtype == AR_C64) return AR_EINVAL;
+    if (!h || (algo != AR_ALGO_AUTO && algo != AR_ALGO_ONESHOT && algo != AR_ALGO_TWOSHOT &&
+               algo != AR_ALGO_TAGGED))
+        return AR_EINVAL;
+    if ((algo == AR_ALGO_TWOSHOT || algo == AR_ALGO_TAGGED) && h->dtype == AR_C64) return AR_EINVAL;
     h->algo = algo;
     return AR_OK;
 }
@@ -627,6 +689,7 @@ AR_API int ar_get_tactics(const ar_handle *h, ar_tactics *t) {
     t->twoshot_min_bytes = h->twoshot_min_bytes;
     t->twoshot_sub = h->twoshot_sub;
     t->max_blocks = h->max_blocks;
+    t->tagged_max_bytes = h->tagged_max_bytes;
     return AR_OK;
 }
 
@@ -638,6 +701,7 @@ AR_API int ar_set_tactics(ar_handle *h, const ar_tactics *t) {
     h->twoshot_min_bytes = t->twoshot_min_bytes;
     h->twoshot_sub = t->twoshot_sub;
     h->max_blocks = t->max_blocks;
+    h->tagged_max_bytes = t->tagged_max_bytes;
     return AR_OK;
 }
 
@@ -658,7 +722,7 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) 
     int algo = AR_ALGO_ONESHOT, bps = h->bps_ag;
     if (op == 0) {
         algo = handle_algo(h, bytes);
-        bps = algo == AR_ALGO_TWOSHOT ? h->bps_two : h->bps_one;
+        bps = handle_bps(h, algo, false);
     }
     int rc = plan_compute_sub(h->R, bytes, vec, algo, op == 0 ? handle_twoshot_sub(h, bytes) : 0, tda::kThreads,
                               h->sm_count, bps, plan);

@@ -7,6 +7,8 @@
 //   ctr   : [R ranks][bmax blocks] x {seq, calls}    HBM; private to one block
 //   abort : one 32-bit word in HBM, non-zero once any block has given up
 //   err   : one ar_error_info in mapped pinned host memory
+//   ll    : [2 parities][R ranks][ll_vecs] x 16 B   same memory as the slots; the
+//           tagged-word form's exchange buffers (8 payload bytes per 16 B)
 #pragma once
 
 #include <cstdint>
@@ -24,6 +26,8 @@ constexpr uint64_t kSlotAlign = 256;
 // magnitude is the sub-tile size in vectors (256, 128 or 64).
 constexpr int twoshot_variant(int sub) { return -sub; }
 constexpr int twoshot_sub(int variant) { return -variant; }
+// Kernel variant code of the tagged-word form.
+constexpr int kTaggedVariant = 0;
 
 // Per-(rank, block) counters.  `seq` counts the stages this block has
 // published over all calls (its flag's value at the end of the last call);
@@ -45,6 +49,8 @@ struct DevState {
     uint64_t timeout_ns;
     int bmax;
     int sys_scope;             // 1: slots/flags in host memory, system-scope ordering
+    ulonglong2 *ll;            // [2][R][ll_vecs] tagged-word buffers (same memory as the slots)
+    uint64_t ll_vecs;          // 16-byte tagged vectors per rank and parity: 2 per 16 payload bytes
 };
 
 // The input and output pointers of every rank, passed by value to a launch

@@ -72,6 +72,8 @@ __global__ void __launch_bounds__(kThreads)
     d.timeout_ns = timeout_ns;
     d.bmax = kNoAllocMaxBlocks;
     d.sys_scope = 0;
+    d.ll = nullptr;
+    d.ll_vecs = 0;
 
     const uint64_t nvec_full = numel / 8;
     const int tail = (int)(numel % 8);

@@ -70,6 +70,25 @@ __device__ __forceinline__ unsigned char ld_cg_u8(const void *p) {
     return __ldcg(reinterpret_cast<const unsigned char *>(p));
 }
 
+// Tagged-word exchange: 16-byte accesses of two 64-bit words, each word's
+// high half a tag.  Each 64-bit word is read and written whole (single-copy
+// atomic for an aligned 64-bit relaxed access), so a reader that sees the
+// tag it expects also sees the data stored with it; no fence is needed.
+__device__ __forceinline__ ulonglong2 ld_tagged(const ulonglong2 *p, int sys) {
+    ulonglong2 v;
+    if (sys)
+        asm volatile("ld.relaxed.sys.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
+    else
+        asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_tagged(ulonglong2 *p, ulonglong2 v, int sys) {
+    if (sys)
+        asm volatile("st.relaxed.sys.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(v.x), "l"(v.y) : "memory");
+    else
+        asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(v.x), "l"(v.y) : "memory");
+}
+
 // Programmatic dependent launch.  When a rank's next call is launched with the
 // programmatic-serialization attribute, its blocks may become resident before
 // this call ends.  Each kernel therefore waits (griddepcontrol.wait: the

@@ -2,6 +2,7 @@
 entry point include/ar.h declares; host-side argument checks and the launch
 plan arithmetic behave as documented."""
 import ctypes
+import os
 
 import pytest
 
@@ -111,11 +112,32 @@ def test_choose_algo_rule(lib):
     assert tda.ar_set_algo(0, ar.AR_ALGO_ONESHOT) == ar.AR_EINVAL
 
 
-def test_struct_layouts_match_header(lib):
-    # ar_error_info: 4 x int32 + 2 x uint64; ar_info: 12 x int32 + 4 x uint64; ar_plan: 8 x int32 + 3 x uint64
-    assert ctypes.sizeof(ar.ErrorInfo) == 32
-    assert ctypes.sizeof(ar.Info) == 80
-    assert ctypes.sizeof(ar.Plan) == 56
+def test_struct_layouts_match_header(lib, tmp_path):
+    """Every field of the binding's structs sits where a C compiler puts it
+    for include/ar.h (sizes and offsets printed by a program built with gcc)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    structs = {"ar_error_info": ar.ErrorInfo, "ar_info": ar.Info, "ar_plan": ar.Plan, "ar_tactics": ar.Tactics}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "ar.h"', "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append(f'    printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in py._fields_:
+            lines.append(f'    printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines += ["    return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, "-std=c99", "-I", os.path.dirname(ar._build.INCLUDE + "/"), str(src), "-o", str(exe)],
+                   check=True)
+    got = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    c = {tuple(l.split()[:2]): int(l.split()[2]) for l in got if l.strip()}
+    for cname, py in structs.items():
+        assert ctypes.sizeof(py) == c[(cname, "size")], cname
+        for fname, _ in py._fields_:
+            assert getattr(py, fname).offset == c[(cname, fname)], (cname, fname)
 
 
 def test_no_cpu_fallback_when_library_missing(monkeypatch, tmp_path):
