@@ -147,7 +147,8 @@ typedef struct ar_plan {
 } ar_plan;
 
 /* Per-handle tactics: which all-reduce form AR_ALGO_AUTO picks by size, and the
- * launch shape.  ar_create fills them from the built-in table (ar_choose_algo);
+ * launch shape.  ar_create fills them from the built-in table (ar_choose_algo;
+ * tagged_max_bytes 0 for complex64 handles);
  * ar_set_tactics replaces them, for instance with values measured on this GPU
  * and stored by the caller (the Python package's tune module does both). */
 typedef struct ar_tactics {
@@ -298,12 +299,15 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan);
 AR_API int ar_plan_compute(int R, uint64_t bytes, int vec_bytes, int algo, int threads, int sm_count,
                            int blocks_per_sm, ar_plan *plan);
 
-/* The all-reduce form AR_ALGO_AUTO picks for R ranks, `bytes` per rank and a
- * slot kind (a tactic table measured on a GB300): one-shot for R <= 3;
- * two-shot from 512 KiB (R >= 8) or 2 MiB (R = 4..7) with HBM slots, and from
- * 64 KiB (R >= 8) or 256 KiB (R = 4..7) with pinned-host slots, where one-shot
- * reads R(R-1)S bytes over the host link against two-shot's (2R-1)S.  Pure
- * host arithmetic. */
+/* The all-reduce form a new handle's AR_ALGO_AUTO picks for R ranks, `bytes`
+ * per rank and a slot kind (a tactic table measured on a GB300; a handle's own
+ * tactics may differ, see ar_tactics).  Tagged-word form up to 512 KiB (R <= 2)
+ * or 64 KiB (R = 3, 4) with HBM slots and up to 16 KiB (R <= 2) with
+ * pinned-host slots (within ar_info.tagged_capacity_bytes).  Otherwise
+ * one-shot for R <= 3; two-shot from 512 KiB (R >= 8) or 2 MiB (R = 4..7)
+ * with HBM slots, and from 64 KiB (R >= 8) or 256 KiB (R = 4..7) with
+ * pinned-host slots, where one-shot reads R(R-1)S bytes over the host link
+ * against two-shot's (2R-1)S.  Pure host arithmetic. */
 AR_API int ar_choose_algo(int R, uint64_t bytes, int slot_kind);
 
 /* Launch this handle's kernels as programmatic dependents of the preceding

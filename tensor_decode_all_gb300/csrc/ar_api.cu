@@ -226,7 +226,23 @@ uint64_t twoshot_threshold(int R, int slot_kind) {
     return R >= 8 ? (512ull << 10) : (2ull << 20);
 }
 
+// Largest call the tagged-word form takes under AR_ALGO_AUTO.  Measured on a
+// GB300 (bf16, graphs of 100 calls, tagged vs the flag forms): in HBM it is
+// faster at every size up to 512 KiB at R = 2 (2 KiB: 2.7 vs 3.2 us; 256 KiB:
+// 3.5 vs 3.7 us) and up to 64 KiB at R = 4, and slower at R = 8, where every
+// thread polls 14 tagged vectors instead of one warp polling 8 flags.  Over
+// the host link its polls re-read words that have not landed yet, so it wins
+// only for small calls at R = 2 (8 KiB: 3.5 vs 4.0 us; up to 16 KiB).  R = 3
+// takes R = 4's value.
+uint64_t tagged_threshold(int R, int slot_kind) {
+    if (slot_kind == AR_SLOT_PINNED_HOST) return R <= 2 ? (16ull << 10) : 0;
+    if (R <= 2) return 512ull << 10;
+    return R <= 4 ? (64ull << 10) : 0;
+}
+
 int choose_algo(int R, uint64_t bytes, int slot_kind) {
+    const uint64_t tagged = tagged_threshold(R, slot_kind);
+    if (tagged && bytes <= tagged) return AR_ALGO_TAGGED;
     return bytes >= twoshot_threshold(R, slot_kind) ? AR_ALGO_TWOSHOT : AR_ALGO_ONESHOT;
 }
 
@@ -234,7 +250,7 @@ int choose_algo(int R, uint64_t bytes, int slot_kind) {
 int handle_algo(const ar_handle *h, uint64_t bytes) {
     if (h->algo == AR_ALGO_TAGGED) return bytes <= h->tagged_cap ? AR_ALGO_TAGGED : AR_ALGO_ONESHOT;
     if (h->algo != AR_ALGO_AUTO) return h->algo;
-    if (bytes <= h->tagged_max_bytes && bytes <= h->tagged_cap) return AR_ALGO_TAGGED;
+    if (h->tagged_max_bytes && bytes <= h->tagged_max_bytes && bytes <= h->tagged_cap) return AR_ALGO_TAGGED;
     return bytes >= h->twoshot_min_bytes ? AR_ALGO_TWOSHOT : AR_ALGO_ONESHOT;
 }
 
@@ -483,6 +499,7 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
         if (v == 64 || v == 128 || v == 256) h->twoshot_sub = (int)v;
     }
     h->twoshot_min_bytes = twoshot_threshold(R, slot_kind);
+    h->tagged_max_bytes = (dtype == AR_F16 || dtype == AR_BF16) ? tagged_threshold(R, slot_kind) : 0;
     if (const char *e = std::getenv("AR_ALGO")) {
         if (!std::strcmp(e, "oneshot")) h->algo = AR_ALGO_ONESHOT;
         else if (!std::strcmp(e, "twoshot")) h->algo = AR_ALGO_TWOSHOT;

@@ -103,6 +103,14 @@ def test_choose_algo_rule(lib):
     for kind in (ar.AR_SLOT_HBM, ar.AR_SLOT_PINNED_HOST):
         for R in (1, 2, 3):
             assert tda.ar_choose_algo(R, 1 << 30, kind) == ar.AR_ALGO_ONESHOT
+    # tagged-word form for small calls (R, HBM limit, pinned limit; 0 = never)
+    for R, hbm, pinned in ((1, 512 << 10, 16 << 10), (2, 512 << 10, 16 << 10), (3, 64 << 10, 0),
+                           (4, 64 << 10, 0), (5, 0, 0), (8, 0, 0)):
+        for kind, lim in ((ar.AR_SLOT_HBM, hbm), (ar.AR_SLOT_PINNED_HOST, pinned)):
+            if lim:
+                assert tda.ar_choose_algo(R, 16, kind) == ar.AR_ALGO_TAGGED
+                assert tda.ar_choose_algo(R, lim, kind) == ar.AR_ALGO_TAGGED
+            assert tda.ar_choose_algo(R, lim + 16, kind) != ar.AR_ALGO_TAGGED
     # thresholds from the measured crossover (R, HBM, pinned host)
     for R, hbm, pinned in ((4, 2 << 20, 256 << 10), (7, 2 << 20, 256 << 10), (8, 512 << 10, 64 << 10)):
         assert tda.ar_choose_algo(R, hbm - 1, ar.AR_SLOT_HBM) == ar.AR_ALGO_ONESHOT
