@@ -169,8 +169,8 @@ class ClockSampler:
 
 # ------------------------------------------------------------- measurement
 
-KERNEL_SOURCES = ("ar_allreduce.cuh", "ar_sync.cuh", "ar_internal.h", "ar_allreduce_f16.cu", "ar_allreduce_bf16.cu",
-                  "ar_allgather.cu")
+KERNEL_SOURCES = ("ar_allreduce.cuh", "ar_allreduce_tagged.cuh", "ar_sync.cuh", "ar_internal.h",
+                  "ar_allreduce_f16.cu", "ar_allreduce_bf16.cu", "ar_allgather.cu")
 
 
 def kernel_source_sha256() -> str:
@@ -612,6 +612,7 @@ PROFILE_WORKLOADS = {
     "r8_bf16_16MiB_hbm_oneshot_1call": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 1),
     "allgather_c64_r8_hbm_1call": ("allgather", 8, "c64", 500000, "hbm", 4, "normal", 1),
     "r8_bf16_768KiB_hbm_fused_1call": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 1),
+    "r2_fp16_8KiB_pinned_1call": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", 1),
 }
 
 
