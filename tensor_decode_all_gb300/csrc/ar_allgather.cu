@@ -43,8 +43,13 @@ struct Vec<1> {
     static __device__ __forceinline__ T ldcg(const void *p) { return ld_cg_u8(p); }
 };
 
+// Blocks per SM: 5 up to R = 4, 4 above (where the 16-byte two-vector
+// variant holds R - 1 peer vectors per thread and would spill at 5).  Measured
+// on a GB300, complex64 1000 x 500 shards in HBM: R=4 21.8 -> 20.3 us (against
+// the unbounded build's 3 blocks per SM), R=8 64.9 -> 64.3 us, R=8 500 KB
+// 12.0 -> 11.4 us.
 template <int VW, int R, int U, bool F>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
     allgather_kernel(const uint8_t *in_arg, uint8_t *out_arg, uint64_t bytes, int rank_arg, DevState d, RankIO io) {
     using V = typename Vec<VW>::T;
     __shared__ unsigned long long s_seq;
