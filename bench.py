@@ -64,6 +64,7 @@ def parse():
     ap.add_argument("--sweep-max-kib", type=int, default=65536)
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--trace", default=None, help="trace the main workloads with ar_set_trace; write a summary here")
     ap.add_argument("--profile", default=None, choices=sorted(PROFILE_WORKLOADS),
                     help="graph replays of one workload only (for ncu --graph-profiling graph)")
     return ap.parse_args()
@@ -636,6 +637,53 @@ def run_profile(args, dist):
     return None
 
 
+TRACE_WORKLOADS = {
+    "config 2: R=2 fp16 256 KiB pinned": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", False),
+    "config 1: R=2 fp16 8 KiB pinned": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", False),
+    "config 3: R=8 bf16 768 KiB HBM": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", False),
+    "config 3, one cooperative launch": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", True),
+}
+
+
+def sm_clock_mhz(dev: int) -> float:
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(dev), "--query-gpu=clocks.sm", "--format=csv,noheader,nounits"],
+                             capture_output=True, text=True, timeout=10).stdout.strip()
+        return float(out.splitlines()[0])
+    except Exception:
+        return float(measured_peaks().get("sm_max_mhz", 2070.0))
+
+
+def run_trace(args, dist):
+    """Each main workload in a graph of 100 calls with the device trace on:
+    overlap of the rank kernels and the phases of a call (not a timing run)."""
+    import torch
+    import tensor_decode_all_gb300 as tda
+    from tensor_decode_all_gb300 import trace
+    torch.cuda.set_device(0)
+    tda.build()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    out = {}
+    for name, (op, R, dt, n, sl, cfg, dd, fused) in TRACE_WORKLOADS.items():
+        C = 100
+        w = Workload(op, R, dt, n, sl, C, config=cfg, dist=dd, fused=fused)
+        buf = trace.start(w.h, C)
+        w.capture()
+        w.time_graph(3, 0, flush)
+        buf.zero_()
+        ms = w.time_graph(1, 0, flush)
+        w.check(calls=(0, -1))
+        rec = trace.records(buf)
+        summary = trace.summarize(rec, sm_clock_mhz(0))
+        summary["graph_us_per_call"] = round(ms[0] * 1e3 / C, 3)
+        out[name] = summary
+        w.close()
+        print(name, json.dumps(summary), flush=True)
+    with open(args.trace, "w") as f:
+        json.dump(out, f, indent=1)
+    return None
+
+
 def run_reference(args, dist):
     """The CPU oracle as the reference arm: same workload, metric and unit."""
     if dist.rank != 0:
@@ -730,6 +778,8 @@ def main():
             line = run_reference(args, dist)
         elif args.profile:
             line = run_profile(args, dist)
+        elif args.trace:
+            line = run_trace(args, dist)
         elif args.sweep:
             line = run_sweep(args, dist)
         else:

@@ -111,6 +111,22 @@ typedef struct ar_error_info {
     uint64_t seen;      /* flag value it last saw */
 } ar_error_info;
 
+/* One trace record: one block of one rank in one call (see ar_set_trace).
+ * Times from %globaltimer (ns, the same clock on every SM) at the start and
+ * end of the block's work; phase marks in SM clock cycles after the start. */
+typedef struct ar_trace_record {
+    int32_t rank;
+    int32_t block;
+    uint32_t call;          /* the block's call count before this call: 0, 1, 2, ... */
+    uint32_t stages;        /* stages the block ran in this call */
+    uint64_t t_start_ns;    /* after the wait for the preceding work on the stream */
+    uint64_t t_end_ns;      /* after the block's last output store; 0: record not written */
+    uint32_t cyc_published; /* first stage: this block's data published (flag raised) */
+    uint32_t cyc_peers;     /* first stage: every peer's data of that stage seen */
+    uint32_t cyc_end;       /* last output store */
+    uint32_t algo;          /* AR_ALGO_* of the call (allgather: AR_ALGO_ONESHOT) */
+} ar_trace_record;
+
 /* Static facts about a handle, for tests and tools. */
 typedef struct ar_info {
     int32_t R, dtype, slot_kind, device;
@@ -277,6 +293,21 @@ AR_API int ar_destroy(ar_handle *h);
 /* Set the device wait timeout in nanoseconds (>= 1000).  Applies to calls
  * enqueued afterwards; a captured graph keeps the value in force at capture. */
 AR_API int ar_set_timeout(ar_handle *h, uint64_t timeout_ns);
+
+/*
+ * ar_set_trace -- record when each block of each rank ran.  records: device
+ * memory (owned by the caller, zeroed by the caller) holding `capacity`
+ * ar_trace_record entries; NULL stops tracing.  Thread 0 of every block of
+ * every later call (enqueued or captured after this) writes one record, at
+ * index ((call % depth) * R + rank) * max_blocks + block, depth = capacity /
+ * (R * max_blocks) (ar_info.max_blocks), so the last `depth` calls of each
+ * block are kept.  capacity < R * max_blocks returns AR_EINVAL.  Tracing
+ * adds a few stores per block and call; off, it costs one test of a pointer.
+ * The pages measure with serving metrics and a probe; this shows, without an
+ * external profiler, that the R rank kernels of a call run at the same time
+ * and where a call's time goes.
+ */
+AR_API int ar_set_trace(ar_handle *h, void *records, uint64_t capacity);
 
 /* Static facts about the handle. */
 AR_API int ar_query(const ar_handle *h, ar_info *info);

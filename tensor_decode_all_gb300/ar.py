@@ -105,6 +105,7 @@ def lib():
             L.ar_get_tactics.argtypes = [vp, ctypes.POINTER(Tactics)]
             L.ar_set_tactics.argtypes = [vp, ctypes.POINTER(Tactics)]
             L.ar_supports.argtypes = [vp, i32, sz, vp, vp]
+            L.ar_set_trace.argtypes = [vp, vp, u64]
             L.ar_allreduce_noalloc.argtypes = [i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, vp]
             L.ar_allreduce_noalloc.restype = i32
             for name in ("ar_allreduce_fused", "ar_allgather_fused"):
@@ -383,6 +384,12 @@ class Handle:
         rc = ar_set_tactics(self.ptr, t)
         if rc:
             raise ArError(rc, "ar_set_tactics")
+
+    def set_trace(self, buf, capacity: int) -> None:
+        """Trace into `buf` (device memory of `capacity` records), or stop (buf None)."""
+        rc = lib().ar_set_trace(self.ptr, buf.data_ptr() if buf is not None else None, int(capacity))
+        if rc:
+            raise ArError(rc, "ar_set_trace")
 
     def supports(self, op: str, inp, out) -> int:
         """AR_OK if ar_allreduce / ar_allgather would accept these tensors, else its code."""

@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
     __shared__ unsigned long long s_seq;
     __shared__ unsigned long long s_calls;
     __shared__ int s_bail;
+    __shared__ TraceMarks s_tr;
 
     const int rank = block_rank<F>(rank_arg);
     const uint8_t *in = rank_ptr<R, F>(in_arg, io.in, rank);
@@ -70,6 +71,7 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
 
     pdl_wait();
     if (tid == 0) {
+        trace_start(d, s_tr);
         const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
         s_seq = c.seq;
         s_calls = c.calls;
@@ -103,7 +105,10 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
             }
         }
         __syncthreads();
-        if (tid == 0) publish_stage(d, rank, b, seq + s + 1);
+        if (tid == 0) {
+            publish_stage(d, rank, b, seq + s + 1);
+            trace_published(d, s_tr);
+        }
 
         V nxt[U];
         if (s + 1 < nstages) {
@@ -116,6 +121,7 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
         }
 
         if (wait_peers(d, R, rank, b, seq + s + 1, &s_bail)) return;
+        if (tid == 0) trace_peers(d, s_tr);
         // Every peer block of this call has now published its last stage, so
         // all of them are resident: this rank's next call may be scheduled.
         if (s + 1 == nstages) pdl_trigger();
@@ -144,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
         c.seq = seq + nstages;
         c.calls = s_calls + 1;
         d.ctr[(size_t)rank * d.bmax + b] = c;
+        if (d.trace) trace_finish(d, s_tr, R, rank, b, s_calls, nstages);
     }
 }
 

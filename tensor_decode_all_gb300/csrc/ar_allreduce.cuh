@@ -133,6 +133,7 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
     __shared__ unsigned long long s_seq;
     __shared__ unsigned long long s_calls;
     __shared__ int s_bail;
+    __shared__ TraceMarks s_tr;
 
     const int rank = block_rank<F>(rank_arg);
     const uint16_t *in = rank_ptr<R, F>(in_arg, io.in, rank);
@@ -150,6 +151,7 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
 
     pdl_wait();
     if (tid == 0) {
+        trace_start(d, s_tr);
         const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
         s_seq = c.seq;
         s_calls = c.calls;
@@ -182,7 +184,10 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
         }
         __syncthreads();
         // 3. raise the flag
-        if (tid == 0) publish_stage(d, rank, b, seq + s + 1);
+        if (tid == 0) {
+            publish_stage(d, rank, b, seq + s + 1);
+            trace_published(d, s_tr);
+        }
 
         // next stage's input, overlapping the wait
         uint4 nxt[U];
@@ -194,6 +199,7 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
 
         // 4. wait for the peers
         if (wait_peers(d, R, rank, b, seq + s + 1, &s_bail)) return;
+        if (tid == 0) trace_peers(d, s_tr);
         // Every peer block of this call has now published its last stage, so
         // all of them are resident: this rank's next call may be scheduled.
         if (s + 1 == nstages) pdl_trigger();
@@ -231,6 +237,7 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
         c.seq = seq + nstages;
         c.calls = s_calls + 1;
         d.ctr[(size_t)rank * d.bmax + b] = c;
+        if (d.trace) trace_finish(d, s_tr, R, rank, b, s_calls, nstages);
     }
 }
 
@@ -281,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
     __shared__ unsigned long long s_seq;
     __shared__ unsigned long long s_calls;
     __shared__ int s_bail;
+    __shared__ TraceMarks s_tr;
 
     const int rank = block_rank<F>(rank_arg);
     const uint16_t *in = rank_ptr<R, F>(in_arg, io.in, rank);
@@ -300,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
 
     pdl_wait();
     if (tid == 0) {
+        trace_start(d, s_tr);
         const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
         s_seq = c.seq;
         s_calls = c.calls;
@@ -328,8 +337,12 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
             if (li < kTileVecs && tbase + li < nv) my_slot[tbase + li] = pub[u];
         }
         __syncthreads();
-        if (tid == 0) publish_stage(d, rank, b, seq + 2 * s + 1);
+        if (tid == 0) {
+            publish_stage(d, rank, b, seq + 2 * s + 1);
+            trace_published(d, s_tr);
+        }
         if (wait_peers(d, R, rank, b, seq + 2 * s + 1, &s_bail)) return;
+        if (tid == 0) trace_peers(d, s_tr);
 
         // 2. reduce sub-tile `rank` in rank order; the result replaces it in my slot
         const uint64_t vr = tbase + (uint64_t)rank * SUB + tid;
@@ -386,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
         c.seq = seq + 2 * nstages;
         c.calls = s_calls + 1;
         d.ctr[(size_t)rank * d.bmax + b] = c;
+        if (d.trace) trace_finish(d, s_tr, R, rank, b, s_calls, nstages);
     }
 }
 

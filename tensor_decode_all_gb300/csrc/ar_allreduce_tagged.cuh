@@ -35,6 +35,7 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
     __shared__ unsigned long long s_seq;
     __shared__ unsigned long long s_calls;
     __shared__ int s_bail;
+    __shared__ TraceMarks s_tr;
 
     const int rank = block_rank<F>(rank_arg);
     const uint16_t *in = rank_ptr<R, F>(in_arg, io.in, rank);
@@ -50,6 +51,7 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
 
     pdl_wait();
     if (tid == 0) {
+        trace_start(d, s_tr);
         const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
         s_seq = c.seq;
         s_calls = c.calls;
@@ -74,6 +76,7 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
             st_tagged(mine + 2 * v, make_ulonglong2(tag | own.x, tag | own.y), sys);
             st_tagged(mine + 2 * v + 1, make_ulonglong2(tag | own.z, tag | own.w), sys);
         }
+        if (tid == 0) trace_published(d, s_tr);
         // the next stage's input, overlapping the wait
         uint4 nxt = make_uint4(0u, 0u, 0u, 0u);
         if (s + 1 < nstages && !bail) nxt = load_own(in, v + (uint64_t)B * kThreads, nvec_full, tail);
@@ -118,6 +121,7 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
                 if (iter > 32u) __nanosleep(32);
             }
         }
+        if (tid == 0) trace_peers(d, s_tr);
         // Every peer block of this call has now published its last stage, so
         // all of them are resident: this rank's next call may be scheduled.
         if (s + 1 == nstages) {
@@ -150,6 +154,7 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
         c.seq = seq + nstages;
         c.calls = s_calls + 1;
         d.ctr[(size_t)rank * d.bmax + b] = c;
+        if (d.trace) trace_finish(d, s_tr, R, rank, b, s_calls, nstages);
     }
 }
 

@@ -36,6 +36,8 @@ struct ar_handle {
     void *ll_host = nullptr;                   // pinned kind: host address of the tagged buffers
     ulonglong2 *ll_dev = nullptr;              // [2][R][ll_vecs]
     uint64_t ll_vecs = 0, ll_bytes = 0;
+    ar_trace_record *trace = nullptr;          // caller's trace buffer (ar_set_trace), or null
+    uint32_t trace_depth = 0;
     bool pdl = true;                           // launch as programmatic dependents
     void *slots_host = nullptr;            // pinned kind: host address of the slots
     uint8_t *slots_dev = nullptr;          // device address of the slots
@@ -123,6 +125,9 @@ DevState dev_state(const ar_handle *h) {
     d.sys_scope = h->kind == AR_SLOT_PINNED_HOST ? 1 : 0;
     d.ll = h->ll_dev;
     d.ll_vecs = h->ll_vecs;
+    d.trace = h->trace;
+    d.trace_depth = h->trace_depth;
+    d.algo = AR_ALGO_ONESHOT;
     return d;
 }
 
@@ -415,8 +420,9 @@ int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
     const int variant = algo == AR_ALGO_TWOSHOT  ? tda::twoshot_variant(plan.subtile_vecs)
                         : algo == AR_ALGO_TAGGED ? tda::kTaggedVariant
                                                  : plan.unroll;
-    const cudaError_t e = tda::launch_allreduce(h->dtype, h->R, variant, blocks, s, io, numel, rank,
-                                                dev_state(h), h->pdl);
+    DevState d = dev_state(h);
+    d.algo = algo;
+    const cudaError_t e = tda::launch_allreduce(h->dtype, h->R, variant, blocks, s, io, numel, rank, d, h->pdl);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return AR_ECUDA;
@@ -698,6 +704,21 @@ AR_API int ar_set_algo(ar_handle *h, int algo) {
         return AR_EINVAL;
     if ((algo == AR_ALGO_TWOSHOT || algo == AR_ALGO_TAGGED) && h->dtype == AR_C64) return AR_EINVAL;
     h->algo = algo;
+    return AR_OK;
+}
+
+AR_API int ar_set_trace(ar_handle *h, void *records, uint64_t capacity) {
+    if (!h) return AR_EINVAL;
+    if (!records) {
+        h->trace = nullptr;
+        h->trace_depth = 0;
+        return AR_OK;
+    }
+    const uint64_t per_call = (uint64_t)h->R * (uint64_t)h->bmax;
+    if (capacity < per_call || ((uintptr_t)records % 16)) return AR_EINVAL;
+    const uint64_t depth = capacity / per_call;
+    h->trace = static_cast<ar_trace_record *>(records);
+    h->trace_depth = (uint32_t)(depth > 0xffffffffull ? 0xffffffffull : depth);
     return AR_OK;
 }
 

@@ -51,6 +51,9 @@ struct DevState {
     int sys_scope;             // 1: slots/flags in host memory, system-scope ordering
     ulonglong2 *ll;            // [2][R][ll_vecs] tagged-word buffers (same memory as the slots)
     uint64_t ll_vecs;          // 16-byte tagged vectors per rank and parity: 2 per 16 payload bytes
+    ar_trace_record *trace;    // [depth][R][bmax] or null (tracing off)
+    uint32_t trace_depth;
+    int32_t algo;              // AR_ALGO_* of this launch, for the trace
 };
 
 // The input and output pointers of every rank, passed by value to a launch

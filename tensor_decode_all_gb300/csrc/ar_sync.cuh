@@ -89,6 +89,45 @@ __device__ __forceinline__ void st_tagged(ulonglong2 *p, ulonglong2 v, int sys) 
         asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(v.x), "l"(v.y) : "memory");
 }
 
+// Trace of one block in one call, kept in shared memory by thread 0 (no
+// registers held across the kernel); nothing happens when tracing is off.
+struct TraceMarks {
+    unsigned long long t0;
+    long long c0;
+    uint32_t pub, peers;
+};
+
+__device__ __forceinline__ void trace_start(const DevState &d, TraceMarks &m) {
+    if (d.trace) {
+        m.t0 = global_timer_ns();
+        m.c0 = clock64();
+        m.pub = 0;
+        m.peers = 0;
+    }
+}
+__device__ __forceinline__ void trace_published(const DevState &d, TraceMarks &m) {
+    if (d.trace && m.pub == 0) m.pub = (uint32_t)(clock64() - m.c0) | 1u;
+}
+__device__ __forceinline__ void trace_peers(const DevState &d, TraceMarks &m) {
+    if (d.trace && m.peers == 0) m.peers = (uint32_t)(clock64() - m.c0) | 1u;
+}
+__device__ __forceinline__ void trace_finish(const DevState &d, const TraceMarks &m, int R, int rank, int block,
+                                          unsigned long long calls, unsigned long long stages) {
+    const uint64_t i = ((calls % d.trace_depth) * (uint64_t)R + (uint64_t)rank) * (uint64_t)d.bmax + block;
+    ar_trace_record rec;
+    rec.rank = rank;
+    rec.block = block;
+    rec.call = (uint32_t)calls;
+    rec.stages = (uint32_t)stages;
+    rec.t_start_ns = m.t0;
+    rec.t_end_ns = global_timer_ns();
+    rec.cyc_published = m.pub;
+    rec.cyc_peers = m.peers;
+    rec.cyc_end = (uint32_t)(clock64() - m.c0);
+    rec.algo = (uint32_t)d.algo;
+    d.trace[i] = rec;
+}
+
 // Programmatic dependent launch.  When a rank's next call is launched with the
 // programmatic-serialization attribute, its blocks may become resident before
 // this call ends.  Each kernel therefore waits (griddepcontrol.wait: the

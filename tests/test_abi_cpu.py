@@ -128,7 +128,9 @@ def test_struct_layouts_match_header(lib, tmp_path):
     gcc = shutil.which("gcc") or shutil.which("cc")
     if gcc is None:
         pytest.skip("no C compiler")
-    structs = {"ar_error_info": ar.ErrorInfo, "ar_info": ar.Info, "ar_plan": ar.Plan, "ar_tactics": ar.Tactics}
+    from tensor_decode_all_gb300 import trace
+    structs = {"ar_error_info": ar.ErrorInfo, "ar_info": ar.Info, "ar_plan": ar.Plan, "ar_tactics": ar.Tactics,
+               "ar_trace_record": trace.TraceRecord}
     lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "ar.h"', "int main(void) {"]
     for cname, py in structs.items():
         lines.append(f'    printf("{cname} size %zu\\n", sizeof({cname}));')
