@@ -301,8 +301,11 @@ AR_API int ar_set_timeout(ar_handle *h, uint64_t timeout_ns);
  * every later call (enqueued or captured after this) writes one record, at
  * index ((call % depth) * R + rank) * max_blocks + block, depth = capacity /
  * (R * max_blocks) (ar_info.max_blocks), so the last `depth` calls of each
- * block are kept.  capacity < R * max_blocks returns AR_EINVAL.  Tracing
- * adds a few stores per block and call; off, it costs one test of a pointer.
+ * block are kept.  capacity < R * max_blocks or a buffer not 16-byte aligned
+ * returns AR_EINVAL.  Traced calls run kernels built with the trace code (a
+ * few stores per block and call); untraced calls run kernels built without
+ * it, so tracing off costs nothing.  A captured graph keeps the setting in
+ * force at capture (and writes to that buffer while it lives).
  * The pages measure with serving metrics and a probe; this shows, without an
  * external profiler, that the R rank kernels of a call run at the same time
  * and where a call's time goes.

@@ -48,7 +48,7 @@ struct Vec<1> {
 // on a GB300, complex64 1000 x 500 shards in HBM: R=4 21.8 -> 20.3 us (against
 // the unbounded build's 3 blocks per SM), R=8 64.9 -> 64.3 us, R=8 500 KB
 // 12.0 -> 11.4 us.
-template <int VW, int R, int U, bool F>
+template <int VW, int R, int U, bool F, bool T>
 __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
     allgather_kernel(const uint8_t *in_arg, uint8_t *out_arg, uint64_t bytes, int rank_arg, DevState d, RankIO io) {
     using V = typename Vec<VW>::T;
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
 
     pdl_wait();
     if (tid == 0) {
-        trace_start(d, s_tr);
+        trace_start<T>(d, s_tr);
         const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
         s_seq = c.seq;
         s_calls = c.calls;
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
         __syncthreads();
         if (tid == 0) {
             publish_stage(d, rank, b, seq + s + 1);
-            trace_published(d, s_tr);
+            trace_published<T>(d, s_tr);
         }
 
         V nxt[U];
@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
         }
 
         if (wait_peers(d, R, rank, b, seq + s + 1, &s_bail)) return;
-        if (tid == 0) trace_peers(d, s_tr);
+        if (tid == 0) trace_peers<T>(d, s_tr);
         // Every peer block of this call has now published its last stage, so
         // all of them are resident: this rank's next call may be scheduled.
         if (s + 1 == nstages) pdl_trigger();
@@ -150,51 +150,52 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
         c.seq = seq + nstages;
         c.calls = s_calls + 1;
         d.ctr[(size_t)rank * d.bmax + b] = c;
-        if (d.trace) trace_finish(d, s_tr, R, rank, b, s_calls, nstages);
+        trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
     }
 }
 
-template <int VW, int U, bool F>
+template <int VW, int U, bool F, bool T>
 const void *allgather_ptr_ru(int R) {
     switch (R) {
-        case 1: return (const void *)allgather_kernel<VW, 1, U, F>;
-        case 2: return (const void *)allgather_kernel<VW, 2, U, F>;
-        case 3: return (const void *)allgather_kernel<VW, 3, U, F>;
-        case 4: return (const void *)allgather_kernel<VW, 4, U, F>;
-        case 5: return (const void *)allgather_kernel<VW, 5, U, F>;
-        case 6: return (const void *)allgather_kernel<VW, 6, U, F>;
-        case 7: return (const void *)allgather_kernel<VW, 7, U, F>;
-        case 8: return (const void *)allgather_kernel<VW, 8, U, F>;
+        case 1: return (const void *)allgather_kernel<VW, 1, U, F, T>;
+        case 2: return (const void *)allgather_kernel<VW, 2, U, F, T>;
+        case 3: return (const void *)allgather_kernel<VW, 3, U, F, T>;
+        case 4: return (const void *)allgather_kernel<VW, 4, U, F, T>;
+        case 5: return (const void *)allgather_kernel<VW, 5, U, F, T>;
+        case 6: return (const void *)allgather_kernel<VW, 6, U, F, T>;
+        case 7: return (const void *)allgather_kernel<VW, 7, U, F, T>;
+        case 8: return (const void *)allgather_kernel<VW, 8, U, F, T>;
         default: return nullptr;
     }
 }
 
-template <int VW, bool F>
-const void *allgather_ptr_rf(int R, int U) {
-    return U == 1 ? allgather_ptr_ru<VW, 1, F>(R) : allgather_ptr_ru<VW, 2, F>(R);
+template <int VW, bool F, bool T>
+const void *allgather_ptr_rft(int R, int U) {
+    return U == 1 ? allgather_ptr_ru<VW, 1, F, T>(R) : allgather_ptr_ru<VW, 2, F, T>(R);
 }
 
 template <int VW>
-const void *allgather_ptr_r(int R, int U, bool fused) {
-    return fused ? allgather_ptr_rf<VW, true>(R, U) : allgather_ptr_rf<VW, false>(R, U);
+const void *allgather_ptr_r(int R, int U, bool fused, bool traced) {
+    if (traced) return fused ? allgather_ptr_rft<VW, true, true>(R, U) : allgather_ptr_rft<VW, false, true>(R, U);
+    return fused ? allgather_ptr_rft<VW, true, false>(R, U) : allgather_ptr_rft<VW, false, false>(R, U);
 }
 
 }  // namespace
 
-const void *allgather_kernel_ptr(int vec_bytes, int R, int unroll, bool fused) {
+const void *allgather_kernel_ptr(int vec_bytes, int R, int unroll, bool fused, bool traced) {
     switch (vec_bytes) {
-        case 16: return allgather_ptr_r<16>(R, unroll, fused);
-        case 8: return allgather_ptr_r<8>(R, unroll, fused);
-        case 4: return allgather_ptr_r<4>(R, unroll, fused);
-        case 2: return allgather_ptr_r<2>(R, unroll, fused);
-        case 1: return allgather_ptr_r<1>(R, unroll, fused);
+        case 16: return allgather_ptr_r<16>(R, unroll, fused, traced);
+        case 8: return allgather_ptr_r<8>(R, unroll, fused, traced);
+        case 4: return allgather_ptr_r<4>(R, unroll, fused, traced);
+        case 2: return allgather_ptr_r<2>(R, unroll, fused, traced);
+        case 1: return allgather_ptr_r<1>(R, unroll, fused, traced);
         default: return nullptr;
     }
 }
 
 cudaError_t launch_allgather(int vec_bytes, int R, int unroll, int blocks, cudaStream_t s,
                              const RankIO &io, uint64_t bytes, int rank, const DevState &d, bool pdl) {
-    const void *k = allgather_kernel_ptr(vec_bytes, R, unroll, rank < 0);
+    const void *k = allgather_kernel_ptr(vec_bytes, R, unroll, rank < 0, d.trace != nullptr);
     if (!k) return cudaErrorInvalidValue;
     const uint8_t *a0 = static_cast<const uint8_t *>(io.in[0]);
     uint8_t *a1 = static_cast<uint8_t *>(io.out[0]);

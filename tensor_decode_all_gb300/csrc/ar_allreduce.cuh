@@ -127,7 +127,7 @@ __device__ __forceinline__ void store_out(uint16_t *out, uint64_t v, uint64_t nv
     }
 }
 
-template <class Ops, int R, int U, bool F>
+template <class Ops, int R, int U, bool F, bool T>
 __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16_t *out_arg, uint64_t numel,
                                                   int rank_arg, const DevState &d, const RankIO &io) {
     __shared__ unsigned long long s_seq;
@@ -151,7 +151,7 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
 
     pdl_wait();
     if (tid == 0) {
-        trace_start(d, s_tr);
+        trace_start<T>(d, s_tr);
         const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
         s_seq = c.seq;
         s_calls = c.calls;
@@ -186,7 +186,7 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
         // 3. raise the flag
         if (tid == 0) {
             publish_stage(d, rank, b, seq + s + 1);
-            trace_published(d, s_tr);
+            trace_published<T>(d, s_tr);
         }
 
         // next stage's input, overlapping the wait
@@ -199,7 +199,7 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
 
         // 4. wait for the peers
         if (wait_peers(d, R, rank, b, seq + s + 1, &s_bail)) return;
-        if (tid == 0) trace_peers(d, s_tr);
+        if (tid == 0) trace_peers<T>(d, s_tr);
         // Every peer block of this call has now published its last stage, so
         // all of them are resident: this rank's next call may be scheduled.
         if (s + 1 == nstages) pdl_trigger();
@@ -237,24 +237,24 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
         c.seq = seq + nstages;
         c.calls = s_calls + 1;
         d.ctr[(size_t)rank * d.bmax + b] = c;
-        if (d.trace) trace_finish(d, s_tr, R, rank, b, s_calls, nstages);
+        trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
     }
 }
 
 // One rank's launch.
-template <class Ops, int R, int U>
+template <class Ops, int R, int U, bool T>
 __global__ void __launch_bounds__(kThreads)
     allreduce_kernel_rank(const uint16_t *in, uint16_t *out, uint64_t numel, int rank, DevState d, RankIO io) {
-    allreduce_oneshot<Ops, R, U, false>(in, out, numel, rank, d, io);
+    allreduce_oneshot<Ops, R, U, false, T>(in, out, numel, rank, d, io);
 }
 
 // A launch of all ranks, held to the blocks per SM the one-rank kernel gets
 // unasked (5 up to R = 3, else 4): with fewer resident blocks a decode-sized
 // call would need a second stage, and a large one would move less at once.
-template <class Ops, int R, int U>
+template <class Ops, int R, int U, bool T>
 __global__ void __launch_bounds__(kThreads, R <= 3 ? 5 : 4)
     allreduce_kernel_all(const uint16_t *in, uint16_t *out, uint64_t numel, int rank, DevState d, RankIO io) {
-    allreduce_oneshot<Ops, R, U, true>(in, out, numel, rank, d, io);
+    allreduce_oneshot<Ops, R, U, true, T>(in, out, numel, rank, d, io);
 }
 
 // Two-shot variant, for large payloads at R >= 4, where the one-shot form's
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 5 : 4)
 template <int R>
 constexpr int twoshot_min_blocks() { return R <= 4 ? 6 : 4; }
 
-template <class Ops, int R, int SUB, bool F>
+template <class Ops, int R, int SUB, bool F, bool T>
 __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
     allreduce_twoshot_kernel(const uint16_t *in_arg, uint16_t *out_arg, uint64_t numel, int rank_arg, DevState d, RankIO io) {
     static_assert(SUB == 64 || SUB == 128 || SUB == 256, "sub-tile of 64, 128 or 256 vectors");
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
 
     pdl_wait();
     if (tid == 0) {
-        trace_start(d, s_tr);
+        trace_start<T>(d, s_tr);
         const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
         s_seq = c.seq;
         s_calls = c.calls;
@@ -339,10 +339,10 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
         __syncthreads();
         if (tid == 0) {
             publish_stage(d, rank, b, seq + 2 * s + 1);
-            trace_published(d, s_tr);
+            trace_published<T>(d, s_tr);
         }
         if (wait_peers(d, R, rank, b, seq + 2 * s + 1, &s_bail)) return;
-        if (tid == 0) trace_peers(d, s_tr);
+        if (tid == 0) trace_peers<T>(d, s_tr);
 
         // 2. reduce sub-tile `rank` in rank order; the result replaces it in my slot
         const uint64_t vr = tbase + (uint64_t)rank * SUB + tid;
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
         c.seq = seq + 2 * nstages;
         c.calls = s_calls + 1;
         d.ctr[(size_t)rank * d.bmax + b] = c;
-        if (d.trace) trace_finish(d, s_tr, R, rank, b, s_calls, nstages);
+        trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
     }
 }
 
@@ -413,64 +413,65 @@ namespace tda {
 
 namespace tda {
 
-template <class Ops, bool F>
+template <class Ops, bool F, bool T>
 const void *allreduce_tagged_ptr(int R) {
     switch (R) {
-        case 1: return F ? (const void *)allreduce_tagged_all<Ops, 1> : (const void *)allreduce_tagged_rank<Ops, 1>;
-        case 2: return F ? (const void *)allreduce_tagged_all<Ops, 2> : (const void *)allreduce_tagged_rank<Ops, 2>;
-        case 3: return F ? (const void *)allreduce_tagged_all<Ops, 3> : (const void *)allreduce_tagged_rank<Ops, 3>;
-        case 4: return F ? (const void *)allreduce_tagged_all<Ops, 4> : (const void *)allreduce_tagged_rank<Ops, 4>;
-        case 5: return F ? (const void *)allreduce_tagged_all<Ops, 5> : (const void *)allreduce_tagged_rank<Ops, 5>;
-        case 6: return F ? (const void *)allreduce_tagged_all<Ops, 6> : (const void *)allreduce_tagged_rank<Ops, 6>;
-        case 7: return F ? (const void *)allreduce_tagged_all<Ops, 7> : (const void *)allreduce_tagged_rank<Ops, 7>;
-        case 8: return F ? (const void *)allreduce_tagged_all<Ops, 8> : (const void *)allreduce_tagged_rank<Ops, 8>;
+        case 1: return F ? (const void *)allreduce_tagged_all<Ops, 1, T> : (const void *)allreduce_tagged_rank<Ops, 1, T>;
+        case 2: return F ? (const void *)allreduce_tagged_all<Ops, 2, T> : (const void *)allreduce_tagged_rank<Ops, 2, T>;
+        case 3: return F ? (const void *)allreduce_tagged_all<Ops, 3, T> : (const void *)allreduce_tagged_rank<Ops, 3, T>;
+        case 4: return F ? (const void *)allreduce_tagged_all<Ops, 4, T> : (const void *)allreduce_tagged_rank<Ops, 4, T>;
+        case 5: return F ? (const void *)allreduce_tagged_all<Ops, 5, T> : (const void *)allreduce_tagged_rank<Ops, 5, T>;
+        case 6: return F ? (const void *)allreduce_tagged_all<Ops, 6, T> : (const void *)allreduce_tagged_rank<Ops, 6, T>;
+        case 7: return F ? (const void *)allreduce_tagged_all<Ops, 7, T> : (const void *)allreduce_tagged_rank<Ops, 7, T>;
+        case 8: return F ? (const void *)allreduce_tagged_all<Ops, 8, T> : (const void *)allreduce_tagged_rank<Ops, 8, T>;
         default: return nullptr;
     }
 }
 
-// Kernel entry for (element ops, R, unroll, one rank or all ranks), as an
-// untyped address for cudaLaunchKernelExC and the occupancy calculator.
-template <class Ops, int R, int U, bool F>
+// Kernel entry for (element ops, R, unroll, one rank or all ranks, traced or
+// not), as an untyped address for cudaLaunchKernelExC and the occupancy
+// calculator.
+template <class Ops, int R, int U, bool F, bool T>
 constexpr const void *oneshot_entry() {
-    return F ? (const void *)allreduce_kernel_all<Ops, R, U> : (const void *)allreduce_kernel_rank<Ops, R, U>;
+    return F ? (const void *)allreduce_kernel_all<Ops, R, U, T> : (const void *)allreduce_kernel_rank<Ops, R, U, T>;
 }
 
-template <class Ops, int U, bool F>
+template <class Ops, int U, bool F, bool T>
 const void *allreduce_ptr_ru(int R) {
     switch (R) {
-        case 1: return oneshot_entry<Ops, 1, U, F>();
-        case 2: return oneshot_entry<Ops, 2, U, F>();
-        case 3: return oneshot_entry<Ops, 3, U, F>();
-        case 4: return oneshot_entry<Ops, 4, U, F>();
-        case 5: return oneshot_entry<Ops, 5, U, F>();
-        case 6: return oneshot_entry<Ops, 6, U, F>();
-        case 7: return oneshot_entry<Ops, 7, U, F>();
-        case 8: return oneshot_entry<Ops, 8, U, F>();
+        case 1: return oneshot_entry<Ops, 1, U, F, T>();
+        case 2: return oneshot_entry<Ops, 2, U, F, T>();
+        case 3: return oneshot_entry<Ops, 3, U, F, T>();
+        case 4: return oneshot_entry<Ops, 4, U, F, T>();
+        case 5: return oneshot_entry<Ops, 5, U, F, T>();
+        case 6: return oneshot_entry<Ops, 6, U, F, T>();
+        case 7: return oneshot_entry<Ops, 7, U, F, T>();
+        case 8: return oneshot_entry<Ops, 8, U, F, T>();
         default: return nullptr;
     }
 }
 
-template <class Ops, int SUB, bool F>
+template <class Ops, int SUB, bool F, bool T>
 const void *allreduce_twoshot_ptr_r(int R) {
     switch (R) {
-        case 1: return (const void *)allreduce_twoshot_kernel<Ops, 1, SUB, F>;
-        case 2: return (const void *)allreduce_twoshot_kernel<Ops, 2, SUB, F>;
-        case 3: return (const void *)allreduce_twoshot_kernel<Ops, 3, SUB, F>;
-        case 4: return (const void *)allreduce_twoshot_kernel<Ops, 4, SUB, F>;
-        case 5: return (const void *)allreduce_twoshot_kernel<Ops, 5, SUB, F>;
-        case 6: return (const void *)allreduce_twoshot_kernel<Ops, 6, SUB, F>;
-        case 7: return (const void *)allreduce_twoshot_kernel<Ops, 7, SUB, F>;
-        case 8: return (const void *)allreduce_twoshot_kernel<Ops, 8, SUB, F>;
+        case 1: return (const void *)allreduce_twoshot_kernel<Ops, 1, SUB, F, T>;
+        case 2: return (const void *)allreduce_twoshot_kernel<Ops, 2, SUB, F, T>;
+        case 3: return (const void *)allreduce_twoshot_kernel<Ops, 3, SUB, F, T>;
+        case 4: return (const void *)allreduce_twoshot_kernel<Ops, 4, SUB, F, T>;
+        case 5: return (const void *)allreduce_twoshot_kernel<Ops, 5, SUB, F, T>;
+        case 6: return (const void *)allreduce_twoshot_kernel<Ops, 6, SUB, F, T>;
+        case 7: return (const void *)allreduce_twoshot_kernel<Ops, 7, SUB, F, T>;
+        case 8: return (const void *)allreduce_twoshot_kernel<Ops, 8, SUB, F, T>;
         default: return nullptr;
     }
 }
 
-template <class Ops, bool F>
+template <class Ops, bool F, bool T>
 const void *allreduce_twoshot_ptr(int R, int sub) {
     switch (sub) {
-        case 256: return allreduce_twoshot_ptr_r<Ops, 256, F>(R);
-        case 128: return allreduce_twoshot_ptr_r<Ops, 128, F>(R);
-        case 64: return allreduce_twoshot_ptr_r<Ops, 64, F>(R);
+        case 256: return allreduce_twoshot_ptr_r<Ops, 256, F, T>(R);
+        case 128: return allreduce_twoshot_ptr_r<Ops, 128, F, T>(R);
+        case 64: return allreduce_twoshot_ptr_r<Ops, 64, F, T>(R);
         default: return nullptr;
     }
 }
@@ -478,17 +479,19 @@ const void *allreduce_twoshot_ptr(int R, int sub) {
 // U = 1 or 2: one-shot with that many vectors per thread per stage;
 // U = twoshot_variant(sub): the two-shot form with sub-tiles of `sub` vectors;
 // U = kTaggedVariant: the tagged-word form.
-// fused: the kernel for one launch of all ranks (grid blocks x R).
-template <class Ops, bool F>
-const void *allreduce_ptr_f(int R, int U) {
-    if (U == kTaggedVariant) return allreduce_tagged_ptr<Ops, F>(R);
-    if (U < 0) return allreduce_twoshot_ptr<Ops, F>(R, twoshot_sub(U));
-    return U == 1 ? allreduce_ptr_ru<Ops, 1, F>(R) : allreduce_ptr_ru<Ops, 2, F>(R);
+// fused: the kernel for one launch of all ranks (grid blocks x R); traced:
+// the kernel that writes trace records.
+template <class Ops, bool F, bool T>
+const void *allreduce_ptr_ft(int R, int U) {
+    if (U == kTaggedVariant) return allreduce_tagged_ptr<Ops, F, T>(R);
+    if (U < 0) return allreduce_twoshot_ptr<Ops, F, T>(R, twoshot_sub(U));
+    return U == 1 ? allreduce_ptr_ru<Ops, 1, F, T>(R) : allreduce_ptr_ru<Ops, 2, F, T>(R);
 }
 
 template <class Ops>
-const void *allreduce_ptr(int R, int U, bool fused) {
-    return fused ? allreduce_ptr_f<Ops, true>(R, U) : allreduce_ptr_f<Ops, false>(R, U);
+const void *allreduce_ptr(int R, int U, bool fused, bool traced) {
+    if (traced) return fused ? allreduce_ptr_ft<Ops, true, true>(R, U) : allreduce_ptr_ft<Ops, false, true>(R, U);
+    return fused ? allreduce_ptr_ft<Ops, true, false>(R, U) : allreduce_ptr_ft<Ops, false, false>(R, U);
 }
 
 }  // namespace tda

@@ -2,5 +2,7 @@
 #include "ar_allreduce.cuh"
 
 namespace tda {
-const void *allreduce_kernel_ptr_bf16(int R, int U, bool fused) { return allreduce_ptr<BF16Ops>(R, U, fused); }
+const void *allreduce_kernel_ptr_bf16(int R, int U, bool fused, bool traced) {
+    return allreduce_ptr<BF16Ops>(R, U, fused, traced);
+}
 }  // namespace tda

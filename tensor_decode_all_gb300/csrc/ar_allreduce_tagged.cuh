@@ -29,7 +29,7 @@
 
 namespace tda {
 
-template <class Ops, int R, bool F>
+template <class Ops, int R, bool F, bool T>
 __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, uint16_t *out_arg, uint64_t numel,
                                                       int rank_arg, const DevState &d, const RankIO &io) {
     __shared__ unsigned long long s_seq;
@@ -51,7 +51,7 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
 
     pdl_wait();
     if (tid == 0) {
-        trace_start(d, s_tr);
+        trace_start<T>(d, s_tr);
         const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
         s_seq = c.seq;
         s_calls = c.calls;
@@ -76,7 +76,7 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
             st_tagged(mine + 2 * v, make_ulonglong2(tag | own.x, tag | own.y), sys);
             st_tagged(mine + 2 * v + 1, make_ulonglong2(tag | own.z, tag | own.w), sys);
         }
-        if (tid == 0) trace_published(d, s_tr);
+        if (tid == 0) trace_published<T>(d, s_tr);
         // the next stage's input, overlapping the wait
         uint4 nxt = make_uint4(0u, 0u, 0u, 0u);
         if (s + 1 < nstages && !bail) nxt = load_own(in, v + (uint64_t)B * kThreads, nvec_full, tail);
@@ -121,7 +121,7 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
                 if (iter > 32u) __nanosleep(32);
             }
         }
-        if (tid == 0) trace_peers(d, s_tr);
+        if (tid == 0) trace_peers<T>(d, s_tr);
         // Every peer block of this call has now published its last stage, so
         // all of them are resident: this rank's next call may be scheduled.
         if (s + 1 == nstages) {
@@ -154,22 +154,22 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
         c.seq = seq + nstages;
         c.calls = s_calls + 1;
         d.ctr[(size_t)rank * d.bmax + b] = c;
-        if (d.trace) trace_finish(d, s_tr, R, rank, b, s_calls, nstages);
+        trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
     }
 }
 
 // Both entries are held to 64 registers (4 blocks per SM), so that a call
 // spreads over as many blocks as the one-shot form's.
-template <class Ops, int R>
+template <class Ops, int R, bool T>
 __global__ void __launch_bounds__(kThreads, 4)
     allreduce_tagged_rank(const uint16_t *in, uint16_t *out, uint64_t numel, int rank, DevState d, RankIO io) {
-    allreduce_tagged_body<Ops, R, false>(in, out, numel, rank, d, io);
+    allreduce_tagged_body<Ops, R, false, T>(in, out, numel, rank, d, io);
 }
 
-template <class Ops, int R>
+template <class Ops, int R, bool T>
 __global__ void __launch_bounds__(kThreads, 4)
     allreduce_tagged_all(const uint16_t *in, uint16_t *out, uint64_t numel, int rank, DevState d, RankIO io) {
-    allreduce_tagged_body<Ops, R, true>(in, out, numel, rank, d, io);
+    allreduce_tagged_body<Ops, R, true, T>(in, out, numel, rank, d, io);
 }
 
 }  // namespace tda

@@ -19,13 +19,17 @@
 using tda::Ctr;
 using tda::DevState;
 
+// Kernel families, for the occupancy table.
+enum { kOneShot = 0, kTwoShot = 1, kTagged = 2, kAllgather = 3, kFamilies = 4 };
+
 struct ar_handle {
     int R = 0, dtype = 0, kind = 0, device = 0;
     uint64_t max_numel = 0, itemsize = 0, slot_bytes = 0;
     int sm_count = 0;
-    int bps_one = 0, bps_two = 0, bps_ag = 0;  // occupancy per kernel family (one rank's launch)
-    int bps_one_f = 0, bps_two_f = 0, bps_ag_f = 0;  // the same for one launch of all ranks
-    int bps_tag = 0, bps_tag_f = 0;                  // tagged-word form (one rank / all ranks)
+    // Blocks per SM of each kernel family, for [one rank's launch / all ranks
+    // in one launch][untraced / traced kernels][family] (the smallest over
+    // the family's variants).
+    int bps[2][2][kFamilies] = {};
     int bmax = 0;                              // flag/counter slots per rank
     int algo = AR_ALGO_AUTO;
     int twoshot_sub = 0;                       // tactic: two-shot sub-tile (64/128/256); 0 = size rule
@@ -185,38 +189,37 @@ int kernel_occupancy(const void *k, int *bps) {
     return AR_OK;
 }
 
-int family_occupancy(const ar_handle *h, bool fused, int *one, int *two, int *ag) {
-    *one = *two = *ag = 1 << 30;
+// Occupancy of every family for one (launch kind, traced) pair.
+int family_occupancy(const ar_handle *h, bool fused, bool traced, int *bps) {
+    const int kUnset = 1 << 30;
+    for (int f = 0; f < kFamilies; ++f) bps[f] = kUnset;
     int rc = AR_OK;
     if (h->dtype == AR_F16 || h->dtype == AR_BF16) {
         for (int u = 1; u <= 2 && rc == AR_OK; ++u)
-            rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, u, fused), one);
+            rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, u, fused, traced), &bps[kOneShot]);
         for (int sub = 64; sub <= 256 && rc == AR_OK; sub *= 2)
-            rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, tda::twoshot_variant(sub), fused), two);
+            rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, tda::twoshot_variant(sub), fused, traced),
+                                  &bps[kTwoShot]);
+        if (rc == AR_OK)
+            rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, tda::kTaggedVariant, fused, traced),
+                                  &bps[kTagged]);
     }
     for (int u = 1; u <= 2 && rc == AR_OK; ++u)
         for (int vw = 1; vw <= 16 && rc == AR_OK; vw *= 2)
-            rc = kernel_occupancy(tda::allgather_kernel_ptr(vw, h->R, u, fused), ag);
+            rc = kernel_occupancy(tda::allgather_kernel_ptr(vw, h->R, u, fused, traced), &bps[kAllgather]);
     if (rc != AR_OK) return rc;
-    if (*one == 1 << 30) *one = *ag;
-    if (*two == 1 << 30) *two = *ag;
-    if (*one < 1 || *two < 1 || *ag < 1) return AR_ECUDA;
+    for (int f = 0; f < kFamilies; ++f) {
+        if (bps[f] == kUnset) bps[f] = bps[kAllgather];  // complex64 handles launch no all-reduce kernel
+        if (bps[f] < 1) return AR_ECUDA;
+    }
     return AR_OK;
 }
 
 int handle_occupancy(ar_handle *h) {
-    int rc = family_occupancy(h, false, &h->bps_one, &h->bps_two, &h->bps_ag);
-    if (rc == AR_OK) rc = family_occupancy(h, true, &h->bps_one_f, &h->bps_two_f, &h->bps_ag_f);
-    h->bps_tag = h->bps_one;
-    h->bps_tag_f = h->bps_one_f;
-    if (rc == AR_OK && (h->dtype == AR_F16 || h->dtype == AR_BF16)) {
-        int t = 1 << 30, tf = 1 << 30;
-        rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, tda::kTaggedVariant, false), &t);
-        if (rc == AR_OK) rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, tda::kTaggedVariant, true), &tf);
-        if (rc == AR_OK && (t < 1 || tf < 1)) rc = AR_ECUDA;
-        h->bps_tag = t;
-        h->bps_tag_f = tf;
-    }
+    int rc = AR_OK;
+    for (int fused = 0; fused < 2 && rc == AR_OK; ++fused)
+        for (int traced = 0; traced < 2 && rc == AR_OK; ++traced)
+            rc = family_occupancy(h, fused != 0, traced != 0, h->bps[fused][traced]);
     return rc;
 }
 
@@ -261,9 +264,8 @@ int handle_algo(const ar_handle *h, uint64_t bytes) {
 
 // Blocks per SM of the kernel family a call of `algo` launches.
 int handle_bps(const ar_handle *h, int algo, bool fused) {
-    if (algo == AR_ALGO_TWOSHOT) return fused ? h->bps_two_f : h->bps_two;
-    if (algo == AR_ALGO_TAGGED) return fused ? h->bps_tag_f : h->bps_tag;
-    return fused ? h->bps_one_f : h->bps_one;
+    const int f = algo == AR_ALGO_TWOSHOT ? kTwoShot : algo == AR_ALGO_TAGGED ? kTagged : kOneShot;
+    return h->bps[fused ? 1 : 0][h->trace ? 1 : 0][f];
 }
 
 // Blocks per rank a handle launches for a plan: the plan's, within the flag
@@ -289,7 +291,7 @@ int plan_compute_sub(int R, uint64_t bytes, int vec, int algo, int sub, int thre
 
 int handle_twoshot_sub(const ar_handle *h, uint64_t bytes) {
     if (h->twoshot_sub) return h->twoshot_sub;
-    const uint64_t bmax = (uint64_t)h->sm_count * (uint64_t)h->bps_two / (uint64_t)h->R;
+    const uint64_t bmax = (uint64_t)h->sm_count * (uint64_t)handle_bps(h, AR_ALGO_TWOSHOT, false) / (uint64_t)h->R;
     return twoshot_sub_for(h->R, (bytes + 15) / 16, bmax, h->kind);
 }
 
@@ -434,7 +436,7 @@ int enqueue_allgather(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
     const uint64_t bytes = numel * h->itemsize;
     ar_plan plan;
     int rc = plan_compute(h->R, bytes, vw, AR_ALGO_ONESHOT, tda::kThreads, h->sm_count,
-                          rank < 0 ? h->bps_ag_f : h->bps_ag, &plan);
+                          h->bps[rank < 0 ? 1 : 0][h->trace ? 1 : 0][kAllgather], &plan);
     if (rc != AR_OK) return rc;
     const int blocks = handle_blocks(h, plan.blocks);
     const cudaError_t e = tda::launch_allgather(vw, h->R, plan.unroll, blocks, s, io, bytes, rank,
@@ -517,11 +519,12 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
     // (R=4 bf16 32 MiB: 84 vs 101 us at 4 blocks).  Over the host link 4 blocks
     // per SM already keep the link busy and more only add contention (R=4 bf16
     // 8 MiB: 382 vs 362 us), so pinned slots keep 4.
-    if (h->kind == AR_SLOT_PINNED_HOST && h->bps_two > 4) h->bps_two = 4;
-    if (h->kind == AR_SLOT_PINNED_HOST && h->bps_two_f > 4) h->bps_two_f = 4;
-    int bps_max = h->bps_one > h->bps_two ? h->bps_one : h->bps_two;
-    if (h->bps_ag > bps_max) bps_max = h->bps_ag;
-    if (h->bps_tag > bps_max) bps_max = h->bps_tag;
+    int bps_max = 1;
+    for (auto &by_trace : h->bps)
+        for (auto &fam : by_trace) {
+            if (h->kind == AR_SLOT_PINNED_HOST && fam[kTwoShot] > 4) fam[kTwoShot] = 4;
+            for (int f = 0; f < kFamilies; ++f) bps_max = fam[f] > bps_max ? fam[f] : bps_max;
+        }
     h->bmax = h->sm_count * bps_max / R;
     if (const int cap = max_blocks_override()) h->bmax = cap < h->bmax ? cap : h->bmax;
     if (h->bmax < 1) return fail(AR_ECUDA);
@@ -670,9 +673,9 @@ AR_API int ar_query(const ar_handle *h, ar_info *info) {
     info->threads = tda::kThreads;
     info->max_blocks = h->bmax;
     info->sm_count = h->sm_count;
-    info->blocks_per_sm = h->bps_one;
-    info->blocks_per_sm_twoshot = h->bps_two;
-    info->blocks_per_sm_allgather = h->bps_ag;
+    info->blocks_per_sm = h->bps[0][0][kOneShot];
+    info->blocks_per_sm_twoshot = h->bps[0][0][kTwoShot];
+    info->blocks_per_sm_allgather = h->bps[0][0][kAllgather];
     info->algo = h->algo;
     info->pdl = h->pdl ? 1 : 0;
     info->max_numel = h->max_numel;
@@ -680,7 +683,7 @@ AR_API int ar_query(const ar_handle *h, ar_info *info) {
     info->total_slot_bytes = 2ull * (uint64_t)h->R * h->slot_bytes;
     info->timeout_ns = h->timeout_ns.load();
     info->tagged_capacity_bytes = h->tagged_cap;
-    info->blocks_per_sm_tagged = h->bps_tag;
+    info->blocks_per_sm_tagged = h->bps[0][0][kTagged];
     info->reserved = 0;
     return AR_OK;
 }
@@ -757,7 +760,7 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) 
     if (numel > h->max_numel) return AR_ETOOBIG;
     const uint64_t bytes = numel * h->itemsize;
     const int vec = op == 0 ? 16 : allgather_vec(bytes, nullptr, nullptr);
-    int algo = AR_ALGO_ONESHOT, bps = h->bps_ag;
+    int algo = AR_ALGO_ONESHOT, bps = h->bps[0][h->trace ? 1 : 0][kAllgather];
     if (op == 0) {
         algo = handle_algo(h, bytes);
         bps = handle_bps(h, algo, false);
@@ -775,15 +778,15 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) 
 
 namespace tda {
 
-const void *allreduce_kernel_ptr(int dtype, int R, int unroll, bool fused) {
-    if (dtype == AR_F16) return allreduce_kernel_ptr_f16(R, unroll, fused);
-    if (dtype == AR_BF16) return allreduce_kernel_ptr_bf16(R, unroll, fused);
+const void *allreduce_kernel_ptr(int dtype, int R, int unroll, bool fused, bool traced) {
+    if (dtype == AR_F16) return allreduce_kernel_ptr_f16(R, unroll, fused, traced);
+    if (dtype == AR_BF16) return allreduce_kernel_ptr_bf16(R, unroll, fused, traced);
     return nullptr;
 }
 
 cudaError_t launch_allreduce(int dtype, int R, int unroll, int blocks, cudaStream_t s,
                              const RankIO &io, uint64_t numel, int rank, const DevState &d, bool pdl) {
-    const void *k = allreduce_kernel_ptr(dtype, R, unroll, rank < 0);
+    const void *k = allreduce_kernel_ptr(dtype, R, unroll, rank < 0, d.trace != nullptr);
     if (!k) return cudaErrorInvalidValue;
     const uint16_t *a0 = static_cast<const uint16_t *>(io.in[0]);
     uint16_t *a1 = static_cast<uint16_t *>(io.out[0]);

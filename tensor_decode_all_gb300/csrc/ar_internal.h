@@ -81,11 +81,12 @@ cudaError_t launch_allreduce(int dtype, int R, int unroll, int blocks, cudaStrea
 cudaError_t launch_allgather(int vec_bytes, int R, int unroll, int blocks, cudaStream_t s,
                              const RankIO &io, uint64_t bytes, int rank, const DevState &d, bool pdl);
 
-// Kernel entry addresses, for occupancy queries.  fused: the kernel built for
-// one launch of all ranks (grid blocks x R) rather than one rank's launch.
-const void *allreduce_kernel_ptr(int dtype, int R, int unroll, bool fused);
-const void *allreduce_kernel_ptr_f16(int R, int unroll, bool fused);   // ar_allreduce_f16.cu
-const void *allreduce_kernel_ptr_bf16(int R, int unroll, bool fused);  // ar_allreduce_bf16.cu
-const void *allgather_kernel_ptr(int vec_bytes, int R, int unroll, bool fused);
+// Kernel entry addresses, for launches and occupancy queries.  fused: the
+// kernel built for one launch of all ranks (grid blocks x R) rather than one
+// rank's launch; traced: the kernel that writes trace records.
+const void *allreduce_kernel_ptr(int dtype, int R, int unroll, bool fused, bool traced);
+const void *allreduce_kernel_ptr_f16(int R, int unroll, bool fused, bool traced);   // ar_allreduce_f16.cu
+const void *allreduce_kernel_ptr_bf16(int R, int unroll, bool fused, bool traced);  // ar_allreduce_bf16.cu
+const void *allgather_kernel_ptr(int vec_bytes, int R, int unroll, bool fused, bool traced);
 
 }  // namespace tda

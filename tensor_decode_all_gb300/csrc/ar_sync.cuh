@@ -90,42 +90,54 @@ __device__ __forceinline__ void st_tagged(ulonglong2 *p, ulonglong2 v, int sys) 
 }
 
 // Trace of one block in one call, kept in shared memory by thread 0 (no
-// registers held across the kernel); nothing happens when tracing is off.
+// registers held across the kernel).
 struct TraceMarks {
     unsigned long long t0;
     long long c0;
     uint32_t pub, peers;
 };
 
+// T: the kernel is built with tracing (its launches come from a handle with
+// a trace buffer); without it, none of this is compiled in.
+template <bool T>
 __device__ __forceinline__ void trace_start(const DevState &d, TraceMarks &m) {
-    if (d.trace) {
+    if constexpr (T) {
         m.t0 = global_timer_ns();
         m.c0 = clock64();
         m.pub = 0;
         m.peers = 0;
     }
 }
+template <bool T>
 __device__ __forceinline__ void trace_published(const DevState &d, TraceMarks &m) {
-    if (d.trace && m.pub == 0) m.pub = (uint32_t)(clock64() - m.c0) | 1u;
+    if constexpr (T) {
+        if (m.pub == 0) m.pub = (uint32_t)(clock64() - m.c0) | 1u;
+    }
 }
+template <bool T>
 __device__ __forceinline__ void trace_peers(const DevState &d, TraceMarks &m) {
-    if (d.trace && m.peers == 0) m.peers = (uint32_t)(clock64() - m.c0) | 1u;
+    if constexpr (T) {
+        if (m.peers == 0) m.peers = (uint32_t)(clock64() - m.c0) | 1u;
+    }
 }
+template <bool T>
 __device__ __forceinline__ void trace_finish(const DevState &d, const TraceMarks &m, int R, int rank, int block,
-                                          unsigned long long calls, unsigned long long stages) {
-    const uint64_t i = ((calls % d.trace_depth) * (uint64_t)R + (uint64_t)rank) * (uint64_t)d.bmax + block;
-    ar_trace_record rec;
-    rec.rank = rank;
-    rec.block = block;
-    rec.call = (uint32_t)calls;
-    rec.stages = (uint32_t)stages;
-    rec.t_start_ns = m.t0;
-    rec.t_end_ns = global_timer_ns();
-    rec.cyc_published = m.pub;
-    rec.cyc_peers = m.peers;
-    rec.cyc_end = (uint32_t)(clock64() - m.c0);
-    rec.algo = (uint32_t)d.algo;
-    d.trace[i] = rec;
+                                             unsigned long long calls, unsigned long long stages) {
+    if constexpr (T) {
+        const uint64_t i = ((calls % d.trace_depth) * (uint64_t)R + (uint64_t)rank) * (uint64_t)d.bmax + block;
+        ar_trace_record rec;
+        rec.rank = rank;
+        rec.block = block;
+        rec.call = (uint32_t)calls;
+        rec.stages = (uint32_t)stages;
+        rec.t_start_ns = m.t0;
+        rec.t_end_ns = global_timer_ns();
+        rec.cyc_published = m.pub;
+        rec.cyc_peers = m.peers;
+        rec.cyc_end = (uint32_t)(clock64() - m.c0);
+        rec.algo = (uint32_t)d.algo;
+        d.trace[i] = rec;
+    }
 }
 
 // Programmatic dependent launch.  When a rank's next call is launched with the
