@@ -516,13 +516,16 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
     int rc = handle_occupancy(h);
     if (rc != AR_OK) return fail(rc);
     // The two-shot kernel fits 6 blocks per SM up to R = 4, which helps in HBM
-    // (R=4 bf16 32 MiB: 84 vs 101 us at 4 blocks).  Over the host link 4 blocks
-    // per SM already keep the link busy and more only add contention (R=4 bf16
-    // 8 MiB: 382 vs 362 us), so pinned slots keep 4.
+    // (R=4 bf16 32 MiB: 84 vs 101 us at 4 blocks).
+    // Over the host link fewer resident blocks keep the link just as busy with
+    // less contention: pinned handles cap the two-shot form at 4 blocks per SM
+    // (R=4 bf16 8 MiB: 362 us at 4, 382 at 6) and the allgather at 3 (R=4
+    // complex64 4 MB: 267 us at 3, 277 at 5).
     int bps_max = 1;
     for (auto &by_trace : h->bps)
         for (auto &fam : by_trace) {
             if (h->kind == AR_SLOT_PINNED_HOST && fam[kTwoShot] > 4) fam[kTwoShot] = 4;
+            if (h->kind == AR_SLOT_PINNED_HOST && fam[kAllgather] > 3) fam[kAllgather] = 3;
             for (int f = 0; f < kFamilies; ++f) bps_max = fam[f] > bps_max ? fam[f] : bps_max;
         }
     h->bmax = h->sm_count * bps_max / R;
