@@ -5,8 +5,8 @@
  * non-blocking stream; the R kernels of one call run at the same time and meet
  * through a shared, double-buffered slot and per-block flags.  The operation
  * is the flag-synchronised exchange-and-add of "[Kernel] Two-rank FP16
- * all-reduce through pinned host memory for GPUs without P2P" (1Cat-vLLM pull
- * 1216), section "Purpose": a block publishes its share of the data in a shared
+ * all-reduce through pinned host memory for GPUs without P2P", section
+ * "Purpose": a block publishes its share of the data in a shared
  * slot, makes it visible before it sets its own flag, and sums once it has seen
  * the flags of the matching blocks of the other ranks, rounding a single time;
  * consecutive calls use the two halves of the slot in turn; the host only
@@ -24,7 +24,7 @@
  *     blocking streams are refused (AR_ESTREAM): a stream that serialises with
  *     the legacy stream can hold back a peer rank's kernel while this rank's
  *     kernel waits for it ("fix(group): run each rank on a non-blocking
- *     stream", Algorithmiq src-method pull 75, sections "What" and "Why").
+ *     stream", sections "What" and "Why").
  *   - Return value: AR_OK (0) or an ar_code below.  A call that returns an
  *     error other than AR_ECUDA has enqueued nothing, so the caller can keep
  *     its own fallback path ("[SM120] Add optional FlashInfer PCIe-IPC
@@ -195,7 +195,7 @@ typedef struct ar_tactics {
  * gives the code (AR_EINVAL, AR_ENOMEM or AR_ECUDA).
  * The wait timeout starts at 1 s, or at the value of the environment variable
  * AR_SPIN_TIMEOUT_NS if set (bounded device spin: "fix(qwen3): re-enable CUDA
- * Graph under TP via startup decode-graph pre-capture", openinfer pull 611,
+ * Graph under TP via startup decode-graph pre-capture",
  * section "Description": without one, a wedged rank waits forever).
  */
 AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind);

@@ -18,11 +18,11 @@
  *   with IEEE binary32 additions (round to nearest, ties to even), taken in
  *   rank order, and one final rounding to D.  Sources:
  *     - "[Kernel] Two-rank FP16 all-reduce through pinned host memory for GPUs
- *       without P2P" (1Cat-vLLM pull 1216), section "Purpose": each block adds
+ *       without P2P", section "Purpose": each block adds
  *       the peer's chunk; the sum has a single FP16 rounding, is commutative and
  *       gives both ranks the same bits.
  *     - "[SM120] Add optional FlashInfer PCIe-IPC all-reduce for switch-free
- *       hosts" (sglang pull 34528), section "Accuracy": with eight ranks the
+ *       hosts", section "Accuracy": with eight ranks the
  *       accumulation order moves results by one bf16 step, so the order must be
  *       fixed; this oracle fixes it as rank order 0..R-1 on every rank.
  *   Readings where the pages are silent: the accumulator starts at f32(x_0)
@@ -32,7 +32,7 @@
  *
  *   allgather: every rank receives x_0 || x_1 || .. || x_{R-1}, the flat
  *   rank-major concatenation of the shards ("fix(group): run each rank on a
- *   non-blocking stream", Algorithmiq src-method pull 75, sections "What" and
+ *   non-blocking stream", sections "What" and
  *   "Why": DeviceGroup.allgather of the complex64 S_j and core uploads).
  *
  * The conversions between the 16-bit formats and binary32 are written here from
