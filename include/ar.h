@@ -335,9 +335,10 @@ AR_API int ar_plan_compute(int R, uint64_t bytes, int vec_bytes, int algo, int t
 
 /* The all-reduce form a new handle's AR_ALGO_AUTO picks for R ranks, `bytes`
  * per rank and a slot kind (a tactic table measured on a GB300; a handle's own
- * tactics may differ, see ar_tactics).  Tagged-word form up to 512 KiB (R <= 2)
- * or 64 KiB (R = 3, 4) with HBM slots and up to 16 KiB (R <= 2) with
- * pinned-host slots (within ar_info.tagged_capacity_bytes).  Otherwise
+ * tactics may differ, see ar_tactics).  Tagged-word form up to 512 KiB
+ * (R <= 2), 256 KiB (R = 3) or 64 KiB (R = 4) with HBM slots and up to 16 KiB
+ * (R <= 2) or 8 KiB (R = 3) with pinned-host slots (within
+ * ar_info.tagged_capacity_bytes).  Otherwise
  * one-shot for R <= 3; two-shot from 512 KiB (R >= 8) or 2 MiB (R = 4..7)
  * with HBM slots, and from 64 KiB (R >= 8) or 256 KiB (R = 4..7) with
  * pinned-host slots, where one-shot reads R(R-1)S bytes over the host link

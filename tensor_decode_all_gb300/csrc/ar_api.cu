@@ -236,16 +236,17 @@ uint64_t twoshot_threshold(int R, int slot_kind) {
 
 // Largest call the tagged-word form takes under AR_ALGO_AUTO.  Measured on a
 // GB300 (bf16, graphs of 100 calls, tagged vs the flag forms): in HBM it is
-// faster at every size up to 512 KiB at R = 2 (2 KiB: 2.7 vs 3.2 us; 256 KiB:
-// 3.5 vs 3.7 us) and up to 64 KiB at R = 4, and slower at R = 8, where every
-// thread polls 14 tagged vectors instead of one warp polling 8 flags.  Over
-// the host link its polls re-read words that have not landed yet, so it wins
-// only for small calls at R = 2 (8 KiB: 3.5 vs 4.0 us; up to 16 KiB).  R = 3
-// takes R = 4's value.
+// faster up to 512 KiB at R = 2 (2 KiB: 2.7 vs 3.2 us; 256 KiB: 3.5 vs
+// 3.7 us), up to 256 KiB at R = 3 (3.7 vs 4.0 us) and up to 64 KiB at R = 4;
+// from R = 5 on it is level at best and then slower: every thread polls
+// 2(R - 1) tagged vectors where one warp polls R flags.  Over the host link its
+// polls re-read words that have not landed yet, so it wins only for small
+// calls: up to 16 KiB at R = 2 (8 KiB: 3.5 vs 4.0 us) and 8 KiB at R = 3.
 uint64_t tagged_threshold(int R, int slot_kind) {
-    if (slot_kind == AR_SLOT_PINNED_HOST) return R <= 2 ? (16ull << 10) : 0;
+    if (slot_kind == AR_SLOT_PINNED_HOST) return R <= 2 ? (16ull << 10) : R == 3 ? (8ull << 10) : 0;
     if (R <= 2) return 512ull << 10;
-    return R <= 4 ? (64ull << 10) : 0;
+    if (R == 3) return 256ull << 10;
+    return R == 4 ? (64ull << 10) : 0;
 }
 
 int choose_algo(int R, uint64_t bytes, int slot_kind) {

@@ -104,8 +104,8 @@ def test_choose_algo_rule(lib):
         for R in (1, 2, 3):
             assert tda.ar_choose_algo(R, 1 << 30, kind) == ar.AR_ALGO_ONESHOT
     # tagged-word form for small calls (R, HBM limit, pinned limit; 0 = never)
-    for R, hbm, pinned in ((1, 512 << 10, 16 << 10), (2, 512 << 10, 16 << 10), (3, 64 << 10, 0),
-                           (4, 64 << 10, 0), (5, 0, 0), (8, 0, 0)):
+    for R, hbm, pinned in ((1, 512 << 10, 16 << 10), (2, 512 << 10, 16 << 10), (3, 256 << 10, 8 << 10),
+                           (4, 64 << 10, 0), (5, 0, 0), (6, 0, 0), (8, 0, 0)):
         for kind, lim in ((ar.AR_SLOT_HBM, hbm), (ar.AR_SLOT_PINNED_HOST, pinned)):
             if lim:
                 assert tda.ar_choose_algo(R, 16, kind) == ar.AR_ALGO_TAGGED
