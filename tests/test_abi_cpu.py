@@ -49,11 +49,11 @@ def test_null_handle_calls(lib):
     assert lib.ar_query(None, None) == ar.AR_EINVAL
 
 
-@pytest.mark.parametrize("algo", [ar.AR_ALGO_ONESHOT, ar.AR_ALGO_TWOSHOT])
+@pytest.mark.parametrize("algo", [ar.AR_ALGO_ONESHOT, ar.AR_ALGO_TWOSHOT, ar.AR_ALGO_TAGGED])
 @pytest.mark.parametrize("R", [1, 2, 3, 4, 8])
 @pytest.mark.parametrize("vec", [16, 8, 2, 1])
 def test_plan_invariants(lib, R, vec, algo):
-    if algo == ar.AR_ALGO_TWOSHOT and vec != 16:
+    if algo != ar.AR_ALGO_ONESHOT and vec != 16:
         with pytest.raises(tda.ArError):
             tda.ar_plan_compute(R, 4096, vec, algo, 256, 152, 6)
         return
@@ -72,6 +72,9 @@ def test_plan_invariants(lib, R, vec, algo):
             assert p.unroll == -(-R * p.subtile_vecs // threads)
         else:
             assert p.unroll in (1, 2) and p.flag_rounds == 1
+        if algo == ar.AR_ALGO_TAGGED:
+            # one 16-byte payload vector per thread per stage (two tagged vectors)
+            assert p.unroll == 1 and p.tile_bytes == threads * vec and p.subtile_vecs == 0
         if algo == ar.AR_ALGO_ONESHOT:
             assert p.tile_bytes == threads * p.unroll * vec and p.subtile_vecs == 0
         # tiles cover the payload, and no tile is empty
