@@ -96,8 +96,9 @@ enum ar_code {
  *   exchange buffer holds 4 payload bytes and a 4-byte tag naming the stage,
  *   and a reader polls its peers' words until the tags match.  One trip over
  *   the slot memory instead of three, at twice the bytes: for latency-bound
- *   calls up to ar_info.tagged_capacity_bytes per rank (larger calls take the
- *   one-shot form).  Not part of the pages' design.
+ *   calls of one tile (4 KiB) per block, up to ar_info.tagged_capacity_bytes
+ *   per rank (larger calls take the one-shot form).  Not part of the pages'
+ *   design.
  * AR_ALGO_AUTO: chosen per call from the handle's tactics (ar_tactics). */
 enum ar_algo { AR_ALGO_AUTO = -1, AR_ALGO_ONESHOT = 0, AR_ALGO_TWOSHOT = 1, AR_ALGO_TAGGED = 2 };
 
@@ -142,7 +143,8 @@ typedef struct ar_info {
     uint64_t slot_bytes;    /* bytes of one (parity, rank) slot, a multiple of 256 */
     uint64_t total_slot_bytes; /* 2 * R * slot_bytes: the allocation that cannot grow */
     uint64_t timeout_ns;
-    uint64_t tagged_capacity_bytes;  /* largest per-rank call the tagged form takes */
+    uint64_t tagged_capacity_bytes;  /* largest per-rank call the tagged form takes (one 4 KiB tile per
+                                        block of one rank's launch, within the slot; 0: complex64) */
     int32_t blocks_per_sm_tagged;    /* occupancy of the tagged-form kernels */
     int32_t reserved;
 } ar_info;

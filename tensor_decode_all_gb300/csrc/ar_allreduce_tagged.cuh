@@ -12,16 +12,18 @@
 // payload beside it is this stage's.  One trip, at twice the bytes: worth it
 // where the call is bound by latency rather than bandwidth.
 //
-// Per stage, thread t of block b of rank r (payload vector v = tile * 256 + t):
+// Per stage s, thread t of block b of rank r (payload vector v = tile * 256 +
+// t, buffer position w = (s * bmax + b) * 256 + t):
 //   1. loads vector v of in_r (8 elements, 16 bytes) and stores it as two
-//      tagged 16-byte vectors into ll[parity][r] at 2v, 2v + 1;
-//   2. loads the peers' two tagged vectors at 2v, 2v + 1 until their four tags
+//      tagged 16-byte vectors into ll[parity][r] at 2w, 2w + 1;
+//   2. loads the peers' two tagged vectors at 2w, 2w + 1 until their four tags
 //      equal the stage's tag (bounded by the timeout, abandoned on abort);
 //   3. adds the R contributions in fp32 in rank order, rounds once, stores
 //      out_r -- the same arithmetic, so the same bits, as the other forms.
-// Threads do not wait for each other: no barrier inside a stage.  Tags never
-// repeat within 2^32 stages of a block, and parity double-buffering keeps a
-// rank one call ahead from overwriting words a peer still reads.
+// Threads do not wait for each other: no barrier inside a stage.  A buffer
+// position belongs to one block index, whose tags never repeat within 2^32
+// stages, and parity double-buffering keeps a rank one call ahead from
+// overwriting words a peer still reads.
 #pragma once
 
 #include "ar_internal.h"
@@ -69,12 +71,20 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
     for (uint64_t s = 0; s < nstages; ++s) {
         const uint64_t v = ((uint64_t)b + s * B) * kThreads + tid;
         const unsigned long long tag = (unsigned long long)(uint32_t)(seq + s + 1) << 32;
-        const bool live = v < nv && !bail;
+        // The buffer is indexed by (stage, block, thread), not by payload
+        // vector: a word is only ever written by block b of its rank, whose
+        // tags only grow, so a stale word can never carry the tag a reader
+        // expects (indexed by vector, a word could be left by another block
+        // index of an earlier call with another grid size, whose own count
+        // may have passed through the same value).  The host takes this form
+        // only for calls that fit (one stage per block).
+        const uint64_t w = ((uint64_t)s * d.bmax + b) * kThreads + tid;
+        const bool live = v < nv && !bail && 2 * w + 1 < d.ll_vecs;
 
         // 1. publish this vector as two tagged vectors
         if (live) {
-            st_tagged(mine + 2 * v, make_ulonglong2(tag | own.x, tag | own.y), sys);
-            st_tagged(mine + 2 * v + 1, make_ulonglong2(tag | own.z, tag | own.w), sys);
+            st_tagged(mine + 2 * w, make_ulonglong2(tag | own.x, tag | own.y), sys);
+            st_tagged(mine + 2 * w + 1, make_ulonglong2(tag | own.z, tag | own.w), sys);
         }
         if (tid == 0) trace_published<T>(d, s_tr);
         // the next stage's input, overlapping the wait
@@ -91,7 +101,7 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
 #pragma unroll
                 for (int p = 0; p < R; ++p) {
                     if (pending & (1u << p)) {
-                        const ulonglong2 *src = base + (uint64_t)p * d.ll_vecs + 2 * v;
+                        const ulonglong2 *src = base + (uint64_t)p * d.ll_vecs + 2 * w;
                         const ulonglong2 lo = ld_tagged(src, sys);
                         const ulonglong2 hi = ld_tagged(src + 1, sys);
                         if (((lo.x & lo.y & hi.x & hi.y) >> 32) == (tag >> 32) &&

@@ -36,7 +36,6 @@ struct ar_handle {
     uint64_t twoshot_min_bytes = ~0ull;        // tactic: AUTO picks two-shot from this size per rank
     int max_blocks = 0;                        // tactic: cap on blocks per rank; 0 = occupancy
     uint64_t tagged_max_bytes = 0;             // tactic: AUTO picks the tagged form up to this size
-    uint64_t tagged_cap = 0;                   // largest call the tagged buffers hold (bytes per rank)
     void *ll_host = nullptr;                   // pinned kind: host address of the tagged buffers
     ulonglong2 *ll_dev = nullptr;              // [2][R][ll_vecs]
     uint64_t ll_vecs = 0, ll_bytes = 0;
@@ -64,9 +63,6 @@ namespace {
 
 thread_local int g_last_error = AR_OK;
 
-// Largest per-rank payload of the tagged-word form (its buffers hold twice as
-// many bytes, per rank and parity).
-constexpr uint64_t kTaggedMaxBytes = 512ull << 10;
 
 uint64_t itemsize_of(int dtype) {
     switch (dtype) {
@@ -256,10 +252,25 @@ int choose_algo(int R, uint64_t bytes, int slot_kind) {
 }
 
 // The form a handle's call of `bytes` per rank takes: forced, or its tactic.
-int handle_algo(const ar_handle *h, uint64_t bytes) {
-    if (h->algo == AR_ALGO_TAGGED) return bytes <= h->tagged_cap ? AR_ALGO_TAGGED : AR_ALGO_ONESHOT;
+int handle_bps(const ar_handle *h, int algo, bool fused);
+
+// The tagged form runs only calls of one stage: every block one 256-vector
+// tile, so that each buffer position belongs to a single block index.
+bool tagged_fits(const ar_handle *h, uint64_t bytes, bool fused) {
+    if (!h->ll_dev) return false;
+    const uint64_t tiles = ((bytes + 15) / 16 + tda::kThreads - 1) / tda::kThreads;
+    uint64_t blocks = (uint64_t)h->sm_count * (uint64_t)handle_bps(h, AR_ALGO_TAGGED, fused) / (uint64_t)h->R;
+    if (blocks > (uint64_t)h->bmax) blocks = (uint64_t)h->bmax;
+    if (h->max_blocks > 0 && blocks > (uint64_t)h->max_blocks) blocks = (uint64_t)h->max_blocks;
+    return tiles <= blocks;
+}
+
+// The form a call of `bytes` per rank takes: forced, or by the handle's
+// tactics; the tagged form only where it fits (else one-shot).
+int handle_algo(const ar_handle *h, uint64_t bytes, bool fused) {
+    if (h->algo == AR_ALGO_TAGGED) return tagged_fits(h, bytes, fused) ? AR_ALGO_TAGGED : AR_ALGO_ONESHOT;
     if (h->algo != AR_ALGO_AUTO) return h->algo;
-    if (h->tagged_max_bytes && bytes <= h->tagged_max_bytes && bytes <= h->tagged_cap) return AR_ALGO_TAGGED;
+    if (h->tagged_max_bytes && bytes <= h->tagged_max_bytes && tagged_fits(h, bytes, fused)) return AR_ALGO_TAGGED;
     return bytes >= h->twoshot_min_bytes ? AR_ALGO_TWOSHOT : AR_ALGO_ONESHOT;
 }
 
@@ -412,8 +423,8 @@ int begin_fused(ar_handle *h, const void *const *ins, void *const *outs, size_t 
 // handle, then one launch for `rank` (or, rank < 0, all ranks at once).
 int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int rank, cudaStream_t s) {
     const uint64_t bytes = numel * h->itemsize;
-    const int algo = handle_algo(h, bytes);
     const bool fused = rank < 0;
+    const int algo = handle_algo(h, bytes, fused);
     const int bps = handle_bps(h, algo, fused);
     ar_plan plan;
     int rc = plan_compute_sub(h->R, bytes, 16, algo, handle_twoshot_sub(h, bytes), tda::kThreads, h->sm_count, bps,
@@ -551,11 +562,10 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
         if (cudaMalloc((void **)&h->flags_dev, h->flags_bytes) != cudaSuccess) return fail(AR_ENOMEM);
         if (cudaMemset(h->slots_dev, 0, slots_total) != cudaSuccess) return fail(AR_ECUDA);
     }
-    // Tagged-word buffers (fp16/bf16 handles): room for calls of up to
-    // kTaggedMaxBytes per rank, at 32 bytes per 16 payload bytes.
+    // Tagged-word buffers (fp16/bf16 handles): one 256-vector tile per block,
+    // at 32 bytes per 16 payload bytes, per rank and parity.
     if (dtype == AR_F16 || dtype == AR_BF16) {
-        h->tagged_cap = h->slot_bytes < kTaggedMaxBytes ? h->slot_bytes : kTaggedMaxBytes;
-        h->ll_vecs = h->tagged_cap / 16 * 2;
+        h->ll_vecs = (uint64_t)h->bmax * tda::kThreads * 2;
         h->ll_bytes = 2ull * (uint64_t)R * h->ll_vecs * 16ull;
         if (slot_kind == AR_SLOT_PINNED_HOST) {
             if (cudaHostAlloc(&h->ll_host, h->ll_bytes, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess)
@@ -686,7 +696,11 @@ AR_API int ar_query(const ar_handle *h, ar_info *info) {
     info->slot_bytes = h->slot_bytes;
     info->total_slot_bytes = 2ull * (uint64_t)h->R * h->slot_bytes;
     info->timeout_ns = h->timeout_ns.load();
-    info->tagged_capacity_bytes = h->tagged_cap;
+    uint64_t tag_blocks = (uint64_t)h->sm_count * (uint64_t)handle_bps(h, AR_ALGO_TAGGED, false) / (uint64_t)h->R;
+    if (tag_blocks > (uint64_t)h->bmax) tag_blocks = (uint64_t)h->bmax;
+    if (h->max_blocks > 0 && tag_blocks > (uint64_t)h->max_blocks) tag_blocks = (uint64_t)h->max_blocks;
+    const uint64_t tag_bytes = tag_blocks * tda::kThreads * 16ull;
+    info->tagged_capacity_bytes = !h->ll_dev ? 0 : (tag_bytes < h->slot_bytes ? tag_bytes : h->slot_bytes);
     info->blocks_per_sm_tagged = h->bps[0][0][kTagged];
     info->reserved = 0;
     return AR_OK;
@@ -766,7 +780,7 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) 
     const int vec = op == 0 ? 16 : allgather_vec(bytes, nullptr, nullptr);
     int algo = AR_ALGO_ONESHOT, bps = h->bps[0][h->trace ? 1 : 0][kAllgather];
     if (op == 0) {
-        algo = handle_algo(h, bytes);
+        algo = handle_algo(h, bytes, false);
         bps = handle_bps(h, algo, false);
     }
     int rc = plan_compute_sub(h->R, bytes, vec, algo, op == 0 ? handle_twoshot_sub(h, bytes) : 0, tda::kThreads,

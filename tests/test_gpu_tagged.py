@@ -47,7 +47,7 @@ def _check(outs, xs, dtype, what):
     (2, "f16", 131072),        # 256 KiB
     (8, "bf16", 393216 // 4),  # 192 KiB per rank
     (8, "bf16", 8191),
-    (4, "bf16", 262144),       # 512 KiB per rank: the form's capacity
+    (4, "bf16", 262144),       # 512 KiB per rank: 128 blocks of one tile
     (3, "f16", 1000),
     (1, "bf16", 77),
     (2, "f16", 1),
@@ -69,8 +69,10 @@ def test_tagged_matches_oracle(R, dtype, n, slots):
 
 def test_tagged_beyond_capacity_takes_the_oneshot_form():
     h = _handle(2, "f16", 1 << 20, "hbm")
-    cap = h.info().tagged_capacity_bytes
-    assert cap == 512 << 10
+    info = h.info()
+    cap = info.tagged_capacity_bytes
+    # one 4 KiB tile per block of one rank's launch
+    assert cap % 4096 == 0 and cap // 4096 <= info.max_blocks and cap >= 512 << 10
     assert h.plan("allreduce", cap // 2).algo == 2
     assert h.plan("allreduce", cap // 2 + 8).algo == 0
     xs = inputs.allreduce_inputs(5, 2, cap // 2 + 8, "f16", "uniform", 4)
@@ -190,4 +192,38 @@ def test_tagged_missing_peer_times_out_and_reset_restores(slots):
     torch.cuda.synchronize()
     h.check()
     _check(outs, xs, "f16", "after reset")
+    h.destroy()
+
+
+def test_tagged_with_changing_grids_stays_exact():
+    """Calls whose grid changes between calls (a block cap, one launch of all
+    ranks) on one handle.  The tagged form runs one tile per block and keeps
+    each buffer position to one block index, so a word left by another block
+    of an earlier call can never pass for this call's; a call that would need
+    a second stage per block takes the one-shot form instead."""
+    R, dtype = 2, "f16"
+    h = _handle(R, dtype, 8192, "hbm")
+    streams = rank_streams(R)
+    fs = torch.cuda.Stream()
+    # (elements, block cap, fused): 1 tile / 1 block, 4 tiles / 3 blocks,
+    # 4 tiles / 2 blocks -- the grid sequence that lets a stale word carry an
+    # expected tag when the buffer is indexed by payload vector -- then more.
+    seq = [(2048, 1, False), (8192, 3, False), (8192, 2, False), (8192, 0, True), (2048, 1, True),
+           (8192, 0, False), (6144, 2, False), (8192, 4, True), (8192, 0, False)] * 3
+    for call, (n, cap, fused) in enumerate(seq):
+        h.set_tactics(max_blocks=cap)
+        tiles = -(-n // 2048)
+        assert h.plan("allreduce", n).algo == (2 if (cap == 0 or tiles <= cap) else 0)
+        xs = inputs.allreduce_inputs(5, R, n, dtype, "uniform", 300 + call)
+        ins = [to_dev(x, dtype) for x in xs]
+        outs = [torch.empty_like(t) for t in ins]
+        if fused:
+            fs.wait_stream(torch.cuda.current_stream())
+            h.allreduce_fused(ins, outs, fs)
+            torch.cuda.current_stream().wait_stream(fs)
+        else:
+            enqueue(h, "allreduce", ins, outs, streams)
+        torch.cuda.synchronize()
+        h.check()
+        _check(outs, xs, dtype, f"call {call} n={n} cap={cap} fused={fused}")
     h.destroy()
