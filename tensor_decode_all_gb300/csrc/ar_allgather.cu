@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
         d.ctr[(size_t)rank * d.bmax + b] = c;
         trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
     }
+    advance_idle_blocks(d, rank);
 }
 
 template <int VW, int U, bool F, bool T>

@@ -239,6 +239,7 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
         d.ctr[(size_t)rank * d.bmax + b] = c;
         trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
     }
+    advance_idle_blocks(d, rank);
 }
 
 // One rank's launch.
@@ -401,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
         d.ctr[(size_t)rank * d.bmax + b] = c;
         trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
     }
+    advance_idle_blocks(d, rank);
 }
 
 }  // namespace tda

@@ -166,6 +166,7 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
         d.ctr[(size_t)rank * d.bmax + b] = c;
         trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
     }
+    advance_idle_blocks(d, rank);
 }
 
 // Both entries are held to 64 registers (4 blocks per SM), so that a call

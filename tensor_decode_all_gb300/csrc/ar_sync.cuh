@@ -152,6 +152,21 @@ __device__ __forceinline__ void trace_finish(const DevState &d, const TraceMarks
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Block 0 of a rank, at the end of a call: advance the call count of this
+// rank's blocks that the call did not launch (B <= b < bmax).  Every block of
+// a rank then counts the same calls, so the slot parity -- a block's call
+// count & 1 -- is the same for all blocks of a call.  Without it, a call on a
+// smaller grid leaves the counts of the unused blocks behind, and a later call
+// whose tiles map a slot region to another block index could write that
+// region in the same parity half a peer is still reading from the call before.
+// The next call's blocks read their counters only after this grid has
+// completed (griddepcontrol.wait), and no block of this call touches them.
+__device__ __forceinline__ void advance_idle_blocks(const DevState &d, int rank) {
+    if (blockIdx.x != 0) return;
+    for (int b = (int)gridDim.x + (int)threadIdx.x; b < d.bmax; b += (int)blockDim.x)
+        d.ctr[(size_t)rank * d.bmax + b].calls += 1ull;
+}
+
 // The rank a block plays, and its input and output.  A kernel built for one
 // rank's launch (F = false) takes the rank argument and its own in/out
 // arguments, unchanged.  A kernel built for a launch of all ranks at once
