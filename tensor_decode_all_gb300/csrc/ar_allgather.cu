@@ -89,6 +89,7 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
     __syncthreads();
     const unsigned long long seq = s_seq;
     const int parity = (int)(s_calls & 1ull);
+    advance_idle_blocks(d, rank, s_calls + 1ull);
     const uint64_t slot_vecs = d.slot_bytes / VW;
     V *const slot_base = reinterpret_cast<V *>(d.slots) + (uint64_t)parity * R * slot_vecs;
     V *const my_slot = slot_base + (uint64_t)rank * slot_vecs;
@@ -152,7 +153,6 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
         d.ctr[(size_t)rank * d.bmax + b] = c;
         trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
     }
-    advance_idle_blocks(d, rank);
 }
 
 template <int VW, int U, bool F, bool T>

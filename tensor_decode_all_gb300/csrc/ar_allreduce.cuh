@@ -168,6 +168,7 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
     __syncthreads();
     const unsigned long long seq = s_seq;
     const int parity = (int)(s_calls & 1ull);
+    advance_idle_blocks(d, rank, s_calls + 1ull);
     const uint64_t slot_vecs = d.slot_bytes / 16;
     uint4 *const slot_base = reinterpret_cast<uint4 *>(d.slots) + (uint64_t)parity * R * slot_vecs;
     uint4 *const my_slot = slot_base + (uint64_t)rank * slot_vecs;
@@ -239,7 +240,6 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
         d.ctr[(size_t)rank * d.bmax + b] = c;
         trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
     }
-    advance_idle_blocks(d, rank);
 }
 
 // One rank's launch.
@@ -318,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
     __syncthreads();
     const unsigned long long seq = s_seq;
     const int parity = (int)(s_calls & 1ull);
+    advance_idle_blocks(d, rank, s_calls + 1ull);
     const uint64_t slot_vecs = d.slot_bytes / 16;
     uint4 *const slot_base = reinterpret_cast<uint4 *>(d.slots) + (uint64_t)parity * R * slot_vecs;
     uint4 *const my_slot = slot_base + (uint64_t)rank * slot_vecs;
@@ -402,7 +403,6 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
         d.ctr[(size_t)rank * d.bmax + b] = c;
         trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
     }
-    advance_idle_blocks(d, rank);
 }
 
 }  // namespace tda

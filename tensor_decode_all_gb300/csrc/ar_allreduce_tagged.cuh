@@ -63,6 +63,7 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
     __syncthreads();
     const unsigned long long seq = s_seq;
     const int parity = (int)(s_calls & 1ull);
+    advance_idle_blocks(d, rank, s_calls + 1ull);
     ulonglong2 *const base = d.ll + (uint64_t)parity * R * d.ll_vecs;
     ulonglong2 *const mine = base + (uint64_t)rank * d.ll_vecs;
     const int sys = d.sys_scope;
@@ -166,7 +167,6 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
         d.ctr[(size_t)rank * d.bmax + b] = c;
         trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
     }
-    advance_idle_blocks(d, rank);
 }
 
 // Both entries are held to 64 registers (4 blocks per SM), so that a call

@@ -152,19 +152,21 @@ __device__ __forceinline__ void trace_finish(const DevState &d, const TraceMarks
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// Block 0 of a rank, at the end of a call: advance the call count of this
-// rank's blocks that the call did not launch (B <= b < bmax).  Every block of
-// a rank then counts the same calls, so the slot parity -- a block's call
-// count & 1 -- is the same for all blocks of a call.  Without it, a call on a
-// smaller grid leaves the counts of the unused blocks behind, and a later call
-// whose tiles map a slot region to another block index could write that
-// region in the same parity half a peer is still reading from the call before.
-// The next call's blocks read their counters only after this grid has
-// completed (griddepcontrol.wait), and no block of this call touches them.
-__device__ __forceinline__ void advance_idle_blocks(const DevState &d, int rank) {
+// Block 0 of a rank, once it knows its call count: set the call count of this
+// rank's blocks that the call does not launch (gridDim.x <= b < bmax) to the
+// count every launched block will have after the call.  Every block of a rank
+// then counts the same calls, so the slot parity -- a block's call count & 1 --
+// is the same for all blocks of a call.  Without it, a call on a smaller grid
+// leaves the counts of the unused blocks behind, and a later call whose tiles
+// map a slot region to another block index could write that region in the
+// same parity half a peer is still reading from the call before.  No block of
+// this call touches those counters, and the next call's blocks read them only
+// after this grid has completed (griddepcontrol.wait).  Stores only, issued
+// early, so they overlap the call's work.
+__device__ __forceinline__ void advance_idle_blocks(const DevState &d, int rank, unsigned long long calls_after) {
     if (blockIdx.x != 0) return;
     for (int b = (int)gridDim.x + (int)threadIdx.x; b < d.bmax; b += (int)blockDim.x)
-        d.ctr[(size_t)rank * d.bmax + b].calls += 1ull;
+        d.ctr[(size_t)rank * d.bmax + b].calls = calls_after;
 }
 
 // The rank a block plays, and its input and output.  A kernel built for one
