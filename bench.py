@@ -171,7 +171,8 @@ class ClockSampler:
 # ------------------------------------------------------------- measurement
 
 KERNEL_SOURCES = ("ar_allreduce.cuh", "ar_allreduce_tagged.cuh", "ar_sync.cuh", "ar_internal.h",
-                  "ar_allreduce_f16.cu", "ar_allreduce_bf16.cu", "ar_allgather.cu")
+                  "ar_allreduce_f16.cu", "ar_allreduce_bf16.cu", "ar_allreduce_f16_twoshot.cu",
+                  "ar_allreduce_bf16_twoshot.cu", "ar_allgather.cu")
 
 
 def kernel_source_sha256() -> str:

@@ -486,14 +486,25 @@ const void *allreduce_twoshot_ptr(int R, int sub) {
 template <class Ops, bool F, bool T>
 const void *allreduce_ptr_ft(int R, int U) {
     if (U == kTaggedVariant) return allreduce_tagged_ptr<Ops, F, T>(R);
-    if (U < 0) return allreduce_twoshot_ptr<Ops, F, T>(R, twoshot_sub(U));
+    if (U < 0) return nullptr;  // two-shot: allreduce_twoshot_ptr_any, in its own translation unit
     return U == 1 ? allreduce_ptr_ru<Ops, 1, F, T>(R) : allreduce_ptr_ru<Ops, 2, F, T>(R);
 }
 
+// One-shot and tagged-word kernels (U >= 0).
 template <class Ops>
 const void *allreduce_ptr(int R, int U, bool fused, bool traced) {
     if (traced) return fused ? allreduce_ptr_ft<Ops, true, true>(R, U) : allreduce_ptr_ft<Ops, false, true>(R, U);
     return fused ? allreduce_ptr_ft<Ops, true, false>(R, U) : allreduce_ptr_ft<Ops, false, false>(R, U);
+}
+
+// Two-shot kernels (U < 0).  Instantiated by their own translation units, so
+// that a dtype's kernels compile in parallel.
+template <class Ops>
+const void *allreduce_twoshot_ptr_any(int R, int U, bool fused, bool traced) {
+    const int sub = twoshot_sub(U);
+    if (traced)
+        return fused ? allreduce_twoshot_ptr<Ops, true, true>(R, sub) : allreduce_twoshot_ptr<Ops, false, true>(R, sub);
+    return fused ? allreduce_twoshot_ptr<Ops, true, false>(R, sub) : allreduce_twoshot_ptr<Ops, false, false>(R, sub);
 }
 
 }  // namespace tda

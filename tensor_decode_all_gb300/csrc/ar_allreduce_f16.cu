@@ -1,4 +1,4 @@
-// Instantiates the exchange-and-add kernels for IEEE binary16.
+// Instantiates the one-shot and tagged-word exchange-and-add kernels for IEEE binary16.
 #include "ar_allreduce.cuh"
 
 namespace tda {

@@ -797,6 +797,11 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) 
 namespace tda {
 
 const void *allreduce_kernel_ptr(int dtype, int R, int unroll, bool fused, bool traced) {
+    if (unroll < 0) {
+        if (dtype == AR_F16) return allreduce_twoshot_kernel_ptr_f16(R, unroll, fused, traced);
+        if (dtype == AR_BF16) return allreduce_twoshot_kernel_ptr_bf16(R, unroll, fused, traced);
+        return nullptr;
+    }
     if (dtype == AR_F16) return allreduce_kernel_ptr_f16(R, unroll, fused, traced);
     if (dtype == AR_BF16) return allreduce_kernel_ptr_bf16(R, unroll, fused, traced);
     return nullptr;

@@ -87,6 +87,8 @@ cudaError_t launch_allgather(int vec_bytes, int R, int unroll, int blocks, cudaS
 const void *allreduce_kernel_ptr(int dtype, int R, int unroll, bool fused, bool traced);
 const void *allreduce_kernel_ptr_f16(int R, int unroll, bool fused, bool traced);   // ar_allreduce_f16.cu
 const void *allreduce_kernel_ptr_bf16(int R, int unroll, bool fused, bool traced);  // ar_allreduce_bf16.cu
+const void *allreduce_twoshot_kernel_ptr_f16(int R, int unroll, bool fused, bool traced);   // ..._f16_twoshot.cu
+const void *allreduce_twoshot_kernel_ptr_bf16(int R, int unroll, bool fused, bool traced);  // ..._bf16_twoshot.cu
 const void *allgather_kernel_ptr(int vec_bytes, int R, int unroll, bool fused, bool traced);
 
 }  // namespace tda
