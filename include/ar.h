@@ -314,6 +314,17 @@ AR_API int ar_set_timeout(ar_handle *h, uint64_t timeout_ns);
  */
 AR_API int ar_set_trace(ar_handle *h, void *records, uint64_t capacity);
 
+/*
+ * ar_debug_seed_stages -- test hook: synchronise the device, then set the
+ * stage count of every (rank, block) of the handle to `stages` (call counts
+ * unchanged), as if that many stages had run.  Lets a test cross the point
+ * where the tagged-word form's 32-bit tags wrap (near 2^32 - 1 stages)
+ * without running billions of calls.  Use on an idle handle only: every rank
+ * must have completed the same calls.  Errors: AR_EINVAL (NULL handle),
+ * AR_ECUDA.
+ */
+AR_API int ar_debug_seed_stages(ar_handle *h, uint64_t stages);
+
 /* Static facts about the handle. */
 AR_API int ar_query(const ar_handle *h, ar_info *info);
 

@@ -106,6 +106,7 @@ def lib():
             L.ar_set_tactics.argtypes = [vp, ctypes.POINTER(Tactics)]
             L.ar_supports.argtypes = [vp, i32, sz, vp, vp]
             L.ar_set_trace.argtypes = [vp, vp, u64]
+            L.ar_debug_seed_stages.argtypes = [vp, u64]
             L.ar_allreduce_noalloc.argtypes = [i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, vp]
             L.ar_allreduce_noalloc.restype = i32
             for name in ("ar_allreduce_fused", "ar_allgather_fused"):
@@ -390,6 +391,12 @@ class Handle:
         rc = lib().ar_set_trace(self.ptr, buf.data_ptr() if buf is not None else None, int(capacity))
         if rc:
             raise ArError(rc, "ar_set_trace")
+
+    def debug_seed_stages(self, stages: int) -> None:
+        """Test hook: set every block's stage count (see ar_debug_seed_stages)."""
+        rc = lib().ar_debug_seed_stages(self.ptr, int(stages))
+        if rc:
+            raise ArError(rc, "ar_debug_seed_stages")
 
     def supports(self, op: str, inp, out) -> int:
         """AR_OK if ar_allreduce / ar_allgather would accept these tensors, else its code."""

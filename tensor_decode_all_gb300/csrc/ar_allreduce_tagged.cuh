@@ -5,8 +5,8 @@
 // block's slot stores are acknowledged, then for the peer's poll of the flag,
 // then for the peer's read of the data: three trips across the slot memory's
 // link.  Here every 8-byte word of the exchange buffer carries 4 bytes of
-// payload in its low half and a 4-byte tag in its high half, the low 32 bits
-// of the block's stage count (the value the flag would have been raised to).
+// payload in its low half and a 4-byte tag in its high half, derived from the
+// block's stage count (the value the flag would have been raised to).
 // A writer stores its tagged words with plain relaxed stores and no fence; a
 // reader loads its peers' words until every tag matches, which proves the
 // payload beside it is this stage's.  One trip, at twice the bytes: worth it
@@ -21,9 +21,10 @@
 //   3. adds the R contributions in fp32 in rank order, rounds once, stores
 //      out_r -- the same arithmetic, so the same bits, as the other forms.
 // Threads do not wait for each other: no barrier inside a stage.  A buffer
-// position belongs to one block index, whose tags never repeat within 2^32
-// stages, and parity double-buffering keeps a rank one call ahead from
-// overwriting words a peer still reads.
+// position belongs to one block index, whose tags never repeat within 2^32 - 1
+// stages and are never 0 (the buffer's initial contents), and parity
+// double-buffering keeps a rank one call ahead from overwriting words a peer
+// still reads.
 #pragma once
 
 #include "ar_internal.h"
@@ -71,7 +72,7 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
 
     for (uint64_t s = 0; s < nstages; ++s) {
         const uint64_t v = ((uint64_t)b + s * B) * kThreads + tid;
-        const unsigned long long tag = (unsigned long long)(uint32_t)(seq + s + 1) << 32;
+        const unsigned long long tag = stage_tag(seq + s + 1);
         // The buffer is indexed by (stage, block, thread), not by payload
         // vector: a word is only ever written by block b of its rank, whose
         // tags only grow, so a stale word can never carry the tag a reader

@@ -743,6 +743,24 @@ AR_API int ar_set_trace(ar_handle *h, void *records, uint64_t capacity) {
     return AR_OK;
 }
 
+AR_API int ar_debug_seed_stages(ar_handle *h, uint64_t stages) {
+    if (!h) return AR_EINVAL;
+    if (check_device(h) != AR_OK) return AR_EINVAL;
+    if (cudaDeviceSynchronize() != cudaSuccess) return AR_ECUDA;
+    const size_t n = (size_t)h->R * (size_t)h->bmax;
+    Ctr *host = new (std::nothrow) Ctr[n];
+    if (!host) return AR_ENOMEM;
+    int rc = AR_OK;
+    if (cudaMemcpy(host, h->ctr, n * sizeof(Ctr), cudaMemcpyDeviceToHost) != cudaSuccess) rc = AR_ECUDA;
+    if (rc == AR_OK) {
+        for (size_t i = 0; i < n; ++i) host[i].seq = stages;
+        if (cudaMemcpy(h->ctr, host, n * sizeof(Ctr), cudaMemcpyHostToDevice) != cudaSuccess) rc = AR_ECUDA;
+    }
+    delete[] host;
+    if (rc != AR_OK) (void)cudaGetLastError();
+    return rc;
+}
+
 AR_API int ar_get_tactics(const ar_handle *h, ar_tactics *t) {
     if (!h || !t) return AR_EINVAL;
     t->twoshot_min_bytes = h->twoshot_min_bytes;

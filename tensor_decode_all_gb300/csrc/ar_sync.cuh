@@ -140,6 +140,15 @@ __device__ __forceinline__ void trace_finish(const DevState &d, const TraceMarks
     }
 }
 
+// The tag of a block's stage count x in the high half of a tagged word: a
+// value in 1 .. 2^32 - 1, never 0, so a word still holding the buffer's initial
+// zeros never passes for data however long the counts run (x mod (2^32 - 1),
+// plus one: consecutive counts give consecutive tags, wrapping from 2^32 - 1
+// to 1).
+__device__ __forceinline__ unsigned long long stage_tag(unsigned long long x) {
+    return (unsigned long long)((uint32_t)(x % 0xffffffffull) + 1u) << 32;
+}
+
 // Programmatic dependent launch.  When a rank's next call is launched with the
 // programmatic-serialization attribute, its blocks may become resident before
 // this call ends.  Each kernel therefore waits (griddepcontrol.wait: the

@@ -227,3 +227,26 @@ def test_tagged_with_changing_grids_stays_exact():
         h.check()
         _check(outs, xs, dtype, f"call {call} n={n} cap={cap} fused={fused}")
     h.destroy()
+
+
+@pytest.mark.parametrize("slots", ["hbm", "pinned"])
+@pytest.mark.parametrize("algo", ["tagged", "oneshot", "twoshot"])
+def test_stage_counts_across_the_32_bit_wrap(slots, algo):
+    """Stage counts seeded just below 2^32 - 1 (the tag period) and 2^32 (where
+    the low 32 bits of a count are 0): the tagged words' tags wrap from
+    2^32 - 1 to 1 and never take the value 0 of the zeroed buffer, and the flag
+    forms' 64-bit counts run on; every call stays exact."""
+    R, n, dtype = 2, 8192, "f16"
+    for seed in ((1 << 32) - 4, (1 << 32) - 1, (1 << 32) + 3):
+        h = _handle(R, dtype, n, slots, algo=algo)
+        h.debug_seed_stages(seed)
+        streams = rank_streams(R)
+        for call in range(8):
+            xs = inputs.allreduce_inputs(5, R, n, dtype, "uniform", 400 + call)
+            ins = [to_dev(x, dtype) for x in xs]
+            outs = [torch.empty_like(t) for t in ins]
+            enqueue(h, "allreduce", ins, outs, streams)
+            torch.cuda.synchronize()
+            h.check()
+            _check(outs, xs, dtype, f"{algo} {slots} seed {seed:#x} call {call}")
+        h.destroy()
