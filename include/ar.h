@@ -369,9 +369,13 @@ AR_API int ar_choose_algo(int R, uint64_t bytes, int slot_kind);
  * enqueued (or captured) afterwards. */
 AR_API int ar_set_pdl(ar_handle *h, int enable);
 
-/* Force the all-reduce form of a handle (AR_ALGO_AUTO restores the rule).  The
- * environment variable AR_ALGO=oneshot|twoshot sets it at ar_create.  Every
- * rank of a call must see the same setting; set it before enqueuing. */
+/* Force the all-reduce form of a handle (AR_ALGO_AUTO restores the rule):
+ * AR_ALGO_ONESHOT, AR_ALGO_TWOSHOT or AR_ALGO_TAGGED (the last only for calls
+ * of one tile per block; larger calls take the one-shot form).  The
+ * environment variable AR_ALGO=oneshot|twoshot|tagged sets it at ar_create.
+ * Every rank of a call must see the same setting; set it before enqueuing.
+ * AR_EINVAL for an unknown form or a two-shot / tagged form on a complex64
+ * handle. */
 AR_API int ar_set_algo(ar_handle *h, int algo);
 
 /* Read or replace a handle's tactics (see ar_tactics).  Every rank shares the
