@@ -2,7 +2,7 @@
 
 Each translation unit is compiled by nvcc in parallel, then linked into one
 shared library next to this file (git-ignored).  The CUDA runtime is linked
-statically, so the library needs only the driver at run time.
+statically, so the library needs only the CUDA driver at run time.
 """
 from __future__ import annotations
 
