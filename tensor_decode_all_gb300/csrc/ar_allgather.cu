@@ -131,13 +131,22 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
         for (int u = 0; u < U; ++u) {
             const uint64_t v = v0 + (uint64_t)u * kThreads;
             if (v < nv) {
-                V vals[R];
+                // peers in groups of 4: 4 loads in flight, a bounded register set
+                constexpr int kChunk = 4;
 #pragma unroll
-                for (int p = 0; p < R; ++p)
-                    if (p != rank) vals[p] = Vec<VW>::ldcg(slot_base + (uint64_t)p * slot_vecs + v);
+                for (int p0 = 0; p0 < R; p0 += kChunk) {
+                    V vals[kChunk];
 #pragma unroll
-                for (int p = 0; p < R; ++p)
-                    if (p != rank) dst[(uint64_t)p * nv + v] = vals[p];
+                    for (int q = 0; q < kChunk; ++q) {
+                        const int p = p0 + q;
+                        if (p < R && p != rank) vals[q] = Vec<VW>::ldcg(slot_base + (uint64_t)p * slot_vecs + v);
+                    }
+#pragma unroll
+                    for (int q = 0; q < kChunk; ++q) {
+                        const int p = p0 + q;
+                        if (p < R && p != rank) dst[(uint64_t)p * nv + v] = vals[q];
+                    }
+                }
             }
         }
         if (s + 1 < nstages) {
