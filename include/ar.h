@@ -81,8 +81,8 @@ enum ar_code {
     AR_ENOMEM = 4,    /* slot, flag or counter allocation failed in ar_create */
     AR_ECUDA = 5,     /* a CUDA runtime call failed (launch error, no device, ...) */
     AR_ETIMEOUT = 6,  /* recorded on the device: a block waited longer than the timeout for
-                         a peer's flag.  Outputs of that call and of every later call are
-                         undefined until ar_reset(). */
+                         a peer's flag (or tagged words).  Outputs of that call and of every
+                         later call are undefined until ar_reset(). */
     AR_ESTATE = 7     /* the handle needs ar_reset() (a device error is recorded) */
 };
 
@@ -107,9 +107,9 @@ typedef struct ar_error_info {
     int32_t code;       /* AR_OK or AR_ETIMEOUT */
     int32_t rank;       /* rank whose block gave up waiting */
     int32_t block;      /* that block's index */
-    int32_t peer;       /* the first peer whose flag had not arrived */
-    uint64_t want;      /* flag value the block waited for */
-    uint64_t seen;      /* flag value it last saw */
+    int32_t peer;       /* the first peer whose flag (or tagged word) had not arrived */
+    uint64_t want;      /* flag value (stage count) the block waited for */
+    uint64_t seen;      /* flag value it last saw (0 for tagged words) */
 } ar_error_info;
 
 /* One trace record: one block of one rank in one call (see ar_set_trace).
@@ -118,7 +118,7 @@ typedef struct ar_error_info {
 typedef struct ar_trace_record {
     int32_t rank;
     int32_t block;
-    uint32_t call;          /* the block's call count before this call: 0, 1, 2, ... */
+    uint32_t call;          /* the rank's call count before this call (the same for every block) */
     uint32_t stages;        /* stages the block ran in this call */
     uint64_t t_start_ns;    /* after the wait for the preceding work on the stream */
     uint64_t t_end_ns;      /* after the block's last output store; 0: record not written */
