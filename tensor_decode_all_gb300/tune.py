@@ -1,14 +1,16 @@
 """Measure a handle's all-reduce tactics on this GPU, and keep them.
 
 The library's built-in table (ar_choose_algo) puts the one-shot / two-shot
-crossover where it was measured on one GB300.  A caller on another GPU, or
-with another clock or memory configuration, can measure it again: ``tune``
-times both forms at power-of-two sizes, each in a CUDA graph of several calls
+crossover, and the sizes up to which the tagged-word form beats the flag
+protocol, where they were measured on one GB300.  A caller on another GPU, or
+with another clock or memory configuration, can measure them again: ``tune``
+times the forms at power-of-two sizes, each in a CUDA graph of several calls
 of every rank (the way decode replays them), picks the smallest measured size
-from which two-shot is faster at that size and at every larger one, and sets
-it on the handle.  ``save`` / ``load`` keep the result in a JSON file keyed by
-the GPU and the handle's shape, so a later process applies it without
-measuring ("[SM120] Add optional FlashInfer PCIe-IPC all-reduce for
+from which two-shot is faster at that size and at every larger one, and the
+largest size up to which tagged words are faster at every smaller one, and
+sets both on the handle.  ``save`` / ``load`` keep the result in a JSON file
+keyed by the GPU and the handle's shape, so a later process applies it
+without measuring ("[SM120] Add optional FlashInfer PCIe-IPC all-reduce for
 switch-free hosts", section "Modifications": a tuned, per-size choice of
 kernel, with declines for what it does not support).
 
@@ -50,6 +52,20 @@ def crossover(times: dict) -> int:
     return threshold
 
 
+def tagged_limit(times: dict) -> int:
+    """times: {bytes: {"tagged": us, "oneshot": us}}.  The largest size up to
+    which the tagged-word form is faster at every measured size, or 0 (never)
+    if it loses at the smallest one."""
+    limit = 0
+    for size in sorted(times):
+        t = times[size]
+        if t["tagged"] < t["oneshot"]:
+            limit = size
+        else:
+            break
+    return limit
+
+
 def _time_form(handle, algo: str, nbytes: int, calls: int, replays: int) -> float:
     """µs per call of one form at one size: graph of `calls` calls of every rank."""
     import torch
@@ -88,9 +104,10 @@ def _time_form(handle, algo: str, nbytes: int, calls: int, replays: int) -> floa
     return a.elapsed_time(b) * 1e3 / (replays * calls)
 
 
-def measure(handle, sizes=None, replays: int = 5) -> dict:
-    """{bytes: {"oneshot": us, "twoshot": us}} at power-of-two sizes from
-    64 KiB to min(8 MiB, the handle's max payload)."""
+def measure(handle, sizes=None, replays: int = 5, forms=("oneshot", "twoshot")) -> dict:
+    """{bytes: {form: us}} at the given sizes; by default the one-shot and
+    two-shot forms at powers of two from 64 KiB to min(8 MiB, the handle's
+    max payload)."""
     max_bytes = handle.max_numel * 2
     if sizes is None:
         sizes = [1 << k for k in range(16, 24) if (1 << k) <= max_bytes]
@@ -101,20 +118,27 @@ def measure(handle, sizes=None, replays: int = 5) -> dict:
             if nbytes > max_bytes or nbytes % 16:
                 raise ValueError(f"size {nbytes} not a multiple of 16 bytes within the handle's max payload")
             calls = max(4, min(20, (256 << 20) // (handle.R * nbytes * 2)))
-            times[nbytes] = {algo: _time_form(handle, algo, nbytes, calls, replays) for algo in ("oneshot", "twoshot")}
+            times[nbytes] = {algo: _time_form(handle, algo, nbytes, calls, replays) for algo in forms}
     finally:
         handle.set_algo(saved)
     return times
 
 
-def tune(handle, sizes=None, replays: int = 5) -> dict:
-    """Measure, set the two-shot threshold on the handle, return the tactics
-    and the measured times."""
+def tune(handle, sizes=None, tagged_sizes=None, replays: int = 5) -> dict:
+    """Measure both crossovers -- one-shot / two-shot (sizes) and tagged words
+    / one-shot (tagged_sizes: by default powers of two from 2 KiB to the
+    smaller of 512 KiB and the tagged form's capacity) -- set them on the
+    handle, and return the tactics and the measured times."""
     if handle.dtype not in (1, 2):
         raise ValueError("tactics apply to fp16/bf16 all-reduce handles")
     times = measure(handle, sizes, replays)
-    handle.set_tactics(twoshot_min_bytes=crossover(times))
-    return {"tactics": handle.tactics(), "times_us": {str(k): v for k, v in times.items()}}
+    if tagged_sizes is None:
+        cap = min(handle.info().tagged_capacity_bytes, 512 << 10, handle.max_numel * 2)
+        tagged_sizes = [1 << k for k in range(11, 20) if (1 << k) <= cap]
+    tagged_times = measure(handle, tagged_sizes, replays, forms=("tagged", "oneshot")) if tagged_sizes else {}
+    handle.set_tactics(twoshot_min_bytes=crossover(times), tagged_max_bytes=tagged_limit(tagged_times))
+    return {"tactics": handle.tactics(), "times_us": {str(k): v for k, v in times.items()},
+            "tagged_times_us": {str(k): v for k, v in tagged_times.items()}}
 
 
 def save(path: str, key: str, tactics: dict) -> None:

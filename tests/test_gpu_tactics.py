@@ -89,17 +89,21 @@ def test_tune_sets_a_measured_threshold_and_the_file_applies_it(tmp_path):
     import tensor_decode_all_gb300 as tda
     from tensor_decode_all_gb300 import tune
     h = tda.Handle(8, torch.bfloat16, 1 << 20, "hbm")
-    out = tune.tune(h, sizes=[64 << 10, 256 << 10, 1 << 20], replays=3)
+    out = tune.tune(h, sizes=[64 << 10, 256 << 10, 1 << 20], tagged_sizes=[4 << 10, 16 << 10], replays=3)
     thr = out["tactics"]["twoshot_min_bytes"]
     assert thr in (64 << 10, 256 << 10, 1 << 20, tune.NEVER)
     assert thr == tune.crossover({int(k): v for k, v in out["times_us"].items()})
+    lim = out["tactics"]["tagged_max_bytes"]
+    assert lim in (0, 4 << 10, 16 << 10)
+    assert lim == tune.tagged_limit({int(k): v for k, v in out["tagged_times_us"].items()})
     assert h.tactics()["twoshot_min_bytes"] == thr
     assert h.info().algo == -1                       # the forced form was restored to AUTO
     path = str(tmp_path / "tactics.json")
     tune.save(path, tune.handle_key(h), h.tactics())
     g = tda.Handle(8, torch.bfloat16, 1 << 20, "hbm")
-    g.set_tactics(twoshot_min_bytes=12345 * 16)
+    g.set_tactics(twoshot_min_bytes=12345 * 16, tagged_max_bytes=16)
     assert tune.load(path, g) and g.tactics()["twoshot_min_bytes"] == thr
+    assert g.tactics()["tagged_max_bytes"] == lim
     k = tda.Handle(4, torch.bfloat16, 1 << 20, "hbm")
     assert not tune.load(path, k)
     for x in (h, g, k):

@@ -42,3 +42,11 @@ def test_save_and_lookup_keep_other_keys(tmp_path):
     assert tune.lookup(str(tmp_path / "missing.json"), "k1") is None
     with open(path) as f:
         assert sorted(json.load(f)) == ["k1", "k2"]
+
+
+def test_tagged_limit_largest_size_up_to_which_tagged_always_wins():
+    t = {2048: {"tagged": 3.0, "oneshot": 3.5}, 8192: {"tagged": 3.2, "oneshot": 3.6},
+         32768: {"tagged": 4.8, "oneshot": 4.6}, 131072: {"tagged": 5.0, "oneshot": 6.0}}
+    assert tune.tagged_limit(t) == 8192          # the win at 128 KiB after a loss does not count
+    assert tune.tagged_limit({2048: {"tagged": 4.0, "oneshot": 3.5}}) == 0
+    assert tune.tagged_limit({}) == 0
