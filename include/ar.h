@@ -25,7 +25,10 @@
  *     the legacy stream can hold back a peer rank's kernel while this rank's
  *     kernel waits for it ("fix(group): run each rank on a non-blocking
  *     stream", sections "What" and "Why").
- *   - Return value: AR_OK (0) or an ar_code below.  A call that returns an
+ *   - Return value: AR_OK (0) or an ar_code below.  An enqueue call that
+ *     returns AR_ECUDA because its launch failed is not counted as a call of
+ *     its rank (the other ranks' kernels of that call, if they were enqueued,
+ *     time out: reset the handle).  A call that returns an
  *     error other than AR_ECUDA has enqueued nothing, so the caller can keep
  *     its own fallback path ("[SM120] Add optional FlashInfer PCIe-IPC
  *     all-reduce for switch-free hosts", section "Modifications": a shape the

@@ -302,12 +302,32 @@ class Handle:
             raise RuntimeError("handle destroyed")
         return self._h
 
+    def _check_tensors(self, name: str, inp, out, out_factor: int) -> None:
+        """What the C ABI cannot see through raw pointers: both tensors dense,
+        of the handle's dtype, and `out` large enough for the call (numel
+        elements for an all-reduce, R * numel for an allgather), so that a
+        wrong tensor is refused here instead of being read or written past
+        its end on the device."""
+        for what, t in (("input", inp), ("output", out)):
+            if not t.is_contiguous():
+                raise ValueError(f"{name}: {what} tensor is not contiguous")
+            try:
+                code = _dtype_code(t.dtype)
+            except KeyError:
+                code = None
+            if code != self.dtype:
+                raise ValueError(f"{name}: {what} dtype {t.dtype} does not match the handle's")
+        if out.numel() < out_factor * inp.numel():
+            raise ValueError(f"{name}: output holds {out.numel()} elements, the call writes {out_factor * inp.numel()}")
+
     def allreduce(self, rank: int, inp, out, stream=None) -> None:
+        self._check_tensors("ar_allreduce", inp, out, 1)
         rc = ar_allreduce(self.ptr, rank, inp.data_ptr(), out.data_ptr(), inp.numel(), _stream_handle(stream))
         if rc:
             raise ArError(rc, f"ar_allreduce(rank={rank})")
 
     def allgather(self, rank: int, inp, out, stream=None) -> None:
+        self._check_tensors("ar_allgather", inp, out, self.R)
         rc = ar_allgather(self.ptr, rank, inp.data_ptr(), out.data_ptr(), inp.numel(), _stream_handle(stream))
         if rc:
             raise ArError(rc, f"ar_allgather(rank={rank})")
@@ -331,6 +351,11 @@ class Handle:
     def _fused(self, fn, name, ins, outs, stream) -> None:
         if len(ins) != self.R or len(outs) != self.R:
             raise ValueError(f"{name}: need {self.R} inputs and outputs")
+        factor = self.R if fn is ar_allgather_fused else 1
+        for r in range(self.R):
+            if ins[r].numel() != ins[0].numel():
+                raise ValueError(f"{name}: rank {r}'s input has {ins[r].numel()} elements, rank 0's {ins[0].numel()}")
+            self._check_tensors(name, ins[r], outs[r], factor)
         rc = fn(self.ptr, [t.data_ptr() for t in ins], [t.data_ptr() for t in outs], ins[0].numel(),
                 _stream_handle(stream))
         if rc:

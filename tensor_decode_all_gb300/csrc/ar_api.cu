@@ -419,6 +419,16 @@ int begin_fused(ar_handle *h, const void *const *ins, void *const *outs, size_t 
     return AR_OK;
 }
 
+// Closes the bookkeeping of an accepted call: a call whose launch failed
+// enqueued nothing, so it is taken off the host's count for `rank` (every
+// rank for rank < 0), which stays equal to the number of kernels issued.
+int end_call(ar_handle *h, int rank, int rc) {
+    if (rc == AR_OK) return rc;
+    for (int r = 0; r < h->R; ++r)
+        if (rank < 0 || r == rank) h->host_calls[r].fetch_sub(1, std::memory_order_acq_rel);
+    return rc;
+}
+
 // The all-reduce launch both entry points share: form, plan and grid from the
 // handle, then one launch for `rank` (or, rank < 0, all ranks at once).
 int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int rank, cudaStream_t s) {
@@ -598,7 +608,7 @@ AR_API int ar_allreduce(ar_handle *h, int rank, const void *in, void *out, size_
     tda::RankIO io = {};
     io.in[0] = const_cast<void *>(in);
     io.out[0] = out;
-    return enqueue_allreduce(h, io, numel, rank, s);
+    return end_call(h, rank, enqueue_allreduce(h, io, numel, rank, s));
 }
 
 AR_API int ar_allgather(ar_handle *h, int rank, const void *in, void *out, size_t numel,
@@ -611,7 +621,7 @@ AR_API int ar_allgather(ar_handle *h, int rank, const void *in, void *out, size_
     tda::RankIO io = {};
     io.in[0] = const_cast<void *>(in);
     io.out[0] = out;
-    return enqueue_allgather(h, io, numel, rank, allgather_vec(numel * h->itemsize, in, out), s);
+    return end_call(h, rank, enqueue_allgather(h, io, numel, rank, allgather_vec(numel * h->itemsize, in, out), s));
 }
 
 AR_API int ar_allreduce_fused(ar_handle *h, const void *const *ins, void *const *outs, size_t numel,
@@ -621,7 +631,7 @@ AR_API int ar_allreduce_fused(ar_handle *h, const void *const *ins, void *const 
     tda::RankIO io;
     int rc = begin_fused(h, ins, outs, numel, s, &io);
     if (rc != AR_OK || numel == 0) return rc;
-    return enqueue_allreduce(h, io, numel, -1, s);
+    return end_call(h, -1, enqueue_allreduce(h, io, numel, -1, s));
 }
 
 AR_API int ar_allgather_fused(ar_handle *h, const void *const *ins, void *const *outs, size_t numel,
@@ -636,7 +646,7 @@ AR_API int ar_allgather_fused(ar_handle *h, const void *const *ins, void *const 
         const int v = allgather_vec(bytes, ins[r], outs[r]);
         if (v < vw) vw = v;
     }
-    return enqueue_allgather(h, io, numel, -1, vw, s);
+    return end_call(h, -1, enqueue_allgather(h, io, numel, -1, vw, s));
 }
 
 AR_API int ar_status(ar_handle *h, ar_error_info *info) {

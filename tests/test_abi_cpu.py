@@ -158,3 +158,32 @@ def test_no_cpu_fallback_when_library_missing(monkeypatch, tmp_path):
     monkeypatch.setattr(ar._build, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         ar.lib()
+
+
+def test_binding_refuses_tensors_the_pointers_cannot_describe():
+    """The Python binding checks what raw pointers hide (dense layout, the
+    handle's dtype, room in the output) before any call reaches the library;
+    tensors that pass go on to the handle (here a destroyed one)."""
+    import torch
+    h = ar.Handle.__new__(ar.Handle)
+    h.R, h.dtype, h._h = 3, ar.AR_F16, 0
+    x = torch.zeros(64, dtype=torch.float16)
+    bad = [
+        (x[::2], torch.zeros(32, dtype=torch.float16), "not contiguous"),
+        (x, torch.zeros(64, dtype=torch.bfloat16), "dtype"),
+        (torch.zeros(64, dtype=torch.float32), torch.zeros(64, dtype=torch.float32), "dtype"),
+        (x, torch.zeros(63, dtype=torch.float16), "holds 63"),
+    ]
+    for inp, out, msg in bad:
+        with pytest.raises(ValueError, match=msg):
+            h.allreduce(0, inp, out)
+    with pytest.raises(ValueError, match="holds 64"):
+        h.allgather(0, x, torch.zeros(64, dtype=torch.float16))     # needs R * 64
+    with pytest.raises(ValueError, match="rank 1's input"):
+        h.allreduce_fused([x, x[:32], x], [x, x, x])
+    with pytest.raises(ValueError, match="need 3"):
+        h.allreduce_fused([x, x], [x, x])
+    with pytest.raises(RuntimeError, match="destroyed"):
+        h.allreduce(0, x, torch.zeros(64, dtype=torch.float16))
+    with pytest.raises(RuntimeError, match="destroyed"):
+        h.allgather(0, x, torch.zeros(3 * 64, dtype=torch.float16))
