@@ -306,7 +306,8 @@ AR_API int ar_set_timeout(ar_handle *h, uint64_t timeout_ns);
  * every later call (enqueued or captured after this) writes one record, at
  * index ((call % depth) * R + rank) * max_blocks + block, depth = capacity /
  * (R * max_blocks) (ar_info.max_blocks), so the last `depth` calls of each
- * block are kept.  capacity < R * max_blocks or a buffer not 16-byte aligned
+ * block are kept.  capacity < R * max_blocks, a buffer not 16-byte aligned,
+ * or a call that is half issued (traced calls may launch another grid)
  * returns AR_EINVAL.  Traced calls run kernels built with the trace code (a
  * few stores per block and call); untraced calls run kernels built without
  * it, so tracing off costs nothing.  A captured graph keeps the setting in
@@ -377,14 +378,16 @@ AR_API int ar_set_pdl(ar_handle *h, int enable);
  * of one tile per block; larger calls take the one-shot form).  The
  * environment variable AR_ALGO=oneshot|twoshot|tagged sets it at ar_create.
  * Every rank of a call must see the same setting; set it before enqueuing.
- * AR_EINVAL for an unknown form or a two-shot / tagged form on a complex64
- * handle. */
+ * AR_EINVAL for an unknown form, a two-shot / tagged form on a complex64
+ * handle, or a call that is half issued (some rank has enqueued more calls on
+ * the handle than another; the setting is unchanged). */
 AR_API int ar_set_algo(ar_handle *h, int algo);
 
 /* Read or replace a handle's tactics (see ar_tactics).  Every rank shares the
- * handle, so all ranks see the same values; change them only between calls
- * (not while a call is half issued).  Errors: AR_EINVAL for a NULL argument,
- * a sub-tile other than 0/64/128/256, or a negative block cap. */
+ * handle, so all ranks see the same values; change them only between calls.
+ * Errors: AR_EINVAL for a NULL argument, a sub-tile other than 0/64/128/256,
+ * a negative block cap, or a call that is half issued (some rank has enqueued
+ * more calls than another; the tactics are unchanged). */
 AR_API int ar_get_tactics(const ar_handle *h, ar_tactics *t);
 AR_API int ar_set_tactics(ar_handle *h, const ar_tactics *t);
 

@@ -363,6 +363,17 @@ int max_blocks_override() {
     return v > 0 ? (int)v : 0;
 }
 
+// True while some rank has issued more calls on the handle than another: a
+// call is half issued.  The form, the tactics and the trace setting decide a
+// call's kernel and grid, so they change only between calls; changed in
+// between, the ranks of one call would run different forms.
+bool call_half_issued(const ar_handle *h) {
+    const uint64_t c = h->host_calls[0].load(std::memory_order_acquire);
+    for (int r = 1; r < h->R; ++r)
+        if (h->host_calls[r].load(std::memory_order_acquire) != c) return true;
+    return false;
+}
+
 // Common checks and bookkeeping of one enqueue call.
 int begin_call(ar_handle *h, int rank, const void *in, void *out, size_t numel, cudaStream_t s,
                uint64_t *call_index) {
@@ -409,9 +420,7 @@ int begin_fused(ar_handle *h, const void *const *ins, void *const *outs, size_t 
     rc = check_device(h);
     if (rc != AR_OK) return rc;
     if (*reinterpret_cast<volatile int32_t *>(&h->err_host->code) != AR_OK) return AR_ESTATE;
-    const uint64_t c = h->host_calls[0].load(std::memory_order_acquire);
-    for (int r = 1; r < h->R; ++r)
-        if (h->host_calls[r].load(std::memory_order_acquire) != c) return AR_EINVAL;
+    if (call_half_issued(h)) return AR_EINVAL;
     for (int r = 0; r < h->R; ++r) {
         h->host_calls[r].fetch_add(1, std::memory_order_acq_rel);
         h->host_stream[r].store((uintptr_t)s, std::memory_order_release);
@@ -734,12 +743,13 @@ AR_API int ar_set_algo(ar_handle *h, int algo) {
                algo != AR_ALGO_TAGGED))
         return AR_EINVAL;
     if ((algo == AR_ALGO_TWOSHOT || algo == AR_ALGO_TAGGED) && h->dtype == AR_C64) return AR_EINVAL;
+    if (call_half_issued(h)) return AR_EINVAL;
     h->algo = algo;
     return AR_OK;
 }
 
 AR_API int ar_set_trace(ar_handle *h, void *records, uint64_t capacity) {
-    if (!h) return AR_EINVAL;
+    if (!h || call_half_issued(h)) return AR_EINVAL;
     if (!records) {
         h->trace = nullptr;
         h->trace_depth = 0;
@@ -784,7 +794,7 @@ AR_API int ar_set_tactics(ar_handle *h, const ar_tactics *t) {
     if (!h || !t) return AR_EINVAL;
     if (t->twoshot_sub != 0 && t->twoshot_sub != 64 && t->twoshot_sub != 128 && t->twoshot_sub != 256)
         return AR_EINVAL;
-    if (t->max_blocks < 0) return AR_EINVAL;
+    if (t->max_blocks < 0 || call_half_issued(h)) return AR_EINVAL;
     h->twoshot_min_bytes = t->twoshot_min_bytes;
     h->twoshot_sub = t->twoshot_sub;
     h->max_blocks = t->max_blocks;

@@ -108,3 +108,47 @@ def test_tune_sets_a_measured_threshold_and_the_file_applies_it(tmp_path):
     assert not tune.load(path, k)
     for x in (h, g, k):
         x.destroy()
+
+
+def test_settings_are_refused_while_a_call_is_half_issued():
+    """Between the ranks' halves of one call the form, the tactics and the
+    trace setting stay as they are (changed there, the ranks of the call
+    would run different kernels); once the call is complete they change
+    again.  Everything is allocated before rank 0's kernel is enqueued, so
+    nothing on the host waits for it while rank 1's half is outstanding."""
+    import tensor_decode_all_gb300 as tda
+    from tensor_decode_all_gb300 import ar, trace
+    R, n = 2, 65536
+    xs = inputs.allreduce_inputs(5, R, n, "f16", "uniform", 8)
+    h = tda.Handle(R, torch.float16, n, "hbm")
+    ins = [to_dev(x, "f16") for x in xs]
+    outs = [torch.empty_like(t) for t in ins]
+    info = h.info()
+    depth = 2
+    buf = torch.zeros(depth * R * info.max_blocks * trace.RECORD_DTYPE.itemsize, dtype=torch.uint8, device="cuda")
+    streams = rank_streams(R)
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    before = h.tactics()
+    h.allreduce(0, ins[0], outs[0], streams[0])
+    assert ar.ar_set_algo(h.ptr, ar.AR_ALGO_TWOSHOT) == ar.AR_EINVAL
+    t = ar.ar_get_tactics(h.ptr)
+    t.max_blocks = 2
+    assert ar.ar_set_tactics(h.ptr, t) == ar.AR_EINVAL
+    assert ar.lib().ar_set_trace(h.ptr, buf.data_ptr(), depth * R * info.max_blocks) == ar.AR_EINVAL
+    h.allreduce(1, ins[1], outs[1], streams[1])   # completes the call
+    for s in streams:
+        torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    h.check()
+    want = oracle.allreduce(xs, "f16", ranks=[0])[0]
+    for r in range(R):
+        assert_bits_equal(to_bits(outs[r]), want, "f16", f"rank {r}")
+    assert h.tactics() == before and h.info().algo == ar.AR_ALGO_AUTO
+    assert (buf == 0).all()
+    h.set_algo("twoshot")
+    h.set_tactics(max_blocks=2)
+    h.set_trace(buf, depth * R * info.max_blocks)
+    h.set_trace(None, 0)
+    h.destroy()
