@@ -404,8 +404,8 @@ AR_API int ar_set_tactics(ar_handle *h, const ar_tactics *t);
 AR_API int ar_supports(const ar_handle *h, int op, size_t numel, const void *in, const void *out);
 
 /*
- * ar_allreduce_noalloc -- an all-reduce that allocates nothing.  The paper has
- * no counterpart: this entry point is for callers that cannot allocate device
+ * ar_allreduce_noalloc -- an all-reduce that allocates nothing.  None of the
+ * cited sources has a counterpart: this entry point is for callers that cannot allocate device
  * memory where they reduce -- code running inside another library's memory
  * pool or arena, which owns every allocation on the device; code on a
  * latency-critical path where cudaMalloc, which can synchronise the device,
