@@ -141,8 +141,9 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
             pdl_trigger();
         }
 
-        // 3. add in rank order, round once, store
-        if (v < nv && !bail) {
+        // 3. add in rank order, round once, store (only where the peers'
+        // words were read: a position beyond the buffer is never published)
+        if (live && !bail) {
             uint4 vals[R];
 #pragma unroll
             for (int p = 0; p < R; ++p) {
