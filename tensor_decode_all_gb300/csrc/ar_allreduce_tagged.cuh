@@ -141,9 +141,11 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
             pdl_trigger();
         }
 
-        // 3. add in rank order, round once, store (only where the peers'
-        // words were read: a position beyond the buffer is never published)
-        if (live && !bail) {
+        // 3. add in rank order, round once, store.  Where v < nv the peers'
+        // words were read: the host sends this form only calls of one stage
+        // per block, so w = b * 256 + tid stays inside the buffer and `live`
+        // differs from this test only by `bail`, checked here again.
+        if (v < nv && !bail) {
             uint4 vals[R];
 #pragma unroll
             for (int p = 0; p < R; ++p) {
