@@ -175,6 +175,17 @@ KERNEL_SOURCES = ("ar_allreduce.cuh", "ar_allreduce_tagged.cuh", "ar_sync.cuh", 
                   "ar_allreduce_bf16_twoshot.cu", "ar_allgather.cu")
 
 
+HEADLINE_R, HEADLINE_NUMEL = 2, 131072
+
+
+def headline_config(n_gpus: int) -> dict:
+    """The headline workload's config, the same in both arms of the bench."""
+    return {"workload": "R=2 logical ranks, fp16, N=131072 per rank (256 KiB), pinned-host slots, graph-replayed",
+            "R": HEADLINE_R, "numel": HEADLINE_NUMEL, "bytes_per_rank": HEADLINE_NUMEL * 2, "slots": "pinned_host",
+            "l2": "flushed (256 MiB write) before every step, outside the timed events",
+            "parallelism": f"replicas x{n_gpus} (logical ranks share one GPU)"}
+
+
 def kernel_source_sha256() -> str:
     """Hash of the code (comments and blank space removed) the all-reduce and
     allgather kernels are compiled from: profiled counters stay valid across
@@ -535,7 +546,7 @@ def run_ours(args, dist):
     link = tda.ar_probe_host_link(64 << 20, 10)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
 
-    R, numel, C = 2, 131072, args.calls
+    R, numel, C = HEADLINE_R, HEADLINE_NUMEL, args.calls
     w = Workload("allreduce", R, "f16", numel, "pinned", C, config=2, dist="normal4")
     w.capture()
     w.time_graph(1, 0, flush)
@@ -613,11 +624,7 @@ def run_ours(args, dist):
         "warmup": args.warmup, "ms_per_step": round(total_s * 1e3 / len(ms), 4),
         "us_per_call": head["us_per_call"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded 4*N(0,1) cast to fp16)",
-        "config": {"workload": "R=2 logical ranks, fp16, N=131072 per rank (256 KiB), pinned-host slots, "
-                               "graph-replayed", "R": R, "numel": numel, "bytes_per_rank": S,
-                   "calls_per_step": C, "slots": "pinned_host",
-                   "l2": "flushed (256 MiB write) before every step, outside the timed events",
-                   "parallelism": f"replicas x{n} (logical ranks share one GPU)"},
+        "config": headline_config(n), "calls_per_step": C,
         "roofline": head["roofline"],
         "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "form": "zero copy" if zero_value >= pipelined_value else "pipelined copies",
@@ -732,7 +739,7 @@ def run_reference(args, dist):
     import oracle
     from tensor_decode_all_gb300 import inputs
     oracle.build()
-    R, numel, dtype = 2, 131072, "f16"
+    R, numel, dtype = HEADLINE_R, HEADLINE_NUMEL, "f16"
     cores = oracle.max_threads()
     xs = inputs.allreduce_inputs(2, R, numel, dtype, "normal4", 0)
     calls_per_step = 20
@@ -754,8 +761,10 @@ def run_reference(args, dist):
             "us_per_call": round(total / (len(times) * calls_per_step) * 1e6, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic (seeded 4*N(0,1) cast to fp16)",
-            "config": {"workload": "R=2 logical ranks, fp16, N=131072 per rank (256 KiB), CPU oracle",
-                       "R": R, "numel": numel},
+            "config": dict(headline_config(dist.world),
+                           executor="the CPU oracle on the host cores: the same workload and outputs; "
+                                    "slots, graphs and L2 flushing do not apply"),
+            "calls_per_step": calls_per_step,
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
