@@ -48,3 +48,26 @@ def test_two_gloo_ranks_take_the_max_and_only_rank0_reports():
 def test_max_over_ranks_helper():
     import bench
     assert bench.max_over_ranks([1.0, 3.5, 2.0]) == 3.5
+
+
+def test_reference_arm_line_on_one_rank():
+    """The reference arm's JSON line: the oracle timed on the host cores, on
+    the same metric, unit and headline config as the kernels' arm."""
+    import json
+    import subprocess
+    import sys
+    import bench
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "1"],
+                         cwd=root, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["higher_is_better"] is True and line["value"] > 0 and line["steps"] == 1
+    cfg = dict(line["config"])
+    assert cfg.pop("executor").startswith("the CPU oracle")
+    assert cfg == bench.headline_config(1)
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
