@@ -170,9 +170,36 @@ class ClockSampler:
 
 # ------------------------------------------------------------- measurement
 
-KERNEL_SOURCES = ("ar_allreduce.cuh", "ar_allreduce_tagged.cuh", "ar_sync.cuh", "ar_internal.h",
-                  "ar_allreduce_f16.cu", "ar_allreduce_bf16.cu", "ar_allreduce_f16_twoshot.cu",
-                  "ar_allreduce_bf16_twoshot.cu", "ar_allgather.cu")
+# The code each kernel family is compiled from (paths from the repository
+# root).  Profiled counters belong to one family: an edit to another family's
+# code leaves them valid, an edit to their own (or to a shared header, the
+# C header's structs included) voids them.
+_CSRC = "tensor_decode_all_gb300/csrc/"
+_COMMON_SOURCES = ("include/ar.h", _CSRC + "ar_internal.h", _CSRC + "ar_sync.cuh")
+FORM_SOURCES = {
+    "oneshot": _COMMON_SOURCES + (_CSRC + "ar_allreduce.cuh", _CSRC + "ar_allreduce_f16.cu",
+                                  _CSRC + "ar_allreduce_bf16.cu"),
+    "twoshot": _COMMON_SOURCES + (_CSRC + "ar_allreduce.cuh", _CSRC + "ar_allreduce_f16_twoshot.cu",
+                                  _CSRC + "ar_allreduce_bf16_twoshot.cu"),
+    "tagged": _COMMON_SOURCES + (_CSRC + "ar_allreduce.cuh", _CSRC + "ar_allreduce_tagged.cuh",
+                                 _CSRC + "ar_allreduce_f16.cu", _CSRC + "ar_allreduce_bf16.cu"),
+    "allgather": _COMMON_SOURCES + (_CSRC + "ar_allgather.cu",),
+}
+
+
+def source_sha256(form: str) -> str:
+    """Hash of the code (comments and blank space removed) a kernel family is
+    compiled from: profiled counters stay valid across comment edits."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for f in FORM_SOURCES[form]:
+        with open(os.path.join(ROOT, f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update(" ".join(text.split()).encode())
+    return h.hexdigest()
 
 
 HEADLINE_R, HEADLINE_NUMEL = 2, 131072
@@ -186,33 +213,21 @@ def headline_config(n_gpus: int) -> dict:
             "parallelism": f"replicas x{n_gpus} (logical ranks share one GPU)"}
 
 
-def kernel_source_sha256() -> str:
-    """Hash of the code (comments and blank space removed) the all-reduce and
-    allgather kernels are compiled from: profiled counters stay valid across
-    comment edits."""
-    import hashlib
-    import re
-    h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "tensor_decode_all_gb300", "csrc", f)) as fh:
-            text = fh.read()
-        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        text = re.sub(r"//[^\n]*", "", text)
-        h.update(" ".join(text.split()).encode())
-    return h.hexdigest()
-
-
 def profiled_traffic(name: str):
     """DRAM and host-link bytes per call of a workload, from the committed ncu
-    summary (profiles/traffic.json), or None if the kernels changed since."""
+    summary (profiles/traffic.json), or None if its kernel family's code
+    changed since."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
     except Exception:
         return None
-    if t.get("kernel_source_sha256") != kernel_source_sha256():
+    entry = t.get("workloads", {}).get(name)
+    if not entry or entry.get("form") not in FORM_SOURCES:
         return None
-    return t.get("workloads", {}).get(name)
+    if entry.get("source_sha256") != source_sha256(entry["form"]):
+        return None
+    return entry
 
 
 def measured_peaks():

@@ -71,3 +71,39 @@ def test_reference_arm_line_on_one_rank():
     assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_profiled_traffic_follows_each_kernel_family(tmp_path, monkeypatch):
+    """Counters stay attached to their kernel family: a comment edit keeps
+    them, a code edit to one family's source voids that family's counters
+    only, and a code edit to a shared header voids all of them."""
+    import json
+    import shutil
+    import bench
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    files = sorted({f for fs in bench.FORM_SOURCES.values() for f in fs})
+    for f in files:
+        (tmp_path / f).parent.mkdir(parents=True, exist_ok=True)
+        shutil.copy(os.path.join(root, f), tmp_path / f)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "profiles").mkdir()
+    t = {"workloads": {form: {"dram_bytes_per_call": i + 1, "form": form, "source_sha256": bench.source_sha256(form)}
+                       for i, form in enumerate(bench.FORM_SOURCES)}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(t))
+
+    def valid():
+        return {form for form in bench.FORM_SOURCES if bench.profiled_traffic(form) is not None}
+
+    assert valid() == set(bench.FORM_SOURCES)
+    ag = tmp_path / "tensor_decode_all_gb300/csrc/ar_allgather.cu"
+    ag.write_text(ag.read_text() + "\n// a comment\n/* another */\n")
+    assert valid() == set(bench.FORM_SOURCES)
+    ag.write_text(ag.read_text() + "\nnamespace { int unused_edit = 1; }\n")
+    assert valid() == set(bench.FORM_SOURCES) - {"allgather"}
+    tagged = tmp_path / "tensor_decode_all_gb300/csrc/ar_allreduce_tagged.cuh"
+    tagged.write_text(tagged.read_text() + "\n#define EDIT 1\n")
+    assert valid() == {"oneshot", "twoshot"}
+    hdr = tmp_path / "include/ar.h"
+    hdr.write_text(hdr.read_text() + "\n#define EDIT 2\n")
+    assert valid() == set()
+    assert bench.profiled_traffic("no such workload") is None
