@@ -187,3 +187,29 @@ def test_binding_refuses_tensors_the_pointers_cannot_describe():
         h.allreduce(0, x, torch.zeros(64, dtype=torch.float16))
     with pytest.raises(RuntimeError, match="destroyed"):
         h.allgather(0, x, torch.zeros(3 * 64, dtype=torch.float16))
+
+
+def test_header_is_plain_c_and_cpp(tmp_path):
+    """include/ar.h stands alone for a C caller (C99 and C11, pedantic,
+    warnings as errors) and a C++ caller (declarations get C linkage)."""
+    import shutil
+    import subprocess
+    inc = os.path.dirname(ar._build.INCLUDE + "/")
+    gcc, gxx = shutil.which("gcc"), shutil.which("g++")
+    if gcc is None or gxx is None:
+        pytest.skip("no C/C++ compiler")
+    c = tmp_path / "use.c"
+    c.write_text('#include "ar.h"\nint f(void) { ar_tactics t; ar_plan p; (void)t; (void)p; '
+                 'return (int)sizeof(ar_error_info) + AR_OK; }\n')
+    for std in ("c99", "c11"):
+        subprocess.run([gcc, f"-std={std}", "-pedantic", "-Wall", "-Wextra", "-Werror", "-I", inc, "-c", str(c),
+                        "-o", str(tmp_path / f"use_{std}.o")], check=True)
+    cc = tmp_path / "use.cc"
+    cc.write_text('#include "ar.h"\n#include "ar.h"\n'
+                  'extern "C" int probe() { return ar_last_error(); }\n'
+                  'int g() { return (int)sizeof(ar_info) + probe(); }\n')
+    obj = tmp_path / "use_cc.o"
+    subprocess.run([gxx, "-std=c++17", "-Wall", "-Wextra", "-Werror", "-I", inc, "-c", str(cc), "-o", str(obj)],
+                   check=True)
+    syms = subprocess.run(["nm", str(obj)], check=True, capture_output=True, text=True).stdout
+    assert " U ar_last_error" in syms      # an unmangled (C linkage) reference
