@@ -36,6 +36,11 @@
  *   - Errors found on the device (a peer that never arrives) cannot be
  *     returned by the enqueueing call; they are recorded in the handle and read
  *     with ar_status() after the caller has synchronised.
+ *   - Host threads: the enqueue calls of different ranks may come from
+ *     different threads at the same time (one thread per rank, each on its own
+ *     stream).  The calls that change a handle's settings (ar_set_algo,
+ *     ar_set_tactics, ar_set_trace, ar_set_pdl, ar_set_timeout), ar_reset and
+ *     ar_destroy must not run concurrently with any other call on the handle.
  */
 #ifndef TDA_AR_H
 #define TDA_AR_H
