@@ -278,14 +278,21 @@ AR_API int ar_allgather_fused(ar_handle *h, const void *const *ins, void *const 
  * ar_status -- the first device-side error recorded in the handle (AR_OK or
  * AR_ETIMEOUT), copied into *info if info is not NULL.  Reads mapped host
  * memory only (no CUDA call); the answer covers the kernels the caller has
- * already synchronised with.
+ * already synchronised with.  This is the library's watchdog report: a rank
+ * that never arrives ends its peers' bounded waits with a recorded code
+ * instead of a hang ("fix(qwen3): re-enable CUDA Graph under TP via startup
+ * decode-graph pre-capture", section "Description": NCCL has no device-side
+ * timeout, so a wedged rank would otherwise wait forever).
  */
 AR_API int ar_status(ar_handle *h, ar_error_info *info);
 
 /*
  * ar_reset -- synchronise the device, then zero every flag, counter and the
  * error record.  Required after AR_ETIMEOUT; afterwards the handle behaves as
- * if just created.  No graph that uses the handle may be running.
+ * if just created.  No graph that uses the handle may be running.  The
+ * recovery half of the watchdog of "fix(qwen3): re-enable CUDA Graph under TP
+ * via startup decode-graph pre-capture", section "Description": after a
+ * timeout the caller resets the exchange state rather than the process.
  */
 AR_API int ar_reset(ar_handle *h);
 
@@ -433,10 +440,36 @@ AR_API int ar_supports(const ar_handle *h, int op, size_t numel, const void *in,
  * so all R ranks' blocks are resident together.  Every call shares the array
  * and it keeps the last call's contents: calls that overlap on the GPU (on
  * streams with no ordering between them) race and give undefined results.
+ * A wait for a peer is bounded (1 s).  A block whose wait runs out leaves
+ * without writing its part of the outputs and records itself in an error
+ * record inside the same array; the call itself has already returned AR_OK.
+ * Read that record with ar_noalloc_status() after synchronising with
+ * `stream` and before the next call on the device, which clears it.
  * Errors: AR_EINVAL, AR_ETOOBIG, AR_ECUDA.
  */
 AR_API int ar_allreduce_noalloc(int R, int dtype, const void *const *ins, void *const *outs, size_t numel,
                                 ar_stream_t stream);
+
+/*
+ * ar_noalloc_status -- the error record of ar_allreduce_noalloc's array on
+ * the current device: AR_OK, or AR_ETIMEOUT with the rank, block and peer of
+ * the first block whose wait ran out (copied into *info if info is not NULL).
+ * It covers the calls the caller has synchronised with since the last call
+ * that started on the device (each call clears the record before it
+ * launches).  A synchronous copy out of the array; allocates nothing.  Does
+ * the device's first-call set-up if no call has run on it yet.
+ * Returns the recorded code, or AR_ECUDA if the record could not be read.
+ */
+AR_API int ar_noalloc_status(ar_error_info *info);
+
+/*
+ * ar_noalloc_debug_record -- test hook: write *info into the error record of
+ * ar_allreduce_noalloc's array on the current device, as a block that timed
+ * out would, so the status plumbing can be checked without making a wait run
+ * out.  The next ar_allreduce_noalloc call on the device clears it.  Use while
+ * no call is running on the device.  Errors: AR_EINVAL (NULL), AR_ECUDA.
+ */
+AR_API int ar_noalloc_debug_record(const ar_error_info *info);
 
 /* Human-readable name of an ar_code.  Never NULL. */
 AR_API const char *ar_strerror(int code);

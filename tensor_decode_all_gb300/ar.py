@@ -109,6 +109,10 @@ def lib():
             L.ar_debug_seed_stages.argtypes = [vp, u64]
             L.ar_allreduce_noalloc.argtypes = [i32, i32, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, vp]
             L.ar_allreduce_noalloc.restype = i32
+            L.ar_noalloc_status.argtypes = [ctypes.POINTER(ErrorInfo)]
+            L.ar_noalloc_status.restype = i32
+            L.ar_noalloc_debug_record.argtypes = [ctypes.POINTER(ErrorInfo)]
+            L.ar_noalloc_debug_record.restype = i32
             for name in ("ar_allreduce_fused", "ar_allgather_fused"):
                 f = getattr(L, name)
                 f.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, vp]
@@ -151,6 +155,18 @@ def ar_allreduce_noalloc(R: int, dtype: int, ins, outs, numel: int, stream: int)
     arr_in = (ctypes.c_void_p * R)(*[int(p) for p in ins])
     arr_out = (ctypes.c_void_p * R)(*[int(p) for p in outs])
     return lib().ar_allreduce_noalloc(R, dtype, arr_in, arr_out, numel, stream)
+
+
+def ar_noalloc_status():
+    """(code, ErrorInfo) of ar_allreduce_noalloc's error record on the current device."""
+    info = ErrorInfo()
+    rc = lib().ar_noalloc_status(ctypes.byref(info))
+    return rc, info
+
+
+def ar_noalloc_debug_record(info: ErrorInfo) -> int:
+    """Test hook: write an error record into ar_allreduce_noalloc's array."""
+    return lib().ar_noalloc_debug_record(ctypes.byref(info))
 
 
 def ar_get_tactics(h: int) -> Tactics:

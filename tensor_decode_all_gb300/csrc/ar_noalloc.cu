@@ -14,11 +14,21 @@
 // It is a single-launch form of the one-shot exchange-and-add kernel: one
 // cooperative grid of B x R blocks, block (b, r) playing block b of rank r, so
 // all R ranks are resident together by construction.  Each call first clears
-// the flags (cudaMemsetAsync on the array), then launches.  Calls on one
-// stream follow each other; calls that overlap on the GPU (different streams,
-// no ordering between them) share the array and race.
+// the flags, the abort word and the error record (cudaMemsetAsync on the
+// array), then launches.  Calls on one stream follow each other; calls that
+// overlap on the GPU (different streams, no ordering between them) share the
+// array and race.
+//
+// A block whose wait for a peer runs out of time (which needs the GPU to stop
+// scheduling part of a resident cooperative grid) leaves without writing its
+// outputs and records itself in the array's error record.  The enqueueing call
+// has already returned AR_OK by then, so the record is read separately:
+// ar_noalloc_status() copies it out once the caller has synchronised with the
+// call's stream, and the next call on the device clears it.
+#include <atomic>
 #include <cstring>
 #include <initializer_list>
+#include <mutex>
 
 #include "ar_allreduce.cuh"
 #include "ar_internal.h"
@@ -33,6 +43,9 @@ constexpr uint64_t kNoAllocSlotBytes = (uint64_t)kMaxRanks * kNoAllocMaxBytes;  
 constexpr uint64_t kNoAllocFlagBytes = (uint64_t)kMaxRanks * kNoAllocMaxBlocks * kFlagStrideWords * 8;  // 64 KiB
 constexpr uint64_t kNoAllocMiscBytes = 256;          // abort word + an error record
 constexpr uint64_t kNoAllocScratchBytes = kNoAllocSlotBytes + kNoAllocFlagBytes + kNoAllocMiscBytes;
+constexpr uint64_t kNoAllocAbortOffset = kNoAllocSlotBytes + kNoAllocFlagBytes;
+constexpr uint64_t kNoAllocErrOffset = kNoAllocAbortOffset + 64;
+static_assert(64 + sizeof(ar_error_info) <= kNoAllocMiscBytes, "error record fits the misc area");
 
 // The scratch: [R][kNoAllocMaxBytes] slots, then the flags, then the abort
 // word and an error record.  Device code reaches it through the pointer the
@@ -66,8 +79,8 @@ __global__ void __launch_bounds__(kThreads)
     d.slots = scratch;
     d.flags = reinterpret_cast<unsigned long long *>(scratch + kNoAllocSlotBytes);
     d.ctr = nullptr;
-    d.abort_word = reinterpret_cast<unsigned int *>(scratch + kNoAllocSlotBytes + kNoAllocFlagBytes);
-    d.err = reinterpret_cast<ar_error_info *>(scratch + kNoAllocSlotBytes + kNoAllocFlagBytes + 64);
+    d.abort_word = reinterpret_cast<unsigned int *>(scratch + kNoAllocAbortOffset);
+    d.err = reinterpret_cast<ar_error_info *>(scratch + kNoAllocErrOffset);
     d.slot_bytes = kNoAllocMaxBytes;
     d.timeout_ns = timeout_ns;
     d.bmax = kNoAllocMaxBlocks;
@@ -126,20 +139,30 @@ const void *noalloc_ptr(int R) {
 }
 
 // Per-device set-up, done by the first call on each device: the array's
-// device address, the SM count and the kernels' occupancy.
+// device address, the SM count and the kernels' occupancy.  Host threads may
+// make their first calls at the same time: the set-up runs under a lock, and
+// `done` is published with release order after the other fields, so a thread
+// that reads it true (acquire) without the lock sees them complete.  A set-up
+// that fails leaves `done` false, and the next call tries again.
 constexpr int kMaxDevices = 64;
 struct DeviceSetup {
-    bool done = false;
+    std::atomic<bool> done{false};
     uint8_t *scratch = nullptr;
     int sms = 0;
     int bps = 0;  // smallest occupancy over the 16 kernel variants
 };
 DeviceSetup g_setup[kMaxDevices];
+std::mutex g_setup_lock;
 
 int device_setup(int dev, DeviceSetup **out) {
     if (dev < 0 || dev >= kMaxDevices) return AR_EINVAL;
     DeviceSetup &s = g_setup[dev];
-    if (!s.done) {
+    if (s.done.load(std::memory_order_acquire)) {
+        *out = &s;
+        return AR_OK;
+    }
+    std::lock_guard<std::mutex> guard(g_setup_lock);
+    if (!s.done.load(std::memory_order_relaxed)) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
             (void)cudaGetLastError();
@@ -159,7 +182,7 @@ int device_setup(int dev, DeviceSetup **out) {
         s.scratch = static_cast<uint8_t *>(p);
         s.sms = sms;
         s.bps = bps;
-        s.done = true;
+        s.done.store(true, std::memory_order_release);
     }
     *out = &s;
     return AR_OK;
@@ -196,7 +219,8 @@ extern "C" AR_API int ar_allreduce_noalloc(int R, int dtype, const void *const *
     if (blocks > (uint64_t)kNoAllocMaxBlocks) blocks = kNoAllocMaxBlocks;
     if (blocks > tiles) blocks = tiles;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // Flags, abort word and error record start at zero on every call.
+    // Flags, abort word and error record start at zero on every call (this
+    // clears the record a timed-out earlier call left).
     if (cudaMemsetAsync(ds->scratch + kNoAllocSlotBytes, 0, kNoAllocFlagBytes + kNoAllocMiscBytes, s) != cudaSuccess) {
         (void)cudaGetLastError();
         return AR_ECUDA;
@@ -211,4 +235,42 @@ extern "C" AR_API int ar_allreduce_noalloc(int R, int dtype, const void *const *
         return AR_ECUDA;
     }
     return AR_OK;
+}
+
+// The device's set-up, then a synchronous copy between the host and the
+// array's error record (no allocation: cudaMemcpy between pageable host memory
+// and the array stages through the driver's own buffers).
+static int noalloc_record_copy(ar_error_info *host, bool to_device) {
+    using namespace tda;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ECUDA;
+    }
+    DeviceSetup *ds = nullptr;
+    const int rc = device_setup(dev, &ds);
+    if (rc != AR_OK) return rc;
+    uint8_t *rec = ds->scratch + kNoAllocErrOffset;
+    const cudaError_t e = to_device ? cudaMemcpy(rec, host, sizeof(ar_error_info), cudaMemcpyHostToDevice)
+                                    : cudaMemcpy(host, rec, sizeof(ar_error_info), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ECUDA;
+    }
+    return AR_OK;
+}
+
+extern "C" AR_API int ar_noalloc_status(ar_error_info *info) {
+    ar_error_info e;
+    std::memset(&e, 0, sizeof(e));
+    const int rc = noalloc_record_copy(&e, false);
+    if (rc != AR_OK) return rc;
+    if (info) *info = e;
+    return e.code;
+}
+
+extern "C" AR_API int ar_noalloc_debug_record(const ar_error_info *info) {
+    if (!info) return AR_EINVAL;
+    ar_error_info e = *info;
+    return noalloc_record_copy(&e, true);
 }

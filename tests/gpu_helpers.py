@@ -3,6 +3,11 @@
 Nothing here computes the operation: expected values always come from the
 CPU oracle (oracle/), inputs from tensor_decode_all_gb300.inputs.
 """
+import ctypes
+import ctypes.util
+import glob
+import os
+
 import numpy as np
 import torch
 
@@ -80,3 +85,54 @@ def assert_bits_equal(got, want, dtype, what=""):
         i = np.flatnonzero(bad)[:8]
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} differ; first at {i.tolist()}: "
                              f"got {[hex(int(x)) for x in got[i]]} want {[hex(int(x)) for x in want[i]]}")
+
+
+def cudart():
+    """The CUDA runtime library through ctypes (the toolkit's, or the one the
+    torch wheel ships), for the few runtime calls torch does not expose."""
+    cands = [ctypes.util.find_library("cudart"), "libcudart.so.13", "libcudart.so",
+             "/usr/local/cuda/lib64/libcudart.so.13", "/usr/local/cuda/lib64/libcudart.so"]
+    torch_dir = os.path.dirname(torch.__file__)
+    cands += sorted(glob.glob(os.path.join(os.path.dirname(torch_dir), "nvidia", "cu*", "lib", "libcudart.so*")))
+    cands += sorted(glob.glob(os.path.join(os.path.dirname(torch_dir), "nvidia", "cuda_runtime", "lib",
+                                           "libcudart.so*")))
+    cands += sorted(glob.glob(os.path.join(torch_dir, "lib", "libcudart*.so*")))
+    for c in cands:
+        if not c:
+            continue
+        try:
+            return ctypes.CDLL(c)
+        except OSError:
+            continue
+    raise RuntimeError("libcudart not found")
+
+
+class BlockingStream:
+    """A stream created with cudaStreamDefault flags (blocking: it serialises
+    with the legacy default stream), which torch's stream pool never hands out."""
+
+    def __init__(self):
+        self.rt = cudart()
+        self.rt.cudaStreamCreateWithFlags.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_uint]
+        self.rt.cudaStreamCreateWithFlags.restype = ctypes.c_int
+        self.rt.cudaStreamGetFlags.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint)]
+        self.rt.cudaStreamGetFlags.restype = ctypes.c_int
+        self.rt.cudaStreamDestroy.argtypes = [ctypes.c_void_p]
+        self.rt.cudaStreamDestroy.restype = ctypes.c_int
+        h = ctypes.c_void_p()
+        rc = self.rt.cudaStreamCreateWithFlags(ctypes.byref(h), 0)
+        if rc != 0:
+            raise RuntimeError(f"cudaStreamCreateWithFlags: {rc}")
+        self.handle = int(h.value)
+
+    def flags(self) -> int:
+        f = ctypes.c_uint()
+        rc = self.rt.cudaStreamGetFlags(ctypes.c_void_p(self.handle), ctypes.byref(f))
+        if rc != 0:
+            raise RuntimeError(f"cudaStreamGetFlags: {rc}")
+        return int(f.value)
+
+    def destroy(self):
+        if self.handle:
+            self.rt.cudaStreamDestroy(ctypes.c_void_p(self.handle))
+            self.handle = 0

@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from tensor_decode_all_gb300 import inputs
-from tests.gpu_helpers import assert_bits_equal, enqueue, rank_streams, to_bits, to_dev
+from tests.gpu_helpers import BlockingStream, assert_bits_equal, enqueue, rank_streams, to_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -86,15 +86,36 @@ def test_same_stream_for_two_ranks_is_refused():
 
 
 def test_blocking_stream_is_refused():
+    """A blocking stream serialises with the legacy stream, which can hold back
+    a peer rank while this rank's kernel waits for it ("fix(group): run each
+    rank on a non-blocking stream", sections "What" and "Why"): refused, with
+    nothing enqueued, for the per-rank and the fused calls alike."""
     tda = _tda()
-    rt = pytest.importorskip("cuda.bindings.runtime")
-    err, s = rt.cudaStreamCreateWithFlags(0)  # cudaStreamDefault: blocking
-    assert int(err) == 0
-    h = tda.Handle(2, torch.float16, 64, "hbm")
-    a = torch.zeros(64, dtype=torch.float16, device="cuda")
-    assert tda.ar_allreduce(h.ptr, 0, a.data_ptr(), a.data_ptr(), 64, int(s)) == tda.ar.AR_ESTREAM
-    rt.cudaStreamDestroy(s)
-    h.destroy()
+    bs = BlockingStream()
+    try:
+        assert bs.flags() & 1 == 0          # cudaStreamNonBlocking not set
+        h = tda.Handle(2, torch.float16, 64, "hbm")
+        a = torch.zeros(64, dtype=torch.float16, device="cuda")
+        assert tda.ar_allreduce(h.ptr, 0, a.data_ptr(), a.data_ptr(), 64, bs.handle) == tda.ar.AR_ESTREAM
+        assert tda.ar_allgather(h.ptr, 0, a.data_ptr(), a.data_ptr(), 32, bs.handle) == tda.ar.AR_ESTREAM
+        assert tda.ar.ar_allreduce_fused(h.ptr, [a.data_ptr()] * 2, [a.data_ptr()] * 2, 64,
+                                         bs.handle) == tda.ar.AR_ESTREAM
+        torch.cuda.synchronize()
+        assert h.status().code == tda.ar.AR_OK
+        # nothing was counted: a normal call pair still completes
+        s0, s1 = rank_streams(2)
+        xs = inputs.allreduce_inputs(5, 2, 64, "f16", "uniform", 3)
+        ins = [to_dev(x, "f16") for x in xs]
+        outs = [torch.empty_like(t) for t in ins]
+        enqueue(h, "allreduce", ins, outs, [s0, s1])
+        torch.cuda.synchronize()
+        h.check()
+        want = oracle.allreduce(xs, "f16", ranks=[0])[0]
+        for r in range(2):
+            assert_bits_equal(to_bits(outs[r]), want, "f16")
+        h.destroy()
+    finally:
+        bs.destroy()
 
 
 @pytest.mark.parametrize("slots", ["hbm", "pinned"])
