@@ -509,9 +509,28 @@ def roofline(op, R, S, slots, t_call_s, link, hbm_gbs, algo=None):
                 "peak_source": "host-link probe in this run (ar_probe_host_link, of measured): link bytes over "
                                "max(W/BW_w, Rd/BW_r), each direction at its own measured rate"}
     achieved = b["dram"] / t_call_s / 1e9
+    least = R * S + R * R * S if op == "allgather" else 2 * R * S
     return {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm_gbs, "unit": "GB/s",
             "frac": round(achieved / hbm_gbs, 4), "traffic": None, "algorithmic_bytes_per_call": b["dram"],
-            "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)"}
+            "least_dram_bytes_per_call": least,
+            "frac_least": round(least / t_call_s / 1e9 / hbm_gbs, 4),
+            "dram_frac": None,
+            "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)",
+            "note": "frac counts 4RS (inputs, slot writes, slot reads once, outputs) as DRAM bytes; "
+                    "frac_least counts only what any all-reduce must move through DRAM (inputs read, "
+                    "outputs written: 2RS; allgather RS + R^2 S); dram_frac is the ncu-measured DRAM "
+                    "bytes per call of the same kernel over this call time (null without a valid capture)"}
+
+
+def attach_traffic(row, prof, t_call_s, hbm_gbs):
+    """DRAM bytes per call from the committed ncu summary, and the fraction of
+    the measured HBM peak they reach at this call time."""
+    if not prof:
+        return
+    rf = row["roofline"]
+    rf["traffic"] = prof["dram_bytes_per_call"]
+    if rf.get("bound") == "hbm" and prof.get("dram_bytes_per_call"):
+        rf["dram_frac"] = round(prof["dram_bytes_per_call"] / t_call_s / 1e9 / hbm_gbs, 4)
 
 
 def summarize(op, R, dtype, numel, slots, ms_steps, C, link, hbm_gbs, algo=None):
@@ -529,24 +548,66 @@ def summarize(op, R, dtype, numel, slots, ms_steps, C, link, hbm_gbs, algo=None)
             "roofline": roofline(op, R, S, slots, t_call, link, hbm_gbs, algo), "calls": len(ms_steps) * C}
 
 
-def cpu_baseline(R, dtype, numel, seconds=10.0, config=2, dist="normal4"):
-    """The oracle as it stands, all host cores, on a bounded sample of calls."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), and its architecture."""
+    import platform
+    name = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            k, _, v = line.partition(":")
+            if k.strip() in ("Model name", "Model Name") and v.strip() and v.strip() != "-":
+                name = v.strip()
+                break
+        if name:
+            for line in out.splitlines():
+                k, _, v = line.partition(":")
+                if k.strip() == "Vendor ID" and v.strip():
+                    name = f"{v.strip()} {name}"
+                    break
+    except Exception:
+        pass
+    if not name:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        name = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return f"{name or platform.processor() or 'unknown'} ({platform.machine()})"
+
+
+def time_oracle(xs, dtype, nthreads, seconds):
+    """Calls per second of the oracle computing every rank's output of one call."""
+    import oracle
+    oracle.allreduce(xs, dtype, nthreads=nthreads)  # warm
+    t0 = time.perf_counter()
+    calls = 0
+    while time.perf_counter() - t0 < seconds:
+        oracle.allreduce(xs, dtype, nthreads=nthreads)  # every rank's output, as the job computes
+        calls += 1
+    return calls, time.perf_counter() - t0
+
+
+def cpu_baseline(R, dtype, numel, seconds=8.0, config=2, dist="normal4"):
+    """The oracle as it stands on a bounded sample of calls of the headline
+    workload: once on all host cores (the reported value) and once on one core."""
     import oracle
     from tensor_decode_all_gb300 import inputs
     cores = oracle.max_threads()
     xs = inputs.allreduce_inputs(config, R, numel, dtype, dist, 0)
-    oracle.allreduce(xs, dtype, nthreads=cores)  # warm
-    t0 = time.perf_counter()
-    calls = 0
-    while time.perf_counter() - t0 < seconds:
-        oracle.allreduce(xs, dtype, nthreads=cores)  # every rank's output, as the job computes
-        calls += 1
-    dt = time.perf_counter() - t0
     S = numel * 2
+    calls, dt = time_oracle(xs, dtype, cores, seconds)
+    calls1, dt1 = time_oracle(xs, dtype, 1, seconds)
     return {"value": round(S * calls / dt / 1e9, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "us_per_call": round(dt / calls * 1e6, 2),
+            "us_per_call": round(dt / calls * 1e6, 2), "cpu_model": cpu_model(),
+            "single_core": {"value": round(S * calls1 / dt1 / 1e9, 4), "unit": UNIT, "cores": 1,
+                            "us_per_call": round(dt1 / calls1 * 1e6, 2),
+                            "sample": f"{calls1} calls in {dt1:.1f} s"},
             "sample": f"{calls} calls of the headline workload (R={R} {dtype} N={numel}, all {R} ranks' "
-                      f"outputs) in {dt:.1f} s"}
+                      f"outputs) in {dt:.1f} s on {cores} threads; then {calls1} calls in {dt1:.1f} s on one"}
 
 
 def run_ours(args, dist):
@@ -629,9 +690,7 @@ def run_ours(args, dist):
             wx.check(calls=(-1,))
             extras[name] = summarize(op, RR, dt, nn, sl, msx, cc, link, hbm_gbs, wx.algo)
             extras[name]["launch"] = "one cooperative launch per call" if fz else "one launch per rank per call"
-            prof = profiled_traffic(name)
-            if prof:
-                extras[name]["roofline"]["traffic"] = prof["dram_bytes_per_call"]
+            attach_traffic(extras[name], profiled_traffic(name), extras[name]["us_per_call"] * 1e-6, hbm_gbs)
             wx.close()
 
     line = {
@@ -781,7 +840,7 @@ def run_reference(args, dist):
                                     "slots, graphs and L2 flushing do not apply"),
             "calls_per_step": calls_per_step,
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -13,6 +13,7 @@ dataset):
   2  R=2, fp16, N=131072 (256 KiB, the host all-reduce's payload cap), 4*N(0,1), pinned-host
   3  R=8, bf16, N=393216 (48 rows x hidden 8192, the decode-sized max_numel), N(0,1), HBM
   4  allgather, complex64 shards of 1000x500, re/im N(0,1), R=4 and 8, HBM and pinned-host
+     (long runs: each rank's call-0 shard rotated by call + 1 elements per call)
   5  sweep: 2 KiB..64 MiB per rank, fp16/bf16, R=2/4/8, U[-1,1], both slot kinds
 """
 from __future__ import annotations
@@ -80,6 +81,23 @@ def allgather_inputs(config: int, R: int, numel: int, call: int = 0):
         z.imag = im
         out.append(z)
     return out
+
+
+_BASE_SHARDS = {}
+
+
+def allgather_inputs_rotated(config: int, R: int, numel: int, call: int):
+    """R complex64 shards for call `call` of a long run, cheaply: rank r's base
+    shard (allgather_inputs of call 0, re/im N(0,1)) rotated by call + 1
+    elements.  Every call and every rank gets its own contents, so a shard
+    read from the wrong call or rank cannot pass for the right one; the values
+    are still N(0,1) draws.  (Drawing 1000 calls of fresh 4 MB shards takes
+    minutes; a rotation is a copy.)"""
+    key = (config, R, numel)
+    if key not in _BASE_SHARDS:
+        _BASE_SHARDS.clear()
+        _BASE_SHARDS[key] = allgather_inputs(config, R, numel, 0)
+    return [np.roll(b, (call + 1) % max(numel, 1)) for b in _BASE_SHARDS[key]]
 
 
 def numel_for_bytes(nbytes: int, dtype: str) -> int:

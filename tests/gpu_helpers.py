@@ -7,6 +7,7 @@ import ctypes
 import ctypes.util
 import glob
 import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import torch
@@ -136,3 +137,21 @@ class BlockingStream:
         if self.handle:
             self.rt.cudaStreamDestroy(ctypes.c_void_p(self.handle))
             self.handle = 0
+
+
+def generate(fn, args_list, workers=8):
+    """[fn(*a) for a in args_list], drawn on a thread pool (numpy's generators
+    and torch's casts release the GIL): inputs of many calls in seconds."""
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        return list(ex.map(lambda a: fn(*a), args_list))
+
+
+def assert_device_equal(got, want_dev, what=""):
+    """Bytes of a device tensor equal the bytes of the oracle's result (uploaded
+    to the device): for outputs too large to copy back call by call."""
+    g = got.reshape(-1).view(torch.uint8)
+    w = want_dev.reshape(-1).view(torch.uint8)
+    assert g.numel() == w.numel(), (what, g.numel(), w.numel())
+    if not torch.equal(g, w):
+        bad = torch.nonzero(g != w)[:8].reshape(-1).tolist()
+        raise AssertionError(f"{what}: bytes differ from the oracle's at {bad}")

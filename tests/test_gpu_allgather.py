@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from tensor_decode_all_gb300 import inputs
-from tests.gpu_helpers import assert_bits_equal, capture, enqueue, rank_streams, to_bits, to_dev
+from tests.gpu_helpers import assert_bits_equal, assert_device_equal, capture, enqueue, rank_streams, to_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -23,28 +23,34 @@ def _handle(R, n, slots, dtype=torch.complex64):
 
 @pytest.mark.parametrize("slots", ["hbm", "pinned"])
 @pytest.mark.parametrize("R", [4, 8])
-def test_config4_c64_1000x500_graph(R, slots):
-    """Workload 4: complex64 1000x500 shards, graph-replayed, refilled inputs."""
-    n, C, REPLAYS = 1000 * 500, 4, 3
+def test_config4_c64_1000x500_graph_1000_calls(R, slots):
+    """Workload 4: complex64 1000x500 shards, a graph of 100 calls replayed 10
+    times with fresh shards each replay (each rank's base shard rotated per
+    call): 1000 calls, every call of every replay compared byte for byte with
+    the oracle's concatenation on every rank.  The outputs (R x R x 4 MB per
+    call) are compared on the device against the oracle's result uploaded."""
+    n, C, REPLAYS = 1000 * 500, 100, 10
     h = _handle(R, n, slots)
     streams = rank_streams(R)
-    ins = [[torch.empty(n, dtype=torch.complex64, device="cuda") for _ in range(R)] for _ in range(C)]
-    outs = [[torch.empty(R * n, dtype=torch.complex64, device="cuda") for _ in range(R)] for _ in range(C)]
-    g = capture(h, "allgather", ins, outs, streams)
+    ins = torch.empty((C, R, n), dtype=torch.complex64, device="cuda")
+    outs = torch.empty((C, R, R * n), dtype=torch.complex64, device="cuda")
+    g = capture(h, "allgather", [[ins[c, r] for r in range(R)] for c in range(C)],
+                [[outs[c, r] for r in range(R)] for c in range(C)], streams)
+    checked = 0
     for rep in range(REPLAYS):
-        zs_all = []
+        zs_all = [inputs.allgather_inputs_rotated(4, R, n, rep * C + c) for c in range(C)]
         for c in range(C):
-            zs = inputs.allgather_inputs(4, R, n, rep * C + c)
-            for r in range(R):
-                ins[c][r].copy_(to_dev(zs[r], "c64"))
-            zs_all.append(zs)
+            ins[c].copy_(torch.from_numpy(np.stack(zs_all[c])), non_blocking=False)
+        outs.view(torch.int32).fill_(-1)
         g.replay()
         torch.cuda.synchronize()
         h.check()
         for c in range(C):
-            want = oracle.allgather(zs_all[c], ranks=[0])[0]
+            want = torch.from_numpy(oracle.allgather(zs_all[c], ranks=[0])[0]).cuda()
             for r in range(R):
-                assert_bits_equal(to_bits(outs[c][r]), want, "c64", f"rep {rep} call {c} rank {r}")
+                assert_device_equal(outs[c, r], want, f"R={R} {slots} replay {rep} call {c} rank {r}")
+                checked += 1
+    assert checked == C * REPLAYS * R
     del g
     h.destroy()
 

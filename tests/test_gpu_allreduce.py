@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from tensor_decode_all_gb300 import inputs
-from tests.gpu_helpers import assert_bits_equal, capture, enqueue, rank_streams, to_bits, to_dev
+from tests.gpu_helpers import assert_bits_equal, capture, enqueue, generate, rank_streams, to_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -122,58 +122,50 @@ def test_max_numel_exactly_and_one_over():
     h.destroy()
 
 
+def _graph_run(R, dtype, n, slots, config, dist, C, REPLAYS, label):
+    """C calls of all R ranks captured once (every call with its own input and
+    output buffers, ranks on forked streams), replayed REPLAYS times with fresh
+    inputs each replay; every call of every replay compared with the oracle,
+    bit for bit, on every rank (C * REPLAYS calls)."""
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    h = _handle(R, dtype, n, slots)
+    streams = rank_streams(R)
+    ins = torch.empty((C, R, n), dtype=tdt, device="cuda")
+    outs = torch.empty((C, R, n), dtype=tdt, device="cuda")
+    g = capture(h, "allreduce", [[ins[c, r] for r in range(R)] for c in range(C)],
+                [[outs[c, r] for r in range(R)] for c in range(C)], streams)
+    for rep in range(REPLAYS):
+        xs_all = generate(inputs.allreduce_inputs, [(config, R, n, dtype, dist, rep * C + c) for c in range(C)])
+        host = np.stack([np.stack(xs) for xs in xs_all]).view(np.int16)
+        ins.copy_(torch.from_numpy(host).view(tdt))
+        outs.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        h.check()
+        want = generate(lambda xs: oracle.allreduce(xs, dtype, ranks=[0])[0], [(xs,) for xs in xs_all])
+        got = to_bits(outs)
+        for c in range(C):
+            if not np.array_equal(got[c], np.broadcast_to(want[c], (R, n))):
+                for r in range(R):
+                    assert_bits_equal(got[c, r], want[c], dtype, f"{label} replay {rep} call {c} rank {r}")
+    del g
+    h.destroy()
+    return C * REPLAYS
+
+
 def test_config2_graph_1000_calls_double_buffered():
     """Workload 2: R=2 fp16 N=131072 pinned-host; a graph of 100 calls, each
     with its own input and output buffers, replayed 10 times with the inputs
-    refilled between replays (1000 calls, both parities see different data)."""
-    R, n, C, REPLAYS = 2, 131072, 100, 10
-    h = _handle(R, "f16", n, "pinned")
-    streams = rank_streams(R)
-    ins = [[torch.empty(n, dtype=torch.float16, device="cuda") for _ in range(R)] for _ in range(C)]
-    outs = [[torch.empty(n, dtype=torch.float16, device="cuda") for _ in range(R)] for _ in range(C)]
-    g = capture(h, "allreduce", ins, outs, streams)
-    for rep in range(REPLAYS):
-        xs_all = []
-        for c in range(C):
-            xs = inputs.allreduce_inputs(2, R, n, "f16", "normal4", rep * C + c)
-            for r in range(R):
-                ins[c][r].copy_(to_dev(xs[r], "f16"))
-            xs_all.append(xs)
-        g.replay()
-        torch.cuda.synchronize()
-        h.check()
-        for c in (0, 1, C // 2, C - 2, C - 1) if rep < REPLAYS - 1 else range(C):
-            want = oracle.allreduce(xs_all[c], "f16", ranks=[0])[0]
-            for r in range(R):
-                assert_bits_equal(to_bits(outs[c][r]), want, "f16", f"replay {rep} call {c} rank {r}")
-    del g
-    h.destroy()
+    refilled between replays: 1000 calls, every one of them compared with the
+    oracle on both ranks (both parities see different data)."""
+    assert _graph_run(2, "f16", 131072, "pinned", 2, "normal4", 100, 10, "config 2") == 1000
 
 
-def test_config3_r8_bf16_hbm_graph():
-    """Workload 3: R=8, bf16, N=393216, HBM slots, graph-replayed calls."""
-    R, n, C, REPLAYS = 8, 393216, 10, 4
-    h = _handle(R, "bf16", n, "hbm")
-    streams = rank_streams(R)
-    ins = [[torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(R)] for _ in range(C)]
-    outs = [[torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(R)] for _ in range(C)]
-    g = capture(h, "allreduce", ins, outs, streams)
-    for rep in range(REPLAYS):
-        xs_all = []
-        for c in range(C):
-            xs = inputs.allreduce_inputs(3, R, n, "bf16", "normal", rep * C + c)
-            for r in range(R):
-                ins[c][r].copy_(to_dev(xs[r], "bf16"))
-            xs_all.append(xs)
-        g.replay()
-        torch.cuda.synchronize()
-        h.check()
-        for c in range(C):
-            want = oracle.allreduce(xs_all[c], "bf16", ranks=[0])[0]
-            for r in range(R):
-                assert_bits_equal(to_bits(outs[c][r]), want, "bf16", f"replay {rep} call {c} rank {r}")
-    del g
-    h.destroy()
+def test_config3_r8_bf16_hbm_graph_1000_calls():
+    """Workload 3: R=8, bf16, N=393216, HBM slots; a graph of 100 calls
+    replayed 10 times with fresh inputs each replay: 1000 calls, every one
+    compared with the oracle on all eight ranks."""
+    assert _graph_run(8, "bf16", 393216, "hbm", 3, "normal", 100, 10, "config 3") == 1000
 
 
 @pytest.mark.parametrize("algo", ["oneshot", "twoshot"])
