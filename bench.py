@@ -56,13 +56,18 @@ def parse():
     ap.add_argument("--sweep-slots", default="hbm,pinned")
     ap.add_argument("--sweep-dtypes", default="f16,bf16")
     ap.add_argument("--sweep-ranks", default="2,4,8")
-    ap.add_argument("--sweep-algo", default=None, choices=["oneshot", "twoshot", "tagged"],
+    ap.add_argument("--sweep-algo", default=None, choices=["oneshot", "twoshot", "tagged", "cluster"],
                     help="in the sweep, force this all-reduce form in every cell")
     ap.add_argument("--sweep-fused", action="store_true",
-                    help="in the sweep, run every call as one cooperative launch of all ranks (ar_allreduce_fused)")
+                    help="in the sweep, run every call as one launch of all ranks (ar_allreduce_fused)")
+    ap.add_argument("--sweep-launch", default=None, choices=["rank", "fused", "all"],
+                    help="in the sweep, the launch form (default rank, or fused with --sweep-fused)")
+    ap.add_argument("--sweep-tactics", default=None, help="in the sweep, ar_tactics fields to set (JSON object)")
     ap.add_argument("--sweep-min-kib", type=int, default=2)
     ap.add_argument("--sweep-max-kib", type=int, default=65536)
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
+    ap.add_argument("--only", default=None,
+                    help="comma-separated workload names: time only these (no headline, no JSON contract line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--trace", default=None, help="trace the main workloads with ar_set_trace; write a summary here")
     ap.add_argument("--profile", default=None, choices=sorted(PROFILE_WORKLOADS),
@@ -241,20 +246,31 @@ def measured_peaks():
 class Workload:
     """R ranks, C calls, one graph; every call has its own device buffers."""
 
-    def __init__(self, op, R, dtype, numel, slots, calls, config, dist="uniform", algo=None, fused=False):
+    def __init__(self, op, R, dtype, numel, slots, calls, config, dist="uniform", algo=None, fused=False,
+                 launch=None, tactics=None):
         import torch
         import tensor_decode_all_gb300 as tda
-        from tensor_decode_all_gb300 import inputs
+        from tensor_decode_all_gb300 import ar, inputs
         self.torch = torch
         self.op, self.R, self.dtype, self.numel, self.slots, self.C = op, R, dtype, numel, slots, calls
-        self.fused = fused  # one cooperative launch for all ranks of a call, instead of R launches
+        # "rank": one launch per rank per call (ar_allreduce / ar_allgather on R streams);
+        # "fused": one launch of every rank per call (ar_*_fused on one stream);
+        # "all": ar_allreduce_all on the R streams (fused or not by the handle's tactic)
+        self.launch = launch or ("fused" if fused else "rank")
+        self.fused = self.launch == "fused"
         tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "c64": torch.complex64}[dtype]
         self.tdt = tdt
         self.h = tda.Handle(R, tdt, numel, slots)
         if algo:
             self.h.set_algo(algo)
-        self.algo = "allgather" if op == "allgather" else \
-            {0: "oneshot", 1: "twoshot", 2: "tagged"}[self.h.plan("allreduce", numel).algo]
+        if tactics:
+            self.h.set_tactics(**tactics)
+        if op == "allgather":
+            self.algo = "allgather"
+        else:
+            one_launch = self.launch == "fused" or (self.launch == "all" and self.h.tactics()["all_fused"])
+            p = self.h.plan("allreduce_fused" if one_launch else "allreduce", numel)
+            self.algo = ar.ALGO_NAMES[p.algo] + (f"/sub{p.subtile_vecs}" if p.algo == 3 and p.subtile_vecs else "")
         self.streams = [torch.cuda.Stream() for _ in range(R)]
         out_n = numel * (R if op == "allgather" else 1)
         # inputs [C][numel] per rank, contiguous, so one copy moves a whole step
@@ -283,10 +299,18 @@ class Workload:
         with torch.cuda.stream(side):
             with torch.cuda.graph(g, stream=side):
                 cap = torch.cuda.current_stream()
-                if self.fused:
+                if self.launch == "fused":
                     for c in range(self.C):
                         getattr(self.h, self.op + "_fused")([self.ins[r][c] for r in range(self.R)],
                                                             [self.outs[r][c] for r in range(self.R)], cap)
+                elif self.launch == "all":
+                    for s in self.streams:
+                        s.wait_stream(cap)
+                    for c in range(self.C):
+                        self.h.allreduce_all([self.ins[r][c] for r in range(self.R)],
+                                             [self.outs[r][c] for r in range(self.R)], self.streams)
+                    for s in self.streams:
+                        cap.wait_stream(s)
                 else:
                     for s in self.streams:
                         s.wait_stream(cap)
@@ -610,6 +634,116 @@ def cpu_baseline(R, dtype, numel, seconds=8.0, config=2, dist="normal4"):
                       f"outputs) in {dt:.1f} s on {cores} threads; then {calls1} calls in {dt1:.1f} s on one"}
 
 
+LAUNCH_NAMES = {"rank": "one launch per rank per call (R non-blocking streams)",
+                "fused": "one launch of every rank per call (ar_*_fused, one stream)",
+                "all": "ar_allreduce_all on the R streams (one launch of every rank per call by default)"}
+
+# name: (op, R, dtype, numel, slots, input config, distribution, calls per graph, timed steps[, options])
+# options: algo (forced form), launch ("rank" | "fused" | "all"), tactics (ar_tactics fields).
+# Workload 3 first: it is what the summary at the end of the line leads with.
+EXTRA_WORKLOADS = {
+    # workload 3 (R=8 bf16 48 x 8192, HBM slots), graphs of 100 calls and of one call
+    "r8_bf16_393216_hbm": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20),
+    "r8_bf16_393216_hbm_all": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20, {"launch": "all"}),
+    "r8_bf16_393216_hbm_fused_flags": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20,
+                                       {"launch": "fused", "tactics": {"cluster_max_bytes": 0}}),
+    "r8_bf16_393216_hbm_fused": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20, {"launch": "fused"}),
+    "r8_bf16_393216_hbm_graph1": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 1, 200),
+    "r8_bf16_393216_hbm_fused_graph1": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 1, 200,
+                                        {"launch": "fused"}),
+    "r8_bf16_393216_hbm_all_graph1": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 1, 200,
+                                      {"launch": "all"}),
+    # workload 1 (one decode token) and the headline shape through the other launch forms
+    "r2_fp16_4096_pinned": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", 100, 20),
+    "r2_fp16_4096_pinned_all": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", 100, 20, {"launch": "all"}),
+    "r2_fp16_131072_pinned_all": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 100, 20,
+                                  {"launch": "all"}),
+    "r2_fp16_131072_pinned_fused_flags": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 100, 20,
+                                          {"launch": "fused", "tactics": {"cluster_max_bytes": 0}}),
+    "r2_fp16_131072_pinned_graph1": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 1, 200),
+    "r2_fp16_131072_pinned_all_graph1": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 1, 200,
+                                         {"launch": "all"}),
+    # large payloads in HBM (the HBM roofline)
+    "r8_bf16_16MiB_hbm": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 10, 10),
+    "r8_bf16_16MiB_hbm_oneshot": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 10, 10, {"algo": "oneshot"}),
+    "r8_bf16_16MiB_hbm_all": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 10, 10, {"launch": "all"}),
+    "r8_bf16_64MiB_hbm": ("allreduce", 8, "bf16", 32 << 20, "hbm", 5, "uniform", 4, 10),
+    "r2_fp16_16MiB_hbm": ("allreduce", 2, "f16", 8 << 20, "hbm", 5, "uniform", 10, 10),
+    # workload 4: complex64 allgather of 1000 x 500 shards
+    "allgather_c64_r4_hbm": ("allgather", 4, "c64", 500000, "hbm", 4, None, 20, 10),
+    "allgather_c64_r8_hbm": ("allgather", 8, "c64", 500000, "hbm", 4, None, 20, 10),
+    "allgather_c64_r8_hbm_fused": ("allgather", 8, "c64", 500000, "hbm", 4, None, 20, 10, {"launch": "fused"}),
+    "allgather_c64_r4_pinned": ("allgather", 4, "c64", 500000, "pinned", 4, None, 5, 5),
+    "allgather_c64_r8_pinned": ("allgather", 8, "c64", 500000, "pinned", 4, None, 5, 5),
+}
+
+
+# Comparisons for --only (not part of the default line).
+EXPERIMENT_WORKLOADS = {
+    "x_r8_768K_fused_nopdl": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20,
+                              {"launch": "fused", "pdl": False}),
+    "x_r8_768K_all_nopdl": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20,
+                            {"launch": "all", "pdl": False}),
+    "x_r8_768K_all_rank": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20,
+                           {"launch": "all", "tactics": {"all_fused": 0}}),
+    "x_r8_16MiB_fused": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 10, 10, {"launch": "fused"}),
+    "x_r8_16MiB_fused_flags": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 10, 10,
+                               {"launch": "fused", "tactics": {"cluster_max_bytes": 0}}),
+    "x_r2_256K_pinned_fused": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 100, 20, {"launch": "fused"}),
+    "x_r2_8K_pinned_fused": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", 100, 20, {"launch": "fused"}),
+    "x_r2_8K_hbm_fused": ("allreduce", 2, "f16", 4096, "hbm", 1, "uniform", 100, 20, {"launch": "fused"}),
+    "x_r2_8K_hbm": ("allreduce", 2, "f16", 4096, "hbm", 1, "uniform", 100, 20),
+    "x_r8_1M_fused": ("allreduce", 8, "bf16", 1 << 19, "hbm", 5, "uniform", 100, 20, {"launch": "fused"}),
+    "x_r8_1M": ("allreduce", 8, "bf16", 1 << 19, "hbm", 5, "uniform", 100, 20),
+}
+
+
+def workloads_summary(extras):
+    """One short entry per workload: us/call, algbw GB/s, roofline fraction
+    (and the DRAM-counter fraction where a capture is valid), form, launch."""
+    out = {}
+    for name, row in extras.items():
+        rf = row["roofline"]
+        e = {"us": row["us_per_call"], "gbs": row["algbw_gbs"], "frac": rf["frac"], "form": row["algo"],
+             "launch": row["launch"].split(" (")[0]}
+        if rf.get("dram_frac") is not None:
+            e["dram_frac"] = rf["dram_frac"]
+        out[name] = e
+    return out
+
+
+def run_only(args, dist):
+    """Time only the named workloads (EXTRA_WORKLOADS names) and print one
+    summary line each: for comparing forms, not the bench contract."""
+    import torch
+    import tensor_decode_all_gb300 as tda
+    torch.cuda.set_device(0)
+    tda.build()
+    peaks = measured_peaks()
+    hbm_gbs = float(peaks.get("hbm_gbs", 6800.0))
+    link = tda.ar_probe_host_link(64 << 20, 10)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    for name in args.only.split(","):
+        spec = EXTRA_WORKLOADS.get(name) or EXPERIMENT_WORKLOADS[name]
+        op, RR, dt, nn, sl, cfg, dd, cc, st = spec[:9]
+        opts = spec[9] if len(spec) > 9 else {}
+        wx = Workload(op, RR, dt, nn, sl, cc, config=cfg, dist=dd or "uniform", algo=opts.get("algo"),
+                      launch=opts.get("launch", "rank"), tactics=opts.get("tactics"))
+        if "pdl" in opts:
+            wx.h.set_pdl(opts["pdl"])
+        wx.capture()
+        wx.time_graph(1, 0, flush)
+        wx.check(calls=(0, -1))
+        msx = wx.time_graph(max(st, args.steps), 2, flush)
+        wx.check(calls=(-1,))
+        row = summarize(op, RR, dt, nn, sl, msx, cc, link, hbm_gbs, wx.algo)
+        print(json.dumps({"workload": name, "us": row["us_per_call"], "gbs": row["algbw_gbs"],
+                          "frac": row["roofline"]["frac"], "form": row["algo"], "launch": wx.launch,
+                          "cluster_max": wx.h.info().cluster_form}), flush=True)
+        wx.close()
+    return None
+
+
 def run_ours(args, dist):
     import torch
     import tensor_decode_all_gb300 as tda
@@ -657,39 +791,18 @@ def run_ours(args, dist):
 
     extras = {}
     if not args.no_extras:
-        for name, (op, RR, dt, nn, sl, cfg, dd, cc, st, al) in {
-            "r2_fp16_4096_pinned": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", 100, 20, None),
-            "r8_bf16_393216_hbm": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20, None),
-            "r8_bf16_16MiB_hbm": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 10, 10, None),
-            "r8_bf16_16MiB_hbm_oneshot": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 10, 10, "oneshot"),
-            "r8_bf16_64MiB_hbm": ("allreduce", 8, "bf16", 32 << 20, "hbm", 5, "uniform", 4, 10, None),
-            "r2_fp16_16MiB_hbm": ("allreduce", 2, "f16", 8 << 20, "hbm", 5, "uniform", 10, 10, None),
-            "allgather_c64_r4_hbm": ("allgather", 4, "c64", 500000, "hbm", 4, None, 20, 10, None),
-            "allgather_c64_r8_hbm": ("allgather", 8, "c64", 500000, "hbm", 4, None, 20, 10, None),
-            "allgather_c64_r4_pinned": ("allgather", 4, "c64", 500000, "pinned", 4, None, 5, 5, None),
-            "allgather_c64_r8_pinned": ("allgather", 8, "c64", 500000, "pinned", 4, None, 5, 5, None),
-            # the same calls as one cooperative launch of all ranks (ar_*_fused)
-            "r2_fp16_4096_pinned_fused": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", 100, 20, None),
-            "r2_fp16_131072_pinned_fused": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 100, 20, None),
-            "r8_bf16_393216_hbm_fused": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20, None),
-            "r8_bf16_16MiB_hbm_fused": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 10, 10, None),
-            "allgather_c64_r8_hbm_fused": ("allgather", 8, "c64", 500000, "hbm", 4, None, 20, 10, None),
-            # one call per graph replay: the graph-launch overhead included
-            "r2_fp16_131072_pinned_graph1": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 1, 200, None),
-            "r8_bf16_393216_hbm_graph1": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 1, 200, None),
-            "r2_fp16_131072_pinned_graph1_fused": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 1, 200,
-                                                   None),
-            "r8_bf16_393216_hbm_graph1_fused": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 1, 200, None),
-        }.items():
-            fz = name.endswith("_fused")
-            wx = Workload(op, RR, dt, nn, sl, cc, config=cfg, dist=dd or "uniform", algo=al, fused=fz)
+        for name, spec in EXTRA_WORKLOADS.items():
+            op, RR, dt, nn, sl, cfg, dd, cc, st = spec[:9]
+            opts = spec[9] if len(spec) > 9 else {}
+            wx = Workload(op, RR, dt, nn, sl, cc, config=cfg, dist=dd or "uniform", algo=opts.get("algo"),
+                          launch=opts.get("launch", "rank"), tactics=opts.get("tactics"))
             wx.capture()
             wx.time_graph(1, 0, flush)
             wx.check(calls=(0, -1))
             msx = wx.time_graph(st, 2, flush)
             wx.check(calls=(-1,))
             extras[name] = summarize(op, RR, dt, nn, sl, msx, cc, link, hbm_gbs, wx.algo)
-            extras[name]["launch"] = "one cooperative launch per call" if fz else "one launch per rank per call"
+            extras[name]["launch"] = LAUNCH_NAMES[wx.launch]
             attach_traffic(extras[name], profiled_traffic(name), extras[name]["us_per_call"] * 1e-6, hbm_gbs)
             wx.close()
 
@@ -722,6 +835,8 @@ def run_ours(args, dist):
     }
     if dist.rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(R, "f16", numel)
+    # last, so that it survives in the end of the output a log keeps
+    line["workloads_summary"] = workloads_summary(extras)
     return line
 
 
@@ -736,6 +851,10 @@ PROFILE_WORKLOADS = {
     "allgather_c64_r8_hbm_1call": ("allgather", 8, "c64", 500000, "hbm", 4, "normal", 1),
     "r8_bf16_768KiB_hbm_fused_1call": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 1),
     "r2_fp16_8KiB_pinned_1call": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", 1),
+    "r8_bf16_768KiB_hbm_all": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100),
+    "r8_bf16_768KiB_hbm_all_1call": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 1),
+    "r2_fp16_256KiB_pinned_all_1call": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 1),
+    "r8_bf16_16MiB_hbm_all_1call": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 1),
 }
 
 
@@ -748,8 +867,9 @@ def run_profile(args, dist):
     tda.build()
     op, R, dt, n, sl, cfg, dd, C = PROFILE_WORKLOADS[args.profile]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    launch = "all" if "_all" in args.profile else "fused" if "fused" in args.profile else "rank"
     w = Workload(op, R, dt, n, sl, C, config=cfg, dist=dd, algo="oneshot" if "oneshot" in args.profile else None,
-                 fused="fused" in args.profile)
+                 launch=launch)
     w.capture()
     ms = w.time_graph(args.steps, args.warmup, flush)
     w.check(calls=(0, -1))
@@ -763,7 +883,9 @@ TRACE_WORKLOADS = {
     "config 2: R=2 fp16 256 KiB pinned": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", False),
     "config 1: R=2 fp16 8 KiB pinned": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", False),
     "config 3: R=8 bf16 768 KiB HBM": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", False),
-    "config 3, one cooperative launch": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", True),
+    "config 3, one cooperative launch (flag form)": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", "flags"),
+    "config 3, ar_allreduce_all (cluster form)": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", "all"),
+    "config 2, ar_allreduce_all (cluster form)": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", "all"),
 }
 
 
@@ -786,9 +908,10 @@ def run_trace(args, dist):
     tda.build()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     out = {}
-    for name, (op, R, dt, n, sl, cfg, dd, fused) in TRACE_WORKLOADS.items():
+    for name, (op, R, dt, n, sl, cfg, dd, mode) in TRACE_WORKLOADS.items():
         C = 100
-        w = Workload(op, R, dt, n, sl, C, config=cfg, dist=dd, fused=fused)
+        w = Workload(op, R, dt, n, sl, C, config=cfg, dist=dd, launch="fused" if mode == "flags" else mode or "rank",
+                     tactics={"cluster_max_bytes": 0} if mode == "flags" else None)
         buf = trace.start(w.h, C)
         w.capture()
         w.time_graph(3, 0, flush)
@@ -876,7 +999,8 @@ def run_sweep(args, dist):
             C = max(4, min(100, (256 << 20) // max(1, R * S * 2)))
             steps = max(1, total // C)
             w = Workload("allreduce", R, dtype, numel, slots, C, config=5, dist="uniform", algo=algo,
-                         fused=args.sweep_fused)
+                         launch=args.sweep_launch or ("fused" if args.sweep_fused else "rank"),
+                         tactics=json.loads(args.sweep_tactics) if args.sweep_tactics else None)
             w.capture()
             w.time_graph(1, 0, flush)
             w.check(calls=(0, -1))
@@ -884,7 +1008,8 @@ def run_sweep(args, dist):
             w.check(calls=(0, -1))
             row = summarize("allreduce", R, dtype, numel, slots, ms, C, link, hbm_gbs, w.algo)
             row["parity"] = "bit-exact (first and last call)"
-            row["launch"] = "fused" if args.sweep_fused else "per rank"
+            row["launch"] = w.launch
+            row["tactics"] = args.sweep_tactics
             row["host_link_probe_gbs"] = {k: round(v, 2) for k, v in link.items()}
             f.write(json.dumps(row) + "\n")
             f.flush()
@@ -906,6 +1031,8 @@ def main():
             line = run_trace(args, dist)
         elif args.sweep:
             line = run_sweep(args, dist)
+        elif args.only:
+            line = run_only(args, dist)
         else:
             line = run_ours(args, dist)
         if line is not None and dist.rank == 0:

@@ -107,8 +107,15 @@ enum ar_code {
  *   calls of one tile (4 KiB) per block, up to ar_info.tagged_capacity_bytes
  *   per rank (larger calls take the one-shot form).  Not part of the pages'
  *   design.
+ * AR_ALGO_CLUSTER: for calls that launch every rank at once (ar_allreduce_fused,
+ *   ar_allreduce_all) only: block b of every rank forms one thread-block cluster
+ *   and the hardware cluster barrier (arrive with release, wait with acquire)
+ *   takes the place of the per-block flags; the data moves through the same
+ *   slots, one-shot or two-shot by size (ar_tactics.cluster_twoshot_min_bytes).
+ *   Valid because the ranks are logical ranks on one GPU; per-rank calls on a
+ *   handle set to it take the AR_ALGO_AUTO rule.  Not part of the pages' design.
  * AR_ALGO_AUTO: chosen per call from the handle's tactics (ar_tactics). */
-enum ar_algo { AR_ALGO_AUTO = -1, AR_ALGO_ONESHOT = 0, AR_ALGO_TWOSHOT = 1, AR_ALGO_TAGGED = 2 };
+enum ar_algo { AR_ALGO_AUTO = -1, AR_ALGO_ONESHOT = 0, AR_ALGO_TWOSHOT = 1, AR_ALGO_TAGGED = 2, AR_ALGO_CLUSTER = 3 };
 
 /* Details of the first device-side error recorded in a handle. */
 typedef struct ar_error_info {
@@ -154,7 +161,9 @@ typedef struct ar_info {
     uint64_t tagged_capacity_bytes;  /* largest per-rank call the tagged form takes (one 4 KiB tile per
                                         block of one rank's launch, within the slot; 0: complex64) */
     int32_t blocks_per_sm_tagged;    /* occupancy of the tagged-form kernels */
-    int32_t reserved;
+    int32_t cluster_form;            /* clusters of R blocks of the cluster form (AR_ALGO_CLUSTER) the GPU
+                                        holds at once (a call launches at most that many); 0: the form
+                                        cannot run here */
 } ar_info;
 
 /* Launch plan of one call, computed on the host (no GPU needed). */
@@ -179,9 +188,16 @@ typedef struct ar_plan {
  * and stored by the caller (the Python package's tune module does both). */
 typedef struct ar_tactics {
     uint64_t twoshot_min_bytes; /* AUTO picks two-shot from this many bytes per rank; UINT64_MAX: never */
-    int32_t twoshot_sub;        /* two-shot sub-tile in vectors: 64, 128 or 256; 0 = the size rule */
+    int32_t twoshot_sub;        /* two-shot sub-tile in vectors (both two-shot forms): 64, 128 or 256;
+                                   0 = the size rule */
     int32_t max_blocks;         /* cap on blocks per rank (>= 1); 0 = as many as fit (occupancy) */
     uint64_t tagged_max_bytes;  /* AUTO picks the tagged form up to this many bytes per rank; 0: never */
+    uint64_t cluster_twoshot_min_bytes; /* cluster form: two-shot from this many bytes per rank; UINT64_MAX:
+                                           never (one-shot) */
+    uint64_t cluster_max_bytes; /* under AUTO, a launch of every rank at once takes the cluster form up to
+                                   this many bytes per rank, the flag forms above it; 0: never */
+    int32_t all_fused;          /* ar_allreduce_all: 1 = one launch of every rank; 0 = one launch per rank */
+    int32_t reserved;           /* 0 */
 } ar_tactics;
 
 /*
@@ -275,6 +291,29 @@ AR_API int ar_allgather_fused(ar_handle *h, const void *const *ins, void *const 
                               ar_stream_t stream);
 
 /*
+ * ar_allreduce_all -- enqueue one all-reduce call of every rank, rank r's on
+ * streams[r] (a host array of R non-blocking streams, owned by the caller),
+ * for a caller that drives all R logical ranks from one place.  ins[r] /
+ * outs[r] as for ar_allreduce_fused.  The handle's tactic (ar_tactics.all_fused)
+ * decides how: either R per-rank launches, exactly as R ar_allreduce calls, or
+ * one launch of every rank on streams[0], ordered after the work already on
+ * every streams[r] and before the work enqueued on them afterwards (streams[0]
+ * waits for an event recorded on each other stream; each other stream waits
+ * for an event recorded after the launch; the events belong to the handle).
+ * Either way each rank's output is ready on its own stream, with the same
+ * bits.  Graph capture: all R streams in the same capture (forked from it);
+ * a stream whose captured work is already all ahead of streams[0] (nothing
+ * new on it since the previous call's join) adds no edge, so back-to-back
+ * calls keep the programmatic edge between their kernels.
+ * One launch pays a graph's per-kernel launch cost once instead of R times,
+ * which is what a graph replaying one all-reduce is made of.  Errors: as
+ * ar_allreduce_fused; AR_ESTREAM if some of the streams are being captured
+ * and others are not, or two ranks share a stream.
+ */
+AR_API int ar_allreduce_all(ar_handle *h, const void *const *ins, void *const *outs, size_t numel,
+                            const ar_stream_t *streams);
+
+/*
  * ar_status -- the first device-side error recorded in the handle (AR_OK or
  * AR_ETIMEOUT), copied into *info if info is not NULL.  Reads mapped host
  * memory only (no CUDA call); the answer covers the kernels the caller has
@@ -345,8 +384,12 @@ AR_API int ar_debug_seed_stages(ar_handle *h, uint64_t stages);
 AR_API int ar_query(const ar_handle *h, ar_info *info);
 
 /*
- * ar_plan_for -- the launch plan ar_allreduce (op 0) or ar_allgather (op 1)
- * would use for numel elements on this handle.  Pure host arithmetic.
+ * ar_plan_for -- the launch plan ar_allreduce (op 0), ar_allgather (op 1) or a
+ * launch of every rank's all-reduce at once (op 2: ar_allreduce_fused, and
+ * ar_allreduce_all when it fuses) would use for numel elements on this
+ * handle.  For the cluster form, blocks is the number of clusters (each of R
+ * blocks) and flag_rounds the cluster barriers per tile.  Pure host
+ * arithmetic.
  */
 AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan);
 
@@ -386,9 +429,10 @@ AR_API int ar_choose_algo(int R, uint64_t bytes, int slot_kind);
 AR_API int ar_set_pdl(ar_handle *h, int enable);
 
 /* Force the all-reduce form of a handle (AR_ALGO_AUTO restores the rule):
- * AR_ALGO_ONESHOT, AR_ALGO_TWOSHOT or AR_ALGO_TAGGED (the last only for calls
- * of one tile per block; larger calls take the one-shot form).  The
- * environment variable AR_ALGO=oneshot|twoshot|tagged sets it at ar_create.
+ * AR_ALGO_ONESHOT, AR_ALGO_TWOSHOT, AR_ALGO_TAGGED (only for calls of one tile
+ * per block; larger calls take the one-shot form) or AR_ALGO_CLUSTER (only for
+ * launches of every rank at once; per-rank calls take the AUTO rule).  The
+ * environment variable AR_ALGO=oneshot|twoshot|tagged|cluster sets it at ar_create.
  * Every rank of a call must see the same setting; set it before enqueuing.
  * AR_EINVAL for an unknown form, a two-shot / tagged form on a complex64
  * handle, or a call that is half issued (some rank has enqueued more calls on

@@ -20,8 +20,10 @@ from . import builder as _build
 
 AR_F16, AR_BF16, AR_C64 = 1, 2, 3
 AR_SLOT_PINNED_HOST, AR_SLOT_HBM = 0, 1
-AR_ALGO_AUTO, AR_ALGO_ONESHOT, AR_ALGO_TWOSHOT, AR_ALGO_TAGGED = -1, 0, 1, 2
-ALGOS = {"auto": AR_ALGO_AUTO, "oneshot": AR_ALGO_ONESHOT, "twoshot": AR_ALGO_TWOSHOT, "tagged": AR_ALGO_TAGGED}
+AR_ALGO_AUTO, AR_ALGO_ONESHOT, AR_ALGO_TWOSHOT, AR_ALGO_TAGGED, AR_ALGO_CLUSTER = -1, 0, 1, 2, 3
+ALGOS = {"auto": AR_ALGO_AUTO, "oneshot": AR_ALGO_ONESHOT, "twoshot": AR_ALGO_TWOSHOT, "tagged": AR_ALGO_TAGGED,
+         "cluster": AR_ALGO_CLUSTER}
+ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 AR_OK, AR_EINVAL, AR_ETOOBIG, AR_ESTREAM, AR_ENOMEM, AR_ECUDA, AR_ETIMEOUT, AR_ESTATE = range(8)
 CODE_NAMES = {0: "AR_OK", 1: "AR_EINVAL", 2: "AR_ETOOBIG", 3: "AR_ESTREAM", 4: "AR_ENOMEM",
               5: "AR_ECUDA", 6: "AR_ETIMEOUT", 7: "AR_ESTATE"}
@@ -50,12 +52,17 @@ class Info(ctypes.Structure):
                 ("max_numel", ctypes.c_uint64), ("slot_bytes", ctypes.c_uint64),
                 ("total_slot_bytes", ctypes.c_uint64), ("timeout_ns", ctypes.c_uint64),
                 ("tagged_capacity_bytes", ctypes.c_uint64), ("blocks_per_sm_tagged", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("cluster_form", ctypes.c_int32)]
 
 
 class Tactics(ctypes.Structure):
     _fields_ = [("twoshot_min_bytes", ctypes.c_uint64), ("twoshot_sub", ctypes.c_int32),
-                ("max_blocks", ctypes.c_int32), ("tagged_max_bytes", ctypes.c_uint64)]
+                ("max_blocks", ctypes.c_int32), ("tagged_max_bytes", ctypes.c_uint64),
+                ("cluster_twoshot_min_bytes", ctypes.c_uint64), ("cluster_max_bytes", ctypes.c_uint64),
+                ("all_fused", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+TACTIC_FIELDS = [name for name, _ in Tactics._fields_ if name != "reserved"]
 
 
 class Plan(ctypes.Structure):
@@ -117,6 +124,8 @@ def lib():
                 f = getattr(L, name)
                 f.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, vp]
                 f.restype = i32
+            L.ar_allreduce_all.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), sz, ctypes.POINTER(vp)]
+            L.ar_allreduce_all.restype = i32
             L.ar_strerror.argtypes = [i32]
             L.ar_strerror.restype = ctypes.c_char_p
             L.ar_probe_host_link.argtypes = [u64, i32, ctypes.POINTER(ctypes.c_double)]
@@ -197,6 +206,11 @@ def ar_allreduce_fused(h: int, ins, outs, numel: int, stream: int) -> int:
 
 def ar_allgather_fused(h: int, ins, outs, numel: int, stream: int) -> int:
     return lib().ar_allgather_fused(h, _ptr_array(ins), _ptr_array(outs), numel, stream)
+
+
+def ar_allreduce_all(h: int, ins, outs, numel: int, streams) -> int:
+    """Every rank's call, rank r's on streams[r] (R device pointers per side, R stream handles)."""
+    return lib().ar_allreduce_all(h, _ptr_array(ins), _ptr_array(outs), numel, _ptr_array(streams))
 
 
 def ar_status(h: int) -> ErrorInfo:
@@ -349,7 +363,23 @@ class Handle:
             raise ArError(rc, f"ar_allgather(rank={rank})")
 
     def allreduce_all(self, ins, outs, streams) -> None:
-        """Enqueue all R ranks' calls (rank r on streams[r])."""
+        """Enqueue all R ranks' calls, rank r's output ready on streams[r]
+        (ar_allreduce_all: R per-rank launches or one launch of every rank,
+        by the handle's all_fused tactic)."""
+        if len(ins) != self.R or len(outs) != self.R or len(streams) != self.R:
+            raise ValueError(f"ar_allreduce_all: need {self.R} inputs, outputs and streams")
+        for r in range(self.R):
+            if ins[r].numel() != ins[0].numel():
+                raise ValueError(f"ar_allreduce_all: rank {r}'s input has {ins[r].numel()} elements, "
+                                 f"rank 0's {ins[0].numel()}")
+            self._check_tensors("ar_allreduce_all", ins[r], outs[r], 1)
+        rc = ar_allreduce_all(self.ptr, [t.data_ptr() for t in ins], [t.data_ptr() for t in outs], ins[0].numel(),
+                              [_stream_handle(s) for s in streams])
+        if rc:
+            raise ArError(rc, "ar_allreduce_all")
+
+    def allreduce_each(self, ins, outs, streams) -> None:
+        """Enqueue all R ranks' calls as R separate ar_allreduce calls (rank r on streams[r])."""
         for r in range(self.R):
             self.allreduce(r, ins[r], outs[r], streams[r])
 
@@ -397,7 +427,7 @@ class Handle:
             raise ArError(rc, "ar_set_timeout")
 
     def set_algo(self, algo) -> None:
-        """'auto', 'oneshot' or 'twoshot' (or an AR_ALGO_* code)."""
+        """'auto', 'oneshot', 'twoshot', 'tagged' or 'cluster' (or an AR_ALGO_* code)."""
         code = ALGOS[algo] if isinstance(algo, str) else int(algo)
         rc = ar_set_algo(self.ptr, code)
         if rc:
@@ -413,16 +443,17 @@ class Handle:
 
     def tactics(self) -> dict:
         t = ar_get_tactics(self.ptr)
-        return {"twoshot_min_bytes": int(t.twoshot_min_bytes), "twoshot_sub": int(t.twoshot_sub),
-                "max_blocks": int(t.max_blocks), "tagged_max_bytes": int(t.tagged_max_bytes)}
+        return {name: int(getattr(t, name)) for name in TACTIC_FIELDS}
 
-    def set_tactics(self, twoshot_min_bytes=None, twoshot_sub=None, max_blocks=None, tagged_max_bytes=None) -> None:
-        """Replace some or all of the handle's tactics (see ar_tactics in ar.h)."""
+    def set_tactics(self, **changes) -> None:
+        """Replace some or all of the handle's tactics (see ar_tactics in ar.h);
+        keyword names are the struct's fields, None keeps a field."""
+        unknown = set(changes) - set(TACTIC_FIELDS)
+        if unknown:
+            raise TypeError(f"unknown tactics {sorted(unknown)}")
         cur = self.tactics()
-        t = Tactics(int(cur["twoshot_min_bytes"] if twoshot_min_bytes is None else twoshot_min_bytes),
-                    int(cur["twoshot_sub"] if twoshot_sub is None else twoshot_sub),
-                    int(cur["max_blocks"] if max_blocks is None else max_blocks),
-                    int(cur["tagged_max_bytes"] if tagged_max_bytes is None else tagged_max_bytes))
+        cur.update({k: v for k, v in changes.items() if v is not None})
+        t = Tactics(*[int(cur[name]) for name in TACTIC_FIELDS], 0)
         rc = ar_set_tactics(self.ptr, t)
         if rc:
             raise ArError(rc, "ar_set_tactics")
@@ -444,7 +475,9 @@ class Handle:
         return ar_supports(self.ptr, 0 if op == "allreduce" else 1, inp.numel(), inp.data_ptr(), out.data_ptr())
 
     def plan(self, op: str, numel: int) -> Plan:
-        return ar_plan_for(self.ptr, 0 if op == "allreduce" else 1, numel)
+        """op: 'allreduce' (one rank's launch), 'allgather', or 'allreduce_fused'
+        (every rank in one launch)."""
+        return ar_plan_for(self.ptr, {"allreduce": 0, "allgather": 1, "allreduce_fused": 2}[op], numel)
 
     def destroy(self) -> None:
         if self._h:

@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
     pdl_wait();
     if (tid == 0) {
         trace_start<T>(d, s_tr);
-        const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
+        const Ctr c = d.ctr[(size_t)rank * d.cmax + b];
         s_seq = c.seq;
         s_calls = c.calls;
         s_bail = 0;
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
         Ctr c;
         c.seq = seq + nstages;
         c.calls = s_calls + 1;
-        d.ctr[(size_t)rank * d.bmax + b] = c;
+        d.ctr[(size_t)rank * d.cmax + b] = c;
         trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
     }
 }

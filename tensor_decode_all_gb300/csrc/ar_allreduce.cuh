@@ -152,7 +152,7 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
     pdl_wait();
     if (tid == 0) {
         trace_start<T>(d, s_tr);
-        const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
+        const Ctr c = d.ctr[(size_t)rank * d.cmax + b];
         s_seq = c.seq;
         s_calls = c.calls;
         s_bail = 0;
@@ -237,7 +237,7 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
         Ctr c;
         c.seq = seq + nstages;
         c.calls = s_calls + 1;
-        d.ctr[(size_t)rank * d.bmax + b] = c;
+        d.ctr[(size_t)rank * d.cmax + b] = c;
         trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
     }
 }
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
     pdl_wait();
     if (tid == 0) {
         trace_start<T>(d, s_tr);
-        const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
+        const Ctr c = d.ctr[(size_t)rank * d.cmax + b];
         s_seq = c.seq;
         s_calls = c.calls;
         s_bail = 0;
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
         Ctr c;
         c.seq = seq + 2 * nstages;
         c.calls = s_calls + 1;
-        d.ctr[(size_t)rank * d.bmax + b] = c;
+        d.ctr[(size_t)rank * d.cmax + b] = c;
         trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
     }
 }

@@ -55,7 +55,7 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
     pdl_wait();
     if (tid == 0) {
         trace_start<T>(d, s_tr);
-        const Ctr c = d.ctr[(size_t)rank * d.bmax + b];
+        const Ctr c = d.ctr[(size_t)rank * d.cmax + b];
         s_seq = c.seq;
         s_calls = c.calls;
         s_bail = 0;
@@ -168,7 +168,7 @@ __device__ __forceinline__ void allreduce_tagged_body(const uint16_t *in_arg, ui
         Ctr c;
         c.seq = seq + nstages;
         c.calls = s_calls + 1;
-        d.ctr[(size_t)rank * d.bmax + b] = c;
+        d.ctr[(size_t)rank * d.cmax + b] = c;
         trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
     }
 }

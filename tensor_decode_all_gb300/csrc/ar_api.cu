@@ -12,6 +12,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <initializer_list>
 #include <new>
 
 #include "ar_internal.h"
@@ -30,12 +31,20 @@ struct ar_handle {
     // in one launch][untraced / traced kernels][family] (the smallest over
     // the family's variants).
     int bps[2][2][kFamilies] = {};
-    int bmax = 0;                              // flag/counter slots per rank
+    int bmax = 0;                              // flag slots per rank
+    int cmax = 0;                              // counter slots per rank (>= bmax)
     int algo = AR_ALGO_AUTO;
     int twoshot_sub = 0;                       // tactic: two-shot sub-tile (64/128/256); 0 = size rule
     uint64_t twoshot_min_bytes = ~0ull;        // tactic: AUTO picks two-shot from this size per rank
     int max_blocks = 0;                        // tactic: cap on blocks per rank; 0 = occupancy
     uint64_t tagged_max_bytes = 0;             // tactic: AUTO picks the tagged form up to this size
+    uint64_t cluster_twoshot_min_bytes = ~0ull;  // tactic: cluster form is two-shot from this size
+    uint64_t cluster_max_bytes = 0;            // tactic: AUTO runs launches of all ranks in the cluster form up to this size
+    bool all_fused = true;                     // tactic: ar_allreduce_all launches all ranks at once
+    bool cluster_ok = false;                   // the cluster kernels can be scheduled on this GPU
+    int cluster_max = 0;                       // clusters of R blocks of the cluster kernels resident at once
+    cudaEvent_t ev_fork[tda::kMaxRanks] = {};  // ar_allreduce_all: stream r > 0 -> stream 0
+    cudaEvent_t ev_join = nullptr;             // ar_allreduce_all: stream 0 -> streams r > 0
     void *ll_host = nullptr;                   // pinned kind: host address of the tagged buffers
     ulonglong2 *ll_dev = nullptr;              // [2][R][ll_vecs]
     uint64_t ll_vecs = 0, ll_bytes = 0;
@@ -122,6 +131,7 @@ DevState dev_state(const ar_handle *h) {
     d.slot_bytes = h->slot_bytes;
     d.timeout_ns = h->timeout_ns.load(std::memory_order_relaxed);
     d.bmax = h->bmax;
+    d.cmax = h->cmax;
     d.sys_scope = h->kind == AR_SLOT_PINNED_HOST ? 1 : 0;
     d.ll = h->ll_dev;
     d.ll_vecs = h->ll_vecs;
@@ -140,7 +150,12 @@ void free_all(ar_handle *h) {
     else if (h->ll_dev) cudaFree(h->ll_dev);
     if (h->ctr) cudaFree(h->ctr);
     if (h->err_host) cudaFreeHost(h->err_host);
+    for (auto &e : h->ev_fork)
+        if (e) cudaEventDestroy(e);
+    if (h->ev_join) cudaEventDestroy(h->ev_join);
     (void)cudaGetLastError();
+    for (auto &e : h->ev_fork) e = nullptr;
+    h->ev_join = nullptr;
     h->slots_host = nullptr;
     h->slots_dev = nullptr;
     h->flags_host = nullptr;
@@ -219,6 +234,48 @@ int handle_occupancy(ar_handle *h) {
     return rc;
 }
 
+// The cluster form's kernels: load every variant into the context now (no
+// lazy loading during a capture), and check that a cluster of R blocks of the
+// largest variant can be scheduled at all.  A GPU or build without cluster
+// launches leaves the handle on the flag forms (cluster_ok false).
+int cluster_setup(ar_handle *h) {
+    h->cluster_ok = false;
+    if (h->dtype != AR_F16 && h->dtype != AR_BF16) return AR_OK;
+    for (int traced = 0; traced < 2; ++traced)
+        for (int sub : {0, 64, 128, 256}) {
+            const void *k = tda::allreduce_cluster_kernel_ptr(h->dtype, h->R, sub, traced != 0);
+            cudaFuncAttributes attr;
+            if (!k || cudaFuncGetAttributes(&attr, k) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return AR_OK;
+            }
+        }
+    int fit = 1 << 30;
+    for (int sub : {0, 64, 128, 256}) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, (unsigned)h->R);
+        cfg.blockDim = dim3(tda::kThreads);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = (unsigned)h->R;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, tda::allreduce_cluster_kernel_ptr(h->dtype, h->R, sub, false), &cfg) !=
+                cudaSuccess ||
+            n < 1) {
+            (void)cudaGetLastError();
+            return AR_OK;
+        }
+        fit = n < fit ? n : fit;
+    }
+    h->cluster_ok = true;
+    h->cluster_max = fit;
+    return AR_OK;
+}
+
 // Measured on a GB300 (one-shot vs two-shot, bf16, 64 KiB..8 MiB per rank):
 // in HBM two-shot wins from 512 KiB at R = 8 and from about 2 MiB at R = 4;
 // over the host link, where one-shot reads R(R-1)S bytes against two-shot's
@@ -245,6 +302,67 @@ uint64_t tagged_threshold(int R, int slot_kind) {
     return R == 4 ? (64ull << 10) : 0;
 }
 
+// Cluster form (launches of all ranks at once): two-shot from this size per
+// rank.  Measured on a GB300 (bf16, graphs of calls, one-shot / two-shot
+// cluster form, us/call): at R = 2 one-shot wins everywhere (HBM 16 MiB 23.8 /
+// 33.0, pinned 256 KiB 7.1 / 9.4); in HBM two-shot wins from 1 MiB at R = 4
+// (5.5 / 6.8; 512 KiB 4.2 / 5.2) and from 512 KiB at R = 8 (6.9 / 7.9; 256 KiB
+// 4.6 / 5.8); over the host link from 64 KiB at R = 4 (7.4 / 7.6) and 32 KiB
+// at R = 8 (10.4 / 12.2).  R = 3 takes R = 4's size, R = 5..7 R = 8's.
+uint64_t cluster_twoshot_threshold(int R, int slot_kind) {
+    if (R < 3) return ~0ull;
+    if (slot_kind == AR_SLOT_PINNED_HOST) return R >= 5 ? (32ull << 10) : (64ull << 10);
+    return R >= 5 ? (512ull << 10) : (1ull << 20);
+}
+
+// Largest call (bytes per rank) that AUTO runs in the cluster form when all
+// ranks launch at once; larger calls take the flag forms, whose grids keep
+// more blocks resident than clusters of R blocks can.  Measured on a GB300
+// (bf16, graphs of calls; cluster form / the flag forms in the same single
+// launch, us/call): in HBM the cluster form wins up to 4 MiB at R = 2 (7.9 /
+// 8.6; 8 MiB 13.2 / 13.0), up to 8 MiB at R = 4 (26.2 / 29.3; 16 MiB 50.6 /
+// 48.3) and, at R = 8, as long as one stage of 64-vector sub-tiles covers the
+// call (896 KiB: 768 KiB 6.7 / 8.6; 1 MiB 12.6 / 9.7); over the host link at
+// every size at R = 2 (16 MiB 226 / 247), up to 512 KiB at R = 4 (32.3 /
+// 34.0) and up to 4 MiB at R = 8 (398 / 430).  R = 3 takes R = 4's limit,
+// R = 5..7 R = 8's.
+uint64_t cluster_limit(int R, int slot_kind) {
+    if (slot_kind == AR_SLOT_PINNED_HOST) return R <= 2 ? ~0ull : R <= 4 ? (512ull << 10) : (4ull << 20);
+    return R <= 2 ? (4ull << 20) : R <= 4 ? (8ull << 20) : (896ull << 10);
+}
+
+// Under stream capture, true if a dependency edge from stream `sr` into the
+// next node of stream `s0` would add nothing: every node `sr` depends on is
+// already a dependency of `s0`.  In a chain of ar_allreduce_all calls that is
+// the case (after a call's join both depend on that call's kernel), and
+// skipping the redundant edge leaves the next launch with the single
+// programmatic edge from the previous kernel on s0.  Any query failure
+// answers false (keep the edge).
+bool fork_redundant(cudaStream_t s0, cudaStream_t sr) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    const cudaGraphNode_t *d = nullptr;
+    const cudaGraphEdgeData *ed = nullptr;
+    size_t n0 = 0, nr = 0;
+    if (cudaStreamGetCaptureInfo(s0, &st, nullptr, nullptr, &d, &ed, &n0) != cudaSuccess ||
+        st != cudaStreamCaptureStatusActive || n0 > 64) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    cudaGraphNode_t deps0[64];
+    for (size_t i = 0; i < n0; ++i) deps0[i] = d[i];
+    if (cudaStreamGetCaptureInfo(sr, &st, nullptr, nullptr, &d, &ed, &nr) != cudaSuccess ||
+        st != cudaStreamCaptureStatusActive) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    for (size_t i = 0; i < nr; ++i) {
+        bool found = false;
+        for (size_t j = 0; j < n0 && !found; ++j) found = deps0[j] == d[i];
+        if (!found) return false;
+    }
+    return true;
+}
+
 int choose_algo(int R, uint64_t bytes, int slot_kind) {
     const uint64_t tagged = tagged_threshold(R, slot_kind);
     if (tagged && bytes <= tagged) return AR_ALGO_TAGGED;
@@ -269,7 +387,10 @@ bool tagged_fits(const ar_handle *h, uint64_t bytes, bool fused) {
 // tactics; the tagged form only where it fits (else one-shot).
 int handle_algo(const ar_handle *h, uint64_t bytes, bool fused) {
     if (h->algo == AR_ALGO_TAGGED) return tagged_fits(h, bytes, fused) ? AR_ALGO_TAGGED : AR_ALGO_ONESHOT;
-    if (h->algo != AR_ALGO_AUTO) return h->algo;
+    if (fused && h->cluster_ok &&
+        (h->algo == AR_ALGO_CLUSTER || (h->algo == AR_ALGO_AUTO && bytes <= h->cluster_max_bytes)))
+        return AR_ALGO_CLUSTER;
+    if (h->algo != AR_ALGO_AUTO && h->algo != AR_ALGO_CLUSTER) return h->algo;
     if (h->tagged_max_bytes && bytes <= h->tagged_max_bytes && tagged_fits(h, bytes, fused)) return AR_ALGO_TAGGED;
     return bytes >= h->twoshot_min_bytes ? AR_ALGO_TWOSHOT : AR_ALGO_ONESHOT;
 }
@@ -300,6 +421,66 @@ int twoshot_sub_for(int R, uint64_t nv, uint64_t bmax, int slot_kind) {
 }
 
 int plan_compute_sub(int R, uint64_t bytes, int vec, int algo, int sub, int threads, int sms, int bps, ar_plan *p);
+
+// Cluster form: 0 (one-shot) below the handle's two-shot size, else the
+// handle's two-shot sub-tile tactic if set, else the smallest sub-tile whose
+// tiles still fit one per cluster (at most `grid` clusters), else 256.
+// Measured (R = 8 bf16 768 KiB HBM, one stage per cluster): 64-vector
+// sub-tiles 6.7 us (96 clusters), 128: 6.9 (48), 256: 8.0 (24).
+int cluster_sub_for(int R, uint64_t bytes, uint64_t twoshot_min, uint64_t grid, int forced_sub) {
+    if (bytes < twoshot_min) return 0;
+    if (forced_sub) return forced_sub;
+    const uint64_t nv = (bytes + 15) / 16;
+    for (int sub = 64; sub <= 128; sub *= 2)
+        if ((nv + (uint64_t)R * sub - 1) / ((uint64_t)R * sub) <= grid) return sub;
+    return 256;
+}
+
+// The cluster form's sub-tile for a call of `bytes` per rank on this handle
+// (the target is the blocks per rank the handle launches).
+int handle_blocks(const ar_handle *h, int plan_blocks);
+// The most clusters a call launches: the handle's per-(rank, block) counters
+// and the block cap.  Clusters wait on nothing outside themselves, so a grid
+// of more clusters than the GPU holds at once (ar_info.cluster_form) simply
+// runs in waves -- and small single-stage clusters in waves beat fewer
+// clusters that loop over several stages (R = 8 bf16 768 KiB HBM, bf16: 96
+// clusters of 64-vector sub-tiles 6.7 us; 36 clusters, one wave, 128-vector
+// sub-tiles over two stages: 10.4 us).
+int handle_cluster_grid(const ar_handle *h) {
+    // a traced call writes one record per (rank, block) into [depth][R][bmax]
+    int b = h->trace ? h->bmax : h->cmax;
+    if (h->max_blocks > 0 && b > h->max_blocks) b = h->max_blocks;
+    return b;
+}
+
+int handle_cluster_sub(const ar_handle *h, uint64_t bytes) {
+    return cluster_sub_for(h->R, bytes, h->cluster_twoshot_min_bytes, (uint64_t)handle_cluster_grid(h),
+                           h->twoshot_sub);
+}
+
+// Plan of a cluster-form call: one tile of 256 vectors (one-shot) or R
+// sub-tiles (two-shot) per cluster and stage; as many clusters as tiles, up to
+// the handle's blocks per rank (the clusters wait on nothing outside
+// themselves, so they need not all be resident at once).
+void plan_cluster(int R, uint64_t bytes, int sub, int bmax, ar_plan *p) {
+    // (bmax here: the most clusters a call launches -- the handle's blocks per
+    // rank, within the clusters the GPU holds at once)
+    std::memset(p, 0, sizeof(*p));
+    const uint64_t nv = (bytes + 15) / 16;
+    const uint64_t tile_vecs = sub ? (uint64_t)R * (uint64_t)sub : (uint64_t)tda::kThreads;
+    const uint64_t tiles = (nv + tile_vecs - 1) / tile_vecs;
+    const uint64_t blocks = tiles < (uint64_t)bmax ? tiles : (uint64_t)bmax;
+    p->blocks = (int32_t)blocks;
+    p->threads = tda::kThreads;
+    p->vec_bytes = 16;
+    p->unroll = (int32_t)((tile_vecs + tda::kThreads - 1) / tda::kThreads);
+    p->algo = AR_ALGO_CLUSTER;
+    p->flag_rounds = sub ? 2 : 1;
+    p->subtile_vecs = sub;
+    p->tile_bytes = tile_vecs * 16;
+    p->tiles = tiles;
+    p->max_stages = blocks ? (tiles + blocks - 1) / blocks : 0;
+}
 
 int handle_twoshot_sub(const ar_handle *h, uint64_t bytes) {
     if (h->twoshot_sub) return h->twoshot_sub;
@@ -444,6 +625,20 @@ int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
     const uint64_t bytes = numel * h->itemsize;
     const bool fused = rank < 0;
     const int algo = handle_algo(h, bytes, fused);
+    if (algo == AR_ALGO_CLUSTER) {
+        ar_plan plan;
+        plan_cluster(h->R, bytes, handle_cluster_sub(h, bytes), handle_cluster_grid(h), &plan);
+        const int blocks = plan.blocks;  // within handle_cluster_grid: counters, trace, block cap
+        DevState d = dev_state(h);
+        d.algo = AR_ALGO_CLUSTER;
+        const cudaError_t e =
+            tda::launch_allreduce_cluster(h->dtype, h->R, plan.subtile_vecs, blocks, s, io, numel, d, h->pdl);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return AR_ECUDA;
+        }
+        return AR_OK;
+    }
     const int bps = handle_bps(h, algo, fused);
     ar_plan plan;
     int rc = plan_compute_sub(h->R, bytes, 16, algo, handle_twoshot_sub(h, bytes), tda::kThreads, h->sm_count, bps,
@@ -539,13 +734,22 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
     }
     h->twoshot_min_bytes = twoshot_threshold(R, slot_kind);
     h->tagged_max_bytes = (dtype == AR_F16 || dtype == AR_BF16) ? tagged_threshold(R, slot_kind) : 0;
+    h->cluster_twoshot_min_bytes = cluster_twoshot_threshold(R, slot_kind);
     if (const char *e = std::getenv("AR_ALGO")) {
         if (!std::strcmp(e, "oneshot")) h->algo = AR_ALGO_ONESHOT;
         else if (!std::strcmp(e, "twoshot")) h->algo = AR_ALGO_TWOSHOT;
         else if (!std::strcmp(e, "tagged")) h->algo = AR_ALGO_TAGGED;
+        else if (!std::strcmp(e, "cluster")) h->algo = AR_ALGO_CLUSTER;
     }
     int rc = handle_occupancy(h);
     if (rc != AR_OK) return fail(rc);
+    rc = cluster_setup(h);
+    if (rc != AR_OK) return fail(rc);
+    h->cluster_max_bytes = h->cluster_ok ? cluster_limit(R, slot_kind) : 0;
+    h->all_fused = h->cluster_ok;
+    for (int r = 0; r < R; ++r)
+        if (cudaEventCreateWithFlags(&h->ev_fork[r], cudaEventDisableTiming) != cudaSuccess) return fail(AR_ECUDA);
+    if (cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) return fail(AR_ECUDA);
     // The two-shot kernel fits 6 blocks per SM up to R = 4, which helps in HBM
     // (R=4 bf16 32 MiB: 84 vs 101 us at 4 blocks).
     // Over the host link fewer resident blocks keep the link just as busy with
@@ -565,7 +769,8 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
 
     const uint64_t slots_total = 2ull * (uint64_t)R * h->slot_bytes;
     h->flags_bytes = (uint64_t)R * (uint64_t)h->bmax * tda::kFlagStrideWords * 8ull;
-    h->ctr_bytes = round_up((uint64_t)R * (uint64_t)h->bmax * sizeof(Ctr), 256) + 256;
+    h->cmax = h->bmax > tda::kCounterSlots ? h->bmax : tda::kCounterSlots;
+    h->ctr_bytes = round_up((uint64_t)R * (uint64_t)h->cmax * sizeof(Ctr), 256) + 256;
 
     if (slot_kind == AR_SLOT_PINNED_HOST) {
         const unsigned fl = cudaHostAllocMapped | cudaHostAllocPortable;
@@ -658,6 +863,95 @@ AR_API int ar_allgather_fused(ar_handle *h, const void *const *ins, void *const 
     return end_call(h, -1, enqueue_allgather(h, io, numel, -1, vw, s));
 }
 
+AR_API int ar_allreduce_all(ar_handle *h, const void *const *ins, void *const *outs, size_t numel,
+                            const ar_stream_t *streams) {
+    if (!h || !ins || !outs || !streams) return AR_EINVAL;
+    if (h->dtype != AR_F16 && h->dtype != AR_BF16) return AR_EINVAL;
+    if (numel > h->max_numel) return AR_ETOOBIG;
+    if (numel == 0) return AR_OK;
+    const int R = h->R;
+    cudaStream_t st[tda::kMaxRanks];
+    int capturing = -1;
+    for (int r = 0; r < R; ++r) {
+        if (!ins[r] || !outs[r] || (((uintptr_t)ins[r] | (uintptr_t)outs[r]) % 16)) return AR_EINVAL;
+        st[r] = reinterpret_cast<cudaStream_t>(streams[r]);
+        const int rc = check_stream(st[r]);
+        if (rc != AR_OK) return rc;
+        for (int q = 0; q < r; ++q)
+            if (st[q] == st[r]) return AR_ESTREAM;
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st[r], &cs) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return AR_ESTREAM;
+        }
+        const int c = cs == cudaStreamCaptureStatusActive ? 1 : 0;
+        if (capturing >= 0 && c != capturing) return AR_ESTREAM;
+        capturing = c;
+    }
+    int rc = check_device(h);
+    if (rc != AR_OK) return rc;
+    if (*reinterpret_cast<volatile int32_t *>(&h->err_host->code) != AR_OK) return AR_ESTATE;
+    if (call_half_issued(h)) return AR_EINVAL;
+    if (!h->all_fused) {
+        // R per-rank launches, every argument checked above, so no rank is
+        // declined after another has been enqueued.
+        for (int r = 0; r < R; ++r) {
+            rc = ar_allreduce(h, r, ins[r], outs[r], numel, streams[r]);
+            if (rc != AR_OK) return rc;
+        }
+        return AR_OK;
+    }
+    tda::RankIO io;
+    rc = begin_fused(h, ins, outs, numel, st[0], &io);
+    if (rc != AR_OK) return rc;
+    for (int r = 1; r < R; ++r) {
+        if (capturing == 1 && fork_redundant(st[0], st[r])) continue;
+        if (cudaEventRecord(h->ev_fork[r], st[r]) != cudaSuccess || cudaStreamWaitEvent(st[0], h->ev_fork[r], 0) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return end_call(h, -1, AR_ECUDA);
+        }
+    }
+    rc = end_call(h, -1, enqueue_allreduce(h, io, numel, -1, st[0]));
+    if (rc != AR_OK) return rc;
+    if (capturing == 1 && R > 1) {
+        // Join under capture: every other stream now depends on exactly the
+        // launched kernel.  (An event wait would add the kernel to what the
+        // stream already depended on, and a chain of calls would collect an
+        // edge from every earlier call into every later one.)  Nothing is
+        // lost: whatever the stream depended on before was already a
+        // dependency of the kernel, through the fork or through streams[0].
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        const cudaGraphNode_t *d = nullptr;
+        const cudaGraphEdgeData *ed = nullptr;
+        size_t nd = 0;
+        if (cudaStreamGetCaptureInfo(st[0], &cs, nullptr, nullptr, &d, &ed, &nd) != cudaSuccess ||
+            cs != cudaStreamCaptureStatusActive || nd != 1) {
+            (void)cudaGetLastError();
+            return AR_ECUDA;
+        }
+        cudaGraphNode_t kernel = d[0];
+        for (int r = 1; r < R; ++r) {
+            if (cudaStreamUpdateCaptureDependencies(st[r], &kernel, nullptr, 1, cudaStreamSetCaptureDependencies) !=
+                cudaSuccess) {
+                (void)cudaGetLastError();
+                return AR_ECUDA;
+            }
+        }
+        return AR_OK;
+    }
+    if (R > 1 && cudaEventRecord(h->ev_join, st[0]) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return AR_ECUDA;
+    }
+    for (int r = 1; r < R; ++r) {
+        if (cudaStreamWaitEvent(st[r], h->ev_join, 0) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return AR_ECUDA;
+        }
+    }
+    return AR_OK;
+}
+
 AR_API int ar_status(ar_handle *h, ar_error_info *info) {
     if (!h) return AR_EINVAL;
     const volatile ar_error_info *v = h->err_host;
@@ -721,7 +1015,7 @@ AR_API int ar_query(const ar_handle *h, ar_info *info) {
     const uint64_t tag_bytes = tag_blocks * tda::kThreads * 16ull;
     info->tagged_capacity_bytes = !h->ll_dev ? 0 : (tag_bytes < h->slot_bytes ? tag_bytes : h->slot_bytes);
     info->blocks_per_sm_tagged = h->bps[0][0][kTagged];
-    info->reserved = 0;
+    info->cluster_form = h->cluster_ok ? h->cluster_max : 0;
     return AR_OK;
 }
 
@@ -740,9 +1034,10 @@ AR_API int ar_set_pdl(ar_handle *h, int enable) {
 
 AR_API int ar_set_algo(ar_handle *h, int algo) {
     if (!h || (algo != AR_ALGO_AUTO && algo != AR_ALGO_ONESHOT && algo != AR_ALGO_TWOSHOT &&
-               algo != AR_ALGO_TAGGED))
+               algo != AR_ALGO_TAGGED && algo != AR_ALGO_CLUSTER))
         return AR_EINVAL;
-    if ((algo == AR_ALGO_TWOSHOT || algo == AR_ALGO_TAGGED) && h->dtype == AR_C64) return AR_EINVAL;
+    if ((algo == AR_ALGO_TWOSHOT || algo == AR_ALGO_TAGGED || algo == AR_ALGO_CLUSTER) && h->dtype == AR_C64)
+        return AR_EINVAL;
     if (call_half_issued(h)) return AR_EINVAL;
     h->algo = algo;
     return AR_OK;
@@ -767,7 +1062,7 @@ AR_API int ar_debug_seed_stages(ar_handle *h, uint64_t stages) {
     if (!h) return AR_EINVAL;
     if (check_device(h) != AR_OK) return AR_EINVAL;
     if (cudaDeviceSynchronize() != cudaSuccess) return AR_ECUDA;
-    const size_t n = (size_t)h->R * (size_t)h->bmax;
+    const size_t n = (size_t)h->R * (size_t)h->cmax;
     Ctr *host = new (std::nothrow) Ctr[n];
     if (!host) return AR_ENOMEM;
     int rc = AR_OK;
@@ -787,6 +1082,10 @@ AR_API int ar_get_tactics(const ar_handle *h, ar_tactics *t) {
     t->twoshot_sub = h->twoshot_sub;
     t->max_blocks = h->max_blocks;
     t->tagged_max_bytes = h->tagged_max_bytes;
+    t->cluster_twoshot_min_bytes = h->cluster_twoshot_min_bytes;
+    t->cluster_max_bytes = h->cluster_max_bytes;
+    t->all_fused = h->all_fused ? 1 : 0;
+    t->reserved = 0;
     return AR_OK;
 }
 
@@ -795,10 +1094,14 @@ AR_API int ar_set_tactics(ar_handle *h, const ar_tactics *t) {
     if (t->twoshot_sub != 0 && t->twoshot_sub != 64 && t->twoshot_sub != 128 && t->twoshot_sub != 256)
         return AR_EINVAL;
     if (t->max_blocks < 0 || call_half_issued(h)) return AR_EINVAL;
+    if (t->all_fused != 0 && t->all_fused != 1) return AR_EINVAL;
     h->twoshot_min_bytes = t->twoshot_min_bytes;
     h->twoshot_sub = t->twoshot_sub;
     h->max_blocks = t->max_blocks;
     h->tagged_max_bytes = t->tagged_max_bytes;
+    h->cluster_twoshot_min_bytes = t->cluster_twoshot_min_bytes;
+    h->cluster_max_bytes = t->cluster_max_bytes;
+    h->all_fused = t->all_fused == 1;
     return AR_OK;
 }
 
@@ -812,9 +1115,26 @@ AR_API int ar_supports(const ar_handle *h, int op, size_t numel, const void *in,
 }
 
 AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) {
-    if (!h || !plan || (op != 0 && op != 1)) return AR_EINVAL;
+    if (!h || !plan || op < 0 || op > 2) return AR_EINVAL;
     if (numel > h->max_numel) return AR_ETOOBIG;
     const uint64_t bytes = numel * h->itemsize;
+    if (op == 2) {
+        // all ranks in one launch (ar_allreduce_fused; ar_allreduce_all when it fuses)
+        if (h->dtype != AR_F16 && h->dtype != AR_BF16) return AR_EINVAL;
+        const int algo = handle_algo(h, bytes, true);
+        if (algo == AR_ALGO_CLUSTER) {
+            plan_cluster(h->R, bytes, handle_cluster_sub(h, bytes), handle_cluster_grid(h), plan);
+            return AR_OK;
+        }
+        const int rc = plan_compute_sub(h->R, bytes, 16, algo, handle_twoshot_sub(h, bytes), tda::kThreads,
+                                        h->sm_count, handle_bps(h, algo, true), plan);
+        if (rc != AR_OK) return rc;
+        if (plan->blocks > 0) {
+            plan->blocks = handle_blocks(h, plan->blocks);
+            plan->max_stages = (plan->tiles + plan->blocks - 1) / plan->blocks;
+        }
+        return AR_OK;
+    }
     const int vec = op == 0 ? 16 : allgather_vec(bytes, nullptr, nullptr);
     int algo = AR_ALGO_ONESHOT, bps = h->bps[0][h->trace ? 1 : 0][kAllgather];
     if (op == 0) {
@@ -857,6 +1177,44 @@ cudaError_t launch_allreduce(int dtype, int R, int unroll, int blocks, cudaStrea
     RankIO a5 = io;
     void *args[] = {&a0, &a1, &a2, &a3, &a4, &a5};
     return launch(k, blocks, rank < 0 ? R : 1, rank < 0, s, args, pdl);
+}
+
+const void *allreduce_cluster_kernel_ptr(int dtype, int R, int sub, bool traced) {
+    if (dtype == AR_F16) return allreduce_cluster_kernel_ptr_f16(R, sub, traced);
+    if (dtype == AR_BF16) return allreduce_cluster_kernel_ptr_bf16(R, sub, traced);
+    return nullptr;
+}
+
+cudaError_t launch_allreduce_cluster(int dtype, int R, int sub, int blocks, cudaStream_t s, const RankIO &io,
+                                     uint64_t numel, const DevState &d, bool pdl) {
+    const void *k = allreduce_cluster_kernel_ptr(dtype, R, sub, d.trace != nullptr);
+    if (!k || blocks < 1) return cudaErrorInvalidValue;
+    const uint16_t *a0 = static_cast<const uint16_t *>(io.in[0]);
+    uint16_t *a1 = static_cast<uint16_t *>(io.out[0]);
+    uint64_t a2 = numel;
+    int a3 = -1;
+    DevState a4 = d;
+    RankIO a5 = io;
+    void *args[] = {&a0, &a1, &a2, &a3, &a4, &a5};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, (unsigned)R);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 1;
+    attr[n].val.clusterDim.y = (unsigned)R;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelExC(&cfg, k, args);
 }
 
 cudaError_t launch(const void *k, int blocks, int ranks, bool cooperative, cudaStream_t s, void **args,

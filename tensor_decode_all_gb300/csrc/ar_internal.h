@@ -4,7 +4,7 @@
 //   slots : [2 parities][R ranks][slot_bytes]        pinned host or HBM
 //   flags : [R ranks][bmax blocks] x 128 B lines     same memory as the slots;
 //           word 0 of each line is the flag, a 64-bit count of published stages
-//   ctr   : [R ranks][bmax blocks] x {seq, calls}    HBM; private to one block
+//   ctr   : [R ranks][cmax blocks] x {seq, calls}    HBM; private to one block (cmax >= bmax)
 //   abort : one 32-bit word in HBM, non-zero once any block has given up
 //   err   : one ar_error_info in mapped pinned host memory
 //   ll    : [2 parities][R ranks][ll_vecs] x 16 B   same memory as the slots; the
@@ -22,6 +22,9 @@ constexpr int kMaxRanks = 8;
 constexpr int kThreads = 256;           // threads per block of the exchange kernels (>= 64: see kPollWarp)
 constexpr int kFlagStrideWords = 16;    // 16 x 8 B = one 128-byte line per flag
 constexpr uint64_t kSlotAlign = 256;
+// Counter slots per rank: at least this many, so a cluster-form call can run
+// up to this many single-stage clusters (in waves) whatever the flag grids are.
+constexpr int kCounterSlots = 512;
 // Kernel variant codes for the two-shot form: a negative "unroll" whose
 // magnitude is the sub-tile size in vectors (256, 128 or 64).
 constexpr int twoshot_variant(int sub) { return -sub; }
@@ -47,13 +50,14 @@ struct DevState {
     ar_error_info *err;        // device alias of mapped host memory
     uint64_t slot_bytes;
     uint64_t timeout_ns;
-    int bmax;
+    int bmax;                  // flag slots per rank (the largest grid of a flag-protocol launch)
     int sys_scope;             // 1: slots/flags in host memory, system-scope ordering
     ulonglong2 *ll;            // [2][R][ll_vecs] tagged-word buffers (same memory as the slots)
     uint64_t ll_vecs;          // 16-byte tagged vectors per rank and parity: 2 per 16 payload bytes
     ar_trace_record *trace;    // [depth][R][bmax] or null (tracing off)
     uint32_t trace_depth;
     int32_t algo;              // AR_ALGO_* of this launch, for the trace
+    int cmax;                  // counter slots per rank (>= bmax; cluster-form grids may use them all)
 };
 
 // The input and output pointers of every rank, passed by value to a launch
@@ -90,5 +94,14 @@ const void *allreduce_kernel_ptr_bf16(int R, int unroll, bool fused, bool traced
 const void *allreduce_twoshot_kernel_ptr_f16(int R, int unroll, bool fused, bool traced);   // ..._f16_twoshot.cu
 const void *allreduce_twoshot_kernel_ptr_bf16(int R, int unroll, bool fused, bool traced);  // ..._bf16_twoshot.cu
 const void *allgather_kernel_ptr(int vec_bytes, int R, int unroll, bool fused, bool traced);
+// Cluster-barrier form (all ranks in one launch, clusters of 1 x R blocks):
+// sub = 0 one-shot, 64/128/256 two-shot sub-tile.
+const void *allreduce_cluster_kernel_ptr(int dtype, int R, int sub, bool traced);
+const void *allreduce_cluster_kernel_ptr_f16(int R, int sub, bool traced);   // ar_allreduce_f16_cluster.cu
+const void *allreduce_cluster_kernel_ptr_bf16(int R, int sub, bool traced);  // ar_allreduce_bf16_cluster.cu
+// Launch the cluster form: grid blocks x R, clusters of 1 x R, not cooperative
+// (a cluster waits only on itself).
+cudaError_t launch_allreduce_cluster(int dtype, int R, int sub, int blocks, cudaStream_t s, const RankIO &io,
+                                     uint64_t numel, const DevState &d, bool pdl);
 
 }  // namespace tda

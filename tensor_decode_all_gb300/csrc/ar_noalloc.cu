@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kThreads)
     d.slot_bytes = kNoAllocMaxBytes;
     d.timeout_ns = timeout_ns;
     d.bmax = kNoAllocMaxBlocks;
+    d.cmax = kNoAllocMaxBlocks;
     d.sys_scope = 0;
     d.ll = nullptr;
     d.ll_vecs = 0;

@@ -162,7 +162,7 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Block 0 of a rank, once it knows its call count: set the call count of this
-// rank's blocks that the call does not launch (gridDim.x <= b < bmax) to the
+// rank's blocks that the call does not launch (gridDim.x <= b < cmax) to the
 // count every launched block will have after the call.  Every block of a rank
 // then counts the same calls, so the slot parity -- a block's call count & 1 --
 // is the same for all blocks of a call.  Without it, a call on a smaller grid
@@ -174,8 +174,8 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 // early, so they overlap the call's work.
 __device__ __forceinline__ void advance_idle_blocks(const DevState &d, int rank, unsigned long long calls_after) {
     if (blockIdx.x != 0) return;
-    for (int b = (int)gridDim.x + (int)threadIdx.x; b < d.bmax; b += (int)blockDim.x)
-        d.ctr[(size_t)rank * d.bmax + b].calls = calls_after;
+    for (int b = (int)gridDim.x + (int)threadIdx.x; b < d.cmax; b += (int)blockDim.x)
+        d.ctr[(size_t)rank * d.cmax + b].calls = calls_after;
 }
 
 // The rank a block plays, and its input and output.  A kernel built for one

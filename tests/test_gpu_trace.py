@@ -26,13 +26,17 @@ def _built():
     (2, "f16", 131072, "pinned", False),   # one-shot over the host link
     (2, "f16", 4096, "pinned", False),     # tagged words
     (8, "bf16", 393216, "hbm", False),     # two-shot
-    (8, "bf16", 393216, "hbm", True),      # two-shot, one cooperative launch
+    (8, "bf16", 393216, "hbm", "flags"),   # two-shot, one cooperative launch of every rank
+    (8, "bf16", 393216, "hbm", True),      # cluster form (one launch of every rank, AUTO)
+    (2, "f16", 131072, "pinned", True),    # cluster form over the host link
 ])
 def test_trace_shows_rank_kernels_overlap(R, dtype, n, slots, fused):
     import tensor_decode_all_gb300 as tda
     from tensor_decode_all_gb300 import trace
     C, depth = 6, 8
     h = tda.Handle(R, TORCH[dtype], n, slots)
+    if fused == "flags":
+        h.set_tactics(cluster_max_bytes=0)
     buf = trace.start(h, depth)
     xs_all = [inputs.allreduce_inputs(2, R, n, dtype, "uniform", c) for c in range(C)]
     ins = [[to_dev(x, dtype) for x in xs] for xs in xs_all]
@@ -62,7 +66,7 @@ def test_trace_shows_rank_kernels_overlap(R, dtype, n, slots, fused):
     assert trace.overlap_violations(rec) == []
     assert (rec["cyc_published"] > 0).all() and (rec["cyc_peers"] >= rec["cyc_published"]).all()
     assert (rec["cyc_end"] >= rec["cyc_peers"]).all() and (rec["t_end_ns"] >= rec["t_start_ns"]).all()
-    assert set(rec["algo"].tolist()) == {h.plan("allreduce", n).algo}
+    assert set(rec["algo"].tolist()) == {h.plan("allreduce_fused" if fused else "allreduce", n).algo}
     summary = trace.summarize(rec, sm_clock_mhz=2070.0)
     assert summary["overlap_violations"] == 0 and summary["ranks"] == R
     # tracing off: later calls leave the buffer as it is
