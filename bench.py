@@ -66,6 +66,9 @@ def parse():
     ap.add_argument("--sweep-min-kib", type=int, default=2)
     ap.add_argument("--sweep-max-kib", type=int, default=65536)
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
+    ap.add_argument("--push-ab", default=None,
+                    help="time the push form against the pull forms (R=2,4; 8 KiB, 256 KiB, 4 MiB; both slot "
+                         "kinds); write JSON lines to this file")
     ap.add_argument("--only", default=None,
                     help="comma-separated workload names: time only these (no headline, no JSON contract line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -501,11 +504,18 @@ def algo_bytes(op, R, S, slots, algo=None):
     HBM all-reduce (either form): DRAM 4*R*S (inputs, slot writes, slot reads
       once, outputs);
     allgather: HBM R*S + R*S + R*S + R*R*S; pinned W = R*S, Rd = R*(R-1)*S.
+    push all-reduce: every rank writes its tile into each of R-1 peers' areas
+      and reads R-1 tiles from its own: pinned W = Rd = R*(R-1)*S; HBM inputs
+      and outputs 2*R*S plus the areas written and read, 2*R*(R-1)*S.
     """
     if slots == "pinned":
         if op == "allreduce" and algo == "twoshot":
             return {"link_write": (R + 1) * S, "link_read": (2 * R - 1) * S}
+        if op == "allreduce" and algo == "push":
+            return {"link_write": R * (R - 1) * S, "link_read": R * (R - 1) * S}
         return {"link_write": R * S, "link_read": R * (R - 1) * S}
+    if op == "allreduce" and algo == "push":
+        return {"dram": 2 * R * S + 2 * R * (R - 1) * S}
     if op == "allreduce":
         return {"dram": 4 * R * S}
     return {"dram": 3 * R * S + R * R * S}
@@ -710,6 +720,42 @@ def workloads_summary(extras):
             e["dram_frac"] = rf["dram_frac"]
         out[name] = e
     return out
+
+
+def run_push_ab(args, dist):
+    """Push against pull, per-rank launches in graphs, bf16: the forced
+    one-shot pull form, AUTO's pull form and the push form, each checked
+    against the oracle on its first and last call."""
+    import torch
+    import tensor_decode_all_gb300 as tda
+    torch.cuda.set_device(0)
+    tda.build()
+    hbm_gbs = float(measured_peaks().get("hbm_gbs", 6800.0))
+    link = tda.ar_probe_host_link(64 << 20, 10)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    with open(args.push_ab, "w") as f:
+        for slots in ("pinned", "hbm"):
+            for R in (2, 4):
+                for S in (8 << 10, 256 << 10, 4 << 20):
+                    numel = S // 2
+                    C = 100 if S <= (256 << 10) else 20
+                    row = {"slots": slots, "R": R, "bytes_per_rank": S}
+                    for label, algo in (("pull_oneshot", "oneshot"), ("pull_auto", None), ("push", "push")):
+                        w = Workload("allreduce", R, "bf16", numel, slots, C, config=5, dist="uniform", algo=algo)
+                        w.capture()
+                        w.time_graph(1, 0, flush)
+                        w.check(calls=(0, -1))
+                        ms = w.time_graph(max(10, args.steps // 2), 2, flush)
+                        w.check(calls=(0, -1))
+                        sm = summarize("allreduce", R, "bf16", numel, slots, ms, C, link, hbm_gbs, w.algo)
+                        row[label] = {"us": sm["us_per_call"], "form": w.algo, "frac": sm["roofline"]["frac"]}
+                        w.close()
+                    f.write(json.dumps(row) + "\n")
+                    f.flush()
+                    print(f"{slots:6s} R={R} S={S:>8d}: pull one-shot {row['pull_oneshot']['us']:9.2f}  "
+                          f"pull AUTO ({row['pull_auto']['form']}) {row['pull_auto']['us']:9.2f}  "
+                          f"push {row['push']['us']:9.2f} us/call", flush=True)
+    return None
 
 
 def run_only(args, dist):
@@ -1033,6 +1079,8 @@ def main():
             line = run_sweep(args, dist)
         elif args.only:
             line = run_only(args, dist)
+        elif args.push_ab:
+            line = run_push_ab(args, dist)
         else:
             line = run_ours(args, dist)
         if line is not None and dist.rank == 0:

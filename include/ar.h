@@ -114,8 +114,23 @@ enum ar_code {
  *   slots, one-shot or two-shot by size (ar_tactics.cluster_twoshot_min_bytes).
  *   Valid because the ranks are logical ranks on one GPU; per-rank calls on a
  *   handle set to it take the AR_ALGO_AUTO rule.  Not part of the pages' design.
+ * AR_ALGO_PUSH: writers store their tile into a receive area of every peer, one
+ *   peer after another, and each reader sums its own area; one flag per
+ *   (reader, writer, block) ("[SM120] Add optional FlashInfer PCIe-IPC all-reduce
+ *   for switch-free hosts", section "Motivation").  On one GPU every area is in
+ *   the same memory, so it writes R - 1 times the pull form's slot bytes; kept
+ *   for measurement, never chosen by AUTO.  Its receive areas (2 * R * R *
+ *   slot_bytes, in the slots' kind of memory) are allocated when ar_set_algo
+ *   first selects it.
  * AR_ALGO_AUTO: chosen per call from the handle's tactics (ar_tactics). */
-enum ar_algo { AR_ALGO_AUTO = -1, AR_ALGO_ONESHOT = 0, AR_ALGO_TWOSHOT = 1, AR_ALGO_TAGGED = 2, AR_ALGO_CLUSTER = 3 };
+enum ar_algo {
+    AR_ALGO_AUTO = -1,
+    AR_ALGO_ONESHOT = 0,
+    AR_ALGO_TWOSHOT = 1,
+    AR_ALGO_TAGGED = 2,
+    AR_ALGO_CLUSTER = 3,
+    AR_ALGO_PUSH = 4
+};
 
 /* Details of the first device-side error recorded in a handle. */
 typedef struct ar_error_info {
@@ -430,9 +445,11 @@ AR_API int ar_set_pdl(ar_handle *h, int enable);
 
 /* Force the all-reduce form of a handle (AR_ALGO_AUTO restores the rule):
  * AR_ALGO_ONESHOT, AR_ALGO_TWOSHOT, AR_ALGO_TAGGED (only for calls of one tile
- * per block; larger calls take the one-shot form) or AR_ALGO_CLUSTER (only for
- * launches of every rank at once; per-rank calls take the AUTO rule).  The
- * environment variable AR_ALGO=oneshot|twoshot|tagged|cluster sets it at ar_create.
+ * per block; larger calls take the one-shot form), AR_ALGO_CLUSTER (only for
+ * launches of every rank at once; per-rank calls take the AUTO rule) or
+ * AR_ALGO_PUSH (allocates its receive areas on first selection, synchronising
+ * the device; AR_ENOMEM if they do not fit).  The environment variable
+ * AR_ALGO=oneshot|twoshot|tagged|cluster sets it at ar_create.
  * Every rank of a call must see the same setting; set it before enqueuing.
  * AR_EINVAL for an unknown form, a two-shot / tagged form on a complex64
  * handle, or a call that is half issued (some rank has enqueued more calls on

@@ -20,9 +20,9 @@ from . import builder as _build
 
 AR_F16, AR_BF16, AR_C64 = 1, 2, 3
 AR_SLOT_PINNED_HOST, AR_SLOT_HBM = 0, 1
-AR_ALGO_AUTO, AR_ALGO_ONESHOT, AR_ALGO_TWOSHOT, AR_ALGO_TAGGED, AR_ALGO_CLUSTER = -1, 0, 1, 2, 3
+AR_ALGO_AUTO, AR_ALGO_ONESHOT, AR_ALGO_TWOSHOT, AR_ALGO_TAGGED, AR_ALGO_CLUSTER, AR_ALGO_PUSH = -1, 0, 1, 2, 3, 4
 ALGOS = {"auto": AR_ALGO_AUTO, "oneshot": AR_ALGO_ONESHOT, "twoshot": AR_ALGO_TWOSHOT, "tagged": AR_ALGO_TAGGED,
-         "cluster": AR_ALGO_CLUSTER}
+         "cluster": AR_ALGO_CLUSTER, "push": AR_ALGO_PUSH}
 ALGO_NAMES = {v: k for k, v in ALGOS.items()}
 AR_OK, AR_EINVAL, AR_ETOOBIG, AR_ESTREAM, AR_ENOMEM, AR_ECUDA, AR_ETIMEOUT, AR_ESTATE = range(8)
 CODE_NAMES = {0: "AR_OK", 1: "AR_EINVAL", 2: "AR_ETOOBIG", 3: "AR_ESTREAM", 4: "AR_ENOMEM",
@@ -427,7 +427,7 @@ class Handle:
             raise ArError(rc, "ar_set_timeout")
 
     def set_algo(self, algo) -> None:
-        """'auto', 'oneshot', 'twoshot', 'tagged' or 'cluster' (or an AR_ALGO_* code)."""
+        """'auto', 'oneshot', 'twoshot', 'tagged', 'cluster' or 'push' (or an AR_ALGO_* code)."""
         code = ALGOS[algo] if isinstance(algo, str) else int(algo)
         rc = ar_set_algo(self.ptr, code)
         if rc:

@@ -407,11 +407,8 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
 
 }  // namespace tda
 
-namespace tda {
-
-}  // namespace tda
-
 #include "ar_allreduce_tagged.cuh"
+#include "ar_allreduce_push.cuh"
 
 namespace tda {
 
@@ -480,17 +477,18 @@ const void *allreduce_twoshot_ptr(int R, int sub) {
 
 // U = 1 or 2: one-shot with that many vectors per thread per stage;
 // U = twoshot_variant(sub): the two-shot form with sub-tiles of `sub` vectors;
-// U = kTaggedVariant: the tagged-word form.
+// U = kTaggedVariant: the tagged-word form; U = kPushVariant: the push form.
 // fused: the kernel for one launch of all ranks (grid blocks x R); traced:
 // the kernel that writes trace records.
 template <class Ops, bool F, bool T>
 const void *allreduce_ptr_ft(int R, int U) {
     if (U == kTaggedVariant) return allreduce_tagged_ptr<Ops, F, T>(R);
+    if (U == kPushVariant) return allreduce_push_ptr<Ops, F, T>(R);
     if (U < 0) return nullptr;  // two-shot: allreduce_twoshot_ptr_any, in its own translation unit
     return U == 1 ? allreduce_ptr_ru<Ops, 1, F, T>(R) : allreduce_ptr_ru<Ops, 2, F, T>(R);
 }
 
-// One-shot and tagged-word kernels (U >= 0).
+// One-shot, tagged-word and push kernels (U >= 0).
 template <class Ops>
 const void *allreduce_ptr(int R, int U, bool fused, bool traced) {
     if (traced) return fused ? allreduce_ptr_ft<Ops, true, true>(R, U) : allreduce_ptr_ft<Ops, false, true>(R, U);

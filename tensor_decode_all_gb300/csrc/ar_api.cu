@@ -21,7 +21,7 @@ using tda::Ctr;
 using tda::DevState;
 
 // Kernel families, for the occupancy table.
-enum { kOneShot = 0, kTwoShot = 1, kTagged = 2, kAllgather = 3, kFamilies = 4 };
+enum { kOneShot = 0, kTwoShot = 1, kTagged = 2, kAllgather = 3, kPush = 4, kFamilies = 5 };
 
 struct ar_handle {
     int R = 0, dtype = 0, kind = 0, device = 0;
@@ -48,6 +48,12 @@ struct ar_handle {
     void *ll_host = nullptr;                   // pinned kind: host address of the tagged buffers
     ulonglong2 *ll_dev = nullptr;              // [2][R][ll_vecs]
     uint64_t ll_vecs = 0, ll_bytes = 0;
+    void *push_host = nullptr;                 // pinned kind: host address of the push areas
+    uint8_t *push_dev = nullptr;               // push form: [2][R][R][slot_bytes], allocated on first use
+    uint64_t push_bytes = 0;
+    void *pflags_host = nullptr;               // pinned kind: host address of the push flags
+    unsigned long long *pflags_dev = nullptr;  // push form: [R][R][bmax] flag lines
+    uint64_t pflags_bytes = 0;
     ar_trace_record *trace = nullptr;          // caller's trace buffer (ar_set_trace), or null
     uint32_t trace_depth = 0;
     bool pdl = true;                           // launch as programmatic dependents
@@ -138,6 +144,8 @@ DevState dev_state(const ar_handle *h) {
     d.trace = h->trace;
     d.trace_depth = h->trace_depth;
     d.algo = AR_ALGO_ONESHOT;
+    d.push = h->push_dev;
+    d.push_flags = h->pflags_dev;
     return d;
 }
 
@@ -148,6 +156,13 @@ void free_all(ar_handle *h) {
     else if (h->flags_dev) cudaFree(h->flags_dev);
     if (h->ll_host) cudaFreeHost(h->ll_host);
     else if (h->ll_dev) cudaFree(h->ll_dev);
+    if (h->push_host) cudaFreeHost(h->push_host);
+    else if (h->push_dev) cudaFree(h->push_dev);
+    if (h->pflags_host) cudaFreeHost(h->pflags_host);
+    else if (h->pflags_dev) cudaFree(h->pflags_dev);
+    h->push_host = h->pflags_host = nullptr;
+    h->push_dev = nullptr;
+    h->pflags_dev = nullptr;
     if (h->ctr) cudaFree(h->ctr);
     if (h->err_host) cudaFreeHost(h->err_host);
     for (auto &e : h->ev_fork)
@@ -176,6 +191,9 @@ int zero_state(ar_handle *h) {
     // Stale tagged words would carry tags the restarted counters reuse.
     if (h->ll_host) std::memset(h->ll_host, 0, h->ll_bytes);
     else if (h->ll_dev && cudaMemset(h->ll_dev, 0, h->ll_bytes) != cudaSuccess) return AR_ECUDA;
+    // push flags are stage counts too
+    if (h->pflags_host) std::memset(h->pflags_host, 0, h->pflags_bytes);
+    else if (h->pflags_dev && cudaMemset(h->pflags_dev, 0, h->pflags_bytes) != cudaSuccess) return AR_ECUDA;
     std::memset((void *)h->err_host, 0, sizeof(ar_error_info));
     for (int r = 0; r < tda::kMaxRanks; ++r) {
         h->host_calls[r].store(0);
@@ -214,6 +232,9 @@ int family_occupancy(const ar_handle *h, bool fused, bool traced, int *bps) {
         if (rc == AR_OK)
             rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, tda::kTaggedVariant, fused, traced),
                                   &bps[kTagged]);
+        if (rc == AR_OK)
+            rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, tda::kPushVariant, fused, traced),
+                                  &bps[kPush]);
     }
     for (int u = 1; u <= 2 && rc == AR_OK; ++u)
         for (int vw = 1; vw <= 16 && rc == AR_OK; vw *= 2)
@@ -387,6 +408,7 @@ bool tagged_fits(const ar_handle *h, uint64_t bytes, bool fused) {
 // tactics; the tagged form only where it fits (else one-shot).
 int handle_algo(const ar_handle *h, uint64_t bytes, bool fused) {
     if (h->algo == AR_ALGO_TAGGED) return tagged_fits(h, bytes, fused) ? AR_ALGO_TAGGED : AR_ALGO_ONESHOT;
+    if (h->algo == AR_ALGO_PUSH) return h->push_dev ? AR_ALGO_PUSH : AR_ALGO_ONESHOT;
     if (fused && h->cluster_ok &&
         (h->algo == AR_ALGO_CLUSTER || (h->algo == AR_ALGO_AUTO && bytes <= h->cluster_max_bytes)))
         return AR_ALGO_CLUSTER;
@@ -397,7 +419,10 @@ int handle_algo(const ar_handle *h, uint64_t bytes, bool fused) {
 
 // Blocks per SM of the kernel family a call of `algo` launches.
 int handle_bps(const ar_handle *h, int algo, bool fused) {
-    const int f = algo == AR_ALGO_TWOSHOT ? kTwoShot : algo == AR_ALGO_TAGGED ? kTagged : kOneShot;
+    const int f = algo == AR_ALGO_TWOSHOT ? kTwoShot
+                  : algo == AR_ALGO_TAGGED ? kTagged
+                  : algo == AR_ALGO_PUSH   ? kPush
+                                           : kOneShot;
     return h->bps[fused ? 1 : 0][h->trace ? 1 : 0][f];
 }
 
@@ -497,7 +522,8 @@ int plan_compute_sub(int R, uint64_t bytes, int vec, int algo, int sub, int thre
     if (!p || R < 1 || R > tda::kMaxRanks || threads < 32 || threads % 32 || sms < 1 || bps < 1)
         return AR_EINVAL;
     if (vec != 16 && vec != 8 && vec != 4 && vec != 2 && vec != 1) return AR_EINVAL;
-    if (algo != AR_ALGO_ONESHOT && algo != AR_ALGO_TWOSHOT && algo != AR_ALGO_TAGGED) return AR_EINVAL;
+    if (algo != AR_ALGO_ONESHOT && algo != AR_ALGO_TWOSHOT && algo != AR_ALGO_TAGGED && algo != AR_ALGO_PUSH)
+        return AR_EINVAL;
     if (algo != AR_ALGO_ONESHOT && vec != 16) return AR_EINVAL;
     std::memset(p, 0, sizeof(*p));
     const uint64_t bmax = (uint64_t)sms * (uint64_t)bps / (uint64_t)R;
@@ -509,8 +535,8 @@ int plan_compute_sub(int R, uint64_t bytes, int vec, int algo, int sub, int thre
     // per rank, so R vectors per thread per stage.
     if (algo == AR_ALGO_TWOSHOT && sub == 0) sub = 256;
     if (algo == AR_ALGO_TWOSHOT && sub != 64 && sub != 128 && sub != 256) return AR_EINVAL;
-    const uint64_t tile_vecs = algo == AR_ALGO_TWOSHOT  ? (uint64_t)R * (uint64_t)sub
-                               : algo == AR_ALGO_TAGGED ? (uint64_t)threads
+    const uint64_t tile_vecs = algo == AR_ALGO_TWOSHOT                            ? (uint64_t)R * (uint64_t)sub
+                               : (algo == AR_ALGO_TAGGED || algo == AR_ALGO_PUSH) ? (uint64_t)threads
                                                         : (uint64_t)threads * (nv >= bmax * (uint64_t)threads * 2 ? 2 : 1);
     const int unroll = (int)((tile_vecs + threads - 1) / threads);
     const uint64_t tiles = (nv + tile_vecs - 1) / tile_vecs;
@@ -647,6 +673,7 @@ int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
     const int blocks = handle_blocks(h, plan.blocks);
     const int variant = algo == AR_ALGO_TWOSHOT  ? tda::twoshot_variant(plan.subtile_vecs)
                         : algo == AR_ALGO_TAGGED ? tda::kTaggedVariant
+                        : algo == AR_ALGO_PUSH   ? tda::kPushVariant
                                                  : plan.unroll;
     DevState d = dev_state(h);
     d.algo = algo;
@@ -670,6 +697,45 @@ int enqueue_allgather(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return AR_ECUDA;
+    }
+    return AR_OK;
+}
+
+// The push form's receive areas and flags, in the slots' kind of memory:
+// 2 * R * R * slot_bytes and R * R * bmax flag lines, zeroed.  Done once, when
+// the form is first selected; every later call allocates nothing.  Synchronises
+// the device (no call may be running on the handle).
+int alloc_push(ar_handle *h) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return AR_ECUDA;
+    const uint64_t R = (uint64_t)h->R;
+    h->push_bytes = 2ull * R * R * h->slot_bytes;
+    h->pflags_bytes = R * R * (uint64_t)h->bmax * tda::kFlagStrideWords * 8ull;
+    auto undo = [&](int code) {
+        if (h->push_host) cudaFreeHost(h->push_host);
+        else if (h->push_dev) cudaFree(h->push_dev);
+        if (h->pflags_host) cudaFreeHost(h->pflags_host);
+        else if (h->pflags_dev) cudaFree(h->pflags_dev);
+        (void)cudaGetLastError();
+        h->push_host = h->pflags_host = nullptr;
+        h->push_dev = nullptr;
+        h->pflags_dev = nullptr;
+        return code;
+    };
+    if (h->kind == AR_SLOT_PINNED_HOST) {
+        const unsigned fl = cudaHostAllocMapped | cudaHostAllocPortable;
+        if (cudaHostAlloc(&h->push_host, h->push_bytes, fl) != cudaSuccess) return undo(AR_ENOMEM);
+        if (cudaHostGetDevicePointer((void **)&h->push_dev, h->push_host, 0) != cudaSuccess) return undo(AR_ECUDA);
+        if (cudaHostAlloc(&h->pflags_host, h->pflags_bytes, fl) != cudaSuccess) return undo(AR_ENOMEM);
+        if (cudaHostGetDevicePointer((void **)&h->pflags_dev, h->pflags_host, 0) != cudaSuccess)
+            return undo(AR_ECUDA);
+        std::memset(h->push_host, 0, h->push_bytes);
+        std::memset(h->pflags_host, 0, h->pflags_bytes);
+    } else {
+        if (cudaMalloc((void **)&h->push_dev, h->push_bytes) != cudaSuccess) return undo(AR_ENOMEM);
+        if (cudaMalloc((void **)&h->pflags_dev, h->pflags_bytes) != cudaSuccess) return undo(AR_ENOMEM);
+        if (cudaMemset(h->push_dev, 0, h->push_bytes) != cudaSuccess ||
+            cudaMemset(h->pflags_dev, 0, h->pflags_bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+            return undo(AR_ECUDA);
     }
     return AR_OK;
 }
@@ -740,6 +806,7 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
         else if (!std::strcmp(e, "twoshot")) h->algo = AR_ALGO_TWOSHOT;
         else if (!std::strcmp(e, "tagged")) h->algo = AR_ALGO_TAGGED;
         else if (!std::strcmp(e, "cluster")) h->algo = AR_ALGO_CLUSTER;
+        // ("push" needs its receive areas: ar_set_algo allocates them)
     }
     int rc = handle_occupancy(h);
     if (rc != AR_OK) return fail(rc);
@@ -1034,11 +1101,16 @@ AR_API int ar_set_pdl(ar_handle *h, int enable) {
 
 AR_API int ar_set_algo(ar_handle *h, int algo) {
     if (!h || (algo != AR_ALGO_AUTO && algo != AR_ALGO_ONESHOT && algo != AR_ALGO_TWOSHOT &&
-               algo != AR_ALGO_TAGGED && algo != AR_ALGO_CLUSTER))
+               algo != AR_ALGO_TAGGED && algo != AR_ALGO_CLUSTER && algo != AR_ALGO_PUSH))
         return AR_EINVAL;
-    if ((algo == AR_ALGO_TWOSHOT || algo == AR_ALGO_TAGGED || algo == AR_ALGO_CLUSTER) && h->dtype == AR_C64)
+    if ((algo == AR_ALGO_TWOSHOT || algo == AR_ALGO_TAGGED || algo == AR_ALGO_CLUSTER || algo == AR_ALGO_PUSH) &&
+        h->dtype == AR_C64)
         return AR_EINVAL;
     if (call_half_issued(h)) return AR_EINVAL;
+    if (algo == AR_ALGO_PUSH && !h->push_dev) {
+        const int rc = alloc_push(h);
+        if (rc != AR_OK) return rc;
+    }
     h->algo = algo;
     return AR_OK;
 }

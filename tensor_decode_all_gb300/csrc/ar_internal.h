@@ -9,6 +9,9 @@
 //   err   : one ar_error_info in mapped pinned host memory
 //   ll    : [2 parities][R ranks][ll_vecs] x 16 B   same memory as the slots; the
 //           tagged-word form's exchange buffers (8 payload bytes per 16 B)
+//   push  : [2 parities][R readers][R writers][slot_bytes]  same memory as the
+//           slots; the push form's receive areas, allocated when the form is
+//           first selected, with flags [R][R][bmax] x 128 B lines
 #pragma once
 
 #include <cstdint>
@@ -31,6 +34,8 @@ constexpr int twoshot_variant(int sub) { return -sub; }
 constexpr int twoshot_sub(int variant) { return -variant; }
 // Kernel variant code of the tagged-word form.
 constexpr int kTaggedVariant = 0;
+// Kernel variant code of the push form.
+constexpr int kPushVariant = 3;
 
 // Per-(rank, block) counters.  `seq` counts the stages this block has
 // published over all calls (its flag's value at the end of the last call);
@@ -58,6 +63,8 @@ struct DevState {
     uint32_t trace_depth;
     int32_t algo;              // AR_ALGO_* of this launch, for the trace
     int cmax;                  // counter slots per rank (>= bmax; cluster-form grids may use them all)
+    uint8_t *push;             // push form: [2][R reader][R writer][slot_bytes] receive areas, or null
+    unsigned long long *push_flags;  // push form: [R reader][R writer][bmax][kFlagStrideWords]
 };
 
 // The input and output pointers of every rank, passed by value to a launch

@@ -17,7 +17,7 @@ import numpy as np
 RECORD_DTYPE = np.dtype([("rank", "<i4"), ("block", "<i4"), ("call", "<u4"), ("stages", "<u4"),
                          ("t_start_ns", "<u8"), ("t_end_ns", "<u8"), ("cyc_published", "<u4"),
                          ("cyc_peers", "<u4"), ("cyc_end", "<u4"), ("algo", "<u4")])
-ALGO_NAMES = {0: "oneshot", 1: "twoshot", 2: "tagged", 3: "cluster"}
+ALGO_NAMES = {0: "oneshot", 1: "twoshot", 2: "tagged", 3: "cluster", 4: "push"}
 
 
 class TraceRecord(ctypes.Structure):
