@@ -184,13 +184,18 @@ class ClockSampler:
 # C header's structs included) voids them.
 _CSRC = "tensor_decode_all_gb300/csrc/"
 _COMMON_SOURCES = ("include/ar.h", _CSRC + "ar_internal.h", _CSRC + "ar_sync.cuh")
+# ar_allreduce.cuh includes the tagged-word and push headers, so every
+# all-reduce family's translation units see them
+_ALLREDUCE_HEADERS = (_CSRC + "ar_allreduce.cuh", _CSRC + "ar_allreduce_tagged.cuh", _CSRC + "ar_allreduce_push.cuh")
 FORM_SOURCES = {
-    "oneshot": _COMMON_SOURCES + (_CSRC + "ar_allreduce.cuh", _CSRC + "ar_allreduce_f16.cu",
-                                  _CSRC + "ar_allreduce_bf16.cu"),
-    "twoshot": _COMMON_SOURCES + (_CSRC + "ar_allreduce.cuh", _CSRC + "ar_allreduce_f16_twoshot.cu",
-                                  _CSRC + "ar_allreduce_bf16_twoshot.cu"),
-    "tagged": _COMMON_SOURCES + (_CSRC + "ar_allreduce.cuh", _CSRC + "ar_allreduce_tagged.cuh",
-                                 _CSRC + "ar_allreduce_f16.cu", _CSRC + "ar_allreduce_bf16.cu"),
+    "oneshot": _COMMON_SOURCES + _ALLREDUCE_HEADERS + (_CSRC + "ar_allreduce_f16.cu", _CSRC + "ar_allreduce_bf16.cu"),
+    "twoshot": _COMMON_SOURCES + _ALLREDUCE_HEADERS + (_CSRC + "ar_allreduce_f16_twoshot.cu",
+                                                       _CSRC + "ar_allreduce_bf16_twoshot.cu"),
+    "tagged": _COMMON_SOURCES + _ALLREDUCE_HEADERS + (_CSRC + "ar_allreduce_f16.cu", _CSRC + "ar_allreduce_bf16.cu"),
+    "push": _COMMON_SOURCES + _ALLREDUCE_HEADERS + (_CSRC + "ar_allreduce_f16.cu", _CSRC + "ar_allreduce_bf16.cu"),
+    "cluster": _COMMON_SOURCES + _ALLREDUCE_HEADERS + (_CSRC + "ar_allreduce_cluster.cuh",
+                                                       _CSRC + "ar_allreduce_f16_cluster.cu",
+                                                       _CSRC + "ar_allreduce_bf16_cluster.cu"),
     "allgather": _COMMON_SOURCES + (_CSRC + "ar_allgather.cu",),
 }
 

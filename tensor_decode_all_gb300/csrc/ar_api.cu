@@ -324,32 +324,33 @@ uint64_t tagged_threshold(int R, int slot_kind) {
 }
 
 // Cluster form (launches of all ranks at once): two-shot from this size per
-// rank.  Measured on a GB300 (bf16, graphs of calls, one-shot / two-shot
-// cluster form, us/call): at R = 2 one-shot wins everywhere (HBM 16 MiB 23.8 /
-// 33.0, pinned 256 KiB 7.1 / 9.4); in HBM two-shot wins from 1 MiB at R = 4
-// (5.5 / 6.8; 512 KiB 4.2 / 5.2) and from 512 KiB at R = 8 (6.9 / 7.9; 256 KiB
-// 4.6 / 5.8); over the host link from 64 KiB at R = 4 (7.4 / 7.6) and 32 KiB
-// at R = 8 (10.4 / 12.2).  R = 3 takes R = 4's size, R = 5..7 R = 8's.
+// rank.  Measured on a GB300 (bf16, graphs of 100 calls, one-shot / two-shot
+// cluster form, us/call): in HBM one-shot wins at every size the form takes
+// up to R = 4 (R = 4 1 MiB 6.4 / 8.5), and two-shot from 512 KiB at R = 8
+// (6.8 / 7.4; 256 KiB 4.4 / 5.4); over the host link one-shot wins everywhere
+// at R = 2 (256 KiB 7.0 / 9.4), two-shot from 128 KiB at R = 4 (10.3 / 12.1;
+// 64 KiB 7.1 / 7.3) and from 32 KiB at R = 8 (8.3 / 12.1).  R = 3 takes
+// R = 4's size, R = 5..7 R = 8's.
 uint64_t cluster_twoshot_threshold(int R, int slot_kind) {
     if (R < 3) return ~0ull;
-    if (slot_kind == AR_SLOT_PINNED_HOST) return R >= 5 ? (32ull << 10) : (64ull << 10);
-    return R >= 5 ? (512ull << 10) : (1ull << 20);
+    if (slot_kind == AR_SLOT_PINNED_HOST) return R >= 5 ? (32ull << 10) : (128ull << 10);
+    return R >= 5 ? (512ull << 10) : ~0ull;
 }
 
 // Largest call (bytes per rank) that AUTO runs in the cluster form when all
 // ranks launch at once; larger calls take the flag forms, whose grids keep
 // more blocks resident than clusters of R blocks can.  Measured on a GB300
-// (bf16, graphs of calls; cluster form / the flag forms in the same single
-// launch, us/call): in HBM the cluster form wins up to 4 MiB at R = 2 (7.9 /
-// 8.6; 8 MiB 13.2 / 13.0), up to 8 MiB at R = 4 (26.2 / 29.3; 16 MiB 50.6 /
-// 48.3) and, at R = 8, as long as one stage of 64-vector sub-tiles covers the
-// call (896 KiB: 768 KiB 6.7 / 8.6; 1 MiB 12.6 / 9.7); over the host link at
-// every size at R = 2 (16 MiB 226 / 247), up to 512 KiB at R = 4 (32.3 /
-// 34.0) and up to 4 MiB at R = 8 (398 / 430).  R = 3 takes R = 4's limit,
-// R = 5..7 R = 8's.
+// (bf16, graphs of 100 calls; cluster form / best flag form, per-rank or in
+// one launch, us/call): in HBM the cluster form wins up to 2 MiB at R = 2
+// (5.8 / 6.5; 4 MiB 9.4 / 8.1), up to 1 MiB at R = 4 (6.4 / 7.4; 2 MiB 9.8 /
+// 9.2) and, at R = 8, as long as one stage of 64-vector sub-tiles covers the
+// call (896 KiB: 512 KiB 6.8 / 7.9; 1 MiB 12.1 / 9.8); over the host link at
+// every size at R = 2 (16 MiB 227 / 243), up to 4 MiB at R = 4 (2 MiB 106 /
+// 118; 8 MiB 394 / 367) and up to 8 MiB at R = 8 (733 / 760; 16 MiB 1663 /
+// 1416).  R = 3 takes R = 4's limit, R = 5..7 R = 8's.
 uint64_t cluster_limit(int R, int slot_kind) {
-    if (slot_kind == AR_SLOT_PINNED_HOST) return R <= 2 ? ~0ull : R <= 4 ? (512ull << 10) : (4ull << 20);
-    return R <= 2 ? (4ull << 20) : R <= 4 ? (8ull << 20) : (896ull << 10);
+    if (slot_kind == AR_SLOT_PINNED_HOST) return R <= 2 ? ~0ull : R <= 4 ? (4ull << 20) : (8ull << 20);
+    return R <= 2 ? (2ull << 20) : R <= 4 ? (1ull << 20) : (896ull << 10);
 }
 
 // Under stream capture, true if a dependency edge from stream `sr` into the

@@ -100,9 +100,13 @@ def test_profiled_traffic_follows_each_kernel_family(tmp_path, monkeypatch):
     assert valid() == set(bench.FORM_SOURCES)
     ag.write_text(ag.read_text() + "\nnamespace { int unused_edit = 1; }\n")
     assert valid() == set(bench.FORM_SOURCES) - {"allgather"}
+    cl = tmp_path / "tensor_decode_all_gb300/csrc/ar_allreduce_cluster.cuh"
+    cl.write_text(cl.read_text() + "\n#define EDIT 0\n")
+    assert valid() == set(bench.FORM_SOURCES) - {"allgather", "cluster"}
+    # the tagged-word header is included by every all-reduce translation unit
     tagged = tmp_path / "tensor_decode_all_gb300/csrc/ar_allreduce_tagged.cuh"
     tagged.write_text(tagged.read_text() + "\n#define EDIT 1\n")
-    assert valid() == {"oneshot", "twoshot"}
+    assert valid() == set()
     hdr = tmp_path / "include/ar.h"
     hdr.write_text(hdr.read_text() + "\n#define EDIT 2\n")
     assert valid() == set()
