@@ -1,8 +1,9 @@
 """Measure a handle's all-reduce tactics on this GPU, and keep them.
 
 The library's built-in table (ar_choose_algo) puts the one-shot / two-shot
-crossover, and the sizes up to which the tagged-word form beats the flag
-protocol, where they were measured on one GB300.  A caller on another GPU, or
+crossover, the sizes up to which the tagged-word form beats the flag
+protocol, and the sizes up to which the cluster form beats the flag forms
+when every rank launches at once, where they were measured on one GB300.  A caller on another GPU, or
 with another clock or memory configuration, can measure them again: ``tune``
 times the forms at power-of-two sizes, each in a CUDA graph of several calls
 of every rank (the way decode replays them), picks the smallest measured size
@@ -66,8 +67,22 @@ def tagged_limit(times: dict) -> int:
     return limit
 
 
-def _time_form(handle, algo: str, nbytes: int, calls: int, replays: int) -> float:
-    """µs per call of one form at one size: graph of `calls` calls of every rank."""
+def cluster_tactics(times: dict):
+    """times: {bytes: {"cluster_oneshot": us, "cluster_twoshot": us, "flags": us}},
+    measured for launches of every rank at once.  Returns (two-shot size of the
+    cluster form, largest size for the cluster form): the crossover rule between
+    the cluster form's two variants, then the largest size up to which the
+    cluster form (with that crossover) beats the flag forms at every measured
+    size (0: never)."""
+    tw = crossover({b: {"oneshot": t["cluster_oneshot"], "twoshot": t["cluster_twoshot"]} for b, t in times.items()})
+    best = {b: {"tagged": t["cluster_twoshot"] if b >= tw else t["cluster_oneshot"], "oneshot": t["flags"]}
+            for b, t in times.items()}
+    return tw, tagged_limit(best)
+
+
+def _time_form(handle, algo: str, nbytes: int, calls: int, replays: int, fused: bool = False) -> float:
+    """µs per call of one form at one size: graph of `calls` calls of every
+    rank (per-rank launches on forked streams, or one launch of every rank)."""
     import torch
     R = handle.R
     dt = {1: torch.float16, 2: torch.bfloat16}[handle.dtype]
@@ -85,6 +100,9 @@ def _time_form(handle, algo: str, nbytes: int, calls: int, replays: int) -> floa
             for s in streams:
                 s.wait_stream(cap)
             for c in range(calls):
+                if fused:
+                    handle.allreduce_fused(ins[c], outs[c], cap)
+                    continue
                 for r in range(R):
                     handle.allreduce(r, ins[c][r], outs[c][r], streams[r])
             for s in streams:
@@ -124,11 +142,41 @@ def measure(handle, sizes=None, replays: int = 5, forms=("oneshot", "twoshot")) 
     return times
 
 
-def tune(handle, sizes=None, tagged_sizes=None, replays: int = 5) -> dict:
-    """Measure both crossovers -- one-shot / two-shot (sizes) and tagged words
-    / one-shot (tagged_sizes: by default powers of two from 2 KiB to the
-    smaller of 512 KiB and the tagged form's capacity) -- set them on the
-    handle, and return the tactics and the measured times."""
+def measure_cluster(handle, sizes=None, replays: int = 5) -> dict:
+    """{bytes: {"cluster_oneshot", "cluster_twoshot", "flags": us}} for launches
+    of every rank at once: the cluster form forced one-shot and two-shot, and
+    the flag forms the handle's per-rank tactics pick (cluster form off).  By
+    default powers of two from 2 KiB to min(8 MiB, the handle's max payload).
+    The handle's form and tactics are restored afterwards."""
+    max_bytes = handle.max_numel * 2
+    if sizes is None:
+        sizes = [1 << k for k in range(11, 24) if (1 << k) <= max_bytes]
+    saved_algo, saved = handle.info().algo, handle.tactics()
+    variants = (("cluster_oneshot", "cluster", {"cluster_twoshot_min_bytes": NEVER}),
+                ("cluster_twoshot", "cluster", {"cluster_twoshot_min_bytes": 0}),
+                ("flags", "auto", {"cluster_max_bytes": 0}))
+    times = {}
+    try:
+        for nbytes in sizes:
+            calls = max(4, min(20, (256 << 20) // (handle.R * nbytes * 2)))
+            times[nbytes] = {}
+            for name, algo, tactics in variants:
+                handle.set_tactics(**tactics)
+                times[nbytes][name] = _time_form(handle, algo, nbytes, calls, replays, fused=True)
+                handle.set_tactics(**saved)
+    finally:
+        handle.set_algo(saved_algo)
+        handle.set_tactics(**saved)
+    return times
+
+
+def tune(handle, sizes=None, tagged_sizes=None, cluster_sizes=None, replays: int = 5) -> dict:
+    """Measure the crossovers -- one-shot / two-shot (sizes), tagged words /
+    one-shot (tagged_sizes: by default powers of two from 2 KiB to the smaller
+    of 512 KiB and the tagged form's capacity) and, where the GPU runs the
+    cluster form, its two-shot size and its limit against the flag forms for
+    launches of every rank (cluster_sizes) -- set them on the handle, and
+    return the tactics and the measured times."""
     if handle.dtype not in (1, 2):
         raise ValueError("tactics apply to fp16/bf16 all-reduce handles")
     times = measure(handle, sizes, replays)
@@ -137,8 +185,14 @@ def tune(handle, sizes=None, tagged_sizes=None, replays: int = 5) -> dict:
         tagged_sizes = [1 << k for k in range(11, 20) if (1 << k) <= cap]
     tagged_times = measure(handle, tagged_sizes, replays, forms=("tagged", "oneshot")) if tagged_sizes else {}
     handle.set_tactics(twoshot_min_bytes=crossover(times), tagged_max_bytes=tagged_limit(tagged_times))
+    cluster_times = {}
+    if handle.info().cluster_form > 0 and (cluster_sizes is None or cluster_sizes):
+        cluster_times = measure_cluster(handle, cluster_sizes, replays)
+        tw, limit = cluster_tactics(cluster_times)
+        handle.set_tactics(cluster_twoshot_min_bytes=tw, cluster_max_bytes=limit)
     return {"tactics": handle.tactics(), "times_us": {str(k): v for k, v in times.items()},
-            "tagged_times_us": {str(k): v for k, v in tagged_times.items()}}
+            "tagged_times_us": {str(k): v for k, v in tagged_times.items()},
+            "cluster_times_us": {str(k): v for k, v in cluster_times.items()}}
 
 
 def save(path: str, key: str, tactics: dict) -> None:

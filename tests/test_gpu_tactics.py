@@ -89,7 +89,8 @@ def test_tune_sets_a_measured_threshold_and_the_file_applies_it(tmp_path):
     import tensor_decode_all_gb300 as tda
     from tensor_decode_all_gb300 import tune
     h = tda.Handle(8, torch.bfloat16, 1 << 20, "hbm")
-    out = tune.tune(h, sizes=[64 << 10, 256 << 10, 1 << 20], tagged_sizes=[4 << 10, 16 << 10], replays=3)
+    out = tune.tune(h, sizes=[64 << 10, 256 << 10, 1 << 20], tagged_sizes=[4 << 10, 16 << 10],
+                    cluster_sizes=[8 << 10, 512 << 10, 2 << 20], replays=3)
     thr = out["tactics"]["twoshot_min_bytes"]
     assert thr in (64 << 10, 256 << 10, 1 << 20, tune.NEVER)
     assert thr == tune.crossover({int(k): v for k, v in out["times_us"].items()})
@@ -97,6 +98,11 @@ def test_tune_sets_a_measured_threshold_and_the_file_applies_it(tmp_path):
     assert lim in (0, 4 << 10, 16 << 10)
     assert lim == tune.tagged_limit({int(k): v for k, v in out["tagged_times_us"].items()})
     assert h.tactics()["twoshot_min_bytes"] == thr
+    if h.info().cluster_form > 0:
+        ct = {int(k): v for k, v in out["cluster_times_us"].items()}
+        assert sorted(ct) == [8 << 10, 512 << 10, 2 << 20]
+        tw, cl = tune.cluster_tactics(ct)
+        assert (out["tactics"]["cluster_twoshot_min_bytes"], out["tactics"]["cluster_max_bytes"]) == (tw, cl)
     assert h.info().algo == -1                       # the forced form was restored to AUTO
     path = str(tmp_path / "tactics.json")
     tune.save(path, tune.handle_key(h), h.tactics())

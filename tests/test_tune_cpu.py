@@ -50,3 +50,19 @@ def test_tagged_limit_largest_size_up_to_which_tagged_always_wins():
     assert tune.tagged_limit(t) == 8192          # the win at 128 KiB after a loss does not count
     assert tune.tagged_limit({2048: {"tagged": 4.0, "oneshot": 3.5}}) == 0
     assert tune.tagged_limit({}) == 0
+
+
+def test_cluster_tactics_crossover_then_limit_against_the_flag_forms():
+    t = {2048: {"cluster_oneshot": 2.9, "cluster_twoshot": 4.1, "flags": 3.7},
+         65536: {"cluster_oneshot": 3.4, "cluster_twoshot": 4.6, "flags": 4.2},
+         524288: {"cluster_oneshot": 7.4, "cluster_twoshot": 6.8, "flags": 7.9},
+         1048576: {"cluster_oneshot": 12.1, "cluster_twoshot": 12.0, "flags": 9.8},
+         4194304: {"cluster_oneshot": 37.6, "cluster_twoshot": 36.0, "flags": 27.7}}
+    tw, limit = tune.cluster_tactics(t)
+    assert tw == 524288                 # two-shot faster from 512 KiB on
+    assert limit == 524288              # the cluster form loses to the flags from 1 MiB
+    # one-shot throughout, and a cluster form that loses at the smallest size: never
+    t2 = {2048: {"cluster_oneshot": 4.0, "cluster_twoshot": 5.0, "flags": 3.5},
+          8192: {"cluster_oneshot": 3.0, "cluster_twoshot": 5.0, "flags": 3.5}}
+    assert tune.cluster_tactics(t2) == (tune.NEVER, 0)
+    assert tune.cluster_tactics({}) == (tune.NEVER, 0)
