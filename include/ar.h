@@ -190,7 +190,9 @@ typedef struct ar_plan {
     int32_t algo;           /* AR_ALGO_ONESHOT, _TWOSHOT or _TAGGED (allgather: one-shot) */
     int32_t flag_rounds;    /* flag rounds per tile: 1 or 2 */
     int32_t subtile_vecs;   /* two-shot: vectors per sub-tile (64, 128 or 256; a tile is R sub-tiles); else 0 */
-    int32_t reserved;
+    int32_t pace_cycles;    /* SM cycles between the first-stage slot stores of consecutive blocks (the
+                               pace_mbs tactics, slots in host memory); 0: all at once.  ar_plan_for
+                               only; ar_plan_compute leaves it 0 */
     uint64_t tile_bytes;    /* bytes a block handles per stage (threads * unroll * vec_bytes) */
     uint64_t tiles;         /* ceil(bytes / tile_bytes); tile t goes to block t % blocks, stage t / blocks */
     uint64_t max_stages;    /* stages of block 0 = ceil(tiles / blocks) */
@@ -212,6 +214,19 @@ typedef struct ar_tactics {
     uint64_t cluster_max_bytes; /* under AUTO, a launch of every rank at once takes the cluster form up to
                                    this many bytes per rank, the flag forms above it; 0: never */
     int32_t all_fused;          /* ar_allreduce_all: 1 = one launch of every rank; 0 = one launch per rank */
+    int32_t pace_mbs;           /* slots in host memory: the rate (MB/s) at which a call's slot traffic,
+                                   stores and the peers' loads together, is to cross the host link, for
+                                   calls of one stage per block.  The first stage's slot stores of block
+                                   b of every rank start b * R * tile_bytes / (pace * share) after the
+                                   block starts, share = the stores' part of the traffic (1/R one-shot,
+                                   (R+1)/3R two-shot), so the stores reach the link about as fast as it
+                                   drains them rather than all at once.  One-shot, two-shot and cluster
+                                   forms (the cluster form only when all its clusters are resident at
+                                   once).  0 = all at once; otherwise >= 1000.  Default 356000 for
+                                   pinned-host handles; ignored for HBM.  Timing only: the results do
+                                   not change */
+    uint64_t pace_min_bytes;    /* pace only calls of at least this many bytes per rank (default 128 KiB) */
+    int32_t pace_multi_mbs;     /* as pace_mbs, for calls of several stages per block (default 220000) */
     int32_t reserved;           /* 0 */
 } ar_tactics;
 

@@ -59,7 +59,9 @@ class Tactics(ctypes.Structure):
     _fields_ = [("twoshot_min_bytes", ctypes.c_uint64), ("twoshot_sub", ctypes.c_int32),
                 ("max_blocks", ctypes.c_int32), ("tagged_max_bytes", ctypes.c_uint64),
                 ("cluster_twoshot_min_bytes", ctypes.c_uint64), ("cluster_max_bytes", ctypes.c_uint64),
-                ("all_fused", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("all_fused", ctypes.c_int32), ("pace_mbs", ctypes.c_int32),
+                ("pace_min_bytes", ctypes.c_uint64), ("pace_multi_mbs", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 TACTIC_FIELDS = [name for name, _ in Tactics._fields_ if name != "reserved"]
@@ -68,7 +70,7 @@ TACTIC_FIELDS = [name for name, _ in Tactics._fields_ if name != "reserved"]
 class Plan(ctypes.Structure):
     _fields_ = [("blocks", ctypes.c_int32), ("threads", ctypes.c_int32), ("vec_bytes", ctypes.c_int32),
                 ("unroll", ctypes.c_int32), ("algo", ctypes.c_int32), ("flag_rounds", ctypes.c_int32),
-                ("subtile_vecs", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("subtile_vecs", ctypes.c_int32), ("pace_cycles", ctypes.c_int32),
                 ("tile_bytes", ctypes.c_uint64), ("tiles", ctypes.c_uint64),
                 ("max_stages", ctypes.c_uint64)]
 
@@ -453,7 +455,7 @@ class Handle:
             raise TypeError(f"unknown tactics {sorted(unknown)}")
         cur = self.tactics()
         cur.update({k: v for k, v in changes.items() if v is not None})
-        t = Tactics(*[int(cur[name]) for name in TACTIC_FIELDS], 0)
+        t = Tactics(**{name: int(cur[name]) for name in TACTIC_FIELDS})
         rc = ar_set_tactics(self.ptr, t)
         if rc:
             raise ArError(rc, "ar_set_tactics")

@@ -150,6 +150,7 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
     const uint64_t nstages = ntiles > (uint64_t)b ? (ntiles - b + B - 1) / B : 0;
 
     pdl_wait();
+    const long long c0 = clock64();
     if (tid == 0) {
         trace_start<T>(d, s_tr);
         const Ctr c = d.ctr[(size_t)rank * d.cmax + b];
@@ -172,6 +173,7 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
     const uint64_t slot_vecs = d.slot_bytes / 16;
     uint4 *const slot_base = reinterpret_cast<uint4 *>(d.slots) + (uint64_t)parity * R * slot_vecs;
     uint4 *const my_slot = slot_base + (uint64_t)rank * slot_vecs;
+    if (nstages) pace_first_stage(c0, b, d.pace_cycles);
 
     for (uint64_t s = 0; s < nstages; ++s) {
         const uint64_t tile = (uint64_t)b + s * B;
@@ -308,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
     const uint64_t nstages = ntiles > (uint64_t)b ? (ntiles - b + B - 1) / B : 0;
 
     pdl_wait();
+    const long long c0 = clock64();
     if (tid == 0) {
         trace_start<T>(d, s_tr);
         const Ctr c = d.ctr[(size_t)rank * d.cmax + b];
@@ -333,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
             const uint64_t li = (uint64_t)u * kThreads + tid;
             pub[u] = li < kTileVecs ? load_own(in, tbase + li, nvec_full, tail) : make_uint4(0u, 0u, 0u, 0u);
         }
+        if (s == 0) pace_first_stage(c0, b, d.pace_cycles);
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
             const uint64_t li = (uint64_t)u * kThreads + tid;

@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(kThreads, cluster_min_blocks<R, SUB>())
     const uint64_t nstages = ntiles > (uint64_t)b ? (ntiles - b + B - 1) / B : 0;
 
     pdl_wait();
+    const long long c0 = clock64();
     // stage 0's tile of this rank's input, loaded while thread 0 fetches the
     // call count (the slot half it goes to)
     uint4 own[kPer];
@@ -123,6 +124,8 @@ __global__ void __launch_bounds__(kThreads, cluster_min_blocks<R, SUB>())
                 const uint64_t li = (uint64_t)u * kThreads + tid;
                 own[u] = li < kTileVecs ? load_own(in, tbase + li, nvec_full, tail) : make_uint4(0u, 0u, 0u, 0u);
             }
+        } else {
+            pace_first_stage(c0, b, d.pace_cycles);
         }
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {

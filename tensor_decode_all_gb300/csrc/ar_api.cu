@@ -41,6 +41,10 @@ struct ar_handle {
     uint64_t cluster_twoshot_min_bytes = ~0ull;  // tactic: cluster form is two-shot from this size
     uint64_t cluster_max_bytes = 0;            // tactic: AUTO runs launches of all ranks in the cluster form up to this size
     bool all_fused = true;                     // tactic: ar_allreduce_all launches all ranks at once
+    int pace_mbs = 0;                          // tactic: pinned slots, pace of single-stage calls (MB/s); 0 = off
+    int pace_multi_mbs = 0;                    // tactic: the same for calls of several stages per block
+    uint64_t pace_min_bytes = 0;               // tactic: pace calls from this many bytes per rank
+    int clock_khz = 0;                         // peak SM clock, for the pacing delay in cycles
     bool cluster_ok = false;                   // the cluster kernels can be scheduled on this GPU
     int cluster_max = 0;                       // clusters of R blocks of the cluster kernels resident at once
     cudaEvent_t ev_fork[tda::kMaxRanks] = {};  // ar_allreduce_all: stream r > 0 -> stream 0
@@ -146,6 +150,7 @@ DevState dev_state(const ar_handle *h) {
     d.algo = AR_ALGO_ONESHOT;
     d.push = h->push_dev;
     d.push_flags = h->pflags_dev;
+    d.pace_cycles = 0;
     return d;
 }
 
@@ -384,6 +389,20 @@ bool fork_redundant(cudaStream_t s0, cudaStream_t sr) {
     }
     return true;
 }
+
+// Pace of a call's slot traffic over the host link (stores and loads
+// together, MB/s), for calls of one stage per block and of several, and the
+// smallest call paced.  Measured on a GB300 (bf16, per-rank launches, graphs
+// of 100 calls; unpaced / 220 / 280 / 356 / 440 GB/s, us per call): R = 2
+// 256 KiB 7.97 / 8.26 / 7.39 / 7.15 / 7.22, 1 MiB 23.8 / 23.4 / 20.7 / 19.3 /
+// 21.1; R = 8 two-shot 1 MiB 122.5 / 114.4 / 98.4 / 96.0 / 103.1; calls of
+// several stages per block: R = 2 4 MiB 77.0 / 63.5 / 69.5 / 72.5 / 74.2,
+// R = 8 4 MiB 421 / 355 / 366 / 373 / 384; below 128 KiB level or slower
+// (R = 8 32 KiB one-shot 12.8 unpaced, 13.4 at 356).  In the cluster form
+// (one wave of clusters) R = 2 256 KiB 6.98 -> 5.84, 1 MiB 20.5 -> 15.9 at 356.
+constexpr int kPaceSingleMbs = 356000;
+constexpr int kPaceMultiMbs = 220000;
+constexpr uint64_t kPaceMinBytes = 128ull << 10;
 
 int choose_algo(int R, uint64_t bytes, int slot_kind) {
     const uint64_t tagged = tagged_threshold(R, slot_kind);
@@ -646,6 +665,38 @@ int end_call(ar_handle *h, int rank, int rc) {
     return rc;
 }
 
+// Pacing delay between consecutive blocks' first-stage slot stores, in SM
+// cycles, for a call of `bytes` per rank planned as `plan` on `blocks` blocks
+// per rank.  The handle's pace (one for calls of one stage per block, one for
+// calls of several) is the rate at which the call's slot traffic -- stores and
+// the peers' loads together -- is to cross the host link; the stores take
+// their share of it, W / (W + Rd): 1 / R for the one-shot form (W = R S,
+// Rd = R (R - 1) S), (R + 1) / 3R for the two-shot form (W = (R + 1) S,
+// Rd = (2R - 1) S).  So one tile of every rank leaves every
+// R * tile_bytes / (pace * share), converted at the GPU's peak SM clock.  Only
+// for slots in host memory, R >= 2, calls of at least pace_min_bytes per rank
+// and a pace set; capped so that no block of the largest grid waits more than
+// about 2 ms.
+uint32_t pace_cycles(const ar_handle *h, uint64_t bytes, const ar_plan &plan, int blocks) {
+    if (h->kind != AR_SLOT_PINNED_HOST || h->R < 2 || h->clock_khz <= 0 || bytes < h->pace_min_bytes) return 0;
+    const int pace = plan.tiles > (uint64_t)blocks ? h->pace_multi_mbs : h->pace_mbs;
+    if (pace <= 0) return 0;
+    const double R = (double)h->R;
+    const double share = plan.subtile_vecs ? (R + 1.0) / (3.0 * R) : 1.0 / R;
+    const double ns = R * (double)plan.tile_bytes * 1000.0 / ((double)pace * share);
+    double cyc = ns * (double)h->clock_khz / 1e6;
+    const double cap = 4e6 / (double)(h->bmax > 0 ? h->bmax : 1);
+    if (cyc > cap) cyc = cap;
+    return (uint32_t)(cyc + 0.5);
+}
+
+// The cluster form's pacing: only when every cluster of the call is resident
+// at once (a cluster of a later wave starts when an earlier one ends, already
+// behind the others).
+uint32_t cluster_pace_cycles(const ar_handle *h, uint64_t bytes, const ar_plan &plan) {
+    return plan.blocks <= h->cluster_max ? pace_cycles(h, bytes, plan, plan.blocks) : 0;
+}
+
 // The all-reduce launch both entry points share: form, plan and grid from the
 // handle, then one launch for `rank` (or, rank < 0, all ranks at once).
 int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int rank, cudaStream_t s) {
@@ -658,6 +709,7 @@ int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
         const int blocks = plan.blocks;  // within handle_cluster_grid: counters, trace, block cap
         DevState d = dev_state(h);
         d.algo = AR_ALGO_CLUSTER;
+        d.pace_cycles = cluster_pace_cycles(h, bytes, plan);
         const cudaError_t e =
             tda::launch_allreduce_cluster(h->dtype, h->R, plan.subtile_vecs, blocks, s, io, numel, d, h->pdl);
         if (e != cudaSuccess) {
@@ -678,6 +730,7 @@ int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
                                                  : plan.unroll;
     DevState d = dev_state(h);
     d.algo = algo;
+    if (algo == AR_ALGO_ONESHOT || algo == AR_ALGO_TWOSHOT) d.pace_cycles = pace_cycles(h, bytes, plan, blocks);
     const cudaError_t e = tda::launch_allreduce(h->dtype, h->R, variant, blocks, s, io, numel, rank, d, h->pdl);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
@@ -794,6 +847,7 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
     if (cudaGetDevice(&h->device) != cudaSuccess) return fail(AR_ECUDA);
     if (cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess)
         return fail(AR_ECUDA);
+    if (cudaDeviceGetAttribute(&h->clock_khz, cudaDevAttrClockRate, h->device) != cudaSuccess) return fail(AR_ECUDA);
     if (const char *e = std::getenv("AR_PDL")) h->pdl = e[0] != '0';
     if (const char *e = std::getenv("AR_TWOSHOT_SUB")) {
         const long v = std::strtol(e, nullptr, 10);
@@ -802,6 +856,9 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
     h->twoshot_min_bytes = twoshot_threshold(R, slot_kind);
     h->tagged_max_bytes = (dtype == AR_F16 || dtype == AR_BF16) ? tagged_threshold(R, slot_kind) : 0;
     h->cluster_twoshot_min_bytes = cluster_twoshot_threshold(R, slot_kind);
+    h->pace_mbs = slot_kind == AR_SLOT_PINNED_HOST ? kPaceSingleMbs : 0;
+    h->pace_multi_mbs = slot_kind == AR_SLOT_PINNED_HOST ? kPaceMultiMbs : 0;
+    h->pace_min_bytes = kPaceMinBytes;
     if (const char *e = std::getenv("AR_ALGO")) {
         if (!std::strcmp(e, "oneshot")) h->algo = AR_ALGO_ONESHOT;
         else if (!std::strcmp(e, "twoshot")) h->algo = AR_ALGO_TWOSHOT;
@@ -1158,6 +1215,9 @@ AR_API int ar_get_tactics(const ar_handle *h, ar_tactics *t) {
     t->cluster_twoshot_min_bytes = h->cluster_twoshot_min_bytes;
     t->cluster_max_bytes = h->cluster_max_bytes;
     t->all_fused = h->all_fused ? 1 : 0;
+    t->pace_mbs = h->pace_mbs;
+    t->pace_min_bytes = h->pace_min_bytes;
+    t->pace_multi_mbs = h->pace_multi_mbs;
     t->reserved = 0;
     return AR_OK;
 }
@@ -1168,6 +1228,8 @@ AR_API int ar_set_tactics(ar_handle *h, const ar_tactics *t) {
         return AR_EINVAL;
     if (t->max_blocks < 0 || call_half_issued(h)) return AR_EINVAL;
     if (t->all_fused != 0 && t->all_fused != 1) return AR_EINVAL;
+    if ((t->pace_mbs != 0 && t->pace_mbs < 1000) || (t->pace_multi_mbs != 0 && t->pace_multi_mbs < 1000))
+        return AR_EINVAL;
     h->twoshot_min_bytes = t->twoshot_min_bytes;
     h->twoshot_sub = t->twoshot_sub;
     h->max_blocks = t->max_blocks;
@@ -1175,6 +1237,9 @@ AR_API int ar_set_tactics(ar_handle *h, const ar_tactics *t) {
     h->cluster_twoshot_min_bytes = t->cluster_twoshot_min_bytes;
     h->cluster_max_bytes = t->cluster_max_bytes;
     h->all_fused = t->all_fused == 1;
+    h->pace_mbs = t->pace_mbs;
+    h->pace_min_bytes = t->pace_min_bytes;
+    h->pace_multi_mbs = t->pace_multi_mbs;
     return AR_OK;
 }
 
@@ -1197,6 +1262,7 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) 
         const int algo = handle_algo(h, bytes, true);
         if (algo == AR_ALGO_CLUSTER) {
             plan_cluster(h->R, bytes, handle_cluster_sub(h, bytes), handle_cluster_grid(h), plan);
+            plan->pace_cycles = (int32_t)cluster_pace_cycles(h, bytes, *plan);
             return AR_OK;
         }
         const int rc = plan_compute_sub(h->R, bytes, 16, algo, handle_twoshot_sub(h, bytes), tda::kThreads,
@@ -1205,6 +1271,8 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) 
         if (plan->blocks > 0) {
             plan->blocks = handle_blocks(h, plan->blocks);
             plan->max_stages = (plan->tiles + plan->blocks - 1) / plan->blocks;
+            if (algo == AR_ALGO_ONESHOT || algo == AR_ALGO_TWOSHOT)
+                plan->pace_cycles = (int32_t)pace_cycles(h, bytes, *plan, plan->blocks);
         }
         return AR_OK;
     }
@@ -1219,6 +1287,8 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) 
     if (rc == AR_OK && plan->blocks > 0) {
         plan->blocks = handle_blocks(h, plan->blocks);
         plan->max_stages = (plan->tiles + plan->blocks - 1) / plan->blocks;
+        if (op == 0 && (algo == AR_ALGO_ONESHOT || algo == AR_ALGO_TWOSHOT))
+            plan->pace_cycles = (int32_t)pace_cycles(h, bytes, *plan, plan->blocks);
     }
     return rc;
 }

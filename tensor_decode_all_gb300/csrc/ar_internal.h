@@ -65,6 +65,8 @@ struct DevState {
     int cmax;                  // counter slots per rank (>= bmax; cluster-form grids may use them all)
     uint8_t *push;             // push form: [2][R reader][R writer][slot_bytes] receive areas, or null
     unsigned long long *push_flags;  // push form: [R reader][R writer][bmax][kFlagStrideWords]
+    uint32_t pace_cycles;      // block b starts its first stage's slot stores b * pace_cycles SM cycles
+                               // after its start (0: at once); see the pacing tactic
 };
 
 // The input and output pointers of every rank, passed by value to a launch

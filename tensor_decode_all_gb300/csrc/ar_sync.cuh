@@ -161,6 +161,21 @@ __device__ __forceinline__ unsigned long long stage_tag(unsigned long long x) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Pacing of the first stage's slot stores (slots in host memory).  Block b
+// of every rank starts them b * pace SM cycles after its own start, so the
+// call's stores reach the host link about as fast as it drains them instead
+// of all at once.  A block's release then waits for its own stores rather
+// than for the whole call's, its flag comes up early, and the peers' reads of
+// the early blocks' tiles overlap the later blocks' stores (both directions
+// of the link busy at once).  The host bounds b * pace (a few ms at most);
+// pace = 0 stores at once.
+__device__ __forceinline__ void pace_first_stage(long long c0, int b, uint32_t pace) {
+    if (pace == 0) return;
+    const long long until = c0 + (long long)b * (long long)pace;
+    while (clock64() < until) {
+    }
+}
+
 // Block 0 of a rank, once it knows its call count: set the call count of this
 // rank's blocks that the call does not launch (gridDim.x <= b < cmax) to the
 // count every launched block will have after the call.  Every block of a rank
