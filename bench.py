@@ -591,6 +591,29 @@ def roofline(op, R, S, slots, t_call_s, link, hbm_gbs, algo=None):
                     "bytes per call of the same kernel over this call time (null without a valid capture)"}
 
 
+def add_link_floors(rf, lat, link, t_call_s):
+    """Beside the per-direction floor that `frac` uses, two more floors of a
+    host-link call, both measured in this run: the duplex floor (each direction
+    at the rate the probe sees while the other direction is busy too -- the
+    link does not give both directions their solo rates at once) and the
+    latency chain one tile must pass in protocol order (its stores acknowledged
+    by a system-scope fence, the flag's one-way trip, one dependent read round
+    trip).  No call can beat the larger of them; neither counts the launch."""
+    W, Rd = rf["algorithmic_bytes_per_call"]["link_write"], rf["algorithmic_bytes_per_call"]["link_read"]
+    gb = 1e9
+    per_dir = link_floor_s(W, Rd, link)
+    duplex = max(W / (link["bidir_write_gbs"] * gb), Rd / (link["bidir_read_gbs"] * gb))
+    chain = (lat["store_4KiB_fence_sys_ns"] + lat["flag_host_sys_one_way_ns"] + lat["host_load_rtt_ns"]) * 1e-9
+    rf["floors_us"] = {"per_direction": round(per_dir * 1e6, 3), "duplex": round(duplex * 1e6, 3),
+                       "latency_chain": round(chain * 1e6, 3)}
+    rf["frac_duplex"] = round(duplex / t_call_s, 4)
+    rf["link_latency_ns"] = {k: round(v, 1) for k, v in lat.items()}
+    rf["floors_note"] = ("frac = per_direction / t (each direction at its solo rate, both at once: not reachable, "
+                         "the link gives ~138 + 138 GB/s with both directions busy); frac_duplex = duplex / t; "
+                         "latency_chain = publish (4 KiB stores + system-scope fence) + flag one way + one read "
+                         "round trip, from ar_probe_host_link_latency")
+
+
 def attach_traffic(row, prof, t_call_s, hbm_gbs):
     """DRAM bytes per call from the committed ncu summary, and the fraction of
     the measured HBM peak they reach at this call time."""
@@ -866,6 +889,7 @@ def run_ours(args, dist):
         head["roofline"]["link_traffic"] = {"read": prof["link_read_bytes_per_call"],
                                             "write": prof["link_write_bytes_per_call"],
                                             "source": prof["source"]}
+    add_link_floors(head["roofline"], tda.ar_probe_host_link_latency(200), link, head["us_per_call"] * 1e-6)
     S = numel * 2
     n = dist.world
     value = n * S * len(ms) * C / total_s / 1e9

@@ -565,6 +565,24 @@ AR_API const char *ar_strerror(int code);
  *   read + write bytes.
  */
 AR_API int ar_probe_host_link(uint64_t bytes, int reps, double gbs[4]);
+
+/*
+ * ar_probe_host_link_latency: the latencies that bound the protocol at small
+ *   sizes, each the best of three runs of `reps` (1..100000) repetitions, in ns:
+ *   ns[0] = one dependent 8-byte load from mapped pinned host memory (a round
+ *           trip over the host link);
+ *   ns[1] = one block stores 4 KiB to mapped host memory, then a system-scope
+ *           fence returns (the block's stores acknowledged: its publish step);
+ *   ns[2] = a flag's one-way trip through mapped host memory at system scope
+ *           (release store by one block seen by another block's acquire polls:
+ *           half a ping-pong round trip) -- the flag step of a pinned call;
+ *   ns[3] = the same through HBM at GPU scope -- the flag step of an HBM call.
+ * Two blocks of one kernel play the ping-pong (always resident together); each
+ * of their waits is bounded (100 ms): AR_ETIMEOUT if one runs out.  Allocates
+ * and frees its own buffers and stream.  Errors: AR_EINVAL, AR_ENOMEM,
+ * AR_ECUDA, AR_ETIMEOUT.
+ */
+AR_API int ar_probe_host_link_latency(int reps, double ns[4]);
 AR_API int ar_probe_hbm_copy(uint64_t bytes, int reps, double *gbs);
 
 #ifdef __cplusplus

@@ -132,6 +132,8 @@ def lib():
             L.ar_strerror.restype = ctypes.c_char_p
             L.ar_probe_host_link.argtypes = [u64, i32, ctypes.POINTER(ctypes.c_double)]
             L.ar_probe_hbm_copy.argtypes = [u64, i32, ctypes.POINTER(ctypes.c_double)]
+            L.ar_probe_host_link_latency.argtypes = [i32, ctypes.POINTER(ctypes.c_double)]
+            L.ar_probe_host_link_latency.restype = i32
             _lib = L
     return _lib
 
@@ -285,6 +287,15 @@ def ar_probe_host_link(nbytes: int, reps: int):
     if rc:
         raise ArError(rc, "ar_probe_host_link")
     return {"write_gbs": out[0], "read_gbs": out[1], "bidir_write_gbs": out[2], "bidir_read_gbs": out[3]}
+
+
+def ar_probe_host_link_latency(reps: int = 200):
+    out = (ctypes.c_double * 4)()
+    rc = lib().ar_probe_host_link_latency(int(reps), out)
+    if rc:
+        raise ArError(rc, "ar_probe_host_link_latency")
+    return {"host_load_rtt_ns": out[0], "store_4KiB_fence_sys_ns": out[1], "flag_host_sys_one_way_ns": out[2],
+            "flag_hbm_gpu_one_way_ns": out[3]}
 
 
 def ar_probe_hbm_copy(nbytes: int, reps: int) -> float:

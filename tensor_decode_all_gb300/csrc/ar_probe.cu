@@ -1,4 +1,5 @@
-// ar_probe.cu -- bandwidth probes that give the roofline denominators.
+// ar_probe.cu -- bandwidth probes that give the roofline denominators, and
+// latency probes of the host link that bound the small calls.
 //
 // Host link: zero-copy kernels that stream to and from mapped pinned host
 // memory with 16-byte accesses, alone and both directions at once (the pages'
@@ -73,6 +74,75 @@ __global__ void probe_host_copy_kernel(uint4 *dst, const uint4 *src, uint64_t nv
         for (int k = 0; k < kUnroll; ++k) dst[i + k * stride] = v[k];
     }
     for (; i < nvec; i += stride) dst[i] = src[i];
+}
+
+// ---- latencies of the host link (one block or two, so nothing queues)
+
+__device__ __forceinline__ unsigned long long probe_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// n dependent 8-byte loads, each from the line the previous one named: one
+// round trip to the memory behind `buf` per load.
+__global__ void probe_chase_kernel(const unsigned long long *buf, int n, unsigned long long *out) {
+    unsigned long long i = 0;
+    const unsigned long long t0 = probe_timer_ns();
+    for (int k = 0; k < n; ++k) {
+        unsigned long long v;
+        asm volatile("ld.relaxed.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(buf + i * 16) : "memory");
+        i = v;
+    }
+    out[0] = probe_timer_ns() - t0;
+    out[1] = i;
+}
+
+// n rounds of: every thread of one block stores 16 bytes to host memory (4
+// KiB with 256 threads), barrier, thread 0 a system-scope fence (returns once
+// the stores are acknowledged), barrier -- the publish step of a block.
+__global__ void probe_store_fence_kernel(uint4 *dst, int n, unsigned long long *out) {
+    const unsigned long long t0 = probe_timer_ns();
+    for (int k = 0; k < n; ++k) {
+        dst[(uint64_t)(k & 63) * blockDim.x + threadIdx.x] = make_uint4(k, 1, 2, 3);
+        __syncthreads();
+        if (threadIdx.x == 0) asm volatile("fence.sc.sys;" ::: "memory");
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) out[0] = probe_timer_ns() - t0;
+}
+
+// Two blocks pass a counter back and forth n times through two flag words
+// (release store, acquire polls), system or GPU scope.  Every wait is bounded
+// (100 ms); a wait that runs out sets *err and ends the kernel.
+template <int SYS>
+__global__ void probe_pingpong_kernel(unsigned long long *f, int n, unsigned long long *out, unsigned int *err) {
+    if (threadIdx.x != 0) return;
+    unsigned long long *mine = f + (blockIdx.x ? 16 : 0), *theirs = f + (blockIdx.x ? 0 : 16);
+    const unsigned long long t0 = probe_timer_ns();
+    for (int k = 1; k <= n; ++k) {
+        const unsigned long long want = (unsigned long long)k;
+        if (blockIdx.x == 0) {
+            if (SYS) asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(mine), "l"(want) : "memory");
+            else asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(mine), "l"(want) : "memory");
+        }
+        const unsigned long long s = probe_timer_ns();
+        for (;;) {
+            unsigned long long v;
+            if (SYS) asm volatile("ld.acquire.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(theirs) : "memory");
+            else asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(theirs) : "memory");
+            if (v >= want) break;
+            if (*(volatile unsigned int *)err || probe_timer_ns() - s > 100000000ull) {
+                atomicExch(err, 1u);
+                return;
+            }
+        }
+        if (blockIdx.x == 1) {
+            if (SYS) asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(mine), "l"(want) : "memory");
+            else asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(mine), "l"(want) : "memory");
+        }
+    }
+    if (blockIdx.x == 0) out[0] = probe_timer_ns() - t0;
 }
 
 int grid_for(const void *k, int threads) {
@@ -163,6 +233,83 @@ AR_API int ar_probe_host_link(uint64_t bytes, int reps, double gbs[4]) {
     if (hw) cudaFreeHost(hw);
     if (hr) cudaFreeHost(hr);
     if (sink) cudaFree(sink);
+    (void)cudaGetLastError();
+    return rc;
+}
+
+AR_API int ar_probe_host_link_latency(int reps, double ns[4]) {
+    if (!ns || reps < 1 || reps > 100000) return AR_EINVAL;
+    constexpr int kLines = 4096;                  // chase over 4096 lines of 128 B (512 KiB)
+    const uint64_t host_bytes = (uint64_t)kLines * 128;
+    void *hb = nullptr, *hf = nullptr;
+    unsigned long long *dhb = nullptr, *dhf = nullptr, *dflag = nullptr, *dout = nullptr;
+    unsigned int *derr = nullptr;
+    cudaStream_t st = nullptr;
+    int rc = AR_OK;
+    const unsigned fl = cudaHostAllocMapped | cudaHostAllocPortable;
+    if (cudaHostAlloc(&hb, host_bytes, fl) != cudaSuccess || cudaHostAlloc(&hf, 4096, fl) != cudaSuccess ||
+        cudaMalloc((void **)&dflag, 4096) != cudaSuccess || cudaMalloc((void **)&dout, 64) != cudaSuccess ||
+        cudaMalloc((void **)&derr, 64) != cudaSuccess)
+        rc = AR_ENOMEM;
+    if (rc == AR_OK) {
+        unsigned long long *h = static_cast<unsigned long long *>(hb);
+        std::memset(hb, 0, host_bytes);
+        for (int i = 0; i < kLines; ++i) h[(size_t)i * 16] = (unsigned long long)((i * 1237 + 1) % kLines);
+        if (cudaHostGetDevicePointer((void **)&dhb, hb, 0) != cudaSuccess ||
+            cudaHostGetDevicePointer((void **)&dhf, hf, 0) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaMemsetAsync(derr, 0, 64, st) != cudaSuccess)
+            rc = AR_ECUDA;
+    }
+    unsigned long long hout[2] = {0, 0};
+    auto run = [&](auto launch, int per) -> double {
+        double best = 1e30;
+        for (int rep = 0; rep < 3 && rc == AR_OK; ++rep) {
+            launch();
+            if (cudaMemcpyAsync(hout, dout, 16, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+                cudaStreamSynchronize(st) != cudaSuccess) {
+                rc = AR_ECUDA;
+                break;
+            }
+            unsigned int e = 0;
+            if (cudaMemcpy(&e, derr, 4, cudaMemcpyDeviceToHost) != cudaSuccess) rc = AR_ECUDA;
+            else if (e) rc = AR_ETIMEOUT;
+            const double v = (double)hout[0] / per;
+            if (v < best) best = v;
+        }
+        return best;
+    };
+    if (rc == AR_OK) ns[0] = run([&] { probe_chase_kernel<<<1, 1, 0, st>>>(dhb, reps, dout); }, reps);
+    if (rc == AR_OK)
+        ns[1] = run([&] { probe_store_fence_kernel<<<1, 256, 0, st>>>(reinterpret_cast<uint4 *>(dhb), reps, dout); },
+                    reps);
+    if (rc == AR_OK) {
+        std::memset(hf, 0, 4096);
+        // a round trip is two one-way trips
+        ns[2] = run(
+            [&] {
+                std::memset(hf, 0, 4096);
+                probe_pingpong_kernel<1><<<2, 32, 0, st>>>(dhf, reps, dout, derr);
+            },
+            2 * reps);
+    }
+    if (rc == AR_OK)
+        ns[3] = run(
+            [&] {
+                cudaMemsetAsync(dflag, 0, 4096, st);
+                probe_pingpong_kernel<0><<<2, 32, 0, st>>>(dflag, reps, dout, derr);
+            },
+            2 * reps);
+    if (rc == AR_OK && cudaGetLastError() != cudaSuccess) rc = AR_ECUDA;
+    if (st) {
+        cudaStreamSynchronize(st);
+        cudaStreamDestroy(st);
+    }
+    if (hb) cudaFreeHost(hb);
+    if (hf) cudaFreeHost(hf);
+    if (dflag) cudaFree(dflag);
+    if (dout) cudaFree(dout);
+    if (derr) cudaFree(derr);
     (void)cudaGetLastError();
     return rc;
 }

@@ -3,13 +3,15 @@
 The library's built-in table (ar_choose_algo) puts the one-shot / two-shot
 crossover, the sizes up to which the tagged-word form beats the flag
 protocol, and the sizes up to which the cluster form beats the flag forms
-when every rank launches at once, where they were measured on one GB300.  A caller on another GPU, or
+when every rank launches at once, and the pace of the first stage's slot
+stores over the host link, where they were measured on one GB300.  A caller on another GPU, or
 with another clock or memory configuration, can measure them again: ``tune``
 times the forms at power-of-two sizes, each in a CUDA graph of several calls
 of every rank (the way decode replays them), picks the smallest measured size
 from which two-shot is faster at that size and at every larger one, and the
-largest size up to which tagged words are faster at every smaller one, and
-sets both on the handle.  ``save`` / ``load`` keep the result in a JSON file
+largest size up to which tagged words are faster at every smaller one,
+and, for slots in host memory, the fastest pace for a call of one stage per
+block and for one of several, and sets them on the handle.  ``save`` / ``load`` keep the result in a JSON file
 keyed by the GPU and the handle's shape, so a later process applies it
 without measuring ("[SM120] Add optional FlashInfer PCIe-IPC all-reduce for
 switch-free hosts", section "Modifications": a tuned, per-size choice of
@@ -170,6 +172,60 @@ def measure_cluster(handle, sizes=None, replays: int = 5) -> dict:
     return times
 
 
+PACES = (0, 220000, 280000, 356000, 440000)
+
+
+def best_pace(times: dict) -> int:
+    """times: {pace: us}.  The fastest pace (0 = unpaced); ties go to the
+    smaller pace, the gentler on the link."""
+    return min(sorted(times), key=lambda p: times[p])
+
+
+def pace_sizes(handle):
+    """(single, multi): a payload whose call takes one stage per block (the
+    largest power of two up to 1 MiB that does, at least the handle's smallest
+    paced size) and one that takes several (the smallest larger power of two
+    that does); None where the handle's max payload has none."""
+    max_bytes = handle.max_numel * 2
+    min_bytes = max(handle.tactics()["pace_min_bytes"], 1 << 12)
+    single = multi = None
+    for k in range(12, 27):
+        nbytes = 1 << k
+        if nbytes > max_bytes:
+            break
+        p = handle.plan("allreduce", nbytes // 2)
+        if p.tiles <= p.blocks:
+            if nbytes >= min_bytes and nbytes <= (1 << 20):
+                single = nbytes
+        elif multi is None:
+            multi = nbytes
+    return single, multi
+
+
+def measure_pace(handle, paces=PACES, replays: int = 5) -> dict:
+    """{"single": {pace: us}, "multi": {pace: us}}: per-rank launches in the
+    handle's AUTO form at the two sizes of pace_sizes, each pace set for both
+    kinds of call.  The handle's tactics are restored afterwards."""
+    saved_algo, saved = handle.info().algo, handle.tactics()
+    single, multi = pace_sizes(handle)
+    out = {}
+    try:
+        handle.set_algo("auto")
+        for name, nbytes in (("single", single), ("multi", multi)):
+            if nbytes is None:
+                continue
+            calls = max(4, min(20, (256 << 20) // (handle.R * nbytes * 2)))
+            out[name] = {"bytes": nbytes, "us": {}}
+            for pace in paces:
+                handle.set_tactics(pace_mbs=pace, pace_multi_mbs=pace)
+                out[name]["us"][pace] = _time_form(handle, "auto", nbytes, calls, replays)
+            handle.set_tactics(**saved)
+    finally:
+        handle.set_algo(saved_algo)
+        handle.set_tactics(**saved)
+    return out
+
+
 def tune(handle, sizes=None, tagged_sizes=None, cluster_sizes=None, replays: int = 5) -> dict:
     """Measure the crossovers -- one-shot / two-shot (sizes), tagged words /
     one-shot (tagged_sizes: by default powers of two from 2 KiB to the smaller
@@ -190,9 +246,21 @@ def tune(handle, sizes=None, tagged_sizes=None, cluster_sizes=None, replays: int
         cluster_times = measure_cluster(handle, cluster_sizes, replays)
         tw, limit = cluster_tactics(cluster_times)
         handle.set_tactics(cluster_twoshot_min_bytes=tw, cluster_max_bytes=limit)
+    pace_times = {}
+    if handle.info().slot_kind == 0:
+        pace_times = measure_pace(handle, replays=replays)
+        changes = {}
+        if "single" in pace_times:
+            changes["pace_mbs"] = best_pace(pace_times["single"]["us"])
+        if "multi" in pace_times:
+            changes["pace_multi_mbs"] = best_pace(pace_times["multi"]["us"])
+        if changes:
+            handle.set_tactics(**changes)
     return {"tactics": handle.tactics(), "times_us": {str(k): v for k, v in times.items()},
             "tagged_times_us": {str(k): v for k, v in tagged_times.items()},
-            "cluster_times_us": {str(k): v for k, v in cluster_times.items()}}
+            "cluster_times_us": {str(k): v for k, v in cluster_times.items()},
+            "pace_times_us": {k: {"bytes": v["bytes"], "us": {str(p): t for p, t in v["us"].items()}}
+                              for k, v in pace_times.items()}}
 
 
 def save(path: str, key: str, tactics: dict) -> None:

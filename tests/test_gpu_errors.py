@@ -215,6 +215,20 @@ def test_probes_run():
     assert tda.ar_probe_hbm_copy(1 << 30, 5) > 100.0
 
 
+def test_link_latency_probe_is_ordered():
+    """The latency probe's figures are positive and keep the order the
+    hardware implies: an HBM flag at GPU scope is faster than a host-memory
+    flag at system scope, a host round trip is slower than nothing, and the
+    probe rejects nonsense repetition counts."""
+    from tensor_decode_all_gb300 import ar
+    tda = _tda()
+    lat = tda.ar_probe_host_link_latency(100)
+    assert all(20.0 < v < 1e6 for v in lat.values()), lat
+    assert lat["flag_hbm_gpu_one_way_ns"] < lat["flag_host_sys_one_way_ns"], lat
+    with pytest.raises(ar.ArError):
+        tda.ar_probe_host_link_latency(0)
+
+
 def test_one_host_thread_per_rank():
     """Each rank's calls enqueued from its own host thread, as separate
     processes would: the C ABI's host-side bookkeeping is thread-safe and every

@@ -116,6 +116,23 @@ def test_tune_sets_a_measured_threshold_and_the_file_applies_it(tmp_path):
         x.destroy()
 
 
+def test_tune_measures_the_pace_of_a_pinned_handle():
+    """Over the host link the tuner also times each pace on a call of one
+    stage per block and on one of several, and keeps the fastest of each."""
+    import tensor_decode_all_gb300 as tda
+    from tensor_decode_all_gb300 import tune
+    h = tda.Handle(2, torch.float16, 2 << 20, "pinned")
+    out = tune.tune(h, sizes=[256 << 10, 1 << 20], tagged_sizes=[4 << 10], cluster_sizes=[], replays=3)
+    pt = out["pace_times_us"]
+    assert set(pt) == {"single", "multi"}
+    assert pt["single"]["bytes"] == 1 << 20 and pt["multi"]["bytes"] == 2 << 20
+    for kind, field in (("single", "pace_mbs"), ("multi", "pace_multi_mbs")):
+        us = {int(k): v for k, v in pt[kind]["us"].items()}
+        assert sorted(us) == sorted(tune.PACES) and all(v > 0 for v in us.values())
+        assert out["tactics"][field] == tune.best_pace(us) == h.tactics()[field]
+    h.destroy()
+
+
 def test_settings_are_refused_while_a_call_is_half_issued():
     """Between the ranks' halves of one call the form, the tactics and the
     trace setting stay as they are (changed there, the ranks of the call

@@ -66,3 +66,33 @@ def test_cluster_tactics_crossover_then_limit_against_the_flag_forms():
           8192: {"cluster_oneshot": 3.0, "cluster_twoshot": 5.0, "flags": 3.5}}
     assert tune.cluster_tactics(t2) == (tune.NEVER, 0)
     assert tune.cluster_tactics({}) == (tune.NEVER, 0)
+
+
+def test_best_pace_is_the_fastest_and_ties_go_to_the_gentler_pace():
+    assert tune.best_pace({0: 7.9, 220000: 8.2, 356000: 7.1, 440000: 7.2}) == 356000
+    assert tune.best_pace({0: 5.0, 356000: 5.0}) == 0
+    assert tune.best_pace({220000: 63.5, 356000: 72.5, 0: 77.0}) == 220000
+
+
+class _FakePlan:
+    def __init__(self, tiles, blocks):
+        self.tiles, self.blocks = tiles, blocks
+
+
+class _FakeHandle:
+    """A pinned R=2 handle's plans: one 4 KiB tile per block up to 380 blocks."""
+    def __init__(self, max_numel, pace_min=128 << 10):
+        self.max_numel, self.pace_min = max_numel, pace_min
+
+    def tactics(self):
+        return {"pace_min_bytes": self.pace_min}
+
+    def plan(self, op, numel):
+        tiles = -(-numel * 2 // 4096)
+        return _FakePlan(tiles, min(tiles, 380))
+
+
+def test_pace_sizes_pick_a_single_stage_and_a_multi_stage_payload():
+    assert tune.pace_sizes(_FakeHandle(4 << 20)) == (1 << 20, 2 << 20)
+    assert tune.pace_sizes(_FakeHandle(128 << 10)) == (256 << 10, None)     # 256 KiB max payload
+    assert tune.pace_sizes(_FakeHandle(32 << 10)) == (None, None)           # below the smallest paced size
