@@ -188,7 +188,8 @@ typedef struct ar_plan {
     int32_t vec_bytes;      /* bytes per vector access: 16 for all-reduce */
     int32_t unroll;         /* vectors per thread per tile (two-shot: R * subtile_vecs / threads, rounded up) */
     int32_t algo;           /* AR_ALGO_ONESHOT, _TWOSHOT or _TAGGED (allgather: one-shot) */
-    int32_t flag_rounds;    /* flag rounds per tile: 1 or 2 */
+    int32_t flag_rounds;    /* flag rounds of a block with one tile: 1 or 2 (a two-shot block with n tiles
+                               waits n + 1 times: each reduced sub-tile rides on the next tile's round) */
     int32_t subtile_vecs;   /* two-shot: vectors per sub-tile (64, 128 or 256; a tile is R sub-tiles); else 0 */
     int32_t pace_cycles;    /* SM cycles between the first-stage slot stores of consecutive blocks (the
                                pace_mbs tactics, slots in host memory); 0: all at once.  ar_plan_for

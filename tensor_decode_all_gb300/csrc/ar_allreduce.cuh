@@ -263,28 +263,39 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 5 : 4)
 // Two-shot variant, for large payloads at R >= 4, where the one-shot form's
 // R * (R - 1) * S bytes of peer-slot reads per call saturate L2.  A tile is R
 // sub-tiles of SUB vectors (SUB = 256, 128 or 64: smaller sub-tiles spread a
-// mid-sized payload over more blocks).  Per stage, each block of rank r:
+// mid-sized payload over more blocks).  For one tile, each block of rank r:
 //   1. copies the whole tile of in_r into slot[parity][r]; barrier; raises its
-//      flag to seq + 2s + 1 (release);
-//   2. waits for every peer's flag to reach seq + 2s + 1; reduces sub-tile r:
-//      reads it from all R slots, adds in fp32 in rank order 0..R-1, rounds
-//      once, and overwrites sub-tile r of its own slot with the result (only
-//      rank r ever reads sub-tile r of any slot in this round); barrier; raises
-//      its flag to seq + 2s + 2;
-//   3. waits for every peer's flag to reach seq + 2s + 2; copies sub-tile p of
-//      slot p (rank p's rounded result) into out_r for every p.
+//      flag (release);
+//   2. waits for every peer's flag; reduces sub-tile r: reads it from all R
+//      slots, adds in fp32 in rank order 0..R-1, rounds once;
+//   3. writes the result over sub-tile r of its own slot (only rank r ever
+//      reads sub-tile r of any slot as input); barrier; raises its flag;
+//   4. waits for every peer's flag; copies sub-tile p of slot p (rank p's
+//      rounded result) into out_r for every p.
+// With several tiles per block, step 3 of tile k shares its flag round with
+// step 1 of tile k + 1 (one round per tile, plus one), and the next tile's
+// input is copied into shared memory while a round's flags are awaited.
 // Each element is reduced once, by one rank, in rank order, so every rank
 // receives the same bits as the one-shot form and the oracle.  Per call, slot
 // reads fall from R * (R - 1) * S to about 2 * R * S bytes.
 //
-// Blocks per SM: the form is bound by the latency of its two flag rounds per
-// stage, so more resident blocks keep more tiles in flight.  Up to R = 4 the
+// Blocks per SM: the form is bound by the latency of its flag rounds, so more
+// resident blocks keep more tiles in flight.  Up to R = 4 the
 // kernel fits in 40 registers without spilling and runs 6 blocks per SM; above
 // that the sub-tile accumulators need more, and it keeps 4.
 template <int R>
 constexpr int twoshot_min_blocks() { return R <= 4 ? 6 : 4; }
 
-template <class Ops, int R, int SUB, bool F, bool T>
+// 16-byte asynchronous copy from global to shared memory (no register
+// staging), and the waits that make a thread's own copies visible to it.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const unsigned int a = (unsigned int)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(a), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+template <class Ops, int R, int SUB, bool F, bool T, bool M>
 __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
     allreduce_twoshot_kernel(const uint16_t *in_arg, uint16_t *out_arg, uint64_t numel, int rank_arg, DevState d, RankIO io) {
     static_assert(SUB == 64 || SUB == 128 || SUB == 256, "sub-tile of 64, 128 or 256 vectors");
@@ -308,6 +319,10 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
     constexpr int kPer = (int)((kTileVecs + kThreads - 1) / kThreads);
     const uint64_t ntiles = (nv + kTileVecs - 1) / kTileVecs;
     const uint64_t nstages = ntiles > (uint64_t)b ? (ntiles - b + B - 1) / B : 0;
+    // The next stage's tile of in_r, copied asynchronously while this stage's
+    // two flag rounds run.  Each thread copies, and later reads back, only its
+    // own vectors of the tile, so its own wait is the only ordering needed.
+    __shared__ uint4 s_next[kTileVecs];
 
     pdl_wait();
     const long long c0 = clock64();
@@ -326,83 +341,227 @@ __global__ void __launch_bounds__(kThreads, twoshot_min_blocks<R>())
     uint4 *const slot_base = reinterpret_cast<uint4 *>(d.slots) + (uint64_t)parity * R * slot_vecs;
     uint4 *const my_slot = slot_base + (uint64_t)rank * slot_vecs;
 
-    for (uint64_t s = 0; s < nstages; ++s) {
-        const uint64_t tbase = ((uint64_t)b + s * B) * kTileVecs;
+    // M = false: two flag rounds per tile.  M = true: each reduced sub-tile
+    // rides on the next tile's flag round (below); the host picks it for slots
+    // in HBM and calls of several tiles per block.  Measured on a GB300 (bf16,
+    // graphs): merged rounds take R = 8 16 MiB from 92.1 to 82.3 us and 64 MiB
+    // from 340 to 297 us, but cost 2-5 % on single-stage calls of 256-vector
+    // sub-tiles and 3-4 % on multi-stage calls over the host link, which keep
+    // the two rounds.
+    const uint64_t rounds = M ? (nstages ? nstages + 1 : 0) : 2 * nstages;
+    if constexpr (!M) {
+        for (uint64_t s = 0; s < nstages; ++s) {
+            const uint64_t tbase = ((uint64_t)b + s * B) * kTileVecs;
 
-        // 1. publish the whole tile (tile-local vector u * kThreads + tid)
-        uint4 pub[kPer];
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const uint64_t li = (uint64_t)u * kThreads + tid;
-            pub[u] = li < kTileVecs ? load_own(in, tbase + li, nvec_full, tail) : make_uint4(0u, 0u, 0u, 0u);
-        }
-        if (s == 0) pace_first_stage(c0, b, d.pace_cycles);
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const uint64_t li = (uint64_t)u * kThreads + tid;
-            if (li < kTileVecs && tbase + li < nv) my_slot[tbase + li] = pub[u];
-        }
-        __syncthreads();
-        if (tid == 0) {
-            publish_stage(d, rank, b, seq + 2 * s + 1);
-            trace_published<T>(d, s_tr);
-        }
-        if (wait_peers(d, R, rank, b, seq + 2 * s + 1, &s_bail)) return;
-        if (tid == 0) trace_peers<T>(d, s_tr);
-
-        // 2. reduce sub-tile `rank` in rank order; the result replaces it in my slot
-        const uint64_t vr = tbase + (uint64_t)rank * SUB + tid;
-        uint4 res = make_uint4(0u, 0u, 0u, 0u);
-        if (tid < SUB && vr < nv) {
-            uint4 vals[R];
-#pragma unroll
-            for (int p = 0; p < R; ++p) vals[p] = ld_cg_v4(slot_base + (uint64_t)p * slot_vecs + vr);
-            float acc[8];
-            accumulate8<Ops, true>(acc, vals[0]);
-#pragma unroll
-            for (int p = 1; p < R; ++p) accumulate8<Ops, false>(acc, vals[p]);
-            res = narrow8<Ops>(acc);
-            my_slot[vr] = res;
-        }
-        __syncthreads();
-        if (tid == 0) publish_stage(d, rank, b, seq + 2 * s + 2);
-        if (wait_peers(d, R, rank, b, seq + 2 * s + 2, &s_bail)) return;
-        // Every peer block of this call has now published its last stage, so
-        // all of them are resident: this rank's next call may be scheduled.
-        if (s + 1 == nstages) pdl_trigger();
-
-        // 3. gather the R rounded sub-tiles
-        uint4 got[kPer];
-        if constexpr (SUB == kThreads) {
-            // tile-local vector u * kThreads + tid lies in sub-tile u; this
-            // thread reduced vector tid of sub-tile `rank` itself
-#pragma unroll
-            for (int u = 0; u < kPer; ++u) {
-                const uint64_t v = tbase + (uint64_t)u * kThreads + tid;
-                got[u] = res;
-                if (u != rank && v < nv) got[u] = ld_cg_v4(slot_base + (uint64_t)u * slot_vecs + v);
-            }
-        } else {
-            // a sub-tile is narrower than the block: read every result, this
-            // rank's included, from the slots (the barrier above orders them)
+            // 1. publish the whole tile (tile-local vector u * kThreads + tid):
+            // full vectors of a later stage from the prefetched copy, the rest
+            // (stage 0, a partial last vector) loaded here
+            if (s > 0) cp_async_wait_all();
+            uint4 pub[kPer];
 #pragma unroll
             for (int u = 0; u < kPer; ++u) {
                 const uint64_t li = (uint64_t)u * kThreads + tid;
-                const uint64_t v = tbase + li;
-                got[u] = make_uint4(0u, 0u, 0u, 0u);
-                if (li < kTileVecs && v < nv) got[u] = ld_cg_v4(slot_base + (li / SUB) * slot_vecs + v);
+                if (s > 0 && li < kTileVecs && tbase + li < nvec_full)
+                    pub[u] = s_next[li];
+                else
+                    pub[u] = li < kTileVecs ? load_own(in, tbase + li, nvec_full, tail) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (s == 0) pace_first_stage(c0, b, d.pace_cycles);
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const uint64_t li = (uint64_t)u * kThreads + tid;
+                if (li < kTileVecs && tbase + li < nv) my_slot[tbase + li] = pub[u];
+            }
+            __syncthreads();
+            if (tid == 0) {
+                publish_stage(d, rank, b, seq + 2 * s + 1);
+                trace_published<T>(d, s_tr);
+            }
+            if (s + 1 < nstages) {
+                const uint64_t tn = tbase + (uint64_t)B * kTileVecs;
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) {
+                    const uint64_t li = (uint64_t)u * kThreads + tid;
+                    if (li < kTileVecs && tn + li < nvec_full) cp_async16(&s_next[li], in + (tn + li) * 8);
+                }
+                cp_async_commit();
+            }
+            if (wait_peers(d, R, rank, b, seq + 2 * s + 1, &s_bail)) {
+                cp_async_wait_all();
+                return;
+            }
+            if (tid == 0) trace_peers<T>(d, s_tr);
+
+            // 2. reduce sub-tile `rank` in rank order; the result replaces it in my slot
+            const uint64_t vr = tbase + (uint64_t)rank * SUB + tid;
+            uint4 res = make_uint4(0u, 0u, 0u, 0u);
+            if (tid < SUB && vr < nv) {
+                uint4 vals[R];
+#pragma unroll
+                for (int p = 0; p < R; ++p) vals[p] = ld_cg_v4(slot_base + (uint64_t)p * slot_vecs + vr);
+                float acc[8];
+                accumulate8<Ops, true>(acc, vals[0]);
+#pragma unroll
+                for (int p = 1; p < R; ++p) accumulate8<Ops, false>(acc, vals[p]);
+                res = narrow8<Ops>(acc);
+                my_slot[vr] = res;
+            }
+            __syncthreads();
+            if (tid == 0) publish_stage(d, rank, b, seq + 2 * s + 2);
+            if (wait_peers(d, R, rank, b, seq + 2 * s + 2, &s_bail)) {
+                cp_async_wait_all();
+                return;
+            }
+            // Every peer block of this call has now published its last stage, so
+            // all of them are resident: this rank's next call may be scheduled.
+            if (s + 1 == nstages) pdl_trigger();
+
+            // 3. gather the R rounded sub-tiles
+            uint4 got[kPer];
+            if constexpr (SUB == kThreads) {
+                // tile-local vector u * kThreads + tid lies in sub-tile u; this
+                // thread reduced vector tid of sub-tile `rank` itself
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) {
+                    const uint64_t v = tbase + (uint64_t)u * kThreads + tid;
+                    got[u] = res;
+                    if (u != rank && v < nv) got[u] = ld_cg_v4(slot_base + (uint64_t)u * slot_vecs + v);
+                }
+            } else {
+                // a sub-tile is narrower than the block: read every result, this
+                // rank's included, from the slots (the barrier above orders them)
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) {
+                    const uint64_t li = (uint64_t)u * kThreads + tid;
+                    const uint64_t v = tbase + li;
+                    got[u] = make_uint4(0u, 0u, 0u, 0u);
+                    if (li < kTileVecs && v < nv) got[u] = ld_cg_v4(slot_base + (li / SUB) * slot_vecs + v);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const uint64_t li = (uint64_t)u * kThreads + tid;
+                if (li < kTileVecs && tbase + li < nv) store_out(out, tbase + li, nvec_full, tail, got[u]);
             }
         }
+    }
+
+    // Merged rounds, round k = 0 .. nstages:
+    //   publish input tile k (k < nstages) and this rank's reduced sub-tile of
+    //   tile k - 1 (k > 0) into the slot; barrier; raise the flag to seq + k + 1;
+    //   wait for every peer's flag to reach it; copy the R reduced sub-tiles of
+    //   tile k - 1 into out_r (k > 0); reduce sub-tile `rank` of tile k in rank
+    //   order (k < nstages), kept in registers until the next round publishes it.
+    // Each reduced sub-tile rides on the next tile's flag round, so a block
+    // of n stages waits n + 1 times rather than 2n.  The reduced sub-tile r of
+    // tile k - 1 overwrites this rank's own input sub-tile r of that tile, which
+    // only this rank ever reads (it reduced it in the round before); peers read
+    // it only after this round's flag.
+    if constexpr (M) {
+        uint4 res = make_uint4(0u, 0u, 0u, 0u);
+        for (uint64_t k = 0; k < rounds; ++k) {
+            const uint64_t tbase = ((uint64_t)b + k * B) * kTileVecs;    // tile k (k < nstages)
+            const uint64_t pbase = tbase - (uint64_t)B * kTileVecs;       // tile k - 1 (k > 0)
+
+            // 1. publish tile k (tile-local vector u * kThreads + tid): full
+            // vectors of a later stage from the prefetched copy, the rest (stage 0,
+            // a partial last vector) loaded here; and tile k - 1's reduced vector
+            if (k < nstages) {
+                if (k > 0) cp_async_wait_all();
+                uint4 pub[kPer];
 #pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const uint64_t li = (uint64_t)u * kThreads + tid;
-            if (li < kTileVecs && tbase + li < nv) store_out(out, tbase + li, nvec_full, tail, got[u]);
+                for (int u = 0; u < kPer; ++u) {
+                    const uint64_t li = (uint64_t)u * kThreads + tid;
+                    if (k > 0 && li < kTileVecs && tbase + li < nvec_full)
+                        pub[u] = s_next[li];
+                    else
+                        pub[u] = li < kTileVecs ? load_own(in, tbase + li, nvec_full, tail) : make_uint4(0u, 0u, 0u, 0u);
+                }
+                if (k == 0) pace_first_stage(c0, b, d.pace_cycles);
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) {
+                    const uint64_t li = (uint64_t)u * kThreads + tid;
+                    if (li < kTileVecs && tbase + li < nv) my_slot[tbase + li] = pub[u];
+                }
+            }
+            if (k > 0) {
+                const uint64_t vr = pbase + (uint64_t)rank * SUB + tid;
+                if (tid < SUB && vr < nv) my_slot[vr] = res;
+            }
+            __syncthreads();
+            if (tid == 0) {
+                publish_stage(d, rank, b, seq + k + 1);
+                trace_published<T>(d, s_tr);
+            }
+            if (k + 1 < nstages) {
+                const uint64_t tn = tbase + (uint64_t)B * kTileVecs;
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) {
+                    const uint64_t li = (uint64_t)u * kThreads + tid;
+                    if (li < kTileVecs && tn + li < nvec_full) cp_async16(&s_next[li], in + (tn + li) * 8);
+                }
+                cp_async_commit();
+            }
+            if (wait_peers(d, R, rank, b, seq + k + 1, &s_bail)) {
+                cp_async_wait_all();
+                return;
+            }
+            if (tid == 0) trace_peers<T>(d, s_tr);
+            // Every peer block of this call has now published its last round, so
+            // all of them are resident: this rank's next call may be scheduled.
+            if (k + 1 == rounds) pdl_trigger();
+
+            // 2. copy the R rounded sub-tiles of tile k - 1 to out_r
+            if (k > 0) {
+                uint4 got[kPer];
+                if constexpr (SUB == kThreads) {
+                    // tile-local vector u * kThreads + tid lies in sub-tile u; this
+                    // thread reduced vector tid of sub-tile `rank` itself
+#pragma unroll
+                    for (int u = 0; u < kPer; ++u) {
+                        const uint64_t v = pbase + (uint64_t)u * kThreads + tid;
+                        got[u] = res;
+                        if (u != rank && v < nv) got[u] = ld_cg_v4(slot_base + (uint64_t)u * slot_vecs + v);
+                    }
+                } else {
+                    // a sub-tile is narrower than the block: read every result, this
+                    // rank's included, from the slots (the barrier above orders them)
+#pragma unroll
+                    for (int u = 0; u < kPer; ++u) {
+                        const uint64_t li = (uint64_t)u * kThreads + tid;
+                        const uint64_t v = pbase + li;
+                        got[u] = make_uint4(0u, 0u, 0u, 0u);
+                        if (li < kTileVecs && v < nv) got[u] = ld_cg_v4(slot_base + (li / SUB) * slot_vecs + v);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kPer; ++u) {
+                    const uint64_t li = (uint64_t)u * kThreads + tid;
+                    if (li < kTileVecs && pbase + li < nv) store_out(out, pbase + li, nvec_full, tail, got[u]);
+                }
+            }
+
+            // 3. reduce sub-tile `rank` of tile k in rank order (published next round)
+            if (k < nstages) {
+                const uint64_t vr = tbase + (uint64_t)rank * SUB + tid;
+                if (tid < SUB && vr < nv) {
+                    uint4 vals[R];
+#pragma unroll
+                    for (int p = 0; p < R; ++p) vals[p] = ld_cg_v4(slot_base + (uint64_t)p * slot_vecs + vr);
+                    float acc[8];
+                    accumulate8<Ops, true>(acc, vals[0]);
+#pragma unroll
+                    for (int p = 1; p < R; ++p) accumulate8<Ops, false>(acc, vals[p]);
+                    res = narrow8<Ops>(acc);
+                }
+            }
         }
+
     }
 
     if (tid == 0) {
         Ctr c;
-        c.seq = seq + 2 * nstages;
+        c.seq = seq + rounds;
         c.calls = s_calls + 1;
         d.ctr[(size_t)rank * d.cmax + b] = c;
         trace_finish<T>(d, s_tr, R, rank, b, s_calls, nstages);
@@ -454,27 +613,27 @@ const void *allreduce_ptr_ru(int R) {
     }
 }
 
-template <class Ops, int SUB, bool F, bool T>
+template <class Ops, int SUB, bool F, bool T, bool M>
 const void *allreduce_twoshot_ptr_r(int R) {
     switch (R) {
-        case 1: return (const void *)allreduce_twoshot_kernel<Ops, 1, SUB, F, T>;
-        case 2: return (const void *)allreduce_twoshot_kernel<Ops, 2, SUB, F, T>;
-        case 3: return (const void *)allreduce_twoshot_kernel<Ops, 3, SUB, F, T>;
-        case 4: return (const void *)allreduce_twoshot_kernel<Ops, 4, SUB, F, T>;
-        case 5: return (const void *)allreduce_twoshot_kernel<Ops, 5, SUB, F, T>;
-        case 6: return (const void *)allreduce_twoshot_kernel<Ops, 6, SUB, F, T>;
-        case 7: return (const void *)allreduce_twoshot_kernel<Ops, 7, SUB, F, T>;
-        case 8: return (const void *)allreduce_twoshot_kernel<Ops, 8, SUB, F, T>;
+        case 1: return (const void *)allreduce_twoshot_kernel<Ops, 1, SUB, F, T, M>;
+        case 2: return (const void *)allreduce_twoshot_kernel<Ops, 2, SUB, F, T, M>;
+        case 3: return (const void *)allreduce_twoshot_kernel<Ops, 3, SUB, F, T, M>;
+        case 4: return (const void *)allreduce_twoshot_kernel<Ops, 4, SUB, F, T, M>;
+        case 5: return (const void *)allreduce_twoshot_kernel<Ops, 5, SUB, F, T, M>;
+        case 6: return (const void *)allreduce_twoshot_kernel<Ops, 6, SUB, F, T, M>;
+        case 7: return (const void *)allreduce_twoshot_kernel<Ops, 7, SUB, F, T, M>;
+        case 8: return (const void *)allreduce_twoshot_kernel<Ops, 8, SUB, F, T, M>;
         default: return nullptr;
     }
 }
 
-template <class Ops, bool F, bool T>
+template <class Ops, bool F, bool T, bool M>
 const void *allreduce_twoshot_ptr(int R, int sub) {
     switch (sub) {
-        case 256: return allreduce_twoshot_ptr_r<Ops, 256, F, T>(R);
-        case 128: return allreduce_twoshot_ptr_r<Ops, 128, F, T>(R);
-        case 64: return allreduce_twoshot_ptr_r<Ops, 64, F, T>(R);
+        case 256: return allreduce_twoshot_ptr_r<Ops, 256, F, T, M>(R);
+        case 128: return allreduce_twoshot_ptr_r<Ops, 128, F, T, M>(R);
+        case 64: return allreduce_twoshot_ptr_r<Ops, 64, F, T, M>(R);
         default: return nullptr;
     }
 }
@@ -501,12 +660,19 @@ const void *allreduce_ptr(int R, int U, bool fused, bool traced) {
 
 // Two-shot kernels (U < 0).  Instantiated by their own translation units, so
 // that a dtype's kernels compile in parallel.
+// Traced launches always take the kernel of two rounds per tile (no merged
+// traced kernel is built).
 template <class Ops>
 const void *allreduce_twoshot_ptr_any(int R, int U, bool fused, bool traced) {
     const int sub = twoshot_sub(U);
     if (traced)
-        return fused ? allreduce_twoshot_ptr<Ops, true, true>(R, sub) : allreduce_twoshot_ptr<Ops, false, true>(R, sub);
-    return fused ? allreduce_twoshot_ptr<Ops, true, false>(R, sub) : allreduce_twoshot_ptr<Ops, false, false>(R, sub);
+        return fused ? allreduce_twoshot_ptr<Ops, true, true, false>(R, sub)
+                     : allreduce_twoshot_ptr<Ops, false, true, false>(R, sub);
+    if (twoshot_merged(U))
+        return fused ? allreduce_twoshot_ptr<Ops, true, false, true>(R, sub)
+                     : allreduce_twoshot_ptr<Ops, false, false, true>(R, sub);
+    return fused ? allreduce_twoshot_ptr<Ops, true, false, false>(R, sub)
+                 : allreduce_twoshot_ptr<Ops, false, false, false>(R, sub);
 }
 
 }  // namespace tda

@@ -232,8 +232,10 @@ int family_occupancy(const ar_handle *h, bool fused, bool traced, int *bps) {
         for (int u = 1; u <= 2 && rc == AR_OK; ++u)
             rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, u, fused, traced), &bps[kOneShot]);
         for (int sub = 64; sub <= 256 && rc == AR_OK; sub *= 2)
-            rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, tda::twoshot_variant(sub), fused, traced),
-                                  &bps[kTwoShot]);
+            for (int m = 0; m < (traced ? 1 : 2) && rc == AR_OK; ++m)
+                rc = kernel_occupancy(
+                    tda::allreduce_kernel_ptr(h->dtype, h->R, tda::twoshot_variant(sub, m != 0), fused, traced),
+                    &bps[kTwoShot]);
         if (rc == AR_OK)
             rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, tda::kTaggedVariant, fused, traced),
                                   &bps[kTagged]);
@@ -724,7 +726,10 @@ int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
                               &plan);
     if (rc != AR_OK) return rc;
     const int blocks = handle_blocks(h, plan.blocks);
-    const int variant = algo == AR_ALGO_TWOSHOT  ? tda::twoshot_variant(plan.subtile_vecs)
+    // two-shot: flag rounds merged across tiles for slots in HBM and calls of
+    // several tiles per block, untraced (see allreduce_twoshot_kernel)
+    const bool merged = h->kind == AR_SLOT_HBM && !h->trace && plan.tiles > (uint64_t)blocks;
+    const int variant = algo == AR_ALGO_TWOSHOT  ? tda::twoshot_variant(plan.subtile_vecs, merged)
                         : algo == AR_ALGO_TAGGED ? tda::kTaggedVariant
                         : algo == AR_ALGO_PUSH   ? tda::kPushVariant
                                                  : plan.unroll;

@@ -29,9 +29,11 @@ constexpr uint64_t kSlotAlign = 256;
 // up to this many single-stage clusters (in waves) whatever the flag grids are.
 constexpr int kCounterSlots = 512;
 // Kernel variant codes for the two-shot form: a negative "unroll" whose
-// magnitude is the sub-tile size in vectors (256, 128 or 64).
-constexpr int twoshot_variant(int sub) { return -sub; }
-constexpr int twoshot_sub(int variant) { return -variant; }
+// magnitude is the sub-tile size in vectors (256, 128 or 64), plus one for the
+// kernel that merges each reduced sub-tile into the next tile's flag round.
+constexpr int twoshot_variant(int sub, bool merged = false) { return -(sub + (merged ? 1 : 0)); }
+constexpr int twoshot_sub(int variant) { return (-variant) & ~1; }
+constexpr bool twoshot_merged(int variant) { return ((-variant) & 1) != 0; }
 // Kernel variant code of the tagged-word form.
 constexpr int kTaggedVariant = 0;
 // Kernel variant code of the push form.

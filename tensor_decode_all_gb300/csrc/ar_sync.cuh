@@ -270,6 +270,13 @@ __device__ __forceinline__ bool wait_peers(const DevState &d, int R, int rank, i
                     ok = seen >= target;
                 }
                 if (__all_sync(0xffffffffu, ok)) break;
+                // The abort word and the clock every 8th poll only: read each
+                // time, the abort word's round trip would follow every flag
+                // poll's and halve how often the flag is looked at.
+                if ((++iter & 7u) != 0u) {
+                    if (iter > 64u) __nanosleep(64);
+                    continue;
+                }
                 int stop = 0;
                 if (lane == 0) {
                     if (ld_relaxed_u32(d.abort_word) != 0u)
@@ -288,7 +295,7 @@ __device__ __forceinline__ bool wait_peers(const DevState &d, int R, int rank, i
                     if (lane == 0) *s_bail = 1;
                     break;
                 }
-                if (++iter > 64u) __nanosleep(64);
+                if (iter > 64u) __nanosleep(64);
             }
         }
     }
