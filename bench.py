@@ -763,6 +763,15 @@ EXPERIMENT_WORKLOADS = {
     "x_r2_8K_hbm": ("allreduce", 2, "f16", 4096, "hbm", 1, "uniform", 100, 20),
     "x_r8_1M_fused": ("allreduce", 8, "bf16", 1 << 19, "hbm", 5, "uniform", 100, 20, {"launch": "fused"}),
     "x_r8_1M": ("allreduce", 8, "bf16", 1 << 19, "hbm", 5, "uniform", 100, 20),
+    # the allgather over the host link with its first-stage stores unpaced / paced at other rates
+    "x_ag_r4_pinned_pace0": ("allgather", 4, "c64", 500000, "pinned", 4, None, 5, 5,
+                             {"tactics": {"pace_mbs": 0, "pace_multi_mbs": 0}}),
+    "x_ag_r8_pinned_pace0": ("allgather", 8, "c64", 500000, "pinned", 4, None, 5, 5,
+                             {"tactics": {"pace_mbs": 0, "pace_multi_mbs": 0}}),
+    "x_ag_r4_pinned_pace280": ("allgather", 4, "c64", 500000, "pinned", 4, None, 5, 5,
+                               {"tactics": {"pace_multi_mbs": 280000}}),
+    "x_ag_r4_pinned_pace160": ("allgather", 4, "c64", 500000, "pinned", 4, None, 5, 5,
+                               {"tactics": {"pace_multi_mbs": 160000}}),
 }
 
 

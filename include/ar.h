@@ -220,10 +220,10 @@ typedef struct ar_tactics {
                                    calls of one stage per block.  The first stage's slot stores of block
                                    b of every rank start b * R * tile_bytes / (pace * share) after the
                                    block starts, share = the stores' part of the traffic (1/R one-shot,
-                                   (R+1)/3R two-shot), so the stores reach the link about as fast as it
-                                   drains them rather than all at once.  One-shot, two-shot and cluster
-                                   forms (the cluster form only when all its clusters are resident at
-                                   once).  0 = all at once; otherwise >= 1000.  Default 356000 for
+                                   (R+1)/3R two-shot, 1/R allgather), so the stores reach the link about
+                                   as fast as it drains them rather than all at once.  One-shot, two-shot
+                                   and cluster all-reduce forms (the cluster form only when all its
+                                   clusters are resident at once) and the allgather.  0 = all at once; otherwise >= 1000.  Default 356000 for
                                    pinned-host handles; ignored for HBM.  Timing only: the results do
                                    not change */
     uint64_t pace_min_bytes;    /* pace only calls of at least this many bytes per rank (default 128 KiB) */

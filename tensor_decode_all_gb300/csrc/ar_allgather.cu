@@ -4,7 +4,9 @@
 // rank-major concatenation used for the complex64 S_j and core uploads in
 // "fix(group): run each rank on a non-blocking stream", sections "What" and
 // "Why".  It uses the same slot and
-// flag protocol as the all-reduce: per stage, a block copies its tile of the
+// flag protocol as the all-reduce (slots in host memory: with the first
+// stage's slot stores paced as the one-shot form's, the link bytes being the
+// same): per stage, a block copies its tile of the
 // shard into slot[parity][r] and into its own place in out, raises its flag,
 // waits for its peers' flags for the same block index, then copies the peers'
 // tiles from their slots into their places in out.  Pure copies: the result
@@ -70,6 +72,7 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
     const uint64_t nstages = ntiles > (uint64_t)b ? (ntiles - b + B - 1) / B : 0;
 
     pdl_wait();
+    const long long c0 = clock64();
     if (tid == 0) {
         trace_start<T>(d, s_tr);
         const Ctr c = d.ctr[(size_t)rank * d.cmax + b];
@@ -93,6 +96,7 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
     const uint64_t slot_vecs = d.slot_bytes / VW;
     V *const slot_base = reinterpret_cast<V *>(d.slots) + (uint64_t)parity * R * slot_vecs;
     V *const my_slot = slot_base + (uint64_t)rank * slot_vecs;
+    if (nstages) pace_first_stage(c0, b, d.pace_cycles);
 
     for (uint64_t s = 0; s < nstages; ++s) {
         const uint64_t tile = (uint64_t)b + s * B;

@@ -751,8 +751,9 @@ int enqueue_allgather(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
                           h->bps[rank < 0 ? 1 : 0][h->trace ? 1 : 0][kAllgather], &plan);
     if (rc != AR_OK) return rc;
     const int blocks = handle_blocks(h, plan.blocks);
-    const cudaError_t e = tda::launch_allgather(vw, h->R, plan.unroll, blocks, s, io, bytes, rank,
-                                                dev_state(h), h->pdl);
+    DevState d = dev_state(h);
+    d.pace_cycles = pace_cycles(h, bytes, plan, blocks);  // the one-shot form's link bytes: share 1/R
+    const cudaError_t e = tda::launch_allgather(vw, h->R, plan.unroll, blocks, s, io, bytes, rank, d, h->pdl);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return AR_ECUDA;
@@ -1292,7 +1293,7 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) 
     if (rc == AR_OK && plan->blocks > 0) {
         plan->blocks = handle_blocks(h, plan->blocks);
         plan->max_stages = (plan->tiles + plan->blocks - 1) / plan->blocks;
-        if (op == 0 && (algo == AR_ALGO_ONESHOT || algo == AR_ALGO_TWOSHOT))
+        if (op == 1 || algo == AR_ALGO_ONESHOT || algo == AR_ALGO_TWOSHOT)
             plan->pace_cycles = (int32_t)pace_cycles(h, bytes, *plan, plan->blocks);
     }
     return rc;

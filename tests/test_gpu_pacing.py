@@ -161,3 +161,34 @@ def test_paced_headline_calls_replay_in_a_graph():
                 assert_bits_equal(to_bits(outs[c][r]), want, "f16", f"replay {rep} call {c} rank {r}")
     del g
     h.destroy()
+
+
+@pytest.mark.parametrize("pace", [0, 2000, 220000, 4000000])
+@pytest.mark.parametrize("R,n", [(3, 1000 * 37 + 5), (4, 1000 * 500)])
+def test_paced_allgather_matches_oracle(pace, R, n):
+    """The allgather over the host link, paced as the one-shot form (the same
+    link bytes): byte-exact against the oracle's concatenation, per-rank and
+    in one launch of every rank, at paces from 2 GB/s to far faster than the
+    link and none; several stages per block at the config-4 shard size."""
+    import tensor_decode_all_gb300 as tda
+    h = tda.Handle(R, torch.complex64, n, "pinned")
+    h.set_tactics(pace_mbs=pace, pace_multi_mbs=pace, pace_min_bytes=0)
+    assert (h.plan("allgather", n).pace_cycles > 0) == (pace > 0)
+    streams = rank_streams(R)
+    for call, launch in enumerate(("rank", "fused")):
+        zs = inputs.allgather_inputs(4, R, n, 20 + call)
+        ins = [to_dev(z, "c64") for z in zs]
+        outs = [torch.empty(R * n, dtype=torch.complex64, device="cuda") for _ in range(R)]
+        if launch == "rank":
+            enqueue(h, "allgather", ins, outs, streams)
+        else:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            h.allgather_fused(ins, outs, s)
+            torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        h.check()
+        want = oracle.allgather(zs, ranks=[0])[0]
+        for r in range(R):
+            assert_bits_equal(to_bits(outs[r]), want, "c64", f"pace={pace} R={R} {launch} rank {r}")
+    h.destroy()
