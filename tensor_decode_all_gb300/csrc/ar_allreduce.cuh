@@ -127,7 +127,12 @@ __device__ __forceinline__ void store_out(uint16_t *out, uint64_t v, uint64_t nv
     }
 }
 
-template <class Ops, int R, int U, bool F, bool T>
+// A (publish ahead): with several stages per block, a block publishes stage
+// s + 1 (loads its input, stores it into the slot, raises the flag) before it
+// waits for and reads its peers' stage s, so one stage's flag round overlaps
+// the next stage's publish.  Stage s + 1 uses its own slot region, so nothing
+// a peer still reads is touched; the flag counts published stages as before.
+template <class Ops, int R, int U, bool F, bool T, bool A>
 __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16_t *out_arg, uint64_t numel,
                                                   int rank_arg, const DevState &d, const RankIO &io) {
     __shared__ unsigned long long s_seq;
@@ -174,30 +179,59 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
     uint4 *const slot_base = reinterpret_cast<uint4 *>(d.slots) + (uint64_t)parity * R * slot_vecs;
     uint4 *const my_slot = slot_base + (uint64_t)rank * slot_vecs;
     if (nstages) pace_first_stage(c0, b, d.pace_cycles);
+    if (A && nstages) {
+        // stage 0 published before the loop; the loop publishes one ahead
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint64_t v = (uint64_t)b * kTileVecs + (uint64_t)u * kThreads + tid;
+            if (v < nv) my_slot[v] = own[u];
+        }
+        __syncthreads();
+        if (tid == 0) {
+            publish_stage(d, rank, b, seq + 1);
+            trace_published<T>(d, s_tr);
+        }
+    }
 
     for (uint64_t s = 0; s < nstages; ++s) {
         const uint64_t tile = (uint64_t)b + s * B;
         const uint64_t v0 = tile * kTileVecs + tid;
 
-        // 2. publish this stage's data
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint64_t v = v0 + (uint64_t)u * kThreads;
-            if (v < nv) my_slot[v] = own[u];
-        }
-        __syncthreads();
-        // 3. raise the flag
-        if (tid == 0) {
-            publish_stage(d, rank, b, seq + s + 1);
-            trace_published<T>(d, s_tr);
-        }
-
-        // next stage's input, overlapping the wait
         uint4 nxt[U];
-        if (s + 1 < nstages) {
-            const uint64_t vn = (tile + B) * kTileVecs + tid;
+        if constexpr (A) {
+            // 2-3. publish stage s + 1 (its input, its slot stores, its flag)
+            if (s + 1 < nstages) {
+                const uint64_t vn = (tile + B) * kTileVecs + tid;
 #pragma unroll
-            for (int u = 0; u < U; ++u) nxt[u] = load_own(in, vn + (uint64_t)u * kThreads, nvec_full, tail);
+                for (int u = 0; u < U; ++u) nxt[u] = load_own(in, vn + (uint64_t)u * kThreads, nvec_full, tail);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint64_t v = vn + (uint64_t)u * kThreads;
+                    if (v < nv) my_slot[v] = nxt[u];
+                }
+                __syncthreads();
+                if (tid == 0) publish_stage(d, rank, b, seq + s + 2);
+            }
+        } else {
+            // 2. publish this stage's data
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint64_t v = v0 + (uint64_t)u * kThreads;
+                if (v < nv) my_slot[v] = own[u];
+            }
+            __syncthreads();
+            // 3. raise the flag
+            if (tid == 0) {
+                publish_stage(d, rank, b, seq + s + 1);
+                trace_published<T>(d, s_tr);
+            }
+
+            // next stage's input, overlapping the wait
+            if (s + 1 < nstages) {
+                const uint64_t vn = (tile + B) * kTileVecs + tid;
+#pragma unroll
+                for (int u = 0; u < U; ++u) nxt[u] = load_own(in, vn + (uint64_t)u * kThreads, nvec_full, tail);
+            }
         }
 
         // 4. wait for the peers
@@ -245,19 +279,19 @@ __device__ __forceinline__ void allreduce_oneshot(const uint16_t *in_arg, uint16
 }
 
 // One rank's launch.
-template <class Ops, int R, int U, bool T>
+template <class Ops, int R, int U, bool T, bool A = false>
 __global__ void __launch_bounds__(kThreads)
     allreduce_kernel_rank(const uint16_t *in, uint16_t *out, uint64_t numel, int rank, DevState d, RankIO io) {
-    allreduce_oneshot<Ops, R, U, false, T>(in, out, numel, rank, d, io);
+    allreduce_oneshot<Ops, R, U, false, T, A>(in, out, numel, rank, d, io);
 }
 
 // A launch of all ranks, held to the blocks per SM the one-rank kernel gets
 // unasked (5 up to R = 3, else 4): with fewer resident blocks a decode-sized
 // call would need a second stage, and a large one would move less at once.
-template <class Ops, int R, int U, bool T>
+template <class Ops, int R, int U, bool T, bool A = false>
 __global__ void __launch_bounds__(kThreads, R <= 3 ? 5 : 4)
     allreduce_kernel_all(const uint16_t *in, uint16_t *out, uint64_t numel, int rank, DevState d, RankIO io) {
-    allreduce_oneshot<Ops, R, U, true, T>(in, out, numel, rank, d, io);
+    allreduce_oneshot<Ops, R, U, true, T, A>(in, out, numel, rank, d, io);
 }
 
 // Two-shot variant, for large payloads at R >= 4, where the one-shot form's
@@ -593,22 +627,22 @@ const void *allreduce_tagged_ptr(int R) {
 // Kernel entry for (element ops, R, unroll, one rank or all ranks, traced or
 // not), as an untyped address for cudaLaunchKernelExC and the occupancy
 // calculator.
-template <class Ops, int R, int U, bool F, bool T>
+template <class Ops, int R, int U, bool F, bool T, bool A>
 constexpr const void *oneshot_entry() {
-    return F ? (const void *)allreduce_kernel_all<Ops, R, U, T> : (const void *)allreduce_kernel_rank<Ops, R, U, T>;
+    return F ? (const void *)allreduce_kernel_all<Ops, R, U, T, A> : (const void *)allreduce_kernel_rank<Ops, R, U, T, A>;
 }
 
-template <class Ops, int U, bool F, bool T>
+template <class Ops, int U, bool F, bool T, bool A>
 const void *allreduce_ptr_ru(int R) {
     switch (R) {
-        case 1: return oneshot_entry<Ops, 1, U, F, T>();
-        case 2: return oneshot_entry<Ops, 2, U, F, T>();
-        case 3: return oneshot_entry<Ops, 3, U, F, T>();
-        case 4: return oneshot_entry<Ops, 4, U, F, T>();
-        case 5: return oneshot_entry<Ops, 5, U, F, T>();
-        case 6: return oneshot_entry<Ops, 6, U, F, T>();
-        case 7: return oneshot_entry<Ops, 7, U, F, T>();
-        case 8: return oneshot_entry<Ops, 8, U, F, T>();
+        case 1: return oneshot_entry<Ops, 1, U, F, T, A>();
+        case 2: return oneshot_entry<Ops, 2, U, F, T, A>();
+        case 3: return oneshot_entry<Ops, 3, U, F, T, A>();
+        case 4: return oneshot_entry<Ops, 4, U, F, T, A>();
+        case 5: return oneshot_entry<Ops, 5, U, F, T, A>();
+        case 6: return oneshot_entry<Ops, 6, U, F, T, A>();
+        case 7: return oneshot_entry<Ops, 7, U, F, T, A>();
+        case 8: return oneshot_entry<Ops, 8, U, F, T, A>();
         default: return nullptr;
     }
 }
@@ -639,6 +673,8 @@ const void *allreduce_twoshot_ptr(int R, int sub) {
 }
 
 // U = 1 or 2: one-shot with that many vectors per thread per stage;
+// U = oneshot_ahead_variant(1 or 2): the same, publishing one stage ahead
+// (untraced only: a traced launch takes the plain one-shot kernel);
 // U = twoshot_variant(sub): the two-shot form with sub-tiles of `sub` vectors;
 // U = kTaggedVariant: the tagged-word form; U = kPushVariant: the push form.
 // fused: the kernel for one launch of all ranks (grid blocks x R); traced:
@@ -648,7 +684,10 @@ const void *allreduce_ptr_ft(int R, int U) {
     if (U == kTaggedVariant) return allreduce_tagged_ptr<Ops, F, T>(R);
     if (U == kPushVariant) return allreduce_push_ptr<Ops, F, T>(R);
     if (U < 0) return nullptr;  // two-shot: allreduce_twoshot_ptr_any, in its own translation unit
-    return U == 1 ? allreduce_ptr_ru<Ops, 1, F, T>(R) : allreduce_ptr_ru<Ops, 2, F, T>(R);
+    const int u = oneshot_unroll(U);
+    if (!T && oneshot_ahead(U))
+        return u == 1 ? allreduce_ptr_ru<Ops, 1, F, false, true>(R) : allreduce_ptr_ru<Ops, 2, F, false, true>(R);
+    return u == 1 ? allreduce_ptr_ru<Ops, 1, F, T, false>(R) : allreduce_ptr_ru<Ops, 2, F, T, false>(R);
 }
 
 // One-shot, tagged-word and push kernels (U >= 0).

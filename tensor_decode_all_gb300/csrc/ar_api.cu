@@ -230,7 +230,10 @@ int family_occupancy(const ar_handle *h, bool fused, bool traced, int *bps) {
     int rc = AR_OK;
     if (h->dtype == AR_F16 || h->dtype == AR_BF16) {
         for (int u = 1; u <= 2 && rc == AR_OK; ++u)
-            rc = kernel_occupancy(tda::allreduce_kernel_ptr(h->dtype, h->R, u, fused, traced), &bps[kOneShot]);
+            for (int a = 0; a < (traced ? 1 : 2) && rc == AR_OK; ++a)
+                rc = kernel_occupancy(
+                    tda::allreduce_kernel_ptr(h->dtype, h->R, a ? tda::oneshot_ahead_variant(u) : u, fused, traced),
+                    &bps[kOneShot]);
         for (int sub = 64; sub <= 256 && rc == AR_OK; sub *= 2)
             for (int m = 0; m < (traced ? 1 : 2) && rc == AR_OK; ++m)
                 rc = kernel_occupancy(
@@ -729,9 +732,16 @@ int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
     // two-shot: flag rounds merged across tiles for slots in HBM and calls of
     // several tiles per block, untraced (see allreduce_twoshot_kernel)
     const bool merged = h->kind == AR_SLOT_HBM && !h->trace && plan.tiles > (uint64_t)blocks;
+    // one-shot: publish one stage ahead for slots in HBM and calls of several
+    // tiles per block, untraced (see allreduce_oneshot).  Measured on a GB300
+    // (bf16, graphs, A/B on one box): HBM R = 4 1 MiB 7.47 -> 6.63 us, R = 2
+    // 2-8 MiB 4-6 % faster, 64 MiB level; over the host link it lost up to
+    // 12 % (R = 2 8 MiB 124.5 -> 141.1 us), so pinned calls keep the plain form.
+    const bool ahead = h->kind == AR_SLOT_HBM && !h->trace && plan.tiles > (uint64_t)blocks;
     const int variant = algo == AR_ALGO_TWOSHOT  ? tda::twoshot_variant(plan.subtile_vecs, merged)
                         : algo == AR_ALGO_TAGGED ? tda::kTaggedVariant
                         : algo == AR_ALGO_PUSH   ? tda::kPushVariant
+                        : ahead                  ? tda::oneshot_ahead_variant(plan.unroll)
                                                  : plan.unroll;
     DevState d = dev_state(h);
     d.algo = algo;

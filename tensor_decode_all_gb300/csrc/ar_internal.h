@@ -34,6 +34,11 @@ constexpr int kCounterSlots = 512;
 constexpr int twoshot_variant(int sub, bool merged = false) { return -(sub + (merged ? 1 : 0)); }
 constexpr int twoshot_sub(int variant) { return (-variant) & ~1; }
 constexpr bool twoshot_merged(int variant) { return ((-variant) & 1) != 0; }
+// Kernel variant codes of the one-shot form: its vectors per thread per stage
+// (1 or 2), plus 4 for the kernel that publishes one stage ahead.
+constexpr int oneshot_ahead_variant(int unroll) { return 4 + unroll; }
+constexpr int oneshot_unroll(int variant) { return variant > 4 ? variant - 4 : variant; }
+constexpr bool oneshot_ahead(int variant) { return variant > 4; }
 // Kernel variant code of the tagged-word form.
 constexpr int kTaggedVariant = 0;
 // Kernel variant code of the push form.
