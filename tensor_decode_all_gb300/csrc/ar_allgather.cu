@@ -50,7 +50,12 @@ struct Vec<1> {
 // on a GB300, complex64 1000 x 500 shards in HBM: R=4 21.8 -> 20.3 us (against
 // the unbounded build's 3 blocks per SM), R=8 64.9 -> 64.3 us, R=8 500 KB
 // 12.0 -> 11.4 us.
-template <int VW, int R, int U, bool F, bool T>
+// A (publish ahead, slots in HBM, several stages per block): a block
+// publishes stage s + 1 -- loads its input, stores it into the slot and into
+// its own place in out, raises the flag -- before it waits for and copies its
+// peers' stage s, so each flag round overlaps the next stage's publish.  Stage
+// s + 1 has its own slot region, so nothing a peer still reads is touched.
+template <int VW, int R, int U, bool F, bool T, bool A>
 __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
     allgather_kernel(const uint8_t *in_arg, uint8_t *out_arg, uint64_t bytes, int rank_arg, DevState d, RankIO io) {
     using V = typename Vec<VW>::T;
@@ -97,13 +102,11 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
     V *const slot_base = reinterpret_cast<V *>(d.slots) + (uint64_t)parity * R * slot_vecs;
     V *const my_slot = slot_base + (uint64_t)rank * slot_vecs;
     if (nstages) pace_first_stage(c0, b, d.pace_cycles);
-
-    for (uint64_t s = 0; s < nstages; ++s) {
-        const uint64_t tile = (uint64_t)b + s * B;
-        const uint64_t v0 = tile * kTileVecs + tid;
+    if (A && nstages) {
+        // stage 0 published before the loop; the loop publishes one ahead
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const uint64_t v = v0 + (uint64_t)u * kThreads;
+            const uint64_t v = (uint64_t)b * kTileVecs + (uint64_t)u * kThreads + tid;
             if (v < nv) {
                 my_slot[v] = own[u];
                 dst[(uint64_t)rank * nv + v] = own[u];
@@ -111,17 +114,57 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
         }
         __syncthreads();
         if (tid == 0) {
-            publish_stage(d, rank, b, seq + s + 1);
+            publish_stage(d, rank, b, seq + 1);
             trace_published<T>(d, s_tr);
         }
+    }
 
+    for (uint64_t s = 0; s < nstages; ++s) {
+        const uint64_t tile = (uint64_t)b + s * B;
+        const uint64_t v0 = tile * kTileVecs + tid;
         V nxt[U];
-        if (s + 1 < nstages) {
-            const uint64_t vn = (tile + B) * kTileVecs + tid;
+        if constexpr (A) {
+            // publish stage s + 1
+            if (s + 1 < nstages) {
+                const uint64_t vn = (tile + B) * kTileVecs + tid;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint64_t v = vn + (uint64_t)u * kThreads;
+                    if (v < nv) nxt[u] = src[v];
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint64_t v = vn + (uint64_t)u * kThreads;
+                    if (v < nv) {
+                        my_slot[v] = nxt[u];
+                        dst[(uint64_t)rank * nv + v] = nxt[u];
+                    }
+                }
+                __syncthreads();
+                if (tid == 0) publish_stage(d, rank, b, seq + s + 2);
+            }
+        } else {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const uint64_t v = vn + (uint64_t)u * kThreads;
-                if (v < nv) nxt[u] = src[v];
+                const uint64_t v = v0 + (uint64_t)u * kThreads;
+                if (v < nv) {
+                    my_slot[v] = own[u];
+                    dst[(uint64_t)rank * nv + v] = own[u];
+                }
+            }
+            __syncthreads();
+            if (tid == 0) {
+                publish_stage(d, rank, b, seq + s + 1);
+                trace_published<T>(d, s_tr);
+            }
+
+            if (s + 1 < nstages) {
+                const uint64_t vn = (tile + B) * kTileVecs + tid;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint64_t v = vn + (uint64_t)u * kThreads;
+                    if (v < nv) nxt[u] = src[v];
+                }
             }
         }
 
@@ -153,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
                 }
             }
         }
-        if (s + 1 < nstages) {
+        if (!A && s + 1 < nstages) {
 #pragma unroll
             for (int u = 0; u < U; ++u) own[u] = nxt[u];
         }
@@ -168,24 +211,31 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
     }
 }
 
-template <int VW, int U, bool F, bool T>
+template <int VW, int U, bool F, bool T, bool A>
 const void *allgather_ptr_ru(int R) {
     switch (R) {
-        case 1: return (const void *)allgather_kernel<VW, 1, U, F, T>;
-        case 2: return (const void *)allgather_kernel<VW, 2, U, F, T>;
-        case 3: return (const void *)allgather_kernel<VW, 3, U, F, T>;
-        case 4: return (const void *)allgather_kernel<VW, 4, U, F, T>;
-        case 5: return (const void *)allgather_kernel<VW, 5, U, F, T>;
-        case 6: return (const void *)allgather_kernel<VW, 6, U, F, T>;
-        case 7: return (const void *)allgather_kernel<VW, 7, U, F, T>;
-        case 8: return (const void *)allgather_kernel<VW, 8, U, F, T>;
+        case 1: return (const void *)allgather_kernel<VW, 1, U, F, T, A>;
+        case 2: return (const void *)allgather_kernel<VW, 2, U, F, T, A>;
+        case 3: return (const void *)allgather_kernel<VW, 3, U, F, T, A>;
+        case 4: return (const void *)allgather_kernel<VW, 4, U, F, T, A>;
+        case 5: return (const void *)allgather_kernel<VW, 5, U, F, T, A>;
+        case 6: return (const void *)allgather_kernel<VW, 6, U, F, T, A>;
+        case 7: return (const void *)allgather_kernel<VW, 7, U, F, T, A>;
+        case 8: return (const void *)allgather_kernel<VW, 8, U, F, T, A>;
         default: return nullptr;
     }
 }
 
+// The publish-ahead kernels exist for 16- and 8-byte vectors, untraced; any
+// other request for them takes the plain kernel.
 template <int VW, bool F, bool T>
 const void *allgather_ptr_rft(int R, int U) {
-    return U == 1 ? allgather_ptr_ru<VW, 1, F, T>(R) : allgather_ptr_ru<VW, 2, F, T>(R);
+    const int u = oneshot_unroll(U);
+    if constexpr (!T && VW >= 8) {
+        if (oneshot_ahead(U))
+            return u == 1 ? allgather_ptr_ru<VW, 1, F, false, true>(R) : allgather_ptr_ru<VW, 2, F, false, true>(R);
+    }
+    return u == 1 ? allgather_ptr_ru<VW, 1, F, T, false>(R) : allgather_ptr_ru<VW, 2, F, T, false>(R);
 }
 
 template <int VW>

@@ -248,7 +248,10 @@ int family_occupancy(const ar_handle *h, bool fused, bool traced, int *bps) {
     }
     for (int u = 1; u <= 2 && rc == AR_OK; ++u)
         for (int vw = 1; vw <= 16 && rc == AR_OK; vw *= 2)
-            rc = kernel_occupancy(tda::allgather_kernel_ptr(vw, h->R, u, fused, traced), &bps[kAllgather]);
+            for (int a = 0; a < (traced || vw < 8 ? 1 : 2) && rc == AR_OK; ++a)
+                rc = kernel_occupancy(
+                    tda::allgather_kernel_ptr(vw, h->R, a ? tda::oneshot_ahead_variant(u) : u, fused, traced),
+                    &bps[kAllgather]);
     if (rc != AR_OK) return rc;
     for (int f = 0; f < kFamilies; ++f) {
         if (bps[f] == kUnset) bps[f] = bps[kAllgather];  // complex64 handles launch no all-reduce kernel
@@ -763,7 +766,11 @@ int enqueue_allgather(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
     const int blocks = handle_blocks(h, plan.blocks);
     DevState d = dev_state(h);
     d.pace_cycles = pace_cycles(h, bytes, plan, blocks);  // the one-shot form's link bytes: share 1/R
-    const cudaError_t e = tda::launch_allgather(vw, h->R, plan.unroll, blocks, s, io, bytes, rank, d, h->pdl);
+    // publish one stage ahead in HBM for calls of several tiles per block, as
+    // the one-shot all-reduce does (16- and 8-byte vectors, untraced)
+    const bool ahead = h->kind == AR_SLOT_HBM && !h->trace && vw >= 8 && plan.tiles > (uint64_t)blocks;
+    const int unroll = ahead ? tda::oneshot_ahead_variant(plan.unroll) : plan.unroll;
+    const cudaError_t e = tda::launch_allgather(vw, h->R, unroll, blocks, s, io, bytes, rank, d, h->pdl);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return AR_ECUDA;

@@ -87,3 +87,35 @@ def test_fp16_allgather_narrow_vectors(n):
     for r in range(R):
         assert np.array_equal(to_bits(outs[r]), want)
     h.destroy()
+
+
+@pytest.mark.parametrize("slots", ["hbm", "pinned"])
+@pytest.mark.parametrize("launch", ["rank", "fused"])
+@pytest.mark.parametrize("R,n", [(2, 256 * 2 * 7 + 1), (3, 256 * 2 * 9), (5, 4099), (8, 256 * 4 * 5 + 3)])
+def test_several_stages_per_block(slots, launch, R, n):
+    """A block cap of 2 gives each block several stages: in HBM the kernel that
+    publishes one stage ahead (16-byte vectors for an even element count,
+    8-byte ones for an odd count), over the host link the plain one; both
+    byte-exact, per-rank and in one launch of every rank, both parities."""
+    h = _handle(R, n, slots)
+    h.set_tactics(max_blocks=2)
+    p = h.plan("allgather", n)
+    assert p.blocks == 2 and p.tiles > 2
+    streams = rank_streams(R)
+    side = torch.cuda.Stream()
+    for c in range(2):
+        zs = inputs.allgather_inputs(4, R, n, 30 + c)
+        ins = [to_dev(z, "c64") for z in zs]
+        outs = [torch.empty(R * n, dtype=torch.complex64, device="cuda") for _ in range(R)]
+        if launch == "rank":
+            enqueue(h, "allgather", ins, outs, streams)
+        else:
+            side.wait_stream(torch.cuda.current_stream())
+            h.allgather_fused(ins, outs, side)
+            torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        h.check()
+        want = oracle.allgather(zs, ranks=[0])[0]
+        for r in range(R):
+            assert_bits_equal(to_bits(outs[r]), want, "c64", f"{slots} {launch} R={R} n={n} call {c} rank {r}")
+    h.destroy()
