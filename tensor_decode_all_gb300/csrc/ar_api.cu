@@ -735,12 +735,13 @@ int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
     // two-shot: flag rounds merged across tiles for slots in HBM and calls of
     // several tiles per block, untraced (see allreduce_twoshot_kernel)
     const bool merged = h->kind == AR_SLOT_HBM && !h->trace && plan.tiles > (uint64_t)blocks;
-    // one-shot: publish one stage ahead for slots in HBM and calls of several
-    // tiles per block, untraced (see allreduce_oneshot).  Measured on a GB300
-    // (bf16, graphs, A/B on one box): HBM R = 4 1 MiB 7.47 -> 6.63 us, R = 2
-    // 2-8 MiB 4-6 % faster, 64 MiB level; over the host link it lost up to
-    // 12 % (R = 2 8 MiB 124.5 -> 141.1 us), so pinned calls keep the plain form.
-    const bool ahead = h->kind == AR_SLOT_HBM && !h->trace && plan.tiles > (uint64_t)blocks;
+    // one-shot: publish one stage ahead for slots in HBM, R <= 4 and calls of
+    // several tiles per block, untraced (see allreduce_oneshot).  Measured on a
+    // GB300 (bf16, graphs, A/B on one box): HBM R = 4 1 MiB 7.47 -> 6.63 us,
+    // R = 2 2-8 MiB 4-6 % faster, 64 MiB level; at R = 8 (forced one-shot,
+    // 16 MiB) it lost 123 -> 160 us, and over the host link up to 12 % (R = 2
+    // 8 MiB 124.5 -> 141.1 us): those keep the plain form.
+    const bool ahead = h->kind == AR_SLOT_HBM && h->R <= 4 && !h->trace && plan.tiles > (uint64_t)blocks;
     const int variant = algo == AR_ALGO_TWOSHOT  ? tda::twoshot_variant(plan.subtile_vecs, merged)
                         : algo == AR_ALGO_TAGGED ? tda::kTaggedVariant
                         : algo == AR_ALGO_PUSH   ? tda::kPushVariant
