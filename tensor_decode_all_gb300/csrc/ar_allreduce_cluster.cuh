@@ -65,7 +65,12 @@ constexpr int cluster_min_blocks() {
     return (SUB == 256 && R >= 4) ? 1 : 6;
 }
 
-template <class Ops, int R, int SUB, bool T>
+// P: the kernel with the pacing code, for calls whose first-stage slot stores
+// are paced (slots in host memory, a pace set, one wave of clusters) and, as
+// measured faster, for two-shot calls.  Unpaced one-shot calls take the kernel
+// without it: at R = 8, held to 40 registers, its presence cost small calls
+// 0.3-1 us even with no pace.
+template <class Ops, int R, int SUB, bool T, bool P>
 __global__ void __launch_bounds__(kThreads, cluster_min_blocks<R, SUB>())
     allreduce_cluster_kernel(const uint16_t *in_arg, uint16_t *out_arg, uint64_t numel, int rank_arg, DevState d,
                              RankIO io) {
@@ -88,7 +93,8 @@ __global__ void __launch_bounds__(kThreads, cluster_min_blocks<R, SUB>())
     const uint64_t nstages = ntiles > (uint64_t)b ? (ntiles - b + B - 1) / B : 0;
 
     pdl_wait();
-    const long long c0 = clock64();
+    long long c0 = 0;
+    if constexpr (P) c0 = clock64();
     // stage 0's tile of this rank's input, loaded while thread 0 fetches the
     // call count (the slot half it goes to)
     uint4 own[kPer];
@@ -124,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, cluster_min_blocks<R, SUB>())
                 const uint64_t li = (uint64_t)u * kThreads + tid;
                 own[u] = li < kTileVecs ? load_own(in, tbase + li, nvec_full, tail) : make_uint4(0u, 0u, 0u, 0u);
             }
-        } else {
+        } else if constexpr (P) {
             pace_first_stage(c0, b, d.pace_cycles);
         }
 #pragma unroll
@@ -180,33 +186,39 @@ __global__ void __launch_bounds__(kThreads, cluster_min_blocks<R, SUB>())
     if (tid == 0) trace_finish<T>(d, s_tr, R, rank, b, calls, nstages);
 }
 
-template <class Ops, int SUB, bool T>
+template <class Ops, int SUB, bool T, bool P>
 const void *allreduce_cluster_ptr_r(int R) {
     switch (R) {
-        case 1: return (const void *)allreduce_cluster_kernel<Ops, 1, SUB, T>;
-        case 2: return (const void *)allreduce_cluster_kernel<Ops, 2, SUB, T>;
-        case 3: return (const void *)allreduce_cluster_kernel<Ops, 3, SUB, T>;
-        case 4: return (const void *)allreduce_cluster_kernel<Ops, 4, SUB, T>;
-        case 5: return (const void *)allreduce_cluster_kernel<Ops, 5, SUB, T>;
-        case 6: return (const void *)allreduce_cluster_kernel<Ops, 6, SUB, T>;
-        case 7: return (const void *)allreduce_cluster_kernel<Ops, 7, SUB, T>;
-        case 8: return (const void *)allreduce_cluster_kernel<Ops, 8, SUB, T>;
+        case 1: return (const void *)allreduce_cluster_kernel<Ops, 1, SUB, T, P>;
+        case 2: return (const void *)allreduce_cluster_kernel<Ops, 2, SUB, T, P>;
+        case 3: return (const void *)allreduce_cluster_kernel<Ops, 3, SUB, T, P>;
+        case 4: return (const void *)allreduce_cluster_kernel<Ops, 4, SUB, T, P>;
+        case 5: return (const void *)allreduce_cluster_kernel<Ops, 5, SUB, T, P>;
+        case 6: return (const void *)allreduce_cluster_kernel<Ops, 6, SUB, T, P>;
+        case 7: return (const void *)allreduce_cluster_kernel<Ops, 7, SUB, T, P>;
+        case 8: return (const void *)allreduce_cluster_kernel<Ops, 8, SUB, T, P>;
         default: return nullptr;
     }
 }
 
-// sub = 0: one-shot; 64, 128, 256: two-shot with sub-tiles of that many vectors.
-template <class Ops>
-const void *allreduce_cluster_ptr(int R, int sub, bool traced) {
+template <class Ops, bool T, bool P>
+const void *allreduce_cluster_ptr_tp(int R, int sub) {
     switch (sub) {
-        case 0: return traced ? allreduce_cluster_ptr_r<Ops, 0, true>(R) : allreduce_cluster_ptr_r<Ops, 0, false>(R);
-        case 64: return traced ? allreduce_cluster_ptr_r<Ops, 64, true>(R) : allreduce_cluster_ptr_r<Ops, 64, false>(R);
-        case 128:
-            return traced ? allreduce_cluster_ptr_r<Ops, 128, true>(R) : allreduce_cluster_ptr_r<Ops, 128, false>(R);
-        case 256:
-            return traced ? allreduce_cluster_ptr_r<Ops, 256, true>(R) : allreduce_cluster_ptr_r<Ops, 256, false>(R);
+        case 0: return allreduce_cluster_ptr_r<Ops, 0, T, P>(R);
+        case 64: return allreduce_cluster_ptr_r<Ops, 64, T, P>(R);
+        case 128: return allreduce_cluster_ptr_r<Ops, 128, T, P>(R);
+        case 256: return allreduce_cluster_ptr_r<Ops, 256, T, P>(R);
         default: return nullptr;
     }
+}
+
+// sub = 0: one-shot; 64, 128, 256: two-shot with sub-tiles of that many
+// vectors.  paced: the kernel with the pacing code (see P above).
+template <class Ops>
+const void *allreduce_cluster_ptr(int R, int sub, bool traced, bool paced) {
+    if (traced)
+        return paced ? allreduce_cluster_ptr_tp<Ops, true, true>(R, sub) : allreduce_cluster_ptr_tp<Ops, true, false>(R, sub);
+    return paced ? allreduce_cluster_ptr_tp<Ops, false, true>(R, sub) : allreduce_cluster_ptr_tp<Ops, false, false>(R, sub);
 }
 
 }  // namespace tda

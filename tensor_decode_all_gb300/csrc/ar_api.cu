@@ -276,15 +276,17 @@ int cluster_setup(ar_handle *h) {
     h->cluster_ok = false;
     if (h->dtype != AR_F16 && h->dtype != AR_BF16) return AR_OK;
     for (int traced = 0; traced < 2; ++traced)
-        for (int sub : {0, 64, 128, 256}) {
-            const void *k = tda::allreduce_cluster_kernel_ptr(h->dtype, h->R, sub, traced != 0);
-            cudaFuncAttributes attr;
-            if (!k || cudaFuncGetAttributes(&attr, k) != cudaSuccess) {
-                (void)cudaGetLastError();
-                return AR_OK;
+        for (int paced = 0; paced < 2; ++paced)
+            for (int sub : {0, 64, 128, 256}) {
+                const void *k = tda::allreduce_cluster_kernel_ptr(h->dtype, h->R, sub, traced != 0, paced != 0);
+                cudaFuncAttributes attr;
+                if (!k || cudaFuncGetAttributes(&attr, k) != cudaSuccess) {
+                    (void)cudaGetLastError();
+                    return AR_OK;
+                }
             }
-        }
     int fit = 1 << 30;
+    for (int paced = 0; paced < 2; ++paced)
     for (int sub : {0, 64, 128, 256}) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1, (unsigned)h->R);
@@ -297,7 +299,8 @@ int cluster_setup(ar_handle *h) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, tda::allreduce_cluster_kernel_ptr(h->dtype, h->R, sub, false), &cfg) !=
+        if (cudaOccupancyMaxActiveClusters(&n, tda::allreduce_cluster_kernel_ptr(h->dtype, h->R, sub, false, paced != 0),
+                                           &cfg) !=
                 cudaSuccess ||
             n < 1) {
             (void)cudaGetLastError();
@@ -1346,15 +1349,21 @@ cudaError_t launch_allreduce(int dtype, int R, int unroll, int blocks, cudaStrea
     return launch(k, blocks, rank < 0 ? R : 1, rank < 0, s, args, pdl);
 }
 
-const void *allreduce_cluster_kernel_ptr(int dtype, int R, int sub, bool traced) {
-    if (dtype == AR_F16) return allreduce_cluster_kernel_ptr_f16(R, sub, traced);
-    if (dtype == AR_BF16) return allreduce_cluster_kernel_ptr_bf16(R, sub, traced);
+const void *allreduce_cluster_kernel_ptr(int dtype, int R, int sub, bool traced, bool paced) {
+    if (dtype == AR_F16) return allreduce_cluster_kernel_ptr_f16(R, sub, traced, paced);
+    if (dtype == AR_BF16) return allreduce_cluster_kernel_ptr_bf16(R, sub, traced, paced);
     return nullptr;
 }
 
 cudaError_t launch_allreduce_cluster(int dtype, int R, int sub, int blocks, cudaStream_t s, const RankIO &io,
                                      uint64_t numel, const DevState &d, bool pdl) {
-    const void *k = allreduce_cluster_kernel_ptr(dtype, R, sub, d.trace != nullptr);
+    // The kernel with the pacing code for paced calls, and also for two-shot
+    // calls: compiled with the clock read at its start it measured faster in
+    // that variant (R = 8 bf16 768 KiB HBM, 64-vector sub-tiles: 6.60 against
+    // 7.88 us; 512 KiB 6.03 against 6.75 us), a code-generation effect, while
+    // unpaced one-shot calls are faster without it (R = 8 2 KiB: 2.87 against
+    // 3.2 us; over the host link 4.2 against 5.3 us).
+    const void *k = allreduce_cluster_kernel_ptr(dtype, R, sub, d.trace != nullptr, d.pace_cycles != 0 || sub != 0);
     if (!k || blocks < 1) return cudaErrorInvalidValue;
     const uint16_t *a0 = static_cast<const uint16_t *>(io.in[0]);
     uint16_t *a1 = static_cast<uint16_t *>(io.out[0]);

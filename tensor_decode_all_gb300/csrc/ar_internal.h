@@ -112,9 +112,10 @@ const void *allreduce_twoshot_kernel_ptr_bf16(int R, int unroll, bool fused, boo
 const void *allgather_kernel_ptr(int vec_bytes, int R, int unroll, bool fused, bool traced);
 // Cluster-barrier form (all ranks in one launch, clusters of 1 x R blocks):
 // sub = 0 one-shot, 64/128/256 two-shot sub-tile.
-const void *allreduce_cluster_kernel_ptr(int dtype, int R, int sub, bool traced);
-const void *allreduce_cluster_kernel_ptr_f16(int R, int sub, bool traced);   // ar_allreduce_f16_cluster.cu
-const void *allreduce_cluster_kernel_ptr_bf16(int R, int sub, bool traced);  // ar_allreduce_bf16_cluster.cu
+// paced: the kernel with the code that paces the first stage's slot stores.
+const void *allreduce_cluster_kernel_ptr(int dtype, int R, int sub, bool traced, bool paced = false);
+const void *allreduce_cluster_kernel_ptr_f16(int R, int sub, bool traced, bool paced);   // ar_allreduce_f16_cluster.cu
+const void *allreduce_cluster_kernel_ptr_bf16(int R, int sub, bool traced, bool paced);  // ar_allreduce_bf16_cluster.cu
 // Launch the cluster form: grid blocks x R, clusters of 1 x R, not cooperative
 // (a cluster waits only on itself).
 cudaError_t launch_allreduce_cluster(int dtype, int R, int sub, int blocks, cudaStream_t s, const RankIO &io,
