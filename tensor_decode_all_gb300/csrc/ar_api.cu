@@ -356,16 +356,18 @@ uint64_t cluster_twoshot_threshold(int R, int slot_kind) {
 // Largest call (bytes per rank) that AUTO runs in the cluster form when all
 // ranks launch at once; larger calls take the flag forms, whose grids keep
 // more blocks resident than clusters of R blocks can.  Measured on a GB300
-// (bf16, graphs of 100 calls; cluster form / best flag form, per-rank or in
-// one launch, us/call): in HBM the cluster form wins up to 2 MiB at R = 2
-// (5.8 / 6.5; 4 MiB 9.4 / 8.1), up to 1 MiB at R = 4 (6.4 / 7.4; 2 MiB 9.8 /
-// 9.2) and, at R = 8, as long as one stage of 64-vector sub-tiles covers the
-// call (896 KiB: 512 KiB 6.8 / 7.9; 1 MiB 12.1 / 9.8); over the host link at
-// every size at R = 2 (16 MiB 227 / 243), up to 4 MiB at R = 4 (2 MiB 106 /
-// 118; 8 MiB 394 / 367) and up to 8 MiB at R = 8 (733 / 760; 16 MiB 1663 /
-// 1416).  R = 3 takes R = 4's limit, R = 5..7 R = 8's.
+// with the final kernels (bf16, graphs of calls of every rank; cluster form /
+// flag forms in one launch, us/call): in HBM the cluster form wins up to
+// 2 MiB at R = 2 (5.73 / 6.07; 4 MiB 9.54 / 8.02), up to 1 MiB at R = 4 (1 MiB
+// 6.34 / 6.33, 512 KiB 3.64 / 4.45; 2 MiB 9.86 / 9.02) and at R = 8 up to the
+// decode-sized 768 KiB (6.6 / 8.3; 512 KiB 6.00 / 7.58; 1 MiB 10.66 / 9.49);
+// over the host link, where the flag forms' first-stage stores are paced, up to
+// 1 MiB at R = 2 (15.98 / 19.05; 2 MiB 40.53 / 35.97), 256 KiB at R = 4 (14.14 /
+// 17.27; 512 KiB 31.70 / 29.32) and 128 KiB at R = 8 (256 KiB 33.06 / 32.08;
+// 128 KiB 17.9 / 20.4 before pacing).  R = 3 takes R = 4's limit, R = 5..7
+// R = 8's.
 uint64_t cluster_limit(int R, int slot_kind) {
-    if (slot_kind == AR_SLOT_PINNED_HOST) return R <= 2 ? ~0ull : R <= 4 ? (4ull << 20) : (8ull << 20);
+    if (slot_kind == AR_SLOT_PINNED_HOST) return R <= 2 ? (1ull << 20) : R <= 4 ? (256ull << 10) : (128ull << 10);
     return R <= 2 ? (2ull << 20) : R <= 4 ? (1ull << 20) : (896ull << 10);
 }
 

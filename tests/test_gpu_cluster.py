@@ -96,8 +96,10 @@ def test_auto_picks_the_cluster_form_for_launches_of_every_rank():
 def test_config3_through_allreduce_all_1000_calls(slots):
     """Workload 3 (R=8 bf16 N=393216) through the default entry for a caller
     that drives all ranks, ar_allreduce_all, which fuses the ranks into one
-    cluster launch: a graph of 100 calls replayed 10 times with fresh inputs,
-    every call checked on every rank (1000 calls)."""
+    launch (a cluster launch in HBM; over the host link, above the cluster
+    form's limit, one cooperative launch of the flag forms): a graph of 100
+    calls replayed 10 times with fresh inputs, every call checked on every
+    rank (1000 calls)."""
     import tensor_decode_all_gb300 as tda
     R, n, C, REPLAYS, dtype = 8, 393216, 100, 10, "bf16"
     h = tda.Handle(R, torch.bfloat16, n, slots)
