@@ -981,6 +981,10 @@ PROFILE_WORKLOADS = {
     "r8_bf16_16MiB_hbm_1call": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 1),
     "r2_fp16_16MiB_hbm_1call": ("allreduce", 2, "f16", 8 << 20, "hbm", 5, "uniform", 1),
     "allgather_c64_r4_hbm_1call": ("allgather", 4, "c64", 500000, "hbm", 4, "normal", 1),
+    # graphs of 10 calls on distinct buffers: working sets that fit in L2 for one
+    # call spill to DRAM over ten, so bytes / 10 is the steady-state figure
+    "r2_fp16_16MiB_hbm_10call": ("allreduce", 2, "f16", 8 << 20, "hbm", 5, "uniform", 10),
+    "allgather_c64_r4_hbm_10call": ("allgather", 4, "c64", 500000, "hbm", 4, "normal", 10),
     "r8_bf16_16MiB_hbm_oneshot_1call": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 1),
     "allgather_c64_r8_hbm_1call": ("allgather", 8, "c64", 500000, "hbm", 4, "normal", 1),
     "r8_bf16_768KiB_hbm_fused_1call": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 1),
