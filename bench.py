@@ -591,26 +591,33 @@ def roofline(op, R, S, slots, t_call_s, link, hbm_gbs, algo=None):
                     "bytes per call of the same kernel over this call time (null without a valid capture)"}
 
 
-def add_link_floors(rf, lat, link, t_call_s):
+def add_link_floors(rf, lat, link, t_call_s, gpu_scope=True):
     """Beside the per-direction floor that `frac` uses, two more floors of a
     host-link call, both measured in this run: the duplex floor (each direction
     at the rate the probe sees while the other direction is busy too -- the
     link does not give both directions their solo rates at once) and the
-    latency chain one tile must pass in protocol order (its stores acknowledged
-    by a system-scope fence, the flag's one-way trip, one dependent read round
-    trip).  No call can beat the larger of them; neither counts the launch."""
+    latency chain one tile must pass in protocol order (its stores ordered by
+    the release's fence, the flag's one-way trip, one dependent read round
+    trip), at the scope the call's ranks synchronise at: GPU scope (flags in
+    HBM, the default) or system scope (flags in host memory).  No call can beat
+    the larger of them; neither counts the launch."""
     W, Rd = rf["algorithmic_bytes_per_call"]["link_write"], rf["algorithmic_bytes_per_call"]["link_read"]
     gb = 1e9
     per_dir = link_floor_s(W, Rd, link)
     duplex = max(W / (link["bidir_write_gbs"] * gb), Rd / (link["bidir_read_gbs"] * gb))
-    chain = (lat["store_4KiB_fence_sys_ns"] + lat["flag_host_sys_one_way_ns"] + lat["host_load_rtt_ns"]) * 1e-9
+    if gpu_scope:
+        chain = lat["store_4KiB_fence_gpu_ns"] + lat["flag_hbm_gpu_one_way_ns"] + lat["host_load_rtt_ns"]
+    else:
+        chain = lat["store_4KiB_fence_sys_ns"] + lat["flag_host_sys_one_way_ns"] + lat["host_load_rtt_ns"]
+    chain *= 1e-9
     rf["floors_us"] = {"per_direction": round(per_dir * 1e6, 3), "duplex": round(duplex * 1e6, 3),
                        "latency_chain": round(chain * 1e6, 3)}
     rf["frac_duplex"] = round(duplex / t_call_s, 4)
     rf["link_latency_ns"] = {k: round(v, 1) for k, v in lat.items()}
     rf["floors_note"] = ("frac = per_direction / t (each direction at its solo rate, both at once: not reachable, "
                          "the link gives ~138 + 138 GB/s with both directions busy); frac_duplex = duplex / t; "
-                         "latency_chain = publish (4 KiB stores + system-scope fence) + flag one way + one read "
+                         "latency_chain = publish (4 KiB stores + the fence of the call's scope) + flag one way "
+                         "(" + ("HBM, GPU scope" if gpu_scope else "host memory, system scope") + ") + one read "
                          "round trip, from ar_probe_host_link_latency")
 
 
@@ -774,6 +781,30 @@ EXPERIMENT_WORKLOADS = {
                                {"tactics": {"pace_multi_mbs": 160000}}),
 }
 
+# Pinned-host slots with the ranks synchronising at system scope, flags in host
+# memory (_sysscope), or at GPU scope, flags in HBM (_gpuscope); and the
+# headline's shape at GPU scope at other paces.
+for _name, _spec in {
+    "x_r2_256K_pinned": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 100, 20),
+    "x_r2_128K_pinned": ("allreduce", 2, "f16", 65536, "pinned", 5, "uniform", 100, 20),
+    "x_r2_4M_pinned": ("allreduce", 2, "f16", 2 << 20, "pinned", 5, "uniform", 20, 10),
+    "x_r4_1M_pinned": ("allreduce", 4, "bf16", 1 << 19, "pinned", 5, "uniform", 50, 10),
+    "x_r8_256K_pinned": ("allreduce", 8, "bf16", 131072, "pinned", 5, "uniform", 50, 10),
+    "x_ag_r4_pinned": ("allgather", 4, "c64", 500000, "pinned", 4, None, 5, 5),
+    "x_r2_8K_pinned": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", 100, 20),
+    "x_r2_32K_pinned": ("allreduce", 2, "f16", 16384, "pinned", 5, "uniform", 100, 20),
+    "x_r8_64K_pinned": ("allreduce", 8, "bf16", 32768, "pinned", 5, "uniform", 100, 20),
+}.items():
+    for _suffix, _flags in (("sysscope", 0), ("gpuscope", 1)):
+        EXPERIMENT_WORKLOADS[f"{_name}_{_suffix}"] = _spec + ({"tactics": {"gpu_scope": _flags}},)
+for _pace in (0, 240000, 270000, 300000, 330000):
+    EXPERIMENT_WORKLOADS[f"x_r2_256K_pinned_gpuscope_pace{_pace // 1000}"] = (
+        "allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 100, 20,
+        {"tactics": {"gpu_scope": 1, "pace_mbs": _pace}})
+    EXPERIMENT_WORKLOADS[f"x_r2_4M_pinned_gpuscope_pace{_pace // 1000}"] = (
+        "allreduce", 2, "f16", 2 << 20, "pinned", 5, "uniform", 20, 10,
+        {"tactics": {"gpu_scope": 1, "pace_multi_mbs": _pace}})
+
 
 # Order of the summary: the workloads a reader looks for first come last, so
 # that they survive when only the end of the output is kept.
@@ -898,7 +929,8 @@ def run_ours(args, dist):
         head["roofline"]["link_traffic"] = {"read": prof["link_read_bytes_per_call"],
                                             "write": prof["link_write_bytes_per_call"],
                                             "source": prof["source"]}
-    add_link_floors(head["roofline"], tda.ar_probe_host_link_latency(200), link, head["us_per_call"] * 1e-6)
+    add_link_floors(head["roofline"], tda.ar_probe_host_link_latency(200), link, head["us_per_call"] * 1e-6,
+                    gpu_scope=bool(w.h.tactics()["gpu_scope"]))
     S = numel * 2
     n = dist.world
     value = n * S * len(ms) * C / total_s / 1e9
@@ -976,6 +1008,8 @@ def run_ours(args, dist):
 PROFILE_WORKLOADS = {
     "r2_fp16_256KiB_pinned": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 100),
     "r2_fp16_256KiB_pinned_1call": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 1),
+    # the same with the ranks synchronising at system scope (flags in host memory)
+    "r2_fp16_256KiB_pinned_sysscope_1call": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 1),
     "r8_bf16_768KiB_hbm": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100),
     "r8_bf16_768KiB_hbm_1call": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 1),
     "r8_bf16_16MiB_hbm_1call": ("allreduce", 8, "bf16", 8 << 20, "hbm", 5, "uniform", 1),
@@ -1007,7 +1041,7 @@ def run_profile(args, dist):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     launch = "all" if "_all" in args.profile else "fused" if "fused" in args.profile else "rank"
     w = Workload(op, R, dt, n, sl, C, config=cfg, dist=dd, algo="oneshot" if "oneshot" in args.profile else None,
-                 launch=launch)
+                 launch=launch, tactics={"gpu_scope": 0} if "sysscope" in args.profile else None)
     w.capture()
     ms = w.time_graph(args.steps, args.warmup, flush)
     w.check(calls=(0, -1))
@@ -1019,6 +1053,8 @@ def run_profile(args, dist):
 
 TRACE_WORKLOADS = {
     "config 2: R=2 fp16 256 KiB pinned": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", False),
+    "config 2, system scope (flags in host memory)": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4",
+                                                      "sysscope"),
     "config 1: R=2 fp16 8 KiB pinned": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", False),
     "config 3: R=8 bf16 768 KiB HBM": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", False),
     "config 3, one cooperative launch (flag form)": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", "flags"),
@@ -1048,8 +1084,10 @@ def run_trace(args, dist):
     out = {}
     for name, (op, R, dt, n, sl, cfg, dd, mode) in TRACE_WORKLOADS.items():
         C = 100
-        w = Workload(op, R, dt, n, sl, C, config=cfg, dist=dd, launch="fused" if mode == "flags" else mode or "rank",
-                     tactics={"cluster_max_bytes": 0} if mode == "flags" else None)
+        w = Workload(op, R, dt, n, sl, C, config=cfg, dist=dd,
+                     launch="fused" if mode == "flags" else "all" if mode == "all" else "rank",
+                     tactics={"cluster_max_bytes": 0} if mode == "flags" else
+                     {"gpu_scope": 0} if mode == "sysscope" else None)
         buf = trace.start(w.h, C)
         w.capture()
         w.time_graph(3, 0, flush)

@@ -228,7 +228,17 @@ typedef struct ar_tactics {
                                    not change */
     uint64_t pace_min_bytes;    /* pace only calls of at least this many bytes per rank (default 128 KiB) */
     int32_t pace_multi_mbs;     /* as pace_mbs, for calls of several stages per block (default 220000) */
-    int32_t reserved;           /* 0 */
+    int32_t gpu_scope;          /* slots in host memory: the scope at which the ranks synchronise.  1 = GPU
+                                   scope: the per-block flags in HBM, raised and read with GPU-scope
+                                   release/acquire, and the tagged words and push flags (in host memory)
+                                   read and written at GPU scope -- the R ranks are kernels of one GPU, so
+                                   GPU scope holds every thread that observes them.  0 = system scope,
+                                   flags in mapped host memory, as two GPUs that share only the host
+                                   buffer need ("[Kernel] Two-rank FP16 all-reduce through pinned host
+                                   memory for GPUs without P2P", section "Purpose").  The slot data stays
+                                   in host memory either way, so every payload byte still crosses the
+                                   host link; results are the same.  Default 1.  Always 1 for HBM handles
+                                   (0 refused there) */
 } ar_tactics;
 
 /*
@@ -437,15 +447,16 @@ AR_API int ar_plan_compute(int R, uint64_t bytes, int vec_bytes, int algo, int t
                            int blocks_per_sm, ar_plan *plan);
 
 /* The all-reduce form a new handle's AR_ALGO_AUTO picks for R ranks, `bytes`
- * per rank and a slot kind (a tactic table measured on a GB300; a handle's own
- * tactics may differ, see ar_tactics).  Tagged-word form up to 512 KiB
- * (R <= 2), 256 KiB (R = 3) or 64 KiB (R = 4) with HBM slots and up to 16 KiB
- * (R <= 2) or 8 KiB (R = 3) with pinned-host slots (within
- * ar_info.tagged_capacity_bytes).  Otherwise
- * one-shot for R <= 3; two-shot from 512 KiB (R >= 8) or 2 MiB (R = 4..7)
- * with HBM slots, and from 64 KiB (R >= 8) or 256 KiB (R = 4..7) with
- * pinned-host slots, where one-shot reads R(R-1)S bytes over the host link
- * against two-shot's (2R-1)S.  Pure host arithmetic. */
+ * per rank and a slot kind (a tactic table measured on a GB300 with the
+ * default tactics, the ranks synchronising at GPU scope; a handle's own
+ * tactics may differ, see ar_tactics).  HBM slots: tagged-word form up to
+ * 512 KiB (R <= 2), 256 KiB (R = 3) or 64 KiB (R = 4) (within
+ * ar_info.tagged_capacity_bytes); otherwise one-shot for R <= 3, two-shot
+ * from 512 KiB (R >= 8) or 2 MiB (R = 4..7).  Pinned-host slots: never the
+ * tagged form; one-shot for R <= 2, two-shot from 512 KiB (R = 3), 128 KiB
+ * (R = 4), 64 KiB (R = 5..7) or 32 KiB (R >= 8), where one-shot reads
+ * R(R-1)S bytes over the host link against two-shot's (2R-1)S.  Pure host
+ * arithmetic. */
 AR_API int ar_choose_algo(int R, uint64_t bytes, int slot_kind);
 
 /* Launch this handle's kernels as programmatic dependents of the preceding
@@ -577,13 +588,17 @@ AR_API int ar_probe_host_link(uint64_t bytes, int reps, double gbs[4]);
  *   ns[2] = a flag's one-way trip through mapped host memory at system scope
  *           (release store by one block seen by another block's acquire polls:
  *           half a ping-pong round trip) -- the flag step of a pinned call;
- *   ns[3] = the same through HBM at GPU scope -- the flag step of an HBM call.
+ *   ns[3] = the same through HBM at GPU scope -- the flag step of an HBM call,
+ *           and of a pinned call whose ranks synchronise at GPU scope (the
+ *           gpu_scope tactic, the default);
+ *   ns[4] = as ns[1] with a GPU-scope fence -- the publish step of a pinned
+ *           call at GPU scope.
  * Two blocks of one kernel play the ping-pong (always resident together); each
  * of their waits is bounded (100 ms): AR_ETIMEOUT if one runs out.  Allocates
  * and frees its own buffers and stream.  Errors: AR_EINVAL, AR_ENOMEM,
  * AR_ECUDA, AR_ETIMEOUT.
  */
-AR_API int ar_probe_host_link_latency(int reps, double ns[4]);
+AR_API int ar_probe_host_link_latency(int reps, double ns[5]);
 AR_API int ar_probe_hbm_copy(uint64_t bytes, int reps, double *gbs);
 
 #ifdef __cplusplus

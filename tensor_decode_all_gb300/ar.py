@@ -61,10 +61,10 @@ class Tactics(ctypes.Structure):
                 ("cluster_twoshot_min_bytes", ctypes.c_uint64), ("cluster_max_bytes", ctypes.c_uint64),
                 ("all_fused", ctypes.c_int32), ("pace_mbs", ctypes.c_int32),
                 ("pace_min_bytes", ctypes.c_uint64), ("pace_multi_mbs", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("gpu_scope", ctypes.c_int32)]
 
 
-TACTIC_FIELDS = [name for name, _ in Tactics._fields_ if name != "reserved"]
+TACTIC_FIELDS = [name for name, _ in Tactics._fields_]
 
 
 class Plan(ctypes.Structure):
@@ -282,7 +282,7 @@ ar_strerror = strerror
 
 
 def ar_probe_host_link(nbytes: int, reps: int):
-    out = (ctypes.c_double * 4)()
+    out = (ctypes.c_double * 5)()
     rc = lib().ar_probe_host_link(nbytes, reps, out)
     if rc:
         raise ArError(rc, "ar_probe_host_link")
@@ -290,12 +290,12 @@ def ar_probe_host_link(nbytes: int, reps: int):
 
 
 def ar_probe_host_link_latency(reps: int = 200):
-    out = (ctypes.c_double * 4)()
+    out = (ctypes.c_double * 5)()
     rc = lib().ar_probe_host_link_latency(int(reps), out)
     if rc:
         raise ArError(rc, "ar_probe_host_link_latency")
     return {"host_load_rtt_ns": out[0], "store_4KiB_fence_sys_ns": out[1], "flag_host_sys_one_way_ns": out[2],
-            "flag_hbm_gpu_one_way_ns": out[3]}
+            "flag_hbm_gpu_one_way_ns": out[3], "store_4KiB_fence_gpu_ns": out[4]}
 
 
 def ar_probe_hbm_copy(nbytes: int, reps: int) -> float:

@@ -65,6 +65,8 @@ struct ar_handle {
     uint8_t *slots_dev = nullptr;          // device address of the slots
     void *flags_host = nullptr;            // pinned kind: host address of the flags
     unsigned long long *flags_dev = nullptr;
+    unsigned long long *flags_hbm = nullptr;   // pinned kind: the same flag lines in HBM (gpu_scope)
+    bool gpu_scope = true;                 // tactic: pinned kind, the ranks synchronise at GPU scope
     uint64_t flags_bytes = 0;
     Ctr *ctr = nullptr;                    // [R][bmax] then the abort word
     unsigned int *abort_word = nullptr;
@@ -134,7 +136,12 @@ int check_device(const ar_handle *h) {
 DevState dev_state(const ar_handle *h) {
     DevState d;
     d.slots = h->slots_dev;
-    d.flags = h->flags_dev;
+    // Pinned-host slots with the gpu_scope tactic: the flags in HBM, and every
+    // flag, tagged word and push flag at GPU scope (every rank is a kernel of
+    // this GPU); without it, flags in host memory and system scope throughout.
+    // HBM slots: flags in HBM at GPU scope.
+    const bool sys = h->kind == AR_SLOT_PINNED_HOST && !h->gpu_scope;
+    d.flags = h->kind == AR_SLOT_PINNED_HOST && h->gpu_scope ? h->flags_hbm : h->flags_dev;
     d.ctr = h->ctr;
     d.abort_word = h->abort_word;
     d.err = h->err_dev;
@@ -142,7 +149,7 @@ DevState dev_state(const ar_handle *h) {
     d.timeout_ns = h->timeout_ns.load(std::memory_order_relaxed);
     d.bmax = h->bmax;
     d.cmax = h->cmax;
-    d.sys_scope = h->kind == AR_SLOT_PINNED_HOST ? 1 : 0;
+    d.sys_scope = sys ? 1 : 0;
     d.ll = h->ll_dev;
     d.ll_vecs = h->ll_vecs;
     d.trace = h->trace;
@@ -159,6 +166,7 @@ void free_all(ar_handle *h) {
     else if (h->slots_dev) cudaFree(h->slots_dev);
     if (h->flags_host) cudaFreeHost(h->flags_host);
     else if (h->flags_dev) cudaFree(h->flags_dev);
+    if (h->flags_hbm) cudaFree(h->flags_hbm);
     if (h->ll_host) cudaFreeHost(h->ll_host);
     else if (h->ll_dev) cudaFree(h->ll_dev);
     if (h->push_host) cudaFreeHost(h->push_host);
@@ -180,6 +188,7 @@ void free_all(ar_handle *h) {
     h->slots_dev = nullptr;
     h->flags_host = nullptr;
     h->flags_dev = nullptr;
+    h->flags_hbm = nullptr;
     h->ll_host = nullptr;
     h->ll_dev = nullptr;
     h->ctr = nullptr;
@@ -192,6 +201,7 @@ void free_all(ar_handle *h) {
 int zero_state(ar_handle *h) {
     if (h->flags_host) std::memset(h->flags_host, 0, h->flags_bytes);
     else if (cudaMemset(h->flags_dev, 0, h->flags_bytes) != cudaSuccess) return AR_ECUDA;
+    if (h->flags_hbm && cudaMemset(h->flags_hbm, 0, h->flags_bytes) != cudaSuccess) return AR_ECUDA;
     if (cudaMemset(h->ctr, 0, h->ctr_bytes) != cudaSuccess) return AR_ECUDA;
     // Stale tagged words would carry tags the restarted counters reuse.
     if (h->ll_host) std::memset(h->ll_host, 0, h->ll_bytes);
@@ -314,13 +324,18 @@ int cluster_setup(ar_handle *h) {
 }
 
 // Measured on a GB300 (one-shot vs two-shot, bf16, 64 KiB..8 MiB per rank):
-// in HBM two-shot wins from 512 KiB at R = 8 and from about 2 MiB at R = 4;
-// over the host link, where one-shot reads R(R-1)S bytes against two-shot's
-// (2R-1)S, it wins from 64 KiB at R = 8 and from 256 KiB at R = 4.  Ranks in
-// between take the threshold of the smaller measured R; R <= 3 stays one-shot.
+// in HBM two-shot wins from 512 KiB at R = 8 and from about 2 MiB at R = 4
+// (R = 5..7 take R = 4's threshold; R <= 3 stays one-shot).  Over the host
+// link, where one-shot reads R(R-1)S bytes against two-shot's (2R-1)S, with
+// the ranks synchronising at GPU scope (graphs of 200 calls, one-shot /
+// two-shot us/call): from 32 KiB at R = 8 (9.56 vs 11.98; 16 KiB 7.79 vs
+// 8.10), from 128 KiB at R = 4 (9.58 vs 10.90; 64 KiB 6.84 vs 7.67) and from
+// 512 KiB at R = 3 (18.75 vs 18.89, 1 MiB 34.9 vs 45.3; 256 KiB 10.99 vs
+// 11.35).  R = 5..7 take 64 KiB, between R = 4's and R = 8's.
 uint64_t twoshot_threshold(int R, int slot_kind) {
+    if (slot_kind == AR_SLOT_PINNED_HOST)
+        return R <= 2 ? ~0ull : R == 3 ? (512ull << 10) : R == 4 ? (128ull << 10) : R < 8 ? (64ull << 10) : (32ull << 10);
     if (R < 4) return ~0ull;
-    if (slot_kind == AR_SLOT_PINNED_HOST) return R >= 8 ? (64ull << 10) : (256ull << 10);
     return R >= 8 ? (512ull << 10) : (2ull << 20);
 }
 
@@ -330,10 +345,14 @@ uint64_t twoshot_threshold(int R, int slot_kind) {
 // 3.7 us), up to 256 KiB at R = 3 (3.7 vs 4.0 us) and up to 64 KiB at R = 4;
 // from R = 5 on it is level at best and then slower: every thread polls
 // 2(R - 1) tagged vectors where one warp polls R flags.  Over the host link its
-// polls re-read words that have not landed yet, so it wins only for small
-// calls: up to 16 KiB at R = 2 (8 KiB: 3.5 vs 4.0 us) and 8 KiB at R = 3.
+// polls re-read words that have not landed yet.  With the flags in host memory
+// at system scope it won small calls (up to 16 KiB at R = 2, 8 KiB: 3.5 vs
+// 4.0 us; 8 KiB at R = 3); with the ranks synchronising at GPU scope (flags
+// in HBM, the default) the one-shot form wins at every size (R = 2 2 KiB
+// 3.22 vs 3.52 us, 8 KiB 3.32 vs 3.73; R = 3 2 KiB 3.51 vs 4.37), so AUTO
+// never picks it for pinned-host slots.
 uint64_t tagged_threshold(int R, int slot_kind) {
-    if (slot_kind == AR_SLOT_PINNED_HOST) return R <= 2 ? (16ull << 10) : R == 3 ? (8ull << 10) : 0;
+    if (slot_kind == AR_SLOT_PINNED_HOST) return 0;
     if (R <= 2) return 512ull << 10;
     if (R == 3) return 256ull << 10;
     return R == 4 ? (64ull << 10) : 0;
@@ -361,13 +380,13 @@ uint64_t cluster_twoshot_threshold(int R, int slot_kind) {
 // 2 MiB at R = 2 (5.73 / 6.07; 4 MiB 9.54 / 8.02), up to 1 MiB at R = 4 (1 MiB
 // 6.34 / 6.33, 512 KiB 3.64 / 4.45; 2 MiB 9.86 / 9.02) and at R = 8 up to the
 // decode-sized 768 KiB (6.6 / 8.3; 512 KiB 6.00 / 7.58; 1 MiB 10.66 / 9.49);
-// over the host link, where the flag forms' first-stage stores are paced, up to
-// 1 MiB at R = 2 (15.98 / 19.05; 2 MiB 40.53 / 35.97), 256 KiB at R = 4 (14.14 /
-// 17.27; 512 KiB 31.70 / 29.32) and 128 KiB at R = 8 (256 KiB 33.06 / 32.08;
-// 128 KiB 17.9 / 20.4 before pacing).  R = 3 takes R = 4's limit, R = 5..7
-// R = 8's.
+// over the host link, where the flag forms' first-stage stores are paced and
+// their flags are in HBM (GPU scope), up to 512 KiB at R = 2 (9.59 / 9.71;
+// 1 MiB 15.98 / 15.69), 256 KiB at R = 4 (14.48 / 15.15; 512 KiB 31.14 /
+// 23.79) and 64 KiB at R = 8 (10.82 / 12.06; 128 KiB 18.55 / 15.90).  R = 3
+// takes R = 4's limit, R = 5..7 R = 8's.
 uint64_t cluster_limit(int R, int slot_kind) {
-    if (slot_kind == AR_SLOT_PINNED_HOST) return R <= 2 ? (1ull << 20) : R <= 4 ? (256ull << 10) : (128ull << 10);
+    if (slot_kind == AR_SLOT_PINNED_HOST) return R <= 2 ? (512ull << 10) : R <= 4 ? (256ull << 10) : (64ull << 10);
     return R <= 2 ? (2ull << 20) : R <= 4 ? (1ull << 20) : (896ull << 10);
 }
 
@@ -934,6 +953,7 @@ AR_API ar_handle *ar_create(int R, int dtype, size_t max_numel, int slot_kind) {
         if (cudaHostAlloc(&h->flags_host, h->flags_bytes, fl) != cudaSuccess) return fail(AR_ENOMEM);
         if (cudaHostGetDevicePointer((void **)&h->flags_dev, h->flags_host, 0) != cudaSuccess)
             return fail(AR_ECUDA);
+        if (cudaMalloc((void **)&h->flags_hbm, h->flags_bytes) != cudaSuccess) return fail(AR_ENOMEM);
         std::memset(h->slots_host, 0, slots_total);
     } else {
         if (cudaMalloc((void **)&h->slots_dev, slots_total) != cudaSuccess) return fail(AR_ENOMEM);
@@ -1247,7 +1267,7 @@ AR_API int ar_get_tactics(const ar_handle *h, ar_tactics *t) {
     t->pace_mbs = h->pace_mbs;
     t->pace_min_bytes = h->pace_min_bytes;
     t->pace_multi_mbs = h->pace_multi_mbs;
-    t->reserved = 0;
+    t->gpu_scope = h->kind != AR_SLOT_PINNED_HOST || h->gpu_scope ? 1 : 0;
     return AR_OK;
 }
 
@@ -1259,6 +1279,8 @@ AR_API int ar_set_tactics(ar_handle *h, const ar_tactics *t) {
     if (t->all_fused != 0 && t->all_fused != 1) return AR_EINVAL;
     if ((t->pace_mbs != 0 && t->pace_mbs < 1000) || (t->pace_multi_mbs != 0 && t->pace_multi_mbs < 1000))
         return AR_EINVAL;
+    if (t->gpu_scope != 0 && t->gpu_scope != 1) return AR_EINVAL;
+    if (h->kind != AR_SLOT_PINNED_HOST && t->gpu_scope != 1) return AR_EINVAL;
     h->twoshot_min_bytes = t->twoshot_min_bytes;
     h->twoshot_sub = t->twoshot_sub;
     h->max_blocks = t->max_blocks;
@@ -1269,6 +1291,7 @@ AR_API int ar_set_tactics(ar_handle *h, const ar_tactics *t) {
     h->pace_mbs = t->pace_mbs;
     h->pace_min_bytes = t->pace_min_bytes;
     h->pace_multi_mbs = t->pace_multi_mbs;
+    h->gpu_scope = t->gpu_scope == 1;
     return AR_OK;
 }
 

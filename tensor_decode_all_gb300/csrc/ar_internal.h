@@ -2,8 +2,10 @@
 //
 // Memory layout of one handle (all addresses as seen by the GPU):
 //   slots : [2 parities][R ranks][slot_bytes]        pinned host or HBM
-//   flags : [R ranks][bmax blocks] x 128 B lines     same memory as the slots;
-//           word 0 of each line is the flag, a 64-bit count of published stages
+//   flags : [R ranks][bmax blocks] x 128 B lines     HBM; for pinned-host slots also a
+//           copy in mapped host memory, and the gpu_scope tactic picks which one
+//           a call uses; word 0 of each line is the flag, a 64-bit count of
+//           published stages
 //   ctr   : [R ranks][cmax blocks] x {seq, calls}    HBM; private to one block (cmax >= bmax)
 //   abort : one 32-bit word in HBM, non-zero once any block has given up
 //   err   : one ar_error_info in mapped pinned host memory
@@ -63,7 +65,8 @@ struct DevState {
     uint64_t slot_bytes;
     uint64_t timeout_ns;
     int bmax;                  // flag slots per rank (the largest grid of a flag-protocol launch)
-    int sys_scope;             // 1: slots/flags in host memory, system-scope ordering
+    int sys_scope;             // 1: the ranks synchronise at system scope (flags in host memory, the pages'
+                               // two-GPU case); 0: at GPU scope (flags in HBM; slots in either memory)
     ulonglong2 *ll;            // [2][R][ll_vecs] tagged-word buffers (same memory as the slots)
     uint64_t ll_vecs;          // 16-byte tagged vectors per rank and parity: 2 per 16 payload bytes
     ar_trace_record *trace;    // [depth][R][bmax] or null (tracing off)

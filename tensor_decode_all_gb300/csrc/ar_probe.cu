@@ -99,14 +99,21 @@ __global__ void probe_chase_kernel(const unsigned long long *buf, int n, unsigne
 }
 
 // n rounds of: every thread of one block stores 16 bytes to host memory (4
-// KiB with 256 threads), barrier, thread 0 a system-scope fence (returns once
-// the stores are acknowledged), barrier -- the publish step of a block.
+// KiB with 256 threads), barrier, thread 0 a system-scope (SYS) or GPU-scope
+// fence (returns once the stores are ordered for every observer of that
+// scope), barrier -- the publish step of a block.
+template <int SYS>
 __global__ void probe_store_fence_kernel(uint4 *dst, int n, unsigned long long *out) {
     const unsigned long long t0 = probe_timer_ns();
     for (int k = 0; k < n; ++k) {
         dst[(uint64_t)(k & 63) * blockDim.x + threadIdx.x] = make_uint4(k, 1, 2, 3);
         __syncthreads();
-        if (threadIdx.x == 0) asm volatile("fence.sc.sys;" ::: "memory");
+        if (threadIdx.x == 0) {
+            if (SYS)
+                asm volatile("fence.sc.sys;" ::: "memory");
+            else
+                asm volatile("fence.sc.gpu;" ::: "memory");
+        }
         __syncthreads();
     }
     if (threadIdx.x == 0) out[0] = probe_timer_ns() - t0;
@@ -237,7 +244,7 @@ AR_API int ar_probe_host_link(uint64_t bytes, int reps, double gbs[4]) {
     return rc;
 }
 
-AR_API int ar_probe_host_link_latency(int reps, double ns[4]) {
+AR_API int ar_probe_host_link_latency(int reps, double ns[5]) {
     if (!ns || reps < 1 || reps > 100000) return AR_EINVAL;
     constexpr int kLines = 4096;                  // chase over 4096 lines of 128 B (512 KiB)
     const uint64_t host_bytes = (uint64_t)kLines * 128;
@@ -281,7 +288,10 @@ AR_API int ar_probe_host_link_latency(int reps, double ns[4]) {
     };
     if (rc == AR_OK) ns[0] = run([&] { probe_chase_kernel<<<1, 1, 0, st>>>(dhb, reps, dout); }, reps);
     if (rc == AR_OK)
-        ns[1] = run([&] { probe_store_fence_kernel<<<1, 256, 0, st>>>(reinterpret_cast<uint4 *>(dhb), reps, dout); },
+        ns[1] = run([&] { probe_store_fence_kernel<1><<<1, 256, 0, st>>>(reinterpret_cast<uint4 *>(dhb), reps, dout); },
+                    reps);
+    if (rc == AR_OK)
+        ns[4] = run([&] { probe_store_fence_kernel<0><<<1, 256, 0, st>>>(reinterpret_cast<uint4 *>(dhb), reps, dout); },
                     reps);
     if (rc == AR_OK) {
         std::memset(hf, 0, 4096);

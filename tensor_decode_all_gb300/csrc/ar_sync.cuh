@@ -10,8 +10,12 @@
 // order of "[Kernel] Two-rank FP16 all-reduce through pinned host memory for
 // GPUs without P2P", section "Purpose").
 //
-// Scope: slots and flags in mapped host memory use .sys (the pages' case: two
-// GPUs reach the host buffer); in HBM they use .gpu.
+// Scope: flags in mapped host memory use .sys (the pages' case: two GPUs
+// reach the host buffer); flags in HBM use .gpu, whether the slots are in HBM
+// or in host memory (the gpu_scope tactic picks for host-memory slots).  The scope of a release/acquire pair is the set of
+// threads it orders, not a place in memory: when every rank is a kernel of
+// this GPU, a GPU-scope release orders the block's earlier slot stores to host
+// memory before the flag for every reader that acquires it.
 //
 // Every wait is bounded by %globaltimer.  A block that runs out of time sets
 // the sticky abort word, records itself in the handle's error record (the

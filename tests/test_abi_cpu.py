@@ -103,11 +103,13 @@ def test_plan_zero_bytes_and_bad_args(lib):
 
 
 def test_choose_algo_rule(lib):
-    for kind in (ar.AR_SLOT_HBM, ar.AR_SLOT_PINNED_HOST):
-        for R in (1, 2, 3):
-            assert tda.ar_choose_algo(R, 1 << 30, kind) == ar.AR_ALGO_ONESHOT
+    for R in (1, 2, 3):
+        assert tda.ar_choose_algo(R, 1 << 30, ar.AR_SLOT_HBM) == ar.AR_ALGO_ONESHOT
+    for R in (1, 2):
+        assert tda.ar_choose_algo(R, 1 << 30, ar.AR_SLOT_PINNED_HOST) == ar.AR_ALGO_ONESHOT
+        assert tda.ar_choose_algo(R, 16, ar.AR_SLOT_PINNED_HOST) == ar.AR_ALGO_ONESHOT
     # tagged-word form for small calls (R, HBM limit, pinned limit; 0 = never)
-    for R, hbm, pinned in ((1, 512 << 10, 16 << 10), (2, 512 << 10, 16 << 10), (3, 256 << 10, 8 << 10),
+    for R, hbm, pinned in ((1, 512 << 10, 0), (2, 512 << 10, 0), (3, 256 << 10, 0),
                            (4, 64 << 10, 0), (5, 0, 0), (6, 0, 0), (8, 0, 0)):
         for kind, lim in ((ar.AR_SLOT_HBM, hbm), (ar.AR_SLOT_PINNED_HOST, pinned)):
             if lim:
@@ -115,9 +117,11 @@ def test_choose_algo_rule(lib):
                 assert tda.ar_choose_algo(R, lim, kind) == ar.AR_ALGO_TAGGED
             assert tda.ar_choose_algo(R, lim + 16, kind) != ar.AR_ALGO_TAGGED
     # thresholds from the measured crossover (R, HBM, pinned host)
-    for R, hbm, pinned in ((4, 2 << 20, 256 << 10), (7, 2 << 20, 256 << 10), (8, 512 << 10, 64 << 10)):
-        assert tda.ar_choose_algo(R, hbm - 1, ar.AR_SLOT_HBM) == ar.AR_ALGO_ONESHOT
-        assert tda.ar_choose_algo(R, hbm, ar.AR_SLOT_HBM) == ar.AR_ALGO_TWOSHOT
+    for R, hbm, pinned in ((3, None, 512 << 10), (4, 2 << 20, 128 << 10), (5, 2 << 20, 64 << 10),
+                           (7, 2 << 20, 64 << 10), (8, 512 << 10, 32 << 10)):
+        if hbm:
+            assert tda.ar_choose_algo(R, hbm - 1, ar.AR_SLOT_HBM) == ar.AR_ALGO_ONESHOT
+            assert tda.ar_choose_algo(R, hbm, ar.AR_SLOT_HBM) == ar.AR_ALGO_TWOSHOT
         assert tda.ar_choose_algo(R, pinned - 1, ar.AR_SLOT_PINNED_HOST) == ar.AR_ALGO_ONESHOT
         assert tda.ar_choose_algo(R, pinned, ar.AR_SLOT_PINNED_HOST) == ar.AR_ALGO_TWOSHOT
     assert tda.ar_set_algo(0, ar.AR_ALGO_ONESHOT) == ar.AR_EINVAL

@@ -225,6 +225,8 @@ def test_link_latency_probe_is_ordered():
     lat = tda.ar_probe_host_link_latency(100)
     assert all(20.0 < v < 1e6 for v in lat.values()), lat
     assert lat["flag_hbm_gpu_one_way_ns"] < lat["flag_host_sys_one_way_ns"], lat
+    assert set(lat) == {"host_load_rtt_ns", "store_4KiB_fence_sys_ns", "flag_host_sys_one_way_ns",
+                        "flag_hbm_gpu_one_way_ns", "store_4KiB_fence_gpu_ns"}, lat
     with pytest.raises(ar.ArError):
         tda.ar_probe_host_link_latency(0)
 
