@@ -533,7 +533,7 @@ def algo_bytes(op, R, S, slots, algo=None):
 
     pinned-host all-reduce, one-shot: host-link writes W = R*S (each rank
       publishes once), reads Rd = R*(R-1)*S (each rank fetches every peer's chunk);
-    pinned-host all-reduce, two-shot: W = R*S published + S of reduced results,
+    pinned-host all-reduce, two-shot (flag or cluster form): W = R*S published + S of reduced results,
       Rd = R*S (every rank reads its sub-tile from all R slots) + (R-1)*S
       (every rank reads the R-1 other reduced sub-tiles);
     HBM all-reduce (either form): DRAM 4*R*S (inputs, slot writes, slot reads
@@ -544,7 +544,8 @@ def algo_bytes(op, R, S, slots, algo=None):
       and outputs 2*R*S plus the areas written and read, 2*R*(R-1)*S.
     """
     if slots == "pinned":
-        if op == "allreduce" and algo == "twoshot":
+        # the cluster form with sub-tiles ("cluster/sub64") is two-shot too
+        if op == "allreduce" and (algo == "twoshot" or (algo or "").startswith("cluster/sub")):
             return {"link_write": (R + 1) * S, "link_read": (2 * R - 1) * S}
         if op == "allreduce" and algo == "push":
             return {"link_write": R * (R - 1) * S, "link_read": R * (R - 1) * S}

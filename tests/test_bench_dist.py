@@ -111,3 +111,23 @@ def test_profiled_traffic_follows_each_kernel_family(tmp_path, monkeypatch):
     hdr.write_text(hdr.read_text() + "\n#define EDIT 2\n")
     assert valid() == set()
     assert bench.profiled_traffic("no such workload") is None
+
+
+def test_algorithmic_bytes_of_each_form():
+    """The byte counts behind every roofline fraction: pinned-host one-shot
+    W = RS, Rd = R(R-1)S; two-shot, in the flag and the cluster form, W = (R+1)S,
+    Rd = (2R-1)S; push R(R-1)S each way; HBM 4RS; allgather 3RS + R^2 S."""
+    import bench
+    R, S = 8, 1 << 20
+    one = {"link_write": R * S, "link_read": R * (R - 1) * S}
+    two = {"link_write": (R + 1) * S, "link_read": (2 * R - 1) * S}
+    assert bench.algo_bytes("allreduce", R, S, "pinned", "oneshot") == one
+    assert bench.algo_bytes("allreduce", R, S, "pinned", "cluster") == one
+    assert bench.algo_bytes("allreduce", R, S, "pinned", "tagged") == one
+    assert bench.algo_bytes("allreduce", R, S, "pinned", "twoshot") == two
+    assert bench.algo_bytes("allreduce", R, S, "pinned", "cluster/sub64") == two
+    assert bench.algo_bytes("allreduce", R, S, "pinned", "push") == {"link_write": R * (R - 1) * S,
+                                                                   "link_read": R * (R - 1) * S}
+    assert bench.algo_bytes("allreduce", R, S, "hbm", "cluster/sub64") == {"dram": 4 * R * S}
+    assert bench.algo_bytes("allgather", R, S, "hbm") == {"dram": 3 * R * S + R * R * S}
+    assert bench.algo_bytes("allgather", R, S, "pinned") == one
