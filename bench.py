@@ -782,6 +782,18 @@ EXPERIMENT_WORKLOADS = {
                                {"tactics": {"pace_multi_mbs": 160000}}),
 }
 
+# Workload 3 (and the same shape over the host link) with other two-shot
+# sub-tiles and block caps: several tiles per block let HBM calls merge each
+# reduced sub-tile into the next tile's flag round.
+for _sub in (64, 128, 256):
+    for _cap in (0, 48, 24, 12):
+        EXPERIMENT_WORKLOADS[f"x_r8_768K_sub{_sub}_b{_cap}"] = (
+            "allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20,
+            {"tactics": {"twoshot_sub": _sub, "max_blocks": _cap}})
+        EXPERIMENT_WORKLOADS[f"x_r8_768K_pinned_sub{_sub}_b{_cap}"] = (
+            "allreduce", 8, "bf16", 393216, "pinned", 3, "normal", 50, 10,
+            {"tactics": {"twoshot_sub": _sub, "max_blocks": _cap}})
+
 # Pinned-host slots with the ranks synchronising at system scope, flags in host
 # memory (_sysscope), or at GPU scope, flags in HBM (_gpuscope); and the
 # headline's shape at GPU scope at other paces.
