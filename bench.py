@@ -737,6 +737,13 @@ EXTRA_WORKLOADS = {
     "r2_fp16_131072_pinned_fused_flags": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 100, 20,
                                           {"launch": "fused", "tactics": {"cluster_max_bytes": 0}}),
     "r2_fp16_131072_pinned_graph1": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 1, 200),
+    # workloads 2 and 1 with the ranks synchronising at system scope, flags in host
+    # memory (two GPUs sharing only the host buffer need that placement); at that
+    # scope the tagged-word form is the faster one at 8 KiB
+    "r2_fp16_131072_pinned_sysscope": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 100, 20,
+                                       {"tactics": {"gpu_scope": 0}}),
+    "r2_fp16_4096_pinned_sysscope": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", 100, 20,
+                                     {"tactics": {"gpu_scope": 0, "tagged_max_bytes": 16 << 10}}),
     "r2_fp16_131072_pinned_all_graph1": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 1, 200,
                                          {"launch": "all"}),
     # large payloads in HBM (the HBM roofline)

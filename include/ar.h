@@ -219,8 +219,8 @@ typedef struct ar_tactics {
                                    stores and the peers' loads together, is to cross the host link, for
                                    calls of one stage per block.  The first stage's slot stores of block
                                    b of every rank start b * R * tile_bytes / (pace * share) after the
-                                   block starts, share = the stores' part of the traffic (1/R one-shot,
-                                   (R+1)/3R two-shot, 1/R allgather), so the stores reach the link about
+                                   block starts, share = the paced stores' part of the traffic (1/R one-
+                                   shot, 1/3 two-shot, 1/R allgather), so the stores reach the link about
                                    as fast as it drains them rather than all at once.  One-shot, two-shot
                                    and cluster all-reduce forms (the cluster form only when all its
                                    clusters are resident at once) and the allgather.  0 = all at once; otherwise >= 1000.  Default 356000 for

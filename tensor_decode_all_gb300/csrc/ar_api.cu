@@ -701,10 +701,11 @@ int end_call(ar_handle *h, int rank, int rc) {
 // cycles, for a call of `bytes` per rank planned as `plan` on `blocks` blocks
 // per rank.  The handle's pace (one for calls of one stage per block, one for
 // calls of several) is the rate at which the call's slot traffic -- stores and
-// the peers' loads together -- is to cross the host link; the stores take
-// their share of it, W / (W + Rd): 1 / R for the one-shot form (W = R S,
-// Rd = R (R - 1) S), (R + 1) / 3R for the two-shot form (W = (R + 1) S,
-// Rd = (2R - 1) S).  So one tile of every rank leaves every
+// the peers' loads together -- is to cross the host link; the paced stores,
+// the first stage's R S, take their share of it, R S / (W + Rd): 1 / R for
+// the one-shot form (W = R S, Rd = R (R - 1) S) and 1 / 3 for the two-shot
+// form (W = (R + 1) S, Rd = (2R - 1) S; its second-round stores of reduced
+// sub-tiles are not paced).  So one tile of every rank leaves every
 // R * tile_bytes / (pace * share), converted at the GPU's peak SM clock.  Only
 // for slots in host memory, R >= 2, calls of at least pace_min_bytes per rank
 // and a pace set; capped so that no block of the largest grid waits more than
@@ -714,7 +715,7 @@ uint32_t pace_cycles(const ar_handle *h, uint64_t bytes, const ar_plan &plan, in
     const int pace = plan.tiles > (uint64_t)blocks ? h->pace_multi_mbs : h->pace_mbs;
     if (pace <= 0) return 0;
     const double R = (double)h->R;
-    const double share = plan.subtile_vecs ? (R + 1.0) / (3.0 * R) : 1.0 / R;
+    const double share = plan.subtile_vecs ? 1.0 / 3.0 : 1.0 / R;
     const double ns = R * (double)plan.tile_bytes * 1000.0 / ((double)pace * share);
     double cyc = ns * (double)h->clock_khz / 1e6;
     const double cap = 4e6 / (double)(h->bmax > 0 ? h->bmax : 1);

@@ -55,7 +55,7 @@ def test_defaults_rule_and_declines():
             h.set_tactics(**bad)
     assert h.tactics()["pace_mbs"] == 178000                         # a refused change leaves the tactics
     h.destroy()
-    # two-shot share (R + 1) / 3R; one-shot share 1 / R
+    # two-shot share 1 / 3 (the first stage's stores of W + Rd = 3RS); one-shot share 1 / R
     g = tda.Handle(4, torch.bfloat16, 1 << 20, "pinned")
     g.set_tactics(pace_multi_mbs=356000)           # one pace whether a call takes one stage or several
     p2 = g.plan("allreduce", 1 << 19)              # 1 MiB per rank: two-shot at R = 4 over the host link
@@ -64,7 +64,7 @@ def test_defaults_rule_and_declines():
     p1 = g.plan("allreduce", 1 << 19)
     per_byte_2 = p2.pace_cycles / p2.tile_bytes
     per_byte_1 = p1.pace_cycles / p1.tile_bytes
-    assert abs(per_byte_1 / per_byte_2 - (5 / 12) / (1 / 4)) < 0.03, (per_byte_1, per_byte_2)
+    assert abs(per_byte_1 / per_byte_2 - (1 / 3) / (1 / 4)) < 0.03, (per_byte_1, per_byte_2)
     g.destroy()
     # HBM slots are never paced, whatever the tactics say
     k = tda.Handle(2, torch.float16, 1 << 20, "hbm")
