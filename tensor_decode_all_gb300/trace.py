@@ -56,7 +56,9 @@ def overlap_violations(rec: np.ndarray) -> list:
 
 
 def summarize(rec: np.ndarray, sm_clock_mhz: float) -> dict:
-    """Median phases over blocks (µs) and the spread of rank start times per call."""
+    """Median phases over blocks (µs), the spread of rank start times per call,
+    and per call the time from its first block's start to its last block's end
+    and from there to the next call's first start (negative: they overlap)."""
     if len(rec) == 0:
         return {"records": 0}
     us = 1.0 / sm_clock_mhz
@@ -65,10 +67,17 @@ def summarize(rec: np.ndarray, sm_clock_mhz: float) -> dict:
     end = rec["cyc_end"].astype(np.float64) * us
     span = (rec["t_end_ns"] - rec["t_start_ns"]).astype(np.float64) / 1e3
     skew = []
+    first, last = [], []
     for call in np.unique(rec["call"]):
         g = rec[rec["call"] == call]
         starts = [g[g["rank"] == r]["t_start_ns"].min() for r in np.unique(g["rank"])]
         skew.append((max(starts) - min(starts)) / 1e3)
+        first.append(int(g["t_start_ns"].min()))
+        last.append(int(g["t_end_ns"].max()))
+    # per call: its first block's start to its last block's end, and that end to
+    # the next call's first start (calls in order of their call count)
+    call_span = [(b - a) / 1e3 for a, b in zip(first, last)]
+    call_gap = [(first[i + 1] - last[i]) / 1e3 for i in range(len(first) - 1)]
     return {
         "records": int(len(rec)),
         "calls": int(len(np.unique(rec["call"]))),
@@ -80,5 +89,7 @@ def summarize(rec: np.ndarray, sm_clock_mhz: float) -> dict:
                       "peers_seen_to_end": round(float(np.median(end - peers)), 3),
                       "block_span": round(float(np.median(span)), 3)},
         "rank_start_skew_us": {"median": round(float(np.median(skew)), 3), "max": round(float(np.max(skew)), 3)},
+        "call_us": {"span_median": round(float(np.median(call_span)), 3),
+                    "gap_median": round(float(np.median(call_gap)), 3) if call_gap else None},
         "overlap_violations": len(overlap_violations(rec)),
     }

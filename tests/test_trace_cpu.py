@@ -38,3 +38,5 @@ def test_summary_phases_and_start_skew():
                               "peers_seen_to_end": 3.0, "block_span": 7.75}
     assert s["rank_start_skew_us"] == {"median": 1.25, "max": 2.0}
     assert s["overlap_violations"] == 0
+    # call 0 runs 1.0 .. 9.5 us, call 1 20.0 .. 28.0 us
+    assert s["call_us"] == {"span_median": 8.25, "gap_median": 10.5}
