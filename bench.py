@@ -1043,6 +1043,9 @@ PROFILE_WORKLOADS = {
     "allgather_c64_r8_hbm_1call": ("allgather", 8, "c64", 500000, "hbm", 4, "normal", 1),
     "r8_bf16_768KiB_hbm_fused_1call": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 1),
     "r2_fp16_8KiB_pinned_1call": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", 1),
+    # the two-shot form over the host link (AUTO's pick at these sizes)
+    "r8_bf16_256KiB_pinned_1call": ("allreduce", 8, "bf16", 131072, "pinned", 5, "uniform", 1),
+    "r4_bf16_1MiB_pinned_1call": ("allreduce", 4, "bf16", 1 << 19, "pinned", 5, "uniform", 1),
     "r8_bf16_768KiB_hbm_all": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100),
     "r8_bf16_768KiB_hbm_all_1call": ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 1),
     "r2_fp16_256KiB_pinned_all_1call": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 1),

@@ -440,7 +440,8 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan);
  * vec_bytes (16, 8, 4, 2 or 1), algo AR_ALGO_ONESHOT or AR_ALGO_TWOSHOT,
  * `threads` per block, and a GPU that holds sm_count * blocks_per_sm blocks of
  * the kernel at once.  Two-shot plans here use 256-vector sub-tiles; a handle
- * with HBM slots uses 128 when that leaves more than half its blocks idle
+ * with HBM slots uses 128 when that leaves more than half its blocks idle, one
+ * with pinned-host slots 64 while 256 would make fewer than 8 tiles
  * (ar_plan_for shows its choice).
  */
 AR_API int ar_plan_compute(int R, uint64_t bytes, int vec_bytes, int algo, int threads, int sm_count,

@@ -486,14 +486,19 @@ int handle_blocks(const ar_handle *h, int plan_blocks) {
     return b;
 }
 
-// Sub-tile size (vectors) of the two-shot form.  256 unless the slots are in
-// HBM and 256-vector sub-tiles would give fewer than half the blocks the GPU
-// can hold: then 128, which spreads a mid-sized call over twice the blocks.
-// Measured on a GB300, bf16: R=8 768 KiB HBM 9.9 -> 9.5 us; from 2 MiB up,
-// and over the host link, 256 is as fast or faster.
+// Sub-tile size (vectors) of the two-shot form.  In HBM: 256, unless
+// 256-vector sub-tiles would give fewer than half the blocks the GPU can
+// hold: then 128, which spreads a mid-sized call over twice the blocks
+// (measured on a GB300, bf16: R=8 768 KiB 9.9 -> 9.5 us; from 2 MiB up 256
+// is as fast or faster).  Over the host link: 64 while 256-vector sub-tiles
+// would make fewer than 8 tiles, else 256 (GPU-scope flags, bf16, per-rank
+// launches, 64 / 128 / 256 vectors, us/call: R=8 32 KiB 8.17 / 8.63 / 9.57,
+// 64 KiB 11.02 / 11.56 / 11.86, 128 KiB 16.21 / 16.80 / 16.87, 256 KiB (8
+// tiles) 26.59 / 26.90 / 26.56; R=4 128 KiB (8 tiles) 9.81 / 9.63 / 9.53,
+// 1 MiB 48.9 / 47.3 / 43.1).
 int twoshot_sub_for(int R, uint64_t nv, uint64_t bmax, int slot_kind) {
-    if (slot_kind != AR_SLOT_HBM) return 256;
     const uint64_t tiles256 = (nv + 256ull * R - 1) / (256ull * R);
+    if (slot_kind != AR_SLOT_HBM) return tiles256 < 8 ? 64 : 256;
     return 2 * tiles256 < bmax ? 128 : 256;
 }
 

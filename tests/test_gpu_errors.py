@@ -206,6 +206,12 @@ def test_query_and_plan():
     bmax = info.sm_count * info.blocks_per_sm_twoshot // 8
     assert p.subtile_vecs == (128 if 2 * tiles256 < bmax else 256)
     h.destroy()
+    # pinned-host slots: 64-vector sub-tiles while 256-vector ones make fewer than 8 tiles
+    g = tda.Handle(8, torch.bfloat16, 1 << 20, "pinned")
+    g.set_algo("twoshot")
+    for n, sub in ((16384, 64), (65536, 64), (114688, 64), (114688 + 8, 256), (1 << 20, 256)):
+        assert g.plan("allreduce", n).subtile_vecs == sub, n
+    g.destroy()
 
 
 def test_probes_run():
