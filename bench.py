@@ -789,41 +789,47 @@ EXPERIMENT_WORKLOADS = {
                                {"tactics": {"pace_multi_mbs": 160000}}),
 }
 
-# Workload 3 (and the same shape over the host link) with other two-shot
-# sub-tiles and block caps: several tiles per block let HBM calls merge each
-# reduced sub-tile into the next tile's flag round.
-for _sub in (64, 128, 256):
-    for _cap in (0, 48, 24, 12):
-        EXPERIMENT_WORKLOADS[f"x_r8_768K_sub{_sub}_b{_cap}"] = (
-            "allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20,
-            {"tactics": {"twoshot_sub": _sub, "max_blocks": _cap}})
-        EXPERIMENT_WORKLOADS[f"x_r8_768K_pinned_sub{_sub}_b{_cap}"] = (
-            "allreduce", 8, "bf16", 393216, "pinned", 3, "normal", 50, 10,
-            {"tactics": {"twoshot_sub": _sub, "max_blocks": _cap}})
+def _experiment_grids() -> dict:
+    """Workload grids for --only comparisons:
+    - workload 3 (and the same shape over the host link) with other two-shot
+      sub-tiles and block caps: several tiles per block let HBM calls merge
+      each reduced sub-tile into the next tile's flag round;
+    - pinned-host slots with the ranks synchronising at system scope, flags
+      in host memory (_sysscope), or at GPU scope, flags in HBM (_gpuscope);
+    - the headline's shape and R=2 4 MiB at GPU scope at other paces."""
+    grid = {}
+    for sub in (64, 128, 256):
+        for cap in (0, 48, 24, 12):
+            tactics = {"tactics": {"twoshot_sub": sub, "max_blocks": cap}}
+            grid[f"x_r8_768K_sub{sub}_b{cap}"] = ("allreduce", 8, "bf16", 393216, "hbm", 3, "normal", 100, 20,
+                                                  tactics)
+            grid[f"x_r8_768K_pinned_sub{sub}_b{cap}"] = ("allreduce", 8, "bf16", 393216, "pinned", 3, "normal",
+                                                         50, 10, tactics)
+    scoped = {
+        "x_r2_256K_pinned": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 100, 20),
+        "x_r2_128K_pinned": ("allreduce", 2, "f16", 65536, "pinned", 5, "uniform", 100, 20),
+        "x_r2_4M_pinned": ("allreduce", 2, "f16", 2 << 20, "pinned", 5, "uniform", 20, 10),
+        "x_r4_1M_pinned": ("allreduce", 4, "bf16", 1 << 19, "pinned", 5, "uniform", 50, 10),
+        "x_r8_256K_pinned": ("allreduce", 8, "bf16", 131072, "pinned", 5, "uniform", 50, 10),
+        "x_ag_r4_pinned": ("allgather", 4, "c64", 500000, "pinned", 4, None, 5, 5),
+        "x_r2_8K_pinned": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", 100, 20),
+        "x_r2_32K_pinned": ("allreduce", 2, "f16", 16384, "pinned", 5, "uniform", 100, 20),
+        "x_r8_64K_pinned": ("allreduce", 8, "bf16", 32768, "pinned", 5, "uniform", 100, 20),
+    }
+    for name, spec in scoped.items():
+        for suffix, flags in (("sysscope", 0), ("gpuscope", 1)):
+            grid[f"{name}_{suffix}"] = spec + ({"tactics": {"gpu_scope": flags}},)
+    for pace in (0, 240000, 270000, 300000, 330000):
+        grid[f"x_r2_256K_pinned_gpuscope_pace{pace // 1000}"] = (
+            "allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 100, 20,
+            {"tactics": {"gpu_scope": 1, "pace_mbs": pace}})
+        grid[f"x_r2_4M_pinned_gpuscope_pace{pace // 1000}"] = (
+            "allreduce", 2, "f16", 2 << 20, "pinned", 5, "uniform", 20, 10,
+            {"tactics": {"gpu_scope": 1, "pace_multi_mbs": pace}})
+    return grid
 
-# Pinned-host slots with the ranks synchronising at system scope, flags in host
-# memory (_sysscope), or at GPU scope, flags in HBM (_gpuscope); and the
-# headline's shape at GPU scope at other paces.
-for _name, _spec in {
-    "x_r2_256K_pinned": ("allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 100, 20),
-    "x_r2_128K_pinned": ("allreduce", 2, "f16", 65536, "pinned", 5, "uniform", 100, 20),
-    "x_r2_4M_pinned": ("allreduce", 2, "f16", 2 << 20, "pinned", 5, "uniform", 20, 10),
-    "x_r4_1M_pinned": ("allreduce", 4, "bf16", 1 << 19, "pinned", 5, "uniform", 50, 10),
-    "x_r8_256K_pinned": ("allreduce", 8, "bf16", 131072, "pinned", 5, "uniform", 50, 10),
-    "x_ag_r4_pinned": ("allgather", 4, "c64", 500000, "pinned", 4, None, 5, 5),
-    "x_r2_8K_pinned": ("allreduce", 2, "f16", 4096, "pinned", 1, "uniform", 100, 20),
-    "x_r2_32K_pinned": ("allreduce", 2, "f16", 16384, "pinned", 5, "uniform", 100, 20),
-    "x_r8_64K_pinned": ("allreduce", 8, "bf16", 32768, "pinned", 5, "uniform", 100, 20),
-}.items():
-    for _suffix, _flags in (("sysscope", 0), ("gpuscope", 1)):
-        EXPERIMENT_WORKLOADS[f"{_name}_{_suffix}"] = _spec + ({"tactics": {"gpu_scope": _flags}},)
-for _pace in (0, 240000, 270000, 300000, 330000):
-    EXPERIMENT_WORKLOADS[f"x_r2_256K_pinned_gpuscope_pace{_pace // 1000}"] = (
-        "allreduce", 2, "f16", 131072, "pinned", 2, "normal4", 100, 20,
-        {"tactics": {"gpu_scope": 1, "pace_mbs": _pace}})
-    EXPERIMENT_WORKLOADS[f"x_r2_4M_pinned_gpuscope_pace{_pace // 1000}"] = (
-        "allreduce", 2, "f16", 2 << 20, "pinned", 5, "uniform", 20, 10,
-        {"tactics": {"gpu_scope": 1, "pace_multi_mbs": _pace}})
+
+EXPERIMENT_WORKLOADS.update(_experiment_grids())
 
 
 # Order of the summary: the workloads a reader looks for first come last, so
