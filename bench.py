@@ -558,10 +558,13 @@ def algo_bytes(op, R, S, slots, algo=None):
 
 
 def link_floor_s(W, Rd, link):
-    """Shortest time the host link allows for W bytes written and Rd bytes read.
-    NVLink-C2C is full duplex, so each direction has its own limit, measured
-    alone by the probe in this run.  (The probe's both-directions copy figure is
-    reported as well, but it is not a limit: read-heavy calls have gone past it.)"""
+    """Shortest time the host link would allow for W bytes written and Rd bytes
+    read if each direction kept its solo rate (measured alone by the probe in
+    this run) while the other is busy.  It does not quite: with both directions
+    streaming at an even split the probe sees ~170 GB/s each way against ~193 /
+    ~210 alone, and add_link_floors reports that floor beside this one.  This one
+    stays the headline fraction because it holds for any mix of reads and
+    writes; the concurrent rates are measured at one mix."""
     gb = 1e9
     return max(W / (link["write_gbs"] * gb), Rd / (link["read_gbs"] * gb))
 
@@ -595,8 +598,10 @@ def roofline(op, R, S, slots, t_call_s, link, hbm_gbs, algo=None):
 def add_link_floors(rf, lat, link, t_call_s, gpu_scope=True):
     """Beside the per-direction floor that `frac` uses, two more floors of a
     host-link call, both measured in this run: the duplex floor (each direction
-    at the rate the probe sees while the other direction is busy too -- the
-    link does not give both directions their solo rates at once) and the
+    at the rate the probe sees while the other direction streams too, half the
+    blocks storing and half loading -- the link does not give both directions
+    their solo rates at once; a floor for calls that move about as many bytes
+    each way, as the headline does) and the
     latency chain one tile must pass in protocol order (its stores ordered by
     the release's fence, the flag's one-way trip, one dependent read round
     trip), at the scope the call's ranks synchronise at: GPU scope (flags in
@@ -616,7 +621,8 @@ def add_link_floors(rf, lat, link, t_call_s, gpu_scope=True):
     rf["frac_duplex"] = round(duplex / t_call_s, 4)
     rf["link_latency_ns"] = {k: round(v, 1) for k, v in lat.items()}
     rf["floors_note"] = ("frac = per_direction / t (each direction at its solo rate, both at once: not reachable, "
-                         "the link gives ~138 + 138 GB/s with both directions busy); frac_duplex = duplex / t; "
+                         "the link gives about 170 + 170 GB/s with both directions streaming); "
+                         "frac_duplex = duplex / t (each direction at its concurrent rate, measured in this run); "
                          "latency_chain = publish (4 KiB stores + the fence of the call's scope) + flag one way "
                          "(" + ("HBM, GPU scope" if gpu_scope else "host memory, system scope") + ") + one read "
                          "round trip, from ar_probe_host_link_latency")

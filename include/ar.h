@@ -569,11 +569,11 @@ AR_API const char *ar_strerror(int code);
  * times them with CUDA events and frees everything.
  *
  * ar_probe_host_link: GPU kernels stream `bytes` to mapped pinned host memory
- *   (write), from it (read), and both at once (a kernel that reads one mapped
- *   host buffer and writes another, as the exchange kernels do).
+ *   (write), from it (read), and both at once: half the blocks store to one
+ *   mapped host buffer while the other half load from another, for a fixed
+ *   window (at least 1 ms), about as many bytes each way.
  *   gbs[0] = write GB/s, gbs[1] = read GB/s, gbs[2] = write GB/s while reading,
- *   gbs[3] = read GB/s while writing (equal: the copy moves as many bytes each
- *   way).  (1 GB = 1e9 bytes.)
+ *   gbs[3] = read GB/s while writing.  (1 GB = 1e9 bytes.)
  * ar_probe_hbm_copy: a device-to-device copy kernel over `bytes`; *gbs counts
  *   read + write bytes.
  */
