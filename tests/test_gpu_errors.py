@@ -218,6 +218,11 @@ def test_probes_run():
     tda = _tda()
     link = tda.ar_probe_host_link(64 << 20, 5)
     assert all(v > 1.0 for v in link.values()), link
+    # both directions at once: each below its solo rate (with some slack for
+    # noise), together above either alone
+    assert link["bidir_write_gbs"] < 1.1 * link["write_gbs"], link
+    assert link["bidir_read_gbs"] < 1.1 * link["read_gbs"], link
+    assert link["bidir_write_gbs"] + link["bidir_read_gbs"] > max(link["write_gbs"], link["read_gbs"]), link
     assert tda.ar_probe_hbm_copy(1 << 30, 5) > 100.0
 
 
