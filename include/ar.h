@@ -68,13 +68,15 @@ typedef struct ar_handle ar_handle;
  * gather complex64 tensors and never reduce them). */
 enum ar_dtype { AR_F16 = 1, AR_BF16 = 2, AR_C64 = 3 };
 
-/* Where the shared slots and flags live.
+/* Where the shared slots live.
  * AR_SLOT_PINNED_HOST: page-locked host memory mapped into the GPU
  *   (cudaHostAlloc mapped|portable), as on the pages, where two GPUs without
  *   peer access both map it ("[Kernel] Two-rank FP16 all-reduce through pinned
- *   host memory for GPUs without P2P", section "Purpose").  Flags use
- *   system-scope release/acquire.
- * AR_SLOT_HBM: device memory of this GPU; flags use GPU-scope release/acquire. */
+ *   host memory for GPUs without P2P", section "Purpose").  The per-block
+ *   flags are in HBM with GPU-scope release/acquire by default, or in mapped
+ *   host memory with system-scope release/acquire (ar_tactics.gpu_scope = 0).
+ * AR_SLOT_HBM: device memory of this GPU; flags in HBM, GPU-scope
+ *   release/acquire. */
 enum ar_slot_kind { AR_SLOT_PINNED_HOST = 0, AR_SLOT_HBM = 1 };
 
 enum ar_code {
@@ -252,7 +254,8 @@ typedef struct ar_tactics {
  *           itemsize, as for the workspace in "[SM120] Add optional FlashInfer
  *           PCIe-IPC all-reduce for switch-free hosts", section "Modifications";
  *   flags   one 64-bit flag per (rank, block), each on its own 128-byte line, in
- *           the same memory as the slots;
+ *           HBM, and for pinned-host slots a second set in mapped host memory
+ *           (used when ar_tactics.gpu_scope is 0);
  *   counters one 64-bit stage counter and one 64-bit call counter per (rank,
  *           block), in device memory: the call parity that picks the slot buffer
  *           comes from them, never from the host, so captured graphs replay
