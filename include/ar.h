@@ -195,7 +195,7 @@ typedef struct ar_plan {
     int32_t subtile_vecs;   /* two-shot: vectors per sub-tile (64, 128 or 256; a tile is R sub-tiles); else 0 */
     int32_t pace_cycles;    /* SM cycles between the first-stage slot stores of consecutive blocks (the
                                pace_mbs tactics, slots in host memory); 0: all at once.  ar_plan_for
-                               only; ar_plan_compute leaves it 0 */
+                               only, for inputs in device memory (zero-copy calls run unpaced); ar_plan_compute leaves it 0 */
     uint64_t tile_bytes;    /* bytes a block handles per stage (threads * unroll * vec_bytes) */
     uint64_t tiles;         /* ceil(bytes / tile_bytes); tile t goes to block t % blocks, stage t / blocks */
     uint64_t max_stages;    /* stages of block 0 = ceil(tiles / blocks) */
@@ -226,8 +226,10 @@ typedef struct ar_tactics {
                                    as fast as it drains them rather than all at once.  One-shot, two-shot
                                    and cluster all-reduce forms (the cluster form only when all its
                                    clusters are resident at once) and the allgather.  0 = all at once; otherwise >= 1000.  Default 356000 for
-                                   pinned-host handles; ignored for HBM.  Timing only: the results do
-                                   not change */
+                                   pinned-host handles; ignored for HBM.  Calls whose inputs are in
+                                   mapped host memory (zero copy) run unpaced: their input loads cross
+                                   the link first and stagger the stores already.  Timing only:
+                                   the results do not change */
     uint64_t pace_min_bytes;    /* pace only calls of at least this many bytes per rank (default 128 KiB) */
     int32_t pace_multi_mbs;     /* as pace_mbs, for calls of several stages per block (default 220000) */
     int32_t gpu_scope;          /* slots in host memory: the scope at which the ranks synchronise.  1 = GPU

@@ -78,6 +78,13 @@ struct ar_handle {
     // call sequence number on the same stream (that pairing cannot finish).
     std::atomic<uint64_t> host_calls[tda::kMaxRanks];
     std::atomic<uintptr_t> host_stream[tda::kMaxRanks];
+    // Whether recent input pointers are mapped host memory (zero-copy calls
+    // run unpaced): a cache, so that a caller reusing its buffers pays the
+    // runtime query (a few microseconds) once per buffer.  Entries pack the address with the answer in
+    // bit 0 (addresses are 16-byte aligned); 0 is empty.  An entry may outlive
+    // its buffer; the answer only sets when stores start, never the bits.
+    static constexpr int kIoCache = 1024;
+    std::atomic<uintptr_t> io_cache[kIoCache];
 };
 
 namespace {
@@ -213,6 +220,9 @@ int zero_state(ar_handle *h) {
     for (int r = 0; r < tda::kMaxRanks; ++r) {
         h->host_calls[r].store(0);
         h->host_stream[r].store(0);
+    }
+    for (auto &e : h->io_cache) {
+        e.store(0);
     }
     if (cudaDeviceSynchronize() != cudaSuccess) return AR_ECUDA;
     return AR_OK;
@@ -728,6 +738,40 @@ uint32_t pace_cycles(const ar_handle *h, uint64_t bytes, const ar_plan &plan, in
     return (uint32_t)(cyc + 0.5);
 }
 
+// True if an input pointer of the call (the rank's own, or all R for a launch
+// of every rank) is mapped host memory.  Such zero-copy calls read their
+// inputs over the host link before the slot stores, which staggers the stores
+// by itself, so they are not paced: measured on a GB300 (R=2 fp16
+// 256 KiB, in and out in pinned host memory, graphs of 100 calls, GB/s at
+// pace 356 / 300 / 250 / 200 / 150 / none): per-rank launches 31.2 / 30.5 /
+// 31.4 / 28.9 / 26.4 / 33.0, one launch of both ranks 31.0 / 30.5 / 29.9 /
+// 28.7 / 26.8 / 31.4.  Pointers the runtime does not know (an error from the
+// query) count as device memory.
+static_assert(ar_handle::kIoCache == 1024, "host_ptr hashes to 10 bits");
+bool host_ptr(ar_handle *h, const void *p) {
+    const uintptr_t a = (uintptr_t)p;
+    const int slot = (int)((a >> 4) * 0x9E3779B97F4A7C15ull >> 54);  // 10 bits: kIoCache slots
+    const uintptr_t e = h->io_cache[slot].load(std::memory_order_relaxed);
+    if ((e & ~(uintptr_t)1) == a) return (e & 1) != 0;
+    cudaPointerAttributes attr;
+    bool host = false;
+    if (cudaPointerGetAttributes(&attr, p) == cudaSuccess) host = attr.type == cudaMemoryTypeHost;
+    else (void)cudaGetLastError();
+    h->io_cache[slot].store(a | (host ? 1 : 0), std::memory_order_relaxed);
+    return host;
+}
+
+bool host_io(ar_handle *h, const tda::RankIO &io, int n) {
+    for (int r = 0; r < n; ++r)
+        if (io.in[r] && host_ptr(h, io.in[r])) return true;
+    return false;
+}
+
+// The pace of a call: the handle's, unless the call is zero copy.
+uint32_t call_pace(ar_handle *h, uint32_t pace, const tda::RankIO &io, int n) {
+    return pace && host_io(h, io, n) ? 0u : pace;
+}
+
 // The cluster form's pacing: only when every cluster of the call is resident
 // at once (a cluster of a later wave starts when an earlier one ends, already
 // behind the others).
@@ -747,7 +791,7 @@ int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
         const int blocks = plan.blocks;  // within handle_cluster_grid: counters, trace, block cap
         DevState d = dev_state(h);
         d.algo = AR_ALGO_CLUSTER;
-        d.pace_cycles = cluster_pace_cycles(h, bytes, plan);
+        d.pace_cycles = call_pace(h, cluster_pace_cycles(h, bytes, plan), io, fused ? h->R : 1);
         const cudaError_t e =
             tda::launch_allreduce_cluster(h->dtype, h->R, plan.subtile_vecs, blocks, s, io, numel, d, h->pdl);
         if (e != cudaSuccess) {
@@ -779,7 +823,8 @@ int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
                                                  : plan.unroll;
     DevState d = dev_state(h);
     d.algo = algo;
-    if (algo == AR_ALGO_ONESHOT || algo == AR_ALGO_TWOSHOT) d.pace_cycles = pace_cycles(h, bytes, plan, blocks);
+    if (algo == AR_ALGO_ONESHOT || algo == AR_ALGO_TWOSHOT)
+        d.pace_cycles = call_pace(h, pace_cycles(h, bytes, plan, blocks), io, fused ? h->R : 1);
     const cudaError_t e = tda::launch_allreduce(h->dtype, h->R, variant, blocks, s, io, numel, rank, d, h->pdl);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
@@ -796,7 +841,8 @@ int enqueue_allgather(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
     if (rc != AR_OK) return rc;
     const int blocks = handle_blocks(h, plan.blocks);
     DevState d = dev_state(h);
-    d.pace_cycles = pace_cycles(h, bytes, plan, blocks);  // the one-shot form's link bytes: share 1/R
+    // the one-shot form's link bytes: share 1/R; zero-copy calls not paced
+    d.pace_cycles = call_pace(h, pace_cycles(h, bytes, plan, blocks), io, rank < 0 ? h->R : 1);
     // publish one stage ahead in HBM for calls of several tiles per block, as
     // the one-shot all-reduce does (16- and 8-byte vectors, untraced)
     const bool ahead = h->kind == AR_SLOT_HBM && !h->trace && vw >= 8 && plan.tiles > (uint64_t)blocks;
