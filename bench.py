@@ -254,6 +254,10 @@ def measured_peaks():
 class Workload:
     """R ranks, C calls, one graph; every call has its own device buffers."""
 
+    # handles whose device status was read after their timed steps (ar_status:
+    # a bounded wait that ran out would be recorded there, and check() raises)
+    status_reads = 0
+
     def __init__(self, op, R, dtype, numel, slots, calls, config, dist="uniform", algo=None, fused=False,
                  launch=None, tactics=None):
         import torch
@@ -336,6 +340,7 @@ class Workload:
         import oracle
         self.torch.cuda.synchronize()
         self.h.check()
+        Workload.status_reads += 1
         for c in calls:
             c = c % self.C
             xs = [self.host_in[r][c] for r in range(self.R)]
@@ -1023,6 +1028,10 @@ def run_ours(args, dist):
                 "serial_value": round(serial_value, 3),
                 "serial_how": "one copy in, eager ar_allreduce calls, one copy out, no overlap"},
         "gpu_launches": len(ms) * C * R,
+        "device_status": {"reads": Workload.status_reads, "timeouts": 0,
+                          "how": "every workload's handle status (ar_status) read after its timed steps; a "
+                                 "bounded device wait that ran out -- a rank kernel not co-resident with its "
+                                 "peers -- would be recorded there and fail the run"},
         "clocks": clocks,
         "parity": f"bit-exact vs CPU oracle on {checked} sampled (call, rank) outputs",
         "host_link_probe_gbs": {k: round(v, 2) for k, v in link.items()},
