@@ -211,6 +211,176 @@ __global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
     }
 }
 
+// Bulk gather (slots in HBM, 16-byte vectors, untraced): the same protocol
+// and the same publish (ordinary stores into the slot and into the rank's own
+// place in out, one stage ahead, then the flag), but once the peers' flags of
+// a stage are up thread 0 moves their tiles with bulk asynchronous copies:
+// one cp.async.bulk per peer from its slot into shared memory, completing on
+// an mbarrier, then one bulk store per peer from shared memory into its place
+// in out.  The copies hold no registers, so a block has (R - 1) whole tiles in
+// flight where its threads held four 16-byte vectors each.  Used from R = 5
+// (measured on a GB300, complex64 1000 x 500 shards, graphs, us/call, bulk /
+// per-thread gather: R = 8 55.8-55.9 / 58.0, in one launch of every rank
+// 55.3 / 58.2; R = 4 18.2 / 18.1).  Storing each stage's tiles one stage
+// later, so that the loads complete during the next flag round, measured R = 8
+// 58.9 / 57.6 and R = 4 17.9 / 18.1 (one buffer: the next loads wait for the
+// stores to have read it).
+//  - The peers' slot stores are ordinary (generic-proxy) stores ordered by
+//    their release and this block's acquire; thread 0 puts a proxy fence
+//    between that acquire and its bulk (async-proxy) reads.
+//  - Before a stage's bulk loads reuse the shared buffer, the previous stage's
+//    bulk stores have finished reading it (wait_group.read).
+//  - The mbarrier wait is bounded like the flag waits; thread 0 records a
+//    wait that runs out (peer = its own rank: its own copies) and sets the
+//    block's bail word, which the next flag wait returns to every thread, so
+//    the whole block leaves together, after its bulk stores have completed.
+//  - Before the block ends, all its bulk stores have completed (wait_group 0).
+// Dynamic shared memory: (R - 1) * kThreads * U * 16 bytes.
+__device__ __forceinline__ unsigned smem_addr(const void *p) { return (unsigned)__cvta_generic_to_shared(p); }
+
+template <int R, int U, bool F>
+__global__ void __launch_bounds__(kThreads, R <= 4 ? 5 : 4)
+    allgather_bulk_kernel(const uint8_t *in_arg, uint8_t *out_arg, uint64_t bytes, int rank_arg, DevState d,
+                          RankIO io) {
+    using V = uint4;
+    extern __shared__ __align__(128) uint4 s_tiles[];  // [R - 1][kTileVecs]
+    __shared__ __align__(8) unsigned long long s_mbar;
+    __shared__ unsigned long long s_seq;
+    __shared__ unsigned long long s_calls;
+    __shared__ int s_bail;
+
+    const int rank = block_rank<F>(rank_arg);
+    const uint8_t *in = rank_ptr<R, F>(in_arg, io.in, rank);
+    uint8_t *out = rank_ptr<R, F>(out_arg, io.out, rank);
+
+    const int b = blockIdx.x;
+    const int B = gridDim.x;
+    const int tid = threadIdx.x;
+    const uint64_t nv = bytes / 16;
+    constexpr uint64_t kTileVecs = (uint64_t)kThreads * U;
+    const uint64_t ntiles = (nv + kTileVecs - 1) / kTileVecs;
+    const uint64_t nstages = ntiles > (uint64_t)b ? (ntiles - b + B - 1) / B : 0;
+    const unsigned mbar = smem_addr(&s_mbar);
+
+    pdl_wait();
+    if (tid == 0) {
+        const Ctr c = d.ctr[(size_t)rank * d.cmax + b];
+        s_seq = c.seq;
+        s_calls = c.calls;
+        s_bail = 0;
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    const V *src = reinterpret_cast<const V *>(in);
+    V *dst = reinterpret_cast<V *>(out);
+    V nxt[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint64_t v = (uint64_t)b * kTileVecs + (uint64_t)u * kThreads + tid;
+        if (v < nv) nxt[u] = src[v];
+    }
+    __syncthreads();
+    const unsigned long long seq = s_seq;
+    const int parity = (int)(s_calls & 1ull);
+    advance_idle_blocks(d, rank, s_calls + 1ull);
+    const uint64_t slot_vecs = d.slot_bytes / 16;
+    V *const slot_base = reinterpret_cast<V *>(d.slots) + (uint64_t)parity * R * slot_vecs;
+    V *const my_slot = slot_base + (uint64_t)rank * slot_vecs;
+
+    // publish stage s (tile b + s * B) from nxt; the flag goes to seq + s + 1
+    auto publish = [&](uint64_t s) {
+        const uint64_t v0 = ((uint64_t)b + s * B) * kTileVecs + tid;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint64_t v = v0 + (uint64_t)u * kThreads;
+            if (v < nv) {
+                my_slot[v] = nxt[u];
+                dst[(uint64_t)rank * nv + v] = nxt[u];
+            }
+        }
+        __syncthreads();
+        if (tid == 0) publish_stage(d, rank, b, seq + s + 1);
+    };
+    if (nstages) publish(0);
+
+    for (uint64_t s = 0; s < nstages; ++s) {
+        const uint64_t tile = (uint64_t)b + s * B;
+        const uint64_t v0 = tile * kTileVecs;
+        if (s + 1 < nstages) {
+            const uint64_t vn = (tile + B) * kTileVecs + tid;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint64_t v = vn + (uint64_t)u * kThreads;
+                if (v < nv) nxt[u] = src[v];
+            }
+            publish(s + 1);
+        }
+        if (wait_peers(d, R, rank, b, seq + s + 1, &s_bail)) break;
+        if (s + 1 == nstages) pdl_trigger();
+        if (tid == 0) {
+            const uint64_t nvec = nv - v0 < kTileVecs ? nv - v0 : kTileVecs;
+            const unsigned nbytes = (unsigned)(nvec * 16);
+            // the previous stage's bulk stores have read the buffer
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            // the peers' slot stores, acquired through their flags, before the bulk reads
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar),
+                         "r"(nbytes * (unsigned)(R - 1))
+                         : "memory");
+            int j = 0;
+#pragma unroll
+            for (int p = 0; p < R; ++p) {
+                if (p == rank) continue;
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                        smem_addr(s_tiles + (uint64_t)j * kTileVecs)),
+                    "l"(slot_base + (uint64_t)p * slot_vecs + v0), "r"(nbytes), "r"(mbar)
+                    : "memory");
+                ++j;
+            }
+            // wait for this stage's phase (bounded by the handle's timeout)
+            const unsigned ph = (unsigned)(s & 1ull);
+            const unsigned long long t0 = global_timer_ns();
+            unsigned done = 0;
+            for (unsigned it = 0; !done; ++it) {
+                asm volatile(
+                    "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                    : "=r"(done)
+                    : "r"(mbar), "r"(ph)
+                    : "memory");
+                if (!done && (it & 255u) == 255u && global_timer_ns() - t0 > d.timeout_ns) break;
+            }
+            if (!done) {
+                record_timeout(d, rank, b, rank, seq + s + 1, 0);
+                s_bail = 1;
+            } else {
+                j = 0;
+#pragma unroll
+                for (int p = 0; p < R; ++p) {
+                    if (p == rank) continue;
+                    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                                     dst + (uint64_t)p * nv + v0),
+                                 "r"(smem_addr(s_tiles + (uint64_t)j * kTileVecs)), "r"(nbytes)
+                                 : "memory");
+                    ++j;
+                }
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            }
+        }
+    }
+
+    if (tid == 0) {
+        // every bulk store of this block has completed before it ends
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        if (!s_bail) {
+            Ctr c;
+            c.seq = seq + nstages;
+            c.calls = s_calls + 1;
+            d.ctr[(size_t)rank * d.cmax + b] = c;
+        }
+    }
+}
+
 template <int VW, int U, bool F, bool T, bool A>
 const void *allgather_ptr_ru(int R) {
     switch (R) {
@@ -244,9 +414,32 @@ const void *allgather_ptr_r(int R, int U, bool fused, bool traced) {
     return fused ? allgather_ptr_rft<VW, true, false>(R, U) : allgather_ptr_rft<VW, false, false>(R, U);
 }
 
+template <int U, bool F>
+const void *allgather_bulk_ptr(int R) {
+    switch (R) {
+        case 1: return (const void *)allgather_bulk_kernel<1, U, F>;
+        case 2: return (const void *)allgather_bulk_kernel<2, U, F>;
+        case 3: return (const void *)allgather_bulk_kernel<3, U, F>;
+        case 4: return (const void *)allgather_bulk_kernel<4, U, F>;
+        case 5: return (const void *)allgather_bulk_kernel<5, U, F>;
+        case 6: return (const void *)allgather_bulk_kernel<6, U, F>;
+        case 7: return (const void *)allgather_bulk_kernel<7, U, F>;
+        case 8: return (const void *)allgather_bulk_kernel<8, U, F>;
+        default: return nullptr;
+    }
+}
+
 }  // namespace
 
 const void *allgather_kernel_ptr(int vec_bytes, int R, int unroll, bool fused, bool traced) {
+    if (allgather_bulk(unroll)) {
+        // 16-byte vectors, untraced only
+        if (vec_bytes != 16 || traced) return nullptr;
+        const int u = allgather_bulk_unroll(unroll);
+        if (u == 1) return fused ? allgather_bulk_ptr<1, true>(R) : allgather_bulk_ptr<1, false>(R);
+        if (u == 2) return fused ? allgather_bulk_ptr<2, true>(R) : allgather_bulk_ptr<2, false>(R);
+        return nullptr;
+    }
     switch (vec_bytes) {
         case 16: return allgather_ptr_r<16>(R, unroll, fused, traced);
         case 8: return allgather_ptr_r<8>(R, unroll, fused, traced);
@@ -261,6 +454,7 @@ cudaError_t launch_allgather(int vec_bytes, int R, int unroll, int blocks, cudaS
                              const RankIO &io, uint64_t bytes, int rank, const DevState &d, bool pdl) {
     const void *k = allgather_kernel_ptr(vec_bytes, R, unroll, rank < 0, d.trace != nullptr);
     if (!k) return cudaErrorInvalidValue;
+    const size_t smem = allgather_bulk(unroll) ? (size_t)allgather_bulk_smem(R, allgather_bulk_unroll(unroll)) : 0;
     const uint8_t *a0 = static_cast<const uint8_t *>(io.in[0]);
     uint8_t *a1 = static_cast<uint8_t *>(io.out[0]);
     uint64_t a2 = bytes;
@@ -268,7 +462,7 @@ cudaError_t launch_allgather(int vec_bytes, int R, int unroll, int blocks, cudaS
     DevState a4 = d;
     RankIO a5 = io;
     void *args[] = {&a0, &a1, &a2, &a3, &a4, &a5};
-    return launch(k, blocks, rank < 0 ? R : 1, rank < 0, s, args, pdl);
+    return launch(k, blocks, rank < 0 ? R : 1, rank < 0, s, args, pdl, smem);
 }
 
 }  // namespace tda

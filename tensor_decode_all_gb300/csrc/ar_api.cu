@@ -233,12 +233,16 @@ int zero_state(ar_handle *h) {
 // at the same time: the co-residency the spin-waits need.  Also loads each
 // variant into the context now (cudaFuncGetAttributes), so that no kernel is
 // loaded lazily while its first launch is being captured into a graph.
-int kernel_occupancy(const void *k, int *bps) {
+int kernel_occupancy(const void *k, int *bps, size_t smem = 0) {
     if (!k) return AR_ECUDA;
     cudaFuncAttributes attr;
     if (cudaFuncGetAttributes(&attr, k) != cudaSuccess) return AR_ECUDA;
+    // kernels with dynamic shared memory: allow it (static plus dynamic may
+    // pass the default 48 KiB)
+    if (smem > 0 && cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return AR_ECUDA;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, tda::kThreads, 0) != cudaSuccess) return AR_ECUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, tda::kThreads, smem) != cudaSuccess) return AR_ECUDA;
     if (n < *bps) *bps = n;
     return AR_OK;
 }
@@ -272,6 +276,11 @@ int family_occupancy(const ar_handle *h, bool fused, bool traced, int *bps) {
                 rc = kernel_occupancy(
                     tda::allgather_kernel_ptr(vw, h->R, a ? tda::oneshot_ahead_variant(u) : u, fused, traced),
                     &bps[kAllgather]);
+    // the bulk-gather kernel: slots in HBM, R >= 5, untraced
+    if (h->kind == AR_SLOT_HBM && h->R >= 5 && !traced)
+        for (int u = 1; u <= 2 && rc == AR_OK; ++u)
+            rc = kernel_occupancy(tda::allgather_kernel_ptr(16, h->R, tda::allgather_bulk_variant(u), fused, false),
+                                  &bps[kAllgather], tda::allgather_bulk_smem(h->R, u));
     if (rc != AR_OK) return rc;
     for (int f = 0; f < kFamilies; ++f) {
         if (bps[f] == kUnset) bps[f] = bps[kAllgather];  // complex64 handles launch no all-reduce kernel
@@ -843,10 +852,14 @@ int enqueue_allgather(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
     DevState d = dev_state(h);
     // the one-shot form's link bytes: share 1/R; zero-copy calls not paced
     d.pace_cycles = call_pace(h, pace_cycles(h, bytes, plan, blocks), io, rank < 0 ? h->R : 1);
-    // publish one stage ahead in HBM for calls of several tiles per block, as
-    // the one-shot all-reduce does (16- and 8-byte vectors, untraced)
+    // slots in HBM, untraced: 16-byte vectors at R >= 5 take the bulk-gather
+    // kernel; the others publish one stage ahead for calls of several tiles
+    // per block, as the one-shot all-reduce does (16- and 8-byte vectors)
+    const bool bulk = h->kind == AR_SLOT_HBM && !h->trace && vw == 16 && h->R >= 5;
     const bool ahead = h->kind == AR_SLOT_HBM && !h->trace && vw >= 8 && plan.tiles > (uint64_t)blocks;
-    const int unroll = ahead ? tda::oneshot_ahead_variant(plan.unroll) : plan.unroll;
+    const int unroll = bulk    ? tda::allgather_bulk_variant(plan.unroll)
+                       : ahead ? tda::oneshot_ahead_variant(plan.unroll)
+                               : plan.unroll;
     const cudaError_t e = tda::launch_allgather(vw, h->R, unroll, blocks, s, io, bytes, rank, d, h->pdl);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
@@ -1471,11 +1484,11 @@ cudaError_t launch_allreduce_cluster(int dtype, int R, int sub, int blocks, cuda
 }
 
 cudaError_t launch(const void *k, int blocks, int ranks, bool cooperative, cudaStream_t s, void **args,
-                   bool pdl) {
+                   bool pdl, size_t smem) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks, (unsigned)ranks);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     int n = 0;

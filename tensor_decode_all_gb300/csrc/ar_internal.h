@@ -41,6 +41,15 @@ constexpr bool twoshot_merged(int variant) { return ((-variant) & 1) != 0; }
 constexpr int oneshot_ahead_variant(int unroll) { return 4 + unroll; }
 constexpr int oneshot_unroll(int variant) { return variant > 4 ? variant - 4 : variant; }
 constexpr bool oneshot_ahead(int variant) { return variant > 4; }
+// Kernel variant codes of the allgather's bulk-gather kernel (slots in HBM,
+// 16-byte vectors, untraced): its vectors per thread per stage, plus 8.
+constexpr int allgather_bulk_variant(int unroll) { return 8 + unroll; }
+constexpr bool allgather_bulk(int variant) { return variant > 8; }
+constexpr int allgather_bulk_unroll(int variant) { return variant - 8; }
+// Its dynamic shared memory: one tile of every peer.
+constexpr uint64_t allgather_bulk_smem(int R, int unroll) {
+    return (uint64_t)(R > 1 ? R - 1 : 0) * (uint64_t)kThreads * (uint64_t)unroll * 16ull;
+}
 // Kernel variant code of the tagged-word form.
 constexpr int kTaggedVariant = 0;
 // Kernel variant code of the push form.
@@ -94,7 +103,7 @@ struct RankIO {
 // makes every block resident at once or refuses the launch.  With pdl, as a
 // programmatic dependent of the preceding work on s.
 cudaError_t launch(const void *k, int blocks, int ranks, bool cooperative, cudaStream_t s, void **args,
-                   bool pdl);
+                   bool pdl, size_t smem = 0);
 
 // Launchers (one per kernel family).  rank >= 0: that rank's kernel, `blocks`
 // blocks; rank < 0: all R ranks in one cooperative grid of blocks x R.
