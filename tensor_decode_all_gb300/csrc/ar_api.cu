@@ -21,7 +21,10 @@ using tda::Ctr;
 using tda::DevState;
 
 // Kernel families, for the occupancy table.
-enum { kOneShot = 0, kTwoShot = 1, kTagged = 2, kAllgather = 3, kPush = 4, kFamilies = 5 };
+// Kernel families, each with its own blocks per SM (the smallest over its
+// variants): the allgather's bulk-gather kernel holds a tile of every peer in
+// shared memory and fits fewer blocks per SM than the per-thread gather.
+enum { kOneShot = 0, kTwoShot = 1, kTagged = 2, kAllgather = 3, kPush = 4, kAllgatherBulk = 5, kFamilies = 6 };
 
 struct ar_handle {
     int R = 0, dtype = 0, kind = 0, device = 0;
@@ -280,7 +283,7 @@ int family_occupancy(const ar_handle *h, bool fused, bool traced, int *bps) {
     if (h->kind == AR_SLOT_HBM && h->R >= 5 && !traced)
         for (int u = 1; u <= 2 && rc == AR_OK; ++u)
             rc = kernel_occupancy(tda::allgather_kernel_ptr(16, h->R, tda::allgather_bulk_variant(u), fused, false),
-                                  &bps[kAllgather], tda::allgather_bulk_smem(h->R, u));
+                                  &bps[kAllgatherBulk], tda::allgather_bulk_smem(h->R, u));
     if (rc != AR_OK) return rc;
     for (int f = 0; f < kFamilies; ++f) {
         if (bps[f] == kUnset) bps[f] = bps[kAllgather];  // complex64 handles launch no all-reduce kernel
@@ -842,20 +845,25 @@ int enqueue_allreduce(ar_handle *h, const tda::RankIO &io, size_t numel, int ran
     return AR_OK;
 }
 
+// Slots in HBM, untraced: 16-byte vectors at R >= 5 take the allgather's
+// bulk-gather kernel.
+bool allgather_takes_bulk(const ar_handle *h, int vw) {
+    return h->kind == AR_SLOT_HBM && !h->trace && vw == 16 && h->R >= 5;
+}
+
 int enqueue_allgather(ar_handle *h, const tda::RankIO &io, size_t numel, int rank, int vw, cudaStream_t s) {
     const uint64_t bytes = numel * h->itemsize;
+    const bool bulk = allgather_takes_bulk(h, vw);
     ar_plan plan;
     int rc = plan_compute(h->R, bytes, vw, AR_ALGO_ONESHOT, tda::kThreads, h->sm_count,
-                          h->bps[rank < 0 ? 1 : 0][h->trace ? 1 : 0][kAllgather], &plan);
+                          h->bps[rank < 0 ? 1 : 0][h->trace ? 1 : 0][bulk ? kAllgatherBulk : kAllgather], &plan);
     if (rc != AR_OK) return rc;
     const int blocks = handle_blocks(h, plan.blocks);
     DevState d = dev_state(h);
     // the one-shot form's link bytes: share 1/R; zero-copy calls not paced
     d.pace_cycles = call_pace(h, pace_cycles(h, bytes, plan, blocks), io, rank < 0 ? h->R : 1);
-    // slots in HBM, untraced: 16-byte vectors at R >= 5 take the bulk-gather
-    // kernel; the others publish one stage ahead for calls of several tiles
-    // per block, as the one-shot all-reduce does (16- and 8-byte vectors)
-    const bool bulk = h->kind == AR_SLOT_HBM && !h->trace && vw == 16 && h->R >= 5;
+    // the others publish one stage ahead in HBM for calls of several tiles per
+    // block, as the one-shot all-reduce does (16- and 8-byte vectors)
     const bool ahead = h->kind == AR_SLOT_HBM && !h->trace && vw >= 8 && plan.tiles > (uint64_t)blocks;
     const int unroll = bulk    ? tda::allgather_bulk_variant(plan.unroll)
                        : ahead ? tda::oneshot_ahead_variant(plan.unroll)
@@ -1394,7 +1402,8 @@ AR_API int ar_plan_for(const ar_handle *h, int op, size_t numel, ar_plan *plan) 
         return AR_OK;
     }
     const int vec = op == 0 ? 16 : allgather_vec(bytes, nullptr, nullptr);
-    int algo = AR_ALGO_ONESHOT, bps = h->bps[0][h->trace ? 1 : 0][kAllgather];
+    int algo = AR_ALGO_ONESHOT,
+        bps = h->bps[0][h->trace ? 1 : 0][allgather_takes_bulk(h, vec) ? kAllgatherBulk : kAllgather];
     if (op == 0) {
         algo = handle_algo(h, bytes, false);
         bps = handle_bps(h, algo, false);
